@@ -1,0 +1,357 @@
+"""Decode benchmark: one decode step of a Llama-style model per "step".
+
+Default workload: the Llama-3.2-1B-shaped decoder (16 layers, hidden 2048,
+32/8 heads, FFN 8192, vocab 128256, tied), batch 1, KV context 512, timed over
+the workload's 128 teacher-forced decode steps (positions 512..639). Weights and
+caches are seeded synthetic data (random init), resident in HBM before the
+timed region. Every step streams ~2.49 GB (all weights + the KV read), far more
+than the 129 MB L2, so no flush is needed between steps.
+
+Prints ONE JSON line. `--impl reference` times the CPU oracle instead (the
+reference arm of this comparison), on a bounded sample of the same workload.
+Under torchrun (N > 1) every rank runs an independent replica (no collective
+on the data path) and rank 0 prints the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode µs/token & tokens/s, Llama-1B shape batch 1; % of GB300 HBM roofline"
+
+
+def algorithmic_bytes(shape, batch, positions):
+    """Bytes the method must move per step: every weight matrix and norm gain,
+    the final norm, the LM head, one embedding row per sequence, and the KV
+    cache read over slots 0..pos of every layer and sequence (the new slot
+    included). Logit writes and scratch traffic are not counted."""
+    H, D, F, V, L = shape.hidden, shape.head_dim, shape.ffn, shape.vocab, shape.n_layers
+    per_layer = 2 * (H * shape.n_heads * D * 2 + H * shape.n_kv_heads * D * 2 + 3 * H * F + 2 * H)
+    weights = L * per_layer + 2 * H + 2 * V * H + 2 * H * batch
+    kv = sum(L * 2 * shape.n_kv_heads * D * 2 * (p + 1) for p in positions)
+    return weights, kv
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_oracle_rate(wl, w_host, target_s=12.0, max_steps=64):
+    """Times the oracle as it stands on this host's cores: decode steps of the
+    same workload until about target_s seconds of CPU work."""
+    from oracle import oracle as O
+    shape = wl.shape
+    model = O.Model(shape.as_dict(), w_host)
+    from decode_megakernel_03_gb300 import synth
+    kc, vc = synth.make_kv(shape, wl.batch, wl.capacity, wl.ctx, seed=wl.kv_seed)
+    ks = [synth.bits(t).copy() for t in kc]
+    vs = [synth.bits(t).copy() for t in vc]
+    toks = synth.step_tokens(wl)
+    threads = O.default_threads()
+    t0 = time.perf_counter()
+    n = 0
+    while n < max_steps:
+        model.decode_step(ks, vs, [int(t) for t in toks[n % wl.steps]],
+                          synth.step_positions(wl, n % wl.steps), nthreads=threads)
+        n += 1
+        if time.perf_counter() - t0 > target_s:
+            break
+    dt = time.perf_counter() - t0
+    return n * wl.batch / dt, n, dt, threads
+
+
+def run_reference(args, wl):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from decode_megakernel_03_gb300 import synth
+    w = synth.make_weights(wl.shape, seed=wl.weight_seed)
+    w_host = synth.oracle_weights(w)
+    del w
+    from oracle import oracle as O
+    model = O.Model(wl.shape.as_dict(), w_host)
+    kc, vc = synth.make_kv(wl.shape, wl.batch, wl.capacity, wl.ctx, seed=wl.kv_seed)
+    ks = [synth.bits(t).copy() for t in kc]
+    vs = [synth.bits(t).copy() for t in vc]
+    toks = synth.step_tokens(wl)
+    threads = O.default_threads()
+    for s in range(args.warmup):
+        model.decode_step(ks, vs, [int(t) for t in toks[s % wl.steps]],
+                          synth.step_positions(wl, s % wl.steps), nthreads=threads)
+    times = []
+    for s in range(args.steps):
+        t0 = time.perf_counter()
+        model.decode_step(ks, vs, [int(t) for t in toks[s % wl.steps]],
+                          synth.step_positions(wl, s % wl.steps), nthreads=threads)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * sum(times) / len(times)
+    value = wl.batch / (ms / 1e3)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded random init, random KV context)",
+        "config": {"workload": wl.name, "batch": wl.batch, "ctx": list(wl.ctx),
+                   "l2": "inputs larger than L2"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{args.steps} decode steps of {wl.name} after {args.warmup} warm-up"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args, wl):
+    import torch
+    import torch.distributed as dist
+    from decode_megakernel_03_gb300 import build as mkbuild
+    from decode_megakernel_03_gb300 import mk, synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    mkbuild.build()
+
+    shape = wl.shape
+    w = synth.make_weights(shape, seed=wl.weight_seed, device=dev)
+    kc, vc = synth.make_kv(shape, wl.batch, wl.capacity, wl.ctx, seed=wl.kv_seed, device=dev)
+    dec = mk.Decoder(shape, w, kc, vc, wl.batch)
+    logits = torch.empty((wl.batch, shape.vocab), dtype=torch.float32, device=dev)
+    toks = synth.step_tokens(wl)
+    K, W = args.steps, args.warmup
+    stream = torch.cuda.current_stream()
+
+    def tok_pos(s):
+        s = s % wl.steps
+        return [int(t) for t in toks[s]], synth.step_positions(wl, s)
+
+    def timed(mode):
+        for s in range(W):
+            t, p = tok_pos(s)
+            if mode == "mega":
+                dec.step(t, p, logits)
+            else:
+                dec.step_multilaunch(t, p, logits, graph=(mode == "graph"))
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter()
+        for s in range(K):
+            t, p = tok_pos(s)
+            ev[s][0].record(stream)
+            if mode == "mega":
+                dec.step(t, p, logits)
+            else:
+                dec.step_multilaunch(t, p, logits, graph=(mode == "graph"))
+            ev[s][1].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t_wall
+        assert dec.status() == mk.MK_OK, dec.last_error()
+        per = [a.elapsed_time(b) for a, b in ev]
+        return per, wall
+
+    with ClockSampler(local) as clk:
+        per_mega, wall_mega = timed("mega")
+    per_multi, _ = timed("multi")
+    per_graph, _ = timed("graph")
+
+    # end to end through the public call: host ids/positions in, logits read back
+    host_logits = torch.empty((wl.batch, shape.vocab), dtype=torch.float32, pin_memory=True)
+    for s in range(W):
+        t, p = tok_pos(s)
+        dec.step(t, p, logits)
+        host_logits.copy_(logits, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(K):
+        t, p = tok_pos(s)
+        dec.step(t, p, logits)
+        host_logits.copy_(logits, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / K
+
+    ms = sum(per_mega) / K
+    t_max = torch.tensor([ms], device=dev)
+    if world > 1:
+        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+    ms_all = float(t_max.item())
+
+    positions = [synth.step_positions(wl, s % wl.steps) for s in range(K)]
+    wb, kvb = zip(*[algorithmic_bytes(shape, wl.batch, p) for p in positions])
+    bytes_step = (sum(wb) + sum(kvb)) / K
+    peak, peak_kind = read_peaks()
+    achieved = bytes_step / (ms * 1e-3) / 1e9
+    t_min_ms = bytes_step / (peak * 1e9) * 1e3
+    multi_ms = sum(per_multi) / K
+    graph_ms = sum(per_graph) / K
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        w_host = synth.oracle_weights(w)
+        rate, n, dt, cores = cpu_oracle_rate(wl, w_host)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{n} decode steps of {wl.name} ({dt:.1f} s, all host threads)"}
+
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if os.path.exists(prof):
+        try:
+            d = json.load(open(prof))
+            if d.get("workload") == wl.name and d.get("kernel_rev") == KERNEL_REV:
+                traffic = d.get("bytes_per_launch")
+        except Exception:
+            traffic = None
+
+    if rank == 0:
+        clocks = clk.summary()
+        line = {
+            "metric": METRIC,
+            "value": wl.batch * world / (ms_all * 1e-3),
+            "unit": "tokens/s",
+            "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": ms_all,
+            "us_per_token": ms_all * 1e3 / wl.batch,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16 weights/KV, fp32 activations",
+            "data": "synthetic (seeded random init weights, random bf16 KV context)",
+            "config": {"workload": wl.name, "model": shape.name, "batch": wl.batch,
+                       "ctx": list(wl.ctx), "positions": [positions[0][0], positions[-1][0]],
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (2.5 GB/step streamed), no flush"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_kind,
+                         "algorithmic_bytes_per_step": bytes_step, "traffic": traffic,
+                         "t_min_us": t_min_ms * 1e3},
+            "cpu_baseline": cpu,
+            "e2e": {"value": wl.batch / (e2e_ms * 1e-3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": 8 * wl.batch,
+                    "d2h_bytes_per_step": 4 * wl.batch * shape.vocab},
+            "gpu_launches": K,
+            "clocks": clocks,
+            "comparison": {
+                "megakernel_us": ms * 1e3,
+                "megakernel_p50_us": statistics.median(per_mega) * 1e3,
+                "megakernel_p90_us": float(np.percentile(per_mega, 90)) * 1e3,
+                "multilaunch_us": multi_ms * 1e3,
+                "multilaunch_graph_us": graph_ms * 1e3,
+                "multilaunch_launches_per_step": 6 * shape.n_layers + 1,
+                "recovered_overhead_vs_multilaunch": (multi_ms - ms) / (multi_ms - t_min_ms),
+                "recovered_overhead_vs_graph": (graph_ms - ms) / (graph_ms - t_min_ms),
+                "overhead_megakernel": (ms - t_min_ms) / ms,
+                "overhead_multilaunch": (multi_ms - t_min_ms) / multi_ms,
+                "wall_s_megakernel": wall_mega,
+            },
+        }
+        print(json.dumps(line), flush=True)
+    dec.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+KERNEL_REV = "r1"
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=128)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
+    ap.add_argument("--workload", default="llama1b")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from decode_megakernel_03_gb300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    if args.warmup < 3 and args.impl != "reference":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_gpu(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,570 @@
+// C ABI of libmk.so (declared in include/mk.h): handle lifetime, scratch
+// allocation, the plan cache, and the launches of the persistent interpreter
+// (one per decode step) and of the multi-launch comparison build.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <memory>
+#include <string>
+#include <vector>
+
+#include "mk_isa.h"
+#include "mk_sched.h"
+
+namespace mk {
+const void* kernel_for_batch(int B);
+int misc_bytes();
+}  // namespace mk
+
+using namespace mk;
+
+namespace {
+
+thread_local std::string g_create_error;
+
+struct PlanEntry {
+  int key[kMaxBatch + 1];  // partitions per sequence + injection flag
+  Plan plan;
+  Instr* d_instrs = nullptr;
+  int* d_sm_off = nullptr;
+  Instr* d_phase_instrs = nullptr;  // all multi-launch phases, concatenated
+  int* d_phase_off = nullptr;
+  std::vector<int> phase_instr_base, phase_off_base;
+  cudaGraphExec_t gexec = nullptr;
+  cudaGraph_t graph = nullptr;
+  std::vector<cudaGraphNode_t> nodes;
+  unsigned long long last_use = 0;
+};
+
+}  // namespace
+
+struct mk_handle {
+  mk_config cfg;
+  Shape shape;
+  int device = 0;
+  int n_sm = 0;
+  int smem_bytes = 0;
+  Params base{};          // launch parameters without the per-step fields
+  void* d_scratch = nullptr;
+  LayerPtrs* d_layers = nullptr;
+  float2* d_rope = nullptr;
+  int* d_ctr = nullptr;   // two counter sets
+  int n_ctr = 0;
+  int* d_err = nullptr;
+  int* h_err_mirror = nullptr;  // mapped pinned host memory the kernel writes on error
+  std::vector<PlanEntry*> plans;
+  unsigned long long use_clock = 0;
+  unsigned long long steps = 0;
+  int cur_set = 0;        // counter set used by the most recent step
+  int inject = 0;
+  std::string err;
+};
+
+namespace {
+
+int fail(mk_handle* h, int code, const std::string& msg) {
+  if (h) h->err = msg;
+  else g_create_error = msg;
+  return code;
+}
+
+int cuda_fail(mk_handle* h, cudaError_t e, const char* what) {
+  std::string msg = std::string(what) + ": " + cudaGetErrorString(e);
+  int code = (e == cudaErrorMemoryAllocation) ? MK_ERR_OOM : MK_ERR_CUDA;
+  return fail(h, code, msg);
+}
+
+#define MK_CUDA(h, call)                                   \
+  do {                                                     \
+    cudaError_t e_ = (call);                               \
+    if (e_ != cudaSuccess) return cuda_fail((h), e_, #call); \
+  } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+Shape shape_of(const mk_config& c) {
+  Shape s;
+  s.L = c.n_layers;
+  s.H = c.hidden;
+  s.nh = c.n_heads;
+  s.nkv = c.n_kv_heads;
+  s.D = c.head_dim;
+  s.F = c.ffn;
+  s.V = c.vocab;
+  s.B = c.batch;
+  s.S = c.kv_capacity;
+  return s;
+}
+
+int check_config(const mk_config* c, mk_handle* h) {
+  if (!c) return fail(h, MK_ERR_INVALID, "config is NULL");
+  std::string e = check_shape(shape_of(*c));
+  if (!e.empty()) return fail(h, MK_ERR_INVALID, e);
+  if (!(c->rms_eps >= 0.f) || !(c->rope_theta > 0.f))
+    return fail(h, MK_ERR_INVALID, "rms_eps must be >= 0 and rope_theta > 0");
+  return MK_OK;
+}
+
+int check_steps(mk_handle* h, const int32_t* tok, const int32_t* pos) {
+  if (!tok || !pos) return fail(h, MK_ERR_INVALID, "token_ids / positions must be non-NULL");
+  for (int b = 0; b < h->shape.B; ++b) {
+    if (tok[b] < 0 || tok[b] >= h->shape.V)
+      return fail(h, MK_ERR_INVALID, "token id out of range [0, vocab)");
+    if (pos[b] < 0 || pos[b] >= h->shape.S)
+      return fail(h, MK_ERR_INVALID, "position out of range [0, kv_capacity)");
+  }
+  return MK_OK;
+}
+
+void free_plan(PlanEntry* e) {
+  if (e->gexec) cudaGraphExecDestroy(e->gexec);
+  if (e->graph) cudaGraphDestroy(e->graph);
+  cudaFree(e->d_instrs);
+  cudaFree(e->d_sm_off);
+  cudaFree(e->d_phase_instrs);
+  cudaFree(e->d_phase_off);
+  delete e;
+}
+
+// Returns the plan for these positions, building and uploading it if needed.
+int get_plan(mk_handle* h, const int32_t* pos, PlanEntry** out) {
+  int parts[kMaxBatch];
+  choose_partitions(h->shape, h->n_sm, pos, parts);
+  int key[kMaxBatch + 1];
+  for (int b = 0; b < kMaxBatch; ++b) key[b] = b < h->shape.B ? parts[b] : 0;
+  key[kMaxBatch] = h->inject;
+  for (PlanEntry* e : h->plans)
+    if (std::memcmp(e->key, key, sizeof key) == 0) {
+      e->last_use = ++h->use_clock;
+      *out = e;
+      return MK_OK;
+    }
+  std::unique_ptr<PlanEntry> e(new PlanEntry());
+  std::memcpy(e->key, key, sizeof key);
+  std::string why;
+  if (!build_plan(h->shape, h->n_sm, parts, &e->plan, &why)) return fail(h, MK_ERR_INVALID, why);
+  Plan& P = e->plan;
+  if (h->inject) {
+    // raise the first wait of the last SM's queue past what can ever be produced
+    int s = h->n_sm - 1;
+    for (int i = P.sm_off[s]; i < P.sm_off[s + 1]; ++i)
+      if (P.instrs[i].wait_ctr >= 0) {
+        P.instrs[i].wait_target += 1;
+        break;
+      }
+  }
+  // upload (plans change every few hundred tokens, so a synchronous copy is fine)
+  MK_CUDA(h, cudaMalloc(&e->d_instrs, sizeof(Instr) * std::max<size_t>(1, P.instrs.size())));
+  MK_CUDA(h, cudaMalloc(&e->d_sm_off, sizeof(int) * P.sm_off.size()));
+  MK_CUDA(h, cudaMemcpy(e->d_instrs, P.instrs.data(), sizeof(Instr) * P.instrs.size(),
+                        cudaMemcpyHostToDevice));
+  MK_CUDA(h, cudaMemcpy(e->d_sm_off, P.sm_off.data(), sizeof(int) * P.sm_off.size(),
+                        cudaMemcpyHostToDevice));
+  std::vector<Instr> all;
+  std::vector<int> offs;
+  for (auto& ph : P.phases) {
+    e->phase_instr_base.push_back((int)all.size());
+    e->phase_off_base.push_back((int)offs.size());
+    all.insert(all.end(), ph.instrs.begin(), ph.instrs.end());
+    offs.insert(offs.end(), ph.sm_off.begin(), ph.sm_off.end());
+  }
+  MK_CUDA(h, cudaMalloc(&e->d_phase_instrs, sizeof(Instr) * std::max<size_t>(1, all.size())));
+  MK_CUDA(h, cudaMalloc(&e->d_phase_off, sizeof(int) * std::max<size_t>(1, offs.size())));
+  MK_CUDA(h, cudaMemcpy(e->d_phase_instrs, all.data(), sizeof(Instr) * all.size(),
+                        cudaMemcpyHostToDevice));
+  MK_CUDA(h, cudaMemcpy(e->d_phase_off, offs.data(), sizeof(int) * offs.size(),
+                        cudaMemcpyHostToDevice));
+  // keep a handful of plans; evicting one waits for the device to be idle
+  if (h->plans.size() >= 6) {
+    size_t victim = 0;
+    for (size_t i = 1; i < h->plans.size(); ++i)
+      if (h->plans[i]->last_use < h->plans[victim]->last_use) victim = i;
+    MK_CUDA(h, cudaDeviceSynchronize());
+    free_plan(h->plans[victim]);
+    h->plans.erase(h->plans.begin() + victim);
+  }
+  e->last_use = ++h->use_clock;
+  *out = e.release();
+  h->plans.push_back(*out);
+  return MK_OK;
+}
+
+Params step_params(mk_handle* h, const int32_t* tok, const int32_t* pos, float* logits) {
+  Params p = h->base;
+  for (int b = 0; b < kMaxBatch; ++b) {
+    p.tok[b] = b < h->shape.B ? tok[b] : 0;
+    p.pos[b] = b < h->shape.B ? pos[b] : 0;
+  }
+  p.logits = logits;
+  const int set = (int)(h->steps & 1ull);
+  p.ctr = h->d_ctr + (size_t)set * h->n_ctr;
+  p.ctr_zero = h->d_ctr + (size_t)(set ^ 1) * h->n_ctr;
+  return p;
+}
+
+// A device timeout of an earlier step, seen through the mapped host mirror of
+// the error word without synchronising; sticky until mk_get_status.
+int check_sticky(mk_handle* h) {
+  if (h->h_err_mirror && *reinterpret_cast<volatile int*>(h->h_err_mirror) != 0)
+    return fail(h, MK_ERR_TIMEOUT, "an earlier step reported a device timeout; call mk_get_status");
+  return MK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mk_last_error(const mk_handle* h) {
+  return h ? h->err.c_str() : g_create_error.c_str();
+}
+
+int mk_create(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
+              void* const* v_cache, mk_handle** out) {
+  if (!out) return fail(nullptr, MK_ERR_INVALID, "out is NULL");
+  *out = nullptr;
+  int rc = check_config(cfg, nullptr);
+  if (rc) return rc;
+  if (!w || !k_cache || !v_cache) return fail(nullptr, MK_ERR_INVALID, "weights / caches NULL");
+  const int L = cfg->n_layers;
+  if (!w->embed || !w->final_norm || !w->attn_norm || !w->wq || !w->wk || !w->wv || !w->wo ||
+      !w->mlp_norm || !w->wgate || !w->wup || !w->wdown)
+    return fail(nullptr, MK_ERR_INVALID, "a weight pointer is NULL");
+  if (cfg->tied_embeddings ? (w->lm_head != nullptr) : (w->lm_head == nullptr))
+    return fail(nullptr, MK_ERR_INVALID, "lm_head must be NULL iff tied_embeddings");
+  std::vector<const void*> ptrs = {w->embed, w->final_norm};
+  if (w->lm_head) ptrs.push_back(w->lm_head);
+  for (int l = 0; l < L; ++l) {
+    for (const void* p : {w->attn_norm[l], w->wq[l], w->wk[l], w->wv[l], w->wo[l], w->mlp_norm[l],
+                          w->wgate[l], w->wup[l], w->wdown[l], (const void*)k_cache[l],
+                          (const void*)v_cache[l]})
+      ptrs.push_back(p);
+  }
+  for (const void* p : ptrs) {
+    if (!p) return fail(nullptr, MK_ERR_INVALID, "a weight or cache pointer is NULL");
+    if (!aligned16(p)) return fail(nullptr, MK_ERR_INVALID, "pointers must be 16-byte aligned");
+  }
+
+  std::unique_ptr<mk_handle> h(new mk_handle());
+  h->cfg = *cfg;
+  h->shape = shape_of(*cfg);
+  const Shape& s = h->shape;
+  cudaError_t ce = cudaGetDevice(&h->device);
+  if (ce != cudaSuccess) return cuda_fail(nullptr, ce, "cudaGetDevice");
+  int optin = 0;
+  ce = cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, h->device);
+  if (ce == cudaSuccess)
+    ce = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device);
+  if (ce != cudaSuccess) return cuda_fail(nullptr, ce, "cudaDeviceGetAttribute");
+
+  // ---- shared-memory layout: pages | x staging | h staging | results | misc
+  const int B = s.B;
+  int nseg_max = 1;
+  for (int op : {MK_OP_QKV, MK_OP_OPROJ, MK_OP_GATEUP, MK_OP_DOWN, MK_OP_LMHEAD})
+    nseg_max = std::max(nseg_max, geom_of(op, s.H, s.QD(), s.Fc(), B).nseg);
+  const int item_cap = item_cap_for(s);
+  Params& p = h->base;
+  p.x_floats = B * std::max(s.H, s.QD());
+  p.h_floats = B * s.Fc();
+  p.alias_xh = B > 1 ? 1 : 0;
+  p.res_floats = item_cap * 2 * nseg_max * B;
+  int att_scratch = kComputeWarps * s.G() * (s.D + 2);
+  int xh = p.alias_xh ? std::max(p.x_floats, p.h_floats) : p.x_floats + p.h_floats;
+  xh = std::max(xh, att_scratch);
+  xh = (xh + 3) / 4 * 4;
+  const int fixed = xh * 4 + 2 * p.res_floats * 4 + ((misc_bytes() + 127) / 128) * 128;
+  int n_pages = std::min(kMaxPages, (optin - fixed) / kPageBytes);
+  if (n_pages < 4)
+    return fail(nullptr, MK_ERR_INVALID, "configuration leaves fewer than 4 shared-memory pages");
+  p.n_pages = n_pages;
+  p.off_x = n_pages * kPageBytes;
+  p.off_h = p.alias_xh ? p.off_x : p.off_x + p.x_floats * 4;
+  p.off_res = p.off_x + xh * 4;
+  p.off_misc = p.off_res + 2 * p.res_floats * 4;
+  p.off_misc = (p.off_misc + 127) / 128 * 128;
+  h->smem_bytes = p.off_misc + misc_bytes();
+
+  // ---- model constants
+  p.L = s.L; p.H = s.H; p.nh = s.nh; p.nkv = s.nkv; p.D = s.D; p.F = s.F; p.V = s.V;
+  p.B = s.B; p.S = s.S; p.G = s.G(); p.Fc = s.Fc(); p.QD = s.QD();
+  p.eps = cfg->rms_eps;
+  p.embed = static_cast<const uint16_t*>(w->embed);
+  p.lm = static_cast<const uint16_t*>(cfg->tied_embeddings ? w->embed : w->lm_head);
+  p.final_norm = static_cast<const uint16_t*>(w->final_norm);
+  p.timeout_ns = 2000000000ull;
+
+  // ---- scratch: one allocation, 256-byte aligned pieces
+  CounterMap cm{s.L, s.nkv, s.B};
+  h->n_ctr = cm.count();
+  size_t sizes[] = {
+      sizeof(float) * (size_t)B * s.H,                                    // x
+      sizeof(float) * (size_t)B * s.H,                                    // xa
+      sizeof(float) * (size_t)B * s.QD(),                                 // q
+      sizeof(float) * (size_t)B * s.nh * kMaxPartitions * (s.D + 2),      // part
+      sizeof(float) * (size_t)B * s.QD(),                                 // attn
+      sizeof(float) * (size_t)B * s.F,                                    // h
+      sizeof(float) * (size_t)B * s.H,                                    // dacc
+      sizeof(float2) * (size_t)s.S * (s.D / 2),                           // rope
+      sizeof(LayerPtrs) * (size_t)s.L,                                    // layers
+      sizeof(int) * (size_t)2 * h->n_ctr,                                 // counters
+      sizeof(int) * 64,                                                   // error word
+  };
+  const int npieces = sizeof(sizes) / sizeof(sizes[0]);
+  size_t offs[npieces], total = 0;
+  for (int i = 0; i < npieces; ++i) {
+    offs[i] = total;
+    total += (sizes[i] + 255) / 256 * 256;
+  }
+  ce = cudaMalloc(&h->d_scratch, total);
+  if (ce != cudaSuccess) return cuda_fail(nullptr, ce, "cudaMalloc(scratch)");
+  char* base = static_cast<char*>(h->d_scratch);
+  p.x = reinterpret_cast<float*>(base + offs[0]);
+  p.xa = reinterpret_cast<float*>(base + offs[1]);
+  p.q = reinterpret_cast<float*>(base + offs[2]);
+  p.part = reinterpret_cast<float*>(base + offs[3]);
+  p.attn = reinterpret_cast<float*>(base + offs[4]);
+  p.h = reinterpret_cast<float*>(base + offs[5]);
+  p.dacc = reinterpret_cast<float*>(base + offs[6]);
+  h->d_rope = reinterpret_cast<float2*>(base + offs[7]);
+  h->d_layers = reinterpret_cast<LayerPtrs*>(base + offs[8]);
+  h->d_ctr = reinterpret_cast<int*>(base + offs[9]);
+  h->d_err = reinterpret_cast<int*>(base + offs[10]);
+  p.rope = h->d_rope;
+  p.layers = h->d_layers;
+  p.err = h->d_err;
+  p.n_ctr = h->n_ctr;
+
+  ce = cudaMemset(h->d_scratch, 0, total);
+  if (ce != cudaSuccess) {
+    cudaFree(h->d_scratch);
+    return cuda_fail(nullptr, ce, "cudaMemset(scratch)");
+  }
+  ce = cudaHostAlloc(reinterpret_cast<void**>(&h->h_err_mirror), sizeof(int), cudaHostAllocMapped);
+  if (ce == cudaSuccess) {
+    *h->h_err_mirror = 0;
+    ce = cudaHostGetDevicePointer(reinterpret_cast<void**>(&p.err_host), h->h_err_mirror, 0);
+  }
+  if (ce != cudaSuccess) {
+    if (h->h_err_mirror) cudaFreeHost(h->h_err_mirror);
+    cudaFree(h->d_scratch);
+    return cuda_fail(nullptr, ce, "cudaHostAlloc(error mirror)");
+  }
+  // RoPE table: angle = pos * theta^(-2i/D), in double, rounded to fp32
+  std::vector<float2> rope((size_t)s.S * (s.D / 2));
+  for (int pos = 0; pos < s.S; ++pos)
+    for (int i = 0; i < s.D / 2; ++i) {
+      double ang = (double)pos * std::pow((double)cfg->rope_theta, -2.0 * i / (double)s.D);
+      rope[(size_t)pos * (s.D / 2) + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+    }
+  std::vector<LayerPtrs> lp(L);
+  for (int l = 0; l < L; ++l) {
+    lp[l].attn_norm = static_cast<const uint16_t*>(w->attn_norm[l]);
+    lp[l].wq = static_cast<const uint16_t*>(w->wq[l]);
+    lp[l].wk = static_cast<const uint16_t*>(w->wk[l]);
+    lp[l].wv = static_cast<const uint16_t*>(w->wv[l]);
+    lp[l].wo = static_cast<const uint16_t*>(w->wo[l]);
+    lp[l].mlp_norm = static_cast<const uint16_t*>(w->mlp_norm[l]);
+    lp[l].wgate = static_cast<const uint16_t*>(w->wgate[l]);
+    lp[l].wup = static_cast<const uint16_t*>(w->wup[l]);
+    lp[l].wdown = static_cast<const uint16_t*>(w->wdown[l]);
+    lp[l].kc = static_cast<uint16_t*>(k_cache[l]);
+    lp[l].vc = static_cast<uint16_t*>(v_cache[l]);
+  }
+  ce = cudaMemcpy(h->d_rope, rope.data(), sizeof(float2) * rope.size(), cudaMemcpyHostToDevice);
+  if (ce == cudaSuccess)
+    ce = cudaMemcpy(h->d_layers, lp.data(), sizeof(LayerPtrs) * L, cudaMemcpyHostToDevice);
+  if (ce == cudaSuccess)
+    ce = cudaFuncSetAttribute(kernel_for_batch(B), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              h->smem_bytes);
+  if (ce != cudaSuccess) {
+    cudaFree(h->d_scratch);
+    return cuda_fail(nullptr, ce, "mk_create upload");
+  }
+  *out = h.release();
+  return MK_OK;
+}
+
+int mk_destroy(mk_handle* h) {
+  if (!h) return MK_OK;
+  cudaDeviceSynchronize();
+  for (PlanEntry* e : h->plans) free_plan(e);
+  cudaFree(h->d_scratch);
+  if (h->h_err_mirror) cudaFreeHost(h->h_err_mirror);
+  delete h;
+  return MK_OK;
+}
+
+int mk_set_timeout(mk_handle* h, uint64_t ns) {
+  if (!h) return MK_ERR_INVALID;
+  if (ns == 0) return fail(h, MK_ERR_INVALID, "timeout must be positive");
+  h->base.timeout_ns = ns;
+  return MK_OK;
+}
+
+int mk_set_trace(mk_handle* h, mk_trace_record* buf, int capacity) {
+  if (!h) return MK_ERR_INVALID;
+  if (buf && capacity <= 0) return fail(h, MK_ERR_INVALID, "trace capacity must be positive");
+  h->base.trace = buf;
+  h->base.trace_cap = buf ? capacity : 0;
+  return MK_OK;
+}
+
+int mk_debug_inject_unsatisfiable_wait(mk_handle* h, int enable) {
+  if (!h) return MK_ERR_INVALID;
+  h->inject = enable ? 1 : 0;
+  return MK_OK;
+}
+
+int mk_decode_step(mk_handle* h, const int32_t* tok, const int32_t* pos, float* logits,
+                   void* stream) {
+  if (!h) return MK_ERR_INVALID;
+  int rc = check_steps(h, tok, pos);
+  if (rc) return rc;
+  if (!logits || !aligned16(logits)) return fail(h, MK_ERR_INVALID, "logits must be 16-byte aligned");
+  rc = check_sticky(h);
+  if (rc) return rc;
+  PlanEntry* e = nullptr;
+  rc = get_plan(h, pos, &e);
+  if (rc) return rc;
+  Params p = step_params(h, tok, pos, logits);
+  p.instrs = e->d_instrs;
+  p.sm_off = e->d_sm_off;
+  p.no_waits = 0;
+  p.trace_base = 0;
+  void* args[] = {&p};
+  cudaError_t ce = cudaLaunchCooperativeKernel(kernel_for_batch(h->shape.B), dim3(h->n_sm),
+                                               dim3(kThreads), args, (size_t)h->smem_bytes,
+                                               static_cast<cudaStream_t>(stream));
+  if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaLaunchCooperativeKernel");
+  h->cur_set = (int)(h->steps & 1ull);
+  h->steps++;
+  return MK_OK;
+}
+
+int mk_decode_step_multilaunch(mk_handle* h, const int32_t* tok, const int32_t* pos,
+                               float* logits, void* stream, int use_graph) {
+  if (!h) return MK_ERR_INVALID;
+  int rc = check_steps(h, tok, pos);
+  if (rc) return rc;
+  if (!logits || !aligned16(logits)) return fail(h, MK_ERR_INVALID, "logits must be 16-byte aligned");
+  rc = check_sticky(h);
+  if (rc) return rc;
+  PlanEntry* e = nullptr;
+  rc = get_plan(h, pos, &e);
+  if (rc) return rc;
+  Params p = step_params(h, tok, pos, logits);
+  p.no_waits = 1;
+  p.trace = nullptr;
+  p.trace_cap = 0;
+  const void* fn = kernel_for_batch(h->shape.B);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t nph = e->plan.phases.size();
+  std::vector<Params> ps(nph, p);
+  for (size_t k = 0; k < nph; ++k) {
+    ps[k].instrs = e->d_phase_instrs + e->phase_instr_base[k];
+    ps[k].sm_off = e->d_phase_off + e->phase_off_base[k];
+    if (k > 0) ps[k].ctr_zero = nullptr;
+  }
+  if (!use_graph) {
+    for (size_t k = 0; k < nph; ++k) {
+      void* args[] = {&ps[k]};
+      cudaError_t ce = cudaLaunchKernel(fn, dim3(h->n_sm), dim3(kThreads), args,
+                                        (size_t)h->smem_bytes, st);
+      if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaLaunchKernel");
+    }
+  } else {
+    if (!e->gexec) {
+      MK_CUDA(h, cudaGraphCreate(&e->graph, 0));
+      cudaGraphNode_t prev = nullptr;
+      for (size_t k = 0; k < nph; ++k) {
+        cudaKernelNodeParams kp{};
+        void* args[] = {&ps[k]};
+        kp.func = const_cast<void*>(fn);
+        kp.gridDim = dim3(h->n_sm);
+        kp.blockDim = dim3(kThreads);
+        kp.sharedMemBytes = (unsigned)h->smem_bytes;
+        kp.kernelParams = args;
+        cudaGraphNode_t node;
+        MK_CUDA(h, cudaGraphAddKernelNode(&node, e->graph, prev ? &prev : nullptr, prev ? 1 : 0, &kp));
+        e->nodes.push_back(node);
+        prev = node;
+      }
+      MK_CUDA(h, cudaGraphInstantiate(&e->gexec, e->graph, 0));
+    } else {
+      for (size_t k = 0; k < nph; ++k) {
+        cudaKernelNodeParams kp{};
+        void* args[] = {&ps[k]};
+        kp.func = const_cast<void*>(fn);
+        kp.gridDim = dim3(h->n_sm);
+        kp.blockDim = dim3(kThreads);
+        kp.sharedMemBytes = (unsigned)h->smem_bytes;
+        kp.kernelParams = args;
+        MK_CUDA(h, cudaGraphExecKernelNodeSetParams(e->gexec, e->nodes[k], &kp));
+      }
+    }
+    MK_CUDA(h, cudaGraphLaunch(e->gexec, st));
+  }
+  h->cur_set = (int)(h->steps & 1ull);
+  h->steps++;
+  return MK_OK;
+}
+
+int mk_get_status(mk_handle* h, void* stream) {
+  if (!h) return MK_ERR_INVALID;
+  MK_CUDA(h, cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  int e = 0;
+  MK_CUDA(h, cudaMemcpy(&e, h->d_err, sizeof e, cudaMemcpyDeviceToHost));
+  if (h->h_err_mirror) *reinterpret_cast<volatile int*>(h->h_err_mirror) = 0;
+  if (e != 0) {
+    MK_CUDA(h, cudaMemset(h->d_err, 0, sizeof e));
+    int code = (e >> 24) & 0xff;
+    char buf[128];
+    std::snprintf(buf, sizeof buf, "device error word 0x%08x (code %d, site %d)", e, code, e & 0xffffff);
+    return fail(h, code ? code : MK_ERR_CUDA, buf);
+  }
+  return MK_OK;
+}
+
+int mk_read_counters(mk_handle* h, int32_t* out, int capacity, int* n_out) {
+  if (!h || !n_out) return MK_ERR_INVALID;
+  *n_out = h->n_ctr;
+  if (!out || capacity < h->n_ctr) return fail(h, MK_ERR_INVALID, "counter buffer too small");
+  MK_CUDA(h, cudaDeviceSynchronize());
+  MK_CUDA(h, cudaMemcpy(out, h->d_ctr + (size_t)h->cur_set * h->n_ctr, sizeof(int) * h->n_ctr,
+                        cudaMemcpyDeviceToHost));
+  return MK_OK;
+}
+
+int mk_schedule_build(const mk_config* cfg, int n_sm, const int32_t* positions, mk_instr* instrs,
+                      int instr_capacity, int* n_instr, int32_t* sm_offsets, int32_t* targets,
+                      int counter_capacity, int* n_counters) {
+  int rc = check_config(cfg, nullptr);
+  if (rc) return rc;
+  if (n_sm < 1 || !positions) return fail(nullptr, MK_ERR_INVALID, "n_sm / positions");
+  Shape s = shape_of(*cfg);
+  for (int b = 0; b < s.B; ++b)
+    if (positions[b] < 0 || positions[b] >= s.S)
+      return fail(nullptr, MK_ERR_INVALID, "position out of range [0, kv_capacity)");
+  int parts[kMaxBatch];
+  choose_partitions(s, n_sm, positions, parts);
+  Plan P;
+  std::string why;
+  if (!build_plan(s, n_sm, parts, &P, &why)) return fail(nullptr, MK_ERR_INVALID, why);
+  if (n_instr) *n_instr = (int)P.instrs.size();
+  if (n_counters) *n_counters = (int)P.targets.size();
+  if (instrs) {
+    if (instr_capacity < (int)P.instrs.size())
+      return fail(nullptr, MK_ERR_INVALID, "instruction capacity too small");
+    std::memcpy(instrs, P.instrs.data(), sizeof(Instr) * P.instrs.size());
+  }
+  if (sm_offsets) std::memcpy(sm_offsets, P.sm_off.data(), sizeof(int) * P.sm_off.size());
+  if (targets) {
+    if (counter_capacity < (int)P.targets.size())
+      return fail(nullptr, MK_ERR_INVALID, "counter capacity too small");
+    std::memcpy(targets, P.targets.data(), sizeof(int) * P.targets.size());
+  }
+  return MK_OK;
+}
+
+}  // extern "C"

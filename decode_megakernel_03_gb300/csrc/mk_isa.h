@@ -1,0 +1,162 @@
+// Instruction set and kernel parameters of the decode interpreter, shared by
+// the host scheduler and the device code (plain C++ structs, no CUDA types).
+//
+// The interpreter follows "3 · L'interpréteur sur GPU": every SM runs a
+// pre-planned queue of fused instructions (§3.2), weights stream through
+// 16 KB shared-memory pages (§3.3), and dependencies are global counters that
+// start at zero and are bumped by producers and awaited by consumers (§3.4).
+#pragma once
+
+#include <stdint.h>
+#include <vector_types.h>  // float2 (a plain C header of the CUDA toolkit)
+
+#include "../../include/mk.h"
+
+namespace mk {
+
+constexpr int kPageBytes = 16384;   // one shared-memory page (§3.3: 16 KB pages)
+constexpr int kComputeWarps = 6;    // warps in the compute role (8 warps per CTA: 255 registers each)
+constexpr int kThreads = (kComputeWarps + 2) * 32;  // + loader warp + storer warp
+constexpr int kLoaderWarp = kComputeWarps;
+constexpr int kStorerWarp = kComputeWarps + 1;
+constexpr int kMaxBatch = 8;
+constexpr int kMaxPartitions = 64;  // split-KV partitions per (sequence, kv-head)
+constexpr int kChunks = 4;          // MLP hidden state chunks (§3.4: four pieces)
+constexpr int kMaxPages = 14;
+
+using Instr = mk_instr;
+static_assert(sizeof(Instr) == 32, "instruction descriptor is 32 bytes");
+
+// Per-layer weight and cache pointers, uploaded once to device memory.
+struct LayerPtrs {
+  const uint16_t* attn_norm;
+  const uint16_t* wq;
+  const uint16_t* wk;
+  const uint16_t* wv;
+  const uint16_t* wo;
+  const uint16_t* mlp_norm;
+  const uint16_t* wgate;
+  const uint16_t* wup;
+  const uint16_t* wdown;
+  uint16_t* kc;  // [B][nkv][S][D]
+  uint16_t* vc;
+};
+
+// Everything a launch needs, passed by value.
+struct Params {
+  // model
+  int L, H, nh, nkv, D, F, V, B, S, G, Fc, QD;  // QD = nh * D
+  float eps;
+  const LayerPtrs* layers;     // device [L]
+  const uint16_t* embed;
+  const uint16_t* lm;          // == embed when tied
+  const uint16_t* final_norm;
+  const float2* rope;          // [S][D/2] (cos, sin) of pos * theta^(-2i/D)
+  // library scratch (fp32 activations)
+  float* x;      // [B][H] residual stream between layers
+  float* xa;     // [B][H] residual after the attention block
+  float* q;      // [B][nh*D] rotated queries
+  float* part;   // [B][nh][kMaxPartitions][D + 2] attention partials (o, m, l)
+  float* attn;   // [B][nh*D] reduced attention output
+  float* h;      // [B][F] SwiGLU hidden state
+  float* dacc;   // [B][H] down-projection partial sums across chunks
+  float* logits; // [B][V] caller-owned
+  int* ctr;      // counters of this step (zero at launch)
+  int* ctr_zero; // counters of the next step, zeroed by this launch
+  int n_ctr;
+  int* err;      // device error word (0 = fine)
+  int* err_host; // mapped pinned host mirror of the error word (may be null)
+  const Instr* instrs;
+  const int* sm_off;           // [gridDim.x + 1]
+  mk_trace_record* trace;
+  int trace_cap;
+  int trace_base;              // record index of instrs[0] for this launch
+  unsigned long long timeout_ns;
+  int no_waits;                // multi-launch build: kernel boundaries order the work
+  // shared-memory layout (bytes from the dynamic smem base)
+  int n_pages;
+  int off_x, off_h, off_res, off_misc;
+  int x_floats, h_floats, res_floats;
+  int alias_xh;                // x and h staging share one buffer
+  // per step
+  int tok[kMaxBatch];
+  int pos[kMaxBatch];
+};
+
+// Error word layout: code << 24 | where. Codes match MK_ERR_*.
+constexpr int kErrTimeoutCounter = (MK_ERR_TIMEOUT << 24) | 1;
+constexpr int kErrTimeoutPage = (MK_ERR_TIMEOUT << 24) | 2;
+constexpr int kErrTimeoutRes = (MK_ERR_TIMEOUT << 24) | 3;
+constexpr int kErrBadInstr = (MK_ERR_INVALID << 24) | 4;
+
+// ---- geometry of the GEMV-shaped instructions -----------------------------
+// A GEMV instruction walks "items": one weight row, or a pair of rows whose
+// results are combined in the epilogue (q/k/v RoPE pairs, gate/up pairs).
+// Each row contributes a K-long slice (the whole row, or one chunk of it).
+struct Geom {
+  int K;      // columns of each row slice
+  int R;      // rows per item (1 or 2)
+  int ipp;    // items per page
+  int J;      // 256-column blocks per segment held by one warp
+  int nseg;   // segments per row slice (K / (256 * J))
+};
+
+#if defined(__CUDACC__)
+#define MK_HD __host__ __device__ __forceinline__
+#else
+#define MK_HD inline
+#endif
+
+MK_HD bool is_gemv(int op) {
+  return op == MK_OP_QKV || op == MK_OP_OPROJ || op == MK_OP_GATEUP || op == MK_OP_DOWN ||
+         op == MK_OP_LMHEAD;
+}
+
+// Largest J in 1..8 dividing K/256 with J * B <= 8 (activation registers).
+MK_HD int pick_J(int K, int B) {
+  int blocks = K / 256;
+  int jmax = 8 / B;
+  for (int j = jmax; j >= 1; --j)
+    if (blocks % j == 0) return j;
+  return 1;
+}
+
+MK_HD Geom geom_of(int op, int H, int QD, int Fc, int B) {
+  Geom g;
+  g.K = (op == MK_OP_OPROJ) ? QD : (op == MK_OP_DOWN ? Fc : H);
+  g.R = (op == MK_OP_QKV || op == MK_OP_GATEUP) ? 2 : 1;
+  g.ipp = kPageBytes / (g.R * g.K * 2);
+  g.J = pick_J(g.K, B);
+  g.nseg = g.K / (256 * g.J);
+  return g;
+}
+
+// q/k/v row pairs are numbered group-major: for kv-head g, the G q-heads of the
+// group, then k-head g, then v-head g; inside a head, pair i holds rows i and
+// i + D/2 (the rotate-half RoPE partners).
+struct PairRows {
+  int which;  // 0 = q, 1 = k, 2 = v
+  int head;   // q-head or kv-head index
+  int i;      // first dimension of the pair (second is i + D/2)
+  int g;      // kv-head group
+};
+
+MK_HD PairRows pair_rows(int j, int G, int D) {
+  int half = D / 2;
+  int per_group = (G + 2) * half;
+  PairRows p;
+  p.g = j / per_group;
+  int jj = j - p.g * per_group;
+  int slot = jj / half;
+  p.i = jj - slot * half;
+  if (slot < G) {
+    p.which = 0;
+    p.head = p.g * G + slot;
+  } else {
+    p.which = slot - G + 1;
+    p.head = p.g;
+  }
+  return p;
+}
+
+}  // namespace mk

@@ -1,0 +1,291 @@
+// Host scheduler (see mk_sched.h).
+//
+// The queues of all SMs are cut from ONE global order of the step:
+//
+//   for each layer l:
+//     QKV(l)  ATTN(l)  RED(l)  OPROJ(l)
+//     GATEUP(l,0)  GATEUP(l,1) DOWN(l,0)  GATEUP(l,2) DOWN(l,1)  ...  DOWN(l,3)
+//   LMHEAD
+//
+// and every instruction waits only on counters produced by instructions that
+// precede it in that order. Each SM's queue is that order filtered to the SM,
+// so with all SMs co-resident the step cannot deadlock. The down-projection of
+// chunk c is placed after the gate/up of chunk c+1 so that, on every SM, the
+// wait for chunk c overlaps useful work: "la granularité de la dépendance doit
+// correspondre à la granularité de la production" (§3.4, the four-chunk MLP).
+#include "mk_sched.h"
+
+#include <algorithm>
+#include <cstdio>
+
+namespace mk {
+
+std::string check_shape(const Shape& s) {
+  char buf[256];
+  auto bad = [&](const char* what) {
+    std::snprintf(buf, sizeof buf, "unsupported configuration: %s", what);
+    return std::string(buf);
+  };
+  if (s.L < 1 || s.L > 255) return bad("n_layers must be in 1..255");
+  if (s.H < 256 || s.H % 256 || s.H > 4096) return bad("hidden must be a multiple of 256 in 256..4096");
+  if (s.D != 64 && s.D != 128) return bad("head_dim must be 64 or 128");
+  if (s.nh < 1 || s.nkv < 1 || s.nh % s.nkv) return bad("n_heads must be a multiple of n_kv_heads");
+  if (s.nh / s.nkv > 8) return bad("at most 8 q-heads per kv-head");
+  if (s.QD() % 256 || s.QD() > 4096) return bad("n_heads*head_dim must be a multiple of 256, <= 4096");
+  if (s.F < 256 * kChunks || s.F % (256 * kChunks) || s.Fc() > 8192)
+    return bad("ffn must be a multiple of 1024 with ffn/4 <= 8192");
+  if (s.V < 1) return bad("vocab must be positive");
+  if (s.B != 1 && s.B != 2 && s.B != 4 && s.B != 8) return bad("batch must be 1, 2, 4 or 8");
+  if (s.S < 1) return bad("kv_capacity must be positive");
+  return std::string();
+}
+
+int item_cap_for(const Shape& s) { return s.B == 1 ? 64 : (s.B == 2 ? 32 : 16); }
+
+void choose_partitions(const Shape& s, int n_sm, const int* positions, int* parts) {
+  long bucket[kMaxBatch];
+  long work = 0;
+  for (int b = 0; b < s.B; ++b) {
+    long len = (long)positions[b] + 1;
+    bucket[b] = (len + 255) / 256 * 256;
+    work += bucket[b] * s.nkv;
+  }
+  // about one partition per SM over all (sequence, kv-head) pairs, and at
+  // least 64 keys per partition so each stays worth a queue entry
+  long per = std::max<long>(64, (work + n_sm - 1) / std::max(1, n_sm));
+  for (int b = 0; b < kMaxBatch; ++b) parts[b] = 0;
+  for (int b = 0; b < s.B; ++b) {
+    long p = (bucket[b] + per - 1) / per;
+    long len = (long)positions[b] + 1;
+    p = std::min<long>(p, len);  // every partition keeps at least one key
+    p = std::max<long>(1, std::min<long>(p, kMaxPartitions));
+    parts[b] = (int)p;
+  }
+}
+
+namespace {
+
+struct Builder {
+  const Shape& s;
+  int n_sm;
+  CounterMap cm;
+  int cap;
+  // global order: a list of steps, each a list of (sm, instr)
+  struct Step {
+    int op, layer;
+    std::vector<std::pair<int, Instr>> items;
+  };
+  std::vector<Step> steps;
+
+  Builder(const Shape& sh, int n) : s(sh), n_sm(n), cm{sh.L, sh.nkv, sh.B}, cap(item_cap_for(sh)) {}
+
+  int rot_of(int layer, int step) const {
+    return (int)(((long)layer * 61 + (long)step * 23) % n_sm);
+  }
+
+  static Instr make(int op, int layer, int a0, int a1, int a2, int wc, int wt, int sc, int sa) {
+    Instr in;
+    in.op = (int16_t)op;
+    in.layer = (int16_t)layer;
+    in.a0 = a0;
+    in.a1 = a1;
+    in.a2 = a2;
+    in.wait_ctr = wc;
+    in.wait_target = wt;
+    in.sig_ctr = sc;
+    in.sig_amount = sa;
+    return in;
+  }
+
+  // Splits [0, n) into n_sm near-equal contiguous ranges, then each range at
+  // `cap` items and at multiples of `align` (0 = no alignment cut). Range k
+  // goes to SM (k + rot) % n_sm: rotating per step moves the ranges that get
+  // one item more around the SMs, so their totals over the step stay level.
+  template <class F>
+  void spread(int n, int align, int rot, F emit) {
+    for (int k = 0; k < n_sm; ++k) {
+      int sm = (k + rot) % n_sm;
+      int lo = (int)((long)n * k / n_sm);
+      int hi = (int)((long)n * (k + 1) / n_sm);
+      int a = lo;
+      while (a < hi) {
+        int b = std::min(hi, a + cap);
+        if (align > 0) b = std::min(b, (a / align + 1) * align);
+        emit(sm, a, b);
+        a = b;
+      }
+    }
+  }
+
+  void add_layer(int l, const int* parts, int rot) {
+    const int H = s.H, G = s.G(), Fc = s.Fc();
+    const int ppg = s.pairs_per_group();
+    // 1. RMSNorm + QKV + RoPE + KV append
+    {
+      Step st{MK_OP_QKV, l, {}};
+      int wc = l == 0 ? -1 : cm.xout(l - 1);
+      int wt = l == 0 ? 0 : H;
+      spread(s.pairs(), ppg, rot_of(l, 0), [&](int sm, int a, int b) {
+        int g = a / ppg;
+        st.items.push_back({sm, make(MK_OP_QKV, l, a, b, 0, wc, wt, cm.qkv(l, g), b - a)});
+      });
+      steps.push_back(std::move(st));
+    }
+    // 2. split-KV attention: one unit per (sequence, kv-head, partition)
+    {
+      Step st{MK_OP_ATTN, l, {}};
+      int k = 0;
+      for (int b = 0; b < s.B; ++b)
+        for (int g = 0; g < s.nkv; ++g)
+          for (int p = 0; p < parts[b]; ++p, ++k) {
+            int sm = (rot + k) % n_sm;
+            st.items.push_back({sm, make(MK_OP_ATTN, l, b, g, (p << 16) | parts[b], cm.qkv(l, g),
+                                         ppg, cm.att(l, b, g), 1)});
+          }
+      steps.push_back(std::move(st));
+    }
+    // 3. attention reduction: one unit per (sequence, kv-head)
+    {
+      Step st{MK_OP_RED, l, {}};
+      int k = 0;
+      for (int b = 0; b < s.B; ++b)
+        for (int g = 0; g < s.nkv; ++g, ++k) {
+          int sm = (rot + n_sm / 2 + k) % n_sm;
+          st.items.push_back({sm, make(MK_OP_RED, l, b, g, parts[b], cm.att(l, b, g), parts[b],
+                                       cm.red(l), 1)});
+        }
+      steps.push_back(std::move(st));
+    }
+    // 4. O-projection + residual
+    {
+      Step st{MK_OP_OPROJ, l, {}};
+      spread(H, 0, rot_of(l, 1), [&](int sm, int a, int b) {
+        st.items.push_back({sm, make(MK_OP_OPROJ, l, a, b, 0, cm.red(l), s.B * s.nkv, cm.omid(l),
+                                     b - a)});
+      });
+      steps.push_back(std::move(st));
+    }
+    // 5-6. gate/up chunk c, then down chunk c-1
+    auto gateup = [&](int c) {
+      Step st{MK_OP_GATEUP, l, {}};
+      spread(Fc, 0, rot_of(l, 2 + c), [&](int sm, int a, int b) {
+        st.items.push_back({sm, make(MK_OP_GATEUP, l, c * Fc + a, c * Fc + b, c, cm.omid(l), H,
+                                     cm.hch(l, c), b - a)});
+      });
+      steps.push_back(std::move(st));
+    };
+    auto down = [&](int c) {
+      Step st{MK_OP_DOWN, l, {}};
+      bool last = c == kChunks - 1;
+      // every chunk of a row stays on one SM: its storer accumulates the chunks
+      spread(H, 0, rot_of(l, 2 + kChunks), [&](int sm, int a, int b) {
+        st.items.push_back({sm, make(MK_OP_DOWN, l, a, b, c, cm.hch(l, c), Fc,
+                                     last ? cm.xout(l) : -1, last ? b - a : 0)});
+      });
+      steps.push_back(std::move(st));
+    };
+    gateup(0);
+    for (int c = 1; c < kChunks; ++c) {
+      gateup(c);
+      down(c - 1);
+    }
+    down(kChunks - 1);
+  }
+
+  void add_lm_head() {
+    Step st{MK_OP_LMHEAD, -1, {}};
+    spread(s.V, 0, rot_of(s.L, 0), [&](int sm, int a, int b) {
+      st.items.push_back({sm, make(MK_OP_LMHEAD, s.L - 1, a, b, 0, cm.xout(s.L - 1), s.H, cm.lm(),
+                                   b - a)});
+    });
+    steps.push_back(std::move(st));
+  }
+};
+
+void cut_queues(const std::vector<const std::vector<std::pair<int, Instr>>*>& lists, int n_sm,
+                std::vector<Instr>* instrs, std::vector<int>* sm_off) {
+  std::vector<std::vector<Instr>> per(n_sm);
+  for (auto* lst : lists)
+    for (auto& it : *lst) per[it.first].push_back(it.second);
+  instrs->clear();
+  sm_off->assign(n_sm + 1, 0);
+  for (int sm = 0; sm < n_sm; ++sm) {
+    (*sm_off)[sm] = (int)instrs->size();
+    instrs->insert(instrs->end(), per[sm].begin(), per[sm].end());
+  }
+  (*sm_off)[n_sm] = (int)instrs->size();
+}
+
+}  // namespace
+
+bool build_plan(const Shape& s, int n_sm, const int* parts, Plan* out, std::string* why) {
+  std::string e = check_shape(s);
+  if (!e.empty()) {
+    if (why) *why = e;
+    return false;
+  }
+  if (n_sm < 1) {
+    if (why) *why = "n_sm must be positive";
+    return false;
+  }
+  for (int b = 0; b < s.B; ++b)
+    if (parts[b] < 1 || parts[b] > kMaxPartitions) {
+      if (why) *why = "partition count out of range";
+      return false;
+    }
+  Builder bld(s, n_sm);
+  for (int l = 0; l < s.L; ++l) bld.add_layer(l, parts, (l * 37) % n_sm);
+  bld.add_lm_head();
+
+  out->n_sm = n_sm;
+  for (int b = 0; b < kMaxBatch; ++b) out->parts[b] = b < s.B ? parts[b] : 0;
+  std::vector<const std::vector<std::pair<int, Instr>>*> all;
+  for (auto& st : bld.steps) all.push_back(&st.items);
+  cut_queues(all, n_sm, &out->instrs, &out->sm_off);
+
+  // counter targets = what the producers add up to
+  const CounterMap& cm = bld.cm;
+  out->targets.assign(cm.count(), 0);
+  for (auto& in : out->instrs)
+    if (in.sig_ctr >= 0) out->targets[in.sig_ctr] += in.sig_amount;
+  for (auto& in : out->instrs)
+    if (in.wait_ctr >= 0 && in.wait_target != out->targets[in.wait_ctr]) {
+      if (why) *why = "internal: a wait target differs from its counter's production";
+      return false;
+    }
+
+  // multi-launch build: one kernel per (layer, instruction type); the gate/up
+  // chunks form one kernel and the down chunks the next
+  out->phases.clear();
+  size_t i = 0;
+  while (i < bld.steps.size()) {
+    int op = bld.steps[i].op, layer = bld.steps[i].layer;
+    std::vector<const std::vector<std::pair<int, Instr>>*> lists;
+    if (op == MK_OP_GATEUP || op == MK_OP_DOWN) {
+      // collect all GATEUP steps of this layer, then all DOWN steps
+      size_t j = i;
+      std::vector<const std::vector<std::pair<int, Instr>>*> gu, dn;
+      while (j < bld.steps.size() && bld.steps[j].layer == layer &&
+             (bld.steps[j].op == MK_OP_GATEUP || bld.steps[j].op == MK_OP_DOWN)) {
+        (bld.steps[j].op == MK_OP_GATEUP ? gu : dn).push_back(&bld.steps[j].items);
+        ++j;
+      }
+      Phase p1{MK_OP_GATEUP, layer, {}, {}}, p2{MK_OP_DOWN, layer, {}, {}};
+      cut_queues(gu, n_sm, &p1.instrs, &p1.sm_off);
+      cut_queues(dn, n_sm, &p2.instrs, &p2.sm_off);
+      out->phases.push_back(std::move(p1));
+      out->phases.push_back(std::move(p2));
+      i = j;
+      continue;
+    }
+    lists.push_back(&bld.steps[i].items);
+    Phase p{op, layer, {}, {}};
+    cut_queues(lists, n_sm, &p.instrs, &p.sm_off);
+    out->phases.push_back(std::move(p));
+    ++i;
+  }
+  if (why) why->clear();
+  return true;
+}
+
+}  // namespace mk

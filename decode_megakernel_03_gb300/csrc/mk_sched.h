@@ -1,0 +1,68 @@
+// Host scheduler: turns (model shape, batch, positions, SM count) into one
+// pre-planned instruction queue per SM plus the counter targets
+// ("3 · L'interpréteur sur GPU", §3.2: every SM receives a pre-planned
+// sequence of instructions; §3.4: counters start at zero, producers bump them,
+// consumers wait for a target).
+#pragma once
+
+#include <string>
+#include <vector>
+
+#include "mk_isa.h"
+
+namespace mk {
+
+struct Shape {
+  int L, H, nh, nkv, D, F, V, B, S;
+  int G() const { return nh / nkv; }
+  int QD() const { return nh * D; }
+  int Fc() const { return F / kChunks; }
+  int pairs_per_group() const { return (G() + 2) * (D / 2); }
+  int pairs() const { return nkv * pairs_per_group(); }
+};
+
+// Counter ids. Every counter counts produced items and is awaited at its full
+// target, so its final value after a step equals the target.
+struct CounterMap {
+  int L, nkv, B;
+  int xout(int l) const { return l; }                         // target H
+  int omid(int l) const { return L + l; }                     // target H
+  int qkv(int l, int g) const { return 2 * L + l * nkv + g; } // pairs per group
+  int att(int l, int b, int g) const { return 2 * L + L * nkv + (l * B + b) * nkv + g; }
+  int red(int l) const { return 2 * L + L * nkv + L * B * nkv + l; }   // B * nkv
+  int hch(int l, int c) const { return 3 * L + L * nkv + L * B * nkv + l * kChunks + c; }
+  int lm() const { return 3 * L + L * nkv + L * B * nkv + L * kChunks; }
+  int count() const { return lm() + 1; }
+};
+
+struct Phase {                 // one kernel of the multi-launch build
+  int op, layer;
+  std::vector<Instr> instrs;   // SM-major
+  std::vector<int> sm_off;     // n_sm + 1
+};
+
+struct Plan {
+  int n_sm = 0;
+  int parts[kMaxBatch] = {0};
+  std::vector<Instr> instrs;   // SM-major, each SM in execution order
+  std::vector<int> sm_off;     // n_sm + 1
+  std::vector<int> targets;    // per counter
+  std::vector<Phase> phases;   // multi-launch build, in launch order
+};
+
+// Validates a configuration; returns an empty string when supported.
+std::string check_shape(const Shape& s);
+
+// Split-KV partitions per sequence for these positions. Lengths are bucketed
+// to multiples of 256 so that the plan (and its upload) changes rarely; the
+// token range of each partition is recomputed on the device from the exact
+// position.
+void choose_partitions(const Shape& s, int n_sm, const int* positions, int* parts);
+
+// Items (rows or row pairs) per GEMV instruction, bounded by the result
+// buffer the storer drains.
+int item_cap_for(const Shape& s);
+
+bool build_plan(const Shape& s, int n_sm, const int* parts, Plan* out, std::string* why);
+
+}  // namespace mk

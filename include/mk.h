@@ -1,0 +1,196 @@
+/*
+ * mk.h — C ABI of the GB300 decode megakernel library (libmk.so).
+ *
+ * One call runs one decode step of a Llama-style decoder (batch 1..8) as ONE
+ * persistent kernel: an on-GPU interpreter in which every SM executes a
+ * host-prescheduled queue of fused instructions ("3 · L'interpréteur sur GPU",
+ * §3.2 "La solution : un interpréteur" and its table of seven instructions),
+ * each instruction split into loader / compute / storer warp roles (§3.2, the
+ * instruction template), weights streamed into a paged shared-memory allocator
+ * (§3.3 "La solution : un allocateur de pages"), and kernel boundaries replaced
+ * by zero-initialised global-memory counters with chunked dependencies (§3.4
+ * "des compteurs en mémoire globale" and "L'exemple canonique du découpage").
+ *
+ * Conventions shared by every entry point
+ *   - Every function returns an int status: MK_OK (0) or one of MK_ERR_*.
+ *     On failure mk_last_error() describes the cause. Validation failures
+ *     return before anything is launched or allocated.
+ *   - "stream" is a cudaStream_t passed as void*; NULL is the legacy default
+ *     stream. Calls that take a stream are asynchronous on it unless stated.
+ *   - The caller owns the weights, the KV cache and the logits buffer: the
+ *     library never frees, copies or repacks them. The library owns its
+ *     scratch (counters, activations, queues) and frees it in mk_destroy.
+ *   - Weights are bf16, row-major [out][in] (the nn.Linear layout); every
+ *     device pointer must be 16-byte aligned (the weight pages are filled with
+ *     bulk asynchronous copies, which move 16-byte units).
+ *   - A handle is not thread-safe; use one handle per host thread.
+ */
+#ifndef MK_H
+#define MK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MK_OK 0
+#define MK_ERR_INVALID 1 /* bad argument or unsupported configuration */
+#define MK_ERR_CUDA 2    /* a CUDA runtime call failed (see mk_last_error) */
+#define MK_ERR_TIMEOUT 3 /* a device wait ran past its deadline; the step's
+                            outputs are undefined, the context stays usable */
+#define MK_ERR_OOM 4     /* device or pinned host allocation failed */
+
+typedef struct mk_handle mk_handle;
+
+/* Model + run configuration. Supported: head_dim 64 or 128; hidden, n_heads *
+   head_dim and ffn / 4 multiples of 256 and at most 4096, 4096 and 8192;
+   n_heads a multiple of n_kv_heads with at most 8 q-heads per kv-head;
+   batch 1, 2, 4 or 8. */
+typedef struct {
+  int n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab;
+  int tied_embeddings; /* 1: the LM head is the embedding matrix */
+  float rms_eps, rope_theta;
+  int batch;           /* sequences per step, fixed per handle */
+  int kv_capacity;     /* S: KV slots per sequence */
+} mk_config;
+
+/* Device pointers (bf16). The per-layer members are HOST arrays of n_layers
+   device pointers; they are read during mk_create only. */
+typedef struct {
+  const void* embed;          /* [vocab][hidden] */
+  const void* lm_head;        /* [vocab][hidden]; NULL iff tied_embeddings */
+  const void* final_norm;     /* [hidden] */
+  const void* const* attn_norm; /* [hidden] */
+  const void* const* wq;      /* [n_heads*head_dim][hidden] */
+  const void* const* wk;      /* [n_kv_heads*head_dim][hidden] */
+  const void* const* wv;      /* [n_kv_heads*head_dim][hidden] */
+  const void* const* wo;      /* [hidden][n_heads*head_dim] */
+  const void* const* mlp_norm;  /* [hidden] */
+  const void* const* wgate;   /* [ffn][hidden] */
+  const void* const* wup;     /* [ffn][hidden] */
+  const void* const* wdown;   /* [hidden][ffn] */
+} mk_weights;
+
+/* Creates a handle on the current CUDA device. k_cache / v_cache: host arrays
+   of n_layers device pointers, each bf16 [batch][n_kv_heads][kv_capacity]
+   [head_dim], caller-owned and updated in place by every decode step. The
+   handle records the pointers; they must stay valid until mk_destroy.
+   Allocates the scratch (cudaMalloc) and pinned host staging.
+   Errors: MK_ERR_INVALID (NULL, misaligned or unsupported), MK_ERR_OOM,
+   MK_ERR_CUDA. On error *out is set to NULL. */
+int mk_create(const mk_config* cfg, const mk_weights* w,
+              void* const* k_cache, void* const* v_cache, mk_handle** out);
+
+/* One decode step, ONE kernel launch (the persistent interpreter).
+   token_ids, positions: HOST arrays of `batch` int32. Sequence b consumes
+   token_ids[b] at position positions[b]: its new k/v row is written into slot
+   positions[b] of every layer's cache, and it attends to slots
+   0..positions[b] inclusive. The host scheduler needs the positions to size
+   the split-KV attention partitions, which is why they are host data.
+   logits_out: device fp32 [batch][vocab], caller-owned.
+   Asynchronous on `stream`. Returns MK_ERR_INVALID (range checks) before
+   launching, MK_ERR_TIMEOUT if an earlier step on this handle reported a
+   device timeout (sticky until mk_get_status), else MK_OK / MK_ERR_CUDA. */
+int mk_decode_step(mk_handle* h, const int32_t* token_ids, const int32_t* positions,
+                   float* logits_out, void* stream);
+
+/* The same step run as the multi-launch comparison build: the same
+   instruction templates and the same per-SM work units, but one kernel per
+   (layer, instruction type) — kernel boundaries instead of counter waits —
+   about 6 * n_layers + 1 launches. use_graph != 0 replays them as one CUDA
+   graph. Results are bit-identical to mk_decode_step. */
+int mk_decode_step_multilaunch(mk_handle* h, const int32_t* token_ids,
+                               const int32_t* positions, float* logits_out,
+                               void* stream, int use_graph);
+
+/* Synchronises `stream`, reads the device error word and clears it.
+   Returns MK_OK, MK_ERR_TIMEOUT or MK_ERR_CUDA. */
+int mk_get_status(mk_handle* h, void* stream);
+
+/* Frees everything the handle owns (synchronising the device first).
+   Accepts NULL. */
+int mk_destroy(mk_handle* h);
+
+/* Human-readable description of the last error on h (or of the last
+   mk_create failure in this thread when h is NULL). Never NULL. */
+const char* mk_last_error(const mk_handle* h);
+
+/* ---- test / benchmark helpers ------------------------------------------ */
+
+/* Copies the counter array of the most recent step into host_out
+   (synchronising the device). *n_out receives the number of counters; if
+   capacity is too small nothing is copied and MK_ERR_INVALID is returned. */
+int mk_read_counters(mk_handle* h, int32_t* host_out, int capacity, int* n_out);
+
+/* Deadline of every device wait, in nanoseconds (default 2 s). */
+int mk_set_timeout(mk_handle* h, uint64_t timeout_ns);
+
+/* Test-only fault injection on the host schedule: while `enable` is non-zero,
+   the wait target of the first counter wait on the last SM's queue is raised
+   by one, so that wait can never be satisfied and the step ends with
+   MK_ERR_TIMEOUT (device waits are bounded; nothing faults). */
+int mk_debug_inject_unsatisfiable_wait(mk_handle* h, int enable);
+
+/* Per-instruction trace. When dev_buf (device memory holding `capacity`
+   mk_trace_record) is non-NULL, the compute warps of every SM write one record
+   per instruction they run, timestamped with %globaltimer; record k belongs to
+   the k-th instruction of the step in the schedule's SM-major order, so the
+   buffer needs at least as many records as the schedule has instructions
+   (mk_schedule_build reports that count). Records past `capacity` are dropped.
+   Pass NULL to disable. The idle gap between two instructions of one SM is
+   t_start(next) - t_end(prev); the dependency stall is t_ready - t_start. */
+typedef struct {
+  uint32_t sm, index;       /* SM and position in its queue */
+  int32_t op, layer;        /* MK_OP_* and layer (-1 for the LM head) */
+  uint64_t t_start;         /* compute warps start the instruction */
+  uint64_t t_ready;         /* its counter wait (if any) is satisfied */
+  uint64_t t_end;           /* compute warps finish it */
+} mk_trace_record;
+int mk_set_trace(mk_handle* h, mk_trace_record* dev_buf, int capacity);
+
+/* Instruction opcodes (the seven fused instructions of the pages, with the
+   embedding lookup folded into layer 0's first instruction). */
+#define MK_OP_QKV 1   /* RMSNorm + QKV + RoPE + KV append      (instr. 1) */
+#define MK_OP_ATTN 2  /* split-KV attention partial            (instr. 2) */
+#define MK_OP_RED 3   /* attention partial reduction           (instr. 3) */
+#define MK_OP_OPROJ 4 /* O-projection + residual               (instr. 4) */
+#define MK_OP_GATEUP 5 /* RMSNorm + up/gate + SiLU, one chunk  (instr. 5) */
+#define MK_OP_DOWN 6  /* down-projection (+ residual on last chunk) (instr. 6) */
+#define MK_OP_LMHEAD 7 /* final RMSNorm + LM head              (instr. 7) */
+
+/* One queue entry as the host scheduler emits it (32 bytes). Exported for
+   the schedule checks; the meaning of a0..a2 depends on op:
+     QKV:    items [a0, a1) of the layer's (q|k|v) row pairs, group-major
+     ATTN:   a0 = sequence, a1 = kv-head, a2 = partition << 16 | n_partitions
+     RED:    a0 = sequence, a1 = kv-head, a2 = n_partitions
+     OPROJ:  output rows [a0, a1)
+     GATEUP: hidden units [a0, a1) of chunk a2
+     DOWN:   output rows [a0, a1), input chunk a2
+     LMHEAD: vocabulary rows [a0, a1)
+   wait_ctr < 0 means no wait; sig_ctr < 0 means no signal. */
+typedef struct {
+  int16_t op, layer;
+  int32_t a0, a1, a2;
+  int32_t wait_ctr, wait_target;
+  int32_t sig_ctr, sig_amount;
+} mk_instr;
+
+/* Host-only (no CUDA call): builds the schedule that mk_decode_step would run
+   for `cfg` on n_sm SMs at these positions (host array of cfg->batch).
+   Outputs, each optional (NULL to skip) and bounded by its capacity:
+     instrs[*n_instr]          all queues, SM-major, each in execution order
+     sm_offsets[n_sm + 1]      queue of SM s = instrs[sm_offsets[s] .. s+1)
+     targets[*n_counters]      the value each counter holds after a step
+   Returns MK_ERR_INVALID if cfg is unsupported or a capacity is too small
+   (the required sizes are still written to *n_instr / *n_counters). */
+int mk_schedule_build(const mk_config* cfg, int n_sm, const int32_t* positions,
+                      mk_instr* instrs, int instr_capacity, int* n_instr,
+                      int32_t* sm_offsets, int32_t* targets, int counter_capacity,
+                      int* n_counters);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MK_H */

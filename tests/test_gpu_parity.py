@@ -1,0 +1,195 @@
+"""Parity of the CUDA decode path (through the C ABI) with the CPU oracle.
+
+Every test feeds both sides the same seeded inputs and compares the logits of
+every decode step (relative L2 <= 1e-2, max-abs <= 5e-2, top-1 agreement),
+the KV-cache slot each step writes (within one bf16 ulp) and, bit-exactly,
+the untouched slots and the final counter values of the schedule.
+"""
+import numpy as np
+import pytest
+import torch
+
+from decode_megakernel_03_gb300 import mk, synth
+from oracle import oracle as O
+from tests.parity_util import Pair, Tally, bf16_bits, bits_to_f64, check_kv_step, compare_logits, counters_match
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+
+
+def _tiny_prefilled():
+    """The tiny workload: a 64-token prompt prefilled into the KV cache by the
+    oracle's causal forward (the same bytes go to both sides)."""
+    wl = synth.WORKLOADS["tiny"]
+    shape = wl.shape
+    w = synth.make_weights(shape, seed=wl.weight_seed)
+    model = O.Model(shape.as_dict(), synth.oracle_weights(w))
+    prompt = synth.prompt_tokens(wl).numpy()
+    _, kf, vf = model.forward_full(prompt, want_kv=True)
+    ks, vs = [], []
+    for l in range(shape.n_layers):
+        k = np.zeros((1, shape.n_kv_heads, wl.capacity, shape.head_dim), np.uint16)
+        v = k.copy()
+        k[0, :, :wl.prompt] = kf[l]
+        v[0, :, :wl.prompt] = vf[l]
+        ks.append(k)
+        vs.append(v)
+    return wl, ks, vs
+
+
+def test_tiny_teacher_forced_decode():
+    wl, ks, vs = _tiny_prefilled()
+    pair = Pair(wl.shape, 1, wl.capacity, kv_from_oracle=(ks, vs), weight_seed=wl.weight_seed)
+    toks = synth.step_tokens(wl)
+    tally = Tally()
+    for s in range(wl.steps):
+        tok, pos = [int(toks[s, 0])], synth.step_positions(wl, s)
+        bk = [bf16_bits(t) for t in pair.kc]
+        bv = [bf16_bits(t) for t in pair.vc]
+        got = pair.gpu_step(tok, pos)
+        want = pair.oracle_step(tok, pos)
+        tally.add(compare_logits(got, want))
+        check_kv_step(pair, pos, bk, bv)
+        counters_match(pair, pos)
+    print("tiny", tally.check())
+    pair.close()
+
+
+def test_tiny_decode_from_empty_cache_matches_full_forward():
+    """The GPU decodes the whole 80-token sequence one token at a time from an
+    empty cache; its logits and final cache match the oracle's causal forward."""
+    wl = synth.WORKLOADS["tiny"]
+    pair = Pair(wl.shape, 1, wl.capacity, weight_seed=wl.weight_seed)
+    toks = np.concatenate([synth.prompt_tokens(wl).numpy(), synth.step_tokens(wl)[:, 0].numpy()])
+    full, kf, vf = pair.model.forward_full(toks, want_kv=True)
+    tally = Tally()
+    for t in range(len(toks)):
+        got = pair.gpu_step([int(toks[t])], [t])
+        tally.add(compare_logits(got, full[t:t + 1]))
+    for l in range(wl.shape.n_layers):
+        n = len(toks)
+        np.testing.assert_allclose(bits_to_f64(bf16_bits(pair.kc[l])[0, :, :n]), bits_to_f64(kf[l]),
+                                   rtol=2.0 ** -7, atol=1e-3)
+        np.testing.assert_allclose(bits_to_f64(bf16_bits(pair.vc[l])[0, :, :n]), bits_to_f64(vf[l]),
+                                   rtol=2.0 ** -7, atol=1e-3)
+    print("tiny from empty", tally.check())
+    pair.close()
+
+
+@pytest.mark.parametrize("shape_name", ["tiny", "llama1b"])
+def test_multilaunch_and_graph_are_bit_identical(shape_name):
+    wl = synth.WORKLOADS[shape_name]
+    ctx = (200,) if shape_name == "tiny" else wl.ctx
+    cap = 256 if shape_name == "tiny" else wl.capacity
+    toks = synth.step_tokens(wl)
+    outs = {}
+    caches = {}
+    for mode in ("mega", "multi", "graph"):
+        pair = Pair(wl.shape, 1, cap, ctx=ctx)
+        res = []
+        for s in range(3):
+            res.append(pair.gpu_step([int(toks[s, 0])], [ctx[0] + s], mode=mode))
+        outs[mode] = np.stack(res)
+        caches[mode] = [bf16_bits(t) for t in pair.kc + pair.vc]
+        if mode == "mega":
+            counters_match(pair, [ctx[0] + 2])
+        pair.close()
+    np.testing.assert_array_equal(outs["mega"], outs["multi"])
+    np.testing.assert_array_equal(outs["mega"], outs["graph"])
+    for a, b in zip(caches["mega"], caches["multi"]):
+        np.testing.assert_array_equal(a, b)
+
+
+@pytest.mark.parametrize("name,steps", [("llama1b", 3), ("llama1b_ctx8k", 2), ("llama8b", 2),
+                                        ("llama1b_b8", 2)])
+def test_full_size_parity(name, steps):
+    """The workloads at full size, on their seeded contexts, a few steps each."""
+    wl = synth.WORKLOADS[name]
+    pair = Pair(wl.shape, wl.batch, wl.capacity, ctx=wl.ctx, weight_seed=wl.weight_seed,
+                kv_seed=wl.kv_seed)
+    toks = synth.step_tokens(wl)
+    tally = Tally()
+    for s in range(steps):
+        tok = [int(t) for t in toks[s]]
+        pos = synth.step_positions(wl, s)
+        bk = [bf16_bits(t) for t in pair.kc]
+        bv = [bf16_bits(t) for t in pair.vc]
+        got = pair.gpu_step(tok, pos)
+        want = pair.oracle_step(tok, pos)
+        tally.add(compare_logits(got, want))
+        check_kv_step(pair, pos, bk, bv)
+        counters_match(pair, pos)
+    print(name, tally.check())
+    pair.close()
+
+
+def test_edge_positions_first_and_last_slot():
+    shape = synth.TINY
+    cap = 96
+    pair = Pair(shape, 2, cap, ctx=(0, cap - 1))
+    tally = Tally()
+    for tok, pos in (([5, 6], [0, cap - 1]), ([7, 8], [1, cap - 1])):
+        bk = [bf16_bits(t) for t in pair.kc]
+        bv = [bf16_bits(t) for t in pair.vc]
+        got = pair.gpu_step(tok, pos)
+        want = pair.oracle_step(tok, pos)
+        tally.add(compare_logits(got, want))
+        check_kv_step(pair, pos, bk, bv)
+    tally.check()
+    pair.close()
+
+
+@pytest.mark.parametrize("batch", [2, 4])
+def test_other_batch_sizes(batch):
+    shape = synth.TINY
+    cap = 160
+    ctx = tuple(17 + 37 * b for b in range(batch))
+    pair = Pair(shape, batch, cap, ctx=ctx)
+    tally = Tally()
+    for s in range(2):
+        tok = [(11 * s + 3 * b) % shape.vocab for b in range(batch)]
+        pos = [c + s for c in ctx]
+        got = pair.gpu_step(tok, pos)
+        want = pair.oracle_step(tok, pos)
+        tally.add(compare_logits(got, want))
+    tally.check()
+    pair.close()
+
+
+def test_repeated_steps_are_bitwise_deterministic():
+    wl = synth.WORKLOADS["llama1b"]
+    pair = Pair(wl.shape, 1, wl.capacity, ctx=wl.ctx)
+    ref = pair.gpu_step([17], [512]).copy()
+    for _ in range(200):
+        pair.dec.step([17], [512], pair.logits)
+    assert pair.dec.status() == mk.MK_OK
+    np.testing.assert_array_equal(pair.logits.cpu().numpy().astype(np.float64), ref)
+    pair.close()
+
+
+def test_unsatisfiable_wait_times_out_and_recovers():
+    """A host-built schedule with one wait that can never be met: the bounded
+    device wait expires, the step reports MK_ERR_TIMEOUT, the next step call is
+    refused until the status is read, and the handle then works again."""
+    shape = synth.TINY
+    pair = Pair(shape, 1, 128, ctx=(40,))
+    good = pair.gpu_step([3], [40]).copy()
+    pair.dec.set_timeout(50_000_000)  # 50 ms
+    pair.dec.inject_unsatisfiable_wait(True)
+    pair.dec.step([3], [40], pair.logits)
+    torch.cuda.synchronize()
+    with pytest.raises(mk.MkError) as e:
+        pair.dec.step([3], [40], pair.logits)
+    assert e.value.code == mk.MK_ERR_TIMEOUT
+    assert pair.dec.status() == mk.MK_ERR_TIMEOUT
+    assert pair.dec.status() == mk.MK_OK
+    pair.dec.inject_unsatisfiable_wait(False)
+    pair.dec.set_timeout(2_000_000_000)
+    again = pair.gpu_step([3], [40])
+    np.testing.assert_array_equal(again, good)
+    pair.close()

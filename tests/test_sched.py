@@ -1,0 +1,308 @@
+"""Host scheduler checks (no GPU): the per-SM queues cover every output exactly
+once, counter targets equal what the producers add up to, the queues cannot
+deadlock under any interleaving of co-resident SMs, and every read-after-write
+and write-after-read on the shared scratch is ordered by a counter chain.
+
+The queues are the pre-planned per-SM instruction sequences of "3 · L'interpréteur
+sur GPU" (§3.2); the counters are the zero-initialised global counters of §3.4,
+including the four-chunk MLP dependency."""
+import random
+
+import numpy as np
+import pytest
+
+from decode_megakernel_03_gb300 import build as mkbuild
+from decode_megakernel_03_gb300 import mk, synth
+
+OPS = mk
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    mkbuild.build()
+
+
+def _plan(shape, B, S, n_sm, pos):
+    ins, off, tg = mk.schedule(shape, B, S, n_sm, pos)
+    sm = np.zeros(len(ins), dtype=np.int64)
+    for s in range(n_sm):
+        sm[off[s]:off[s + 1]] = s
+    return ins, off, tg, sm
+
+
+CASES = [
+    (synth.TINY, 1, 128, 8, [70]),
+    (synth.TINY, 1, 128, 152, [0]),
+    (synth.TINY, 2, 128, 5, [3, 127]),
+    (synth.LLAMA_1B, 1, 640, 152, [512]),
+    (synth.LLAMA_1B, 1, 8256, 152, [8200]),
+    (synth.LLAMA_8B, 1, 2112, 152, [2048]),
+    (synth.LLAMA_1B, 8, 4160, 152, list(synth.WORKLOADS["llama1b_b8"].ctx)),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0].name}-B{c[1]}-sm{c[3]}")
+def test_deterministic(case):
+    a = mk.schedule(*case)
+    b = mk.schedule(*case)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+
+
+def _ranges(ins, mask):
+    r = sorted((int(a), int(b)) for a, b in zip(ins["a0"][mask], ins["a1"][mask]))
+    return r
+
+
+def _check_partition(r, n):
+    assert r, "no work"
+    assert r[0][0] == 0 and r[-1][1] == n
+    for (a0, a1), (b0, b1) in zip(r, r[1:]):
+        assert a1 == b0
+    assert all(a < b for a, b in r)
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0].name}-B{c[1]}-sm{c[3]}")
+def test_every_output_produced_exactly_once(case):
+    shape, B, S, n_sm, pos = case
+    ins, off, tg, sm = _plan(*case)
+    L, H, G = shape.n_layers, shape.hidden, shape.n_heads // shape.n_kv_heads
+    pairs = shape.n_kv_heads * (G + 2) * (shape.head_dim // 2)
+    Fc = shape.ffn // 4
+    op, layer = ins["op"], ins["layer"]
+    for l in range(L):
+        _check_partition(_ranges(ins, (op == mk.OP_QKV) & (layer == l)), pairs)
+        _check_partition(_ranges(ins, (op == mk.OP_OPROJ) & (layer == l)), H)
+        for c in range(4):
+            gu = (op == mk.OP_GATEUP) & (layer == l) & (ins["a2"] == c)
+            r = _ranges(ins, gu)
+            assert r[0][0] == c * Fc and r[-1][1] == (c + 1) * Fc
+            _check_partition([(a - c * Fc, b - c * Fc) for a, b in r], Fc)
+            _check_partition(_ranges(ins, (op == mk.OP_DOWN) & (layer == l) & (ins["a2"] == c)), H)
+        # attention: each (b, g) has partitions 0..P-1 once, and one reduction with that P
+        att = ins[(op == mk.OP_ATTN) & (layer == l)]
+        red = ins[(op == mk.OP_RED) & (layer == l)]
+        assert len(red) == B * shape.n_kv_heads
+        for r in red:
+            b, g, P = int(r["a0"]), int(r["a1"]), int(r["a2"])
+            mine = att[(att["a0"] == b) & (att["a1"] == g)]
+            assert sorted(int(x) >> 16 for x in mine["a2"]) == list(range(P))
+            assert all((int(x) & 0xFFFF) == P for x in mine["a2"])
+            assert 1 <= P <= min(64, pos[b] + 1)
+        # a QKV instruction never spans two kv-head groups (one counter each)
+        q = ins[(op == mk.OP_QKV) & (layer == l)]
+        per = (G + 2) * (shape.head_dim // 2)
+        assert np.all(q["a0"] // per == (q["a1"] - 1) // per)
+    _check_partition(_ranges(ins, op == mk.OP_LMHEAD), shape.vocab)
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0].name}-B{c[1]}-sm{c[3]}")
+def test_counter_targets(case):
+    ins, off, tg, sm = _plan(*case)
+    sums = np.zeros_like(tg)
+    for c, a in zip(ins["sig_ctr"], ins["sig_amount"]):
+        if c >= 0:
+            sums[c] += a
+    np.testing.assert_array_equal(sums, tg)
+    w = ins["wait_ctr"] >= 0
+    np.testing.assert_array_equal(ins["wait_target"][w], tg[ins["wait_ctr"][w]])
+    assert np.all(tg > 0), "every counter is produced"
+
+
+def _simulate(ins, off, tg, n_sm, pick):
+    """Runs the queues on a CPU model: an SM may run the head of its queue
+    once that instruction's counter reached its target."""
+    ctr = np.zeros(len(tg), dtype=np.int64)
+    head = [int(off[s]) for s in range(n_sm)]
+    end = [int(off[s + 1]) for s in range(n_sm)]
+    done = 0
+    total = int(off[-1])
+    while done < total:
+        ready = []
+        for s in range(n_sm):
+            if head[s] < end[s]:
+                i = head[s]
+                c = ins["wait_ctr"][i]
+                if c < 0 or ctr[c] >= ins["wait_target"][i]:
+                    ready.append(s)
+        if not ready:
+            return False
+        s = pick(ready)
+        i = head[s]
+        if ins["sig_ctr"][i] >= 0:
+            ctr[ins["sig_ctr"][i]] += ins["sig_amount"][i]
+        head[s] += 1
+        done += 1
+    np.testing.assert_array_equal(ctr, tg)
+    return True
+
+
+@pytest.mark.parametrize("case", CASES[:3] + [(synth.LLAMA_1B, 1, 640, 24, [600])],
+                         ids=lambda c: f"{c[0].name}-B{c[1]}-sm{c[3]}")
+def test_no_deadlock_under_any_interleaving(case):
+    shape, B, S, n_sm, pos = case
+    ins, off, tg, sm = _plan(*case)
+    rng = random.Random(7)
+    assert _simulate(ins, off, tg, n_sm, lambda r: r[0])
+    assert _simulate(ins, off, tg, n_sm, lambda r: r[-1])
+    for _ in range(3):
+        assert _simulate(ins, off, tg, n_sm, lambda r: rng.choice(r))
+
+
+def test_simulation_detects_a_bad_schedule():
+    # the same check must fail when a wait can never be met
+    ins, off, tg, sm = _plan(synth.TINY, 1, 128, 4, [10])
+    bad = ins.copy()
+    i = int(np.nonzero(bad["wait_ctr"] >= 0)[0][-1])
+    bad["wait_target"][i] += 1
+    assert not _simulate(bad, off, tg, 4, lambda r: r[0])
+
+
+def _happens_before(ins, off, n_sm):
+    """Ancestor sets (as Python int bitmasks) of the DAG made of per-SM program
+    order and counter edges (every producer of a counter precedes every
+    instruction that waits for it)."""
+    n = len(ins)
+    preds = [[] for _ in range(n)]
+    for s in range(n_sm):
+        for i in range(int(off[s]) + 1, int(off[s + 1])):
+            preds[i].append(i - 1)
+    producers = {}
+    for i in range(n):
+        c = int(ins["sig_ctr"][i])
+        if c >= 0:
+            producers.setdefault(c, []).append(i)
+    for i in range(n):
+        c = int(ins["wait_ctr"][i])
+        if c >= 0:
+            preds[i].extend(producers[c])
+    # topological order by Kahn
+    indeg = [len(p) for p in preds]
+    succ = [[] for _ in range(n)]
+    for i, ps in enumerate(preds):
+        for p in ps:
+            succ[p].append(i)
+    order = [i for i in range(n) if indeg[i] == 0]
+    k = 0
+    while k < len(order):
+        for j in succ[order[k]]:
+            indeg[j] -= 1
+            if indeg[j] == 0:
+                order.append(j)
+        k += 1
+    assert len(order) == n, "cycle in the dependency graph"
+    anc = [0] * n
+    for i in order:
+        a = 0
+        for p in preds[i]:
+            a |= anc[p] | (1 << p)
+        anc[i] = a
+    return anc
+
+
+def _accesses(ins, shape, B):
+    """Exact element keys of the shared scratch each instruction reads and
+    writes (q, x, xa, h, dacc, partials and attention output are one buffer
+    reused by every layer; the KV cache is per layer)."""
+    L, H, D, nkv = shape.n_layers, shape.hidden, shape.head_dim, shape.n_kv_heads
+    G = shape.n_heads // nkv
+    half = D // 2
+    per = (G + 2) * half
+    Fc = shape.ffn // 4
+    acc = []
+    for r in ins:
+        op, l, a0, a1, a2 = int(r["op"]), int(r["layer"]), int(r["a0"]), int(r["a1"]), int(r["a2"])
+        R, W = set(), set()
+        if op == mk.OP_QKV:
+            if l > 0:
+                R |= {("x", k) for k in range(H)}
+            for j in range(a0, a1):
+                slot = (j % per) // half
+                W.add(("q", j) if slot < G else ("kv", l, j))
+        elif op == mk.OP_ATTN:
+            for j in range(a1 * per, (a1 + 1) * per):
+                slot = (j % per) // half
+                R.add(("q", j) if slot < G else ("kv", l, j))
+            W.add(("part", a0, a1, a2 >> 16))
+        elif op == mk.OP_RED:
+            R |= {("part", a0, a1, p) for p in range(a2)}
+            W.add(("attn", a0, a1))
+        elif op == mk.OP_OPROJ:
+            R |= {("attn", b, g) for b in range(B) for g in range(nkv)}
+            if l > 0:
+                R |= {("x", k) for k in range(a0, a1)}
+            W |= {("xa", k) for k in range(a0, a1)}
+        elif op == mk.OP_GATEUP:
+            R |= {("xa", k) for k in range(H)}
+            W |= {("h", j) for j in range(a0, a1)}
+        elif op == mk.OP_DOWN:
+            R |= {("h", j) for j in range(a2 * Fc, (a2 + 1) * Fc)}
+            if a2 > 0:
+                R |= {("dacc", k) for k in range(a0, a1)}
+            if a2 == 3:
+                R |= {("xa", k) for k in range(a0, a1)}
+                W |= {("x", k) for k in range(a0, a1)}
+            else:
+                W |= {("dacc", k) for k in range(a0, a1)}
+        elif op == mk.OP_LMHEAD:
+            R |= {("x", k) for k in range(H)}
+        acc.append((R, W))
+    return acc
+
+
+@pytest.mark.parametrize("case", [(synth.TINY, 1, 128, 7, [70]), (synth.TINY, 2, 128, 3, [5, 90]),
+                                  (synth.TINY, 1, 128, 152, [100])],
+                         ids=lambda c: f"B{c[1]}-sm{c[3]}")
+def test_no_unordered_hazards(case):
+    """Every pair of accesses to one scratch element, at least one of them a
+    write (RAW, WAR, WAW), is ordered by program order or a counter chain."""
+    shape, B, S, n_sm, pos = case
+    ins, off, tg, sm = _plan(*case)
+    anc = _happens_before(ins, off, n_sm)
+    touches = {}
+    for i, (R, W) in enumerate(_accesses(ins, shape, B)):
+        for k in R:
+            touches.setdefault(k, []).append((i, False))
+        for k in W:
+            touches.setdefault(k, []).append((i, True))
+    checked = 0
+    for key, lst in touches.items():
+        writers = [i for i, w in lst if w]
+        for wi in writers:
+            for j, _ in lst:
+                if j == wi:
+                    continue
+                if not ((anc[j] >> wi) & 1 or (anc[wi] >> j) & 1):
+                    raise AssertionError(f"unordered access to {key}: #{wi} {ins[wi]} / #{j} {ins[j]}")
+                checked += 1
+    assert checked > 1000
+
+
+def test_chunked_down_waits_only_for_its_chunk():
+    # the down-projection of chunk c waits for chunk c of h, not for the whole
+    # hidden state, and sits after the gate/up of chunk c+1 on every SM
+    ins, off, tg, sm = _plan(synth.LLAMA_1B, 1, 640, 152, [512])
+    for s in range(152):
+        q = ins[off[s]:off[s + 1]]
+        l0 = q[q["layer"] == 0]
+        seq = [(int(r["op"]), int(r["a2"])) for r in l0 if r["op"] in (mk.OP_GATEUP, mk.OP_DOWN)]
+        assert seq == [(5, 0), (5, 1), (6, 0), (5, 2), (6, 1), (5, 3), (6, 2), (6, 3)], seq
+    dn = ins[ins["op"] == mk.OP_DOWN]
+    gu = ins[ins["op"] == mk.OP_GATEUP]
+    for c in range(4):
+        ctrs_dn = set(dn["wait_ctr"][dn["a2"] == c])
+        ctrs_gu = set(gu["sig_ctr"][gu["a2"] == c])
+        assert len(ctrs_dn) == 16 and ctrs_dn <= ctrs_gu
+
+
+def test_work_is_balanced_across_sms():
+    ins, off, tg, sm = _plan(synth.LLAMA_1B, 1, 640, 152, [512])
+    shape = synth.LLAMA_1B
+    rowb = {mk.OP_QKV: 2 * shape.hidden * 2, mk.OP_OPROJ: shape.n_heads * shape.head_dim * 2,
+            mk.OP_GATEUP: 2 * shape.hidden * 2, mk.OP_DOWN: shape.ffn // 4 * 2,
+            mk.OP_LMHEAD: shape.hidden * 2}
+    per_sm = np.zeros(152)
+    for r, s in zip(ins, sm):
+        if int(r["op"]) in rowb:
+            per_sm[s] += (int(r["a1"]) - int(r["a0"])) * rowb[int(r["op"])]
+    assert per_sm.max() / per_sm.mean() < 1.02
