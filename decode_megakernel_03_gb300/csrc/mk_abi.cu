@@ -48,7 +48,6 @@ struct mk_handle {
   int smem_bytes = 0;
   Params base{};          // launch parameters without the per-step fields
   void* d_scratch = nullptr;
-  LayerPtrs* d_layers = nullptr;
   float2* d_rope = nullptr;
   int* d_ctr = nullptr;   // two counter sets
   int n_ctr = 0;
@@ -260,28 +259,30 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
 
   // ---- shared-memory layout: pages | x staging | h staging | results | misc
   const int B = s.B;
-  int nseg_max = 1;
-  for (int op : {MK_OP_QKV, MK_OP_OPROJ, MK_OP_GATEUP, MK_OP_DOWN, MK_OP_LMHEAD})
-    nseg_max = std::max(nseg_max, geom_of(op, s.H, s.QD(), s.Fc(), B).nseg);
   const int item_cap = item_cap_for(s);
   Params& p = h->base;
   p.x_floats = B * std::max(s.H, s.QD());
   p.h_floats = B * s.Fc();
   p.alias_xh = B > 1 ? 1 : 0;
-  p.res_floats = item_cap * 2 * nseg_max * B;
+  p.res_floats = item_cap * 2 * B;
   int att_scratch = kComputeWarps * s.G() * (s.D + 2);
   int xh = p.alias_xh ? std::max(p.x_floats, p.h_floats) : p.x_floats + p.h_floats;
   xh = std::max(xh, att_scratch);
   xh = (xh + 3) / 4 * 4;
-  const int fixed = xh * 4 + 2 * p.res_floats * 4 + ((misc_bytes() + 127) / 128) * 128;
+  const int fixed = xh * 4 + kResBufs * p.res_floats * 4 + ((misc_bytes() + 127) / 128) * 128;
+  // A page slot is always owned by compute warp (slot % kComputeWarps): with
+  // the slot count a multiple of the warp count, page k and page k + n_pages
+  // (same slot) have the same owner, which consumes them in order, so no warp
+  // can wait on a slot two mbarrier phases ahead of its contents.
   int n_pages = std::min(kMaxPages, (optin - fixed) / kPageBytes);
-  if (n_pages < 4)
-    return fail(nullptr, MK_ERR_INVALID, "configuration leaves fewer than 4 shared-memory pages");
+  n_pages -= n_pages % kComputeWarps;
+  if (n_pages < kComputeWarps)
+    return fail(nullptr, MK_ERR_INVALID, "configuration leaves too few shared-memory pages");
   p.n_pages = n_pages;
   p.off_x = n_pages * kPageBytes;
   p.off_h = p.alias_xh ? p.off_x : p.off_x + p.x_floats * 4;
   p.off_res = p.off_x + xh * 4;
-  p.off_misc = p.off_res + 2 * p.res_floats * 4;
+  p.off_misc = p.off_res + kResBufs * p.res_floats * 4;
   p.off_misc = (p.off_misc + 127) / 128 * 128;
   h->smem_bytes = p.off_misc + misc_bytes();
 
@@ -306,7 +307,6 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
       sizeof(float) * (size_t)B * s.F,                                    // h
       sizeof(float) * (size_t)B * s.H,                                    // dacc
       sizeof(float2) * (size_t)s.S * (s.D / 2),                           // rope
-      sizeof(LayerPtrs) * (size_t)s.L,                                    // layers
       sizeof(int) * (size_t)2 * h->n_ctr,                                 // counters
       sizeof(int) * 64,                                                   // error word
   };
@@ -327,11 +327,9 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
   p.h = reinterpret_cast<float*>(base + offs[5]);
   p.dacc = reinterpret_cast<float*>(base + offs[6]);
   h->d_rope = reinterpret_cast<float2*>(base + offs[7]);
-  h->d_layers = reinterpret_cast<LayerPtrs*>(base + offs[8]);
-  h->d_ctr = reinterpret_cast<int*>(base + offs[9]);
-  h->d_err = reinterpret_cast<int*>(base + offs[10]);
+  h->d_ctr = reinterpret_cast<int*>(base + offs[8]);
+  h->d_err = reinterpret_cast<int*>(base + offs[9]);
   p.rope = h->d_rope;
-  p.layers = h->d_layers;
   p.err = h->d_err;
   p.n_ctr = h->n_ctr;
 
@@ -357,7 +355,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
       double ang = (double)pos * std::pow((double)cfg->rope_theta, -2.0 * i / (double)s.D);
       rope[(size_t)pos * (s.D / 2) + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
     }
-  std::vector<LayerPtrs> lp(L);
+  LayerPtrs* lp = p.layers;
   for (int l = 0; l < L; ++l) {
     lp[l].attn_norm = static_cast<const uint16_t*>(w->attn_norm[l]);
     lp[l].wq = static_cast<const uint16_t*>(w->wq[l]);
@@ -372,8 +370,6 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
     lp[l].vc = static_cast<uint16_t*>(v_cache[l]);
   }
   ce = cudaMemcpy(h->d_rope, rope.data(), sizeof(float2) * rope.size(), cudaMemcpyHostToDevice);
-  if (ce == cudaSuccess)
-    ce = cudaMemcpy(h->d_layers, lp.data(), sizeof(LayerPtrs) * L, cudaMemcpyHostToDevice);
   if (ce == cudaSuccess)
     ce = cudaFuncSetAttribute(kernel_for_batch(B), cudaFuncAttributeMaxDynamicSharedMemorySize,
                               h->smem_bytes);

@@ -10,19 +10,24 @@
 #include <stdint.h>
 #include <vector_types.h>  // float2 (a plain C header of the CUDA toolkit)
 
-#include "../../include/mk.h"
+#include "mk.h"  // include/ is on the include path
 
 namespace mk {
 
 constexpr int kPageBytes = 16384;   // one shared-memory page (§3.3: 16 KB pages)
 constexpr int kComputeWarps = 6;    // warps in the compute role (8 warps per CTA: 255 registers each)
 constexpr int kThreads = (kComputeWarps + 2) * 32;  // + loader warp + storer warp
-constexpr int kLoaderWarp = kComputeWarps;
-constexpr int kStorerWarp = kComputeWarps + 1;
+// Warp w runs on SM sub-partition w % 4. The loader and the storer share
+// sub-partition 2 so that no compute warp competes with the loader for issue
+// slots; the six compute warps fill sub-partitions 0, 1 and 3.
+constexpr int kLoaderWarp = 2;
+constexpr int kStorerWarp = 6;
 constexpr int kMaxBatch = 8;
 constexpr int kMaxPartitions = 64;  // split-KV partitions per (sequence, kv-head)
 constexpr int kChunks = 4;          // MLP hidden state chunks (§3.4: four pieces)
 constexpr int kMaxPages = 14;
+constexpr int kMaxLayers = 64;    // the layer table travels in the kernel parameters
+constexpr int kResBufs = 4;      // result hand-offs in flight between compute and storer
 
 using Instr = mk_instr;
 static_assert(sizeof(Instr) == 32, "instruction descriptor is 32 bytes");
@@ -47,7 +52,7 @@ struct Params {
   // model
   int L, H, nh, nkv, D, F, V, B, S, G, Fc, QD;  // QD = nh * D
   float eps;
-  const LayerPtrs* layers;     // device [L]
+  LayerPtrs layers[kMaxLayers]; // per-layer pointers (constant bank: no global load)
   const uint16_t* embed;
   const uint16_t* lm;          // == embed when tied
   const uint16_t* final_norm;
@@ -93,12 +98,11 @@ constexpr int kErrBadInstr = (MK_ERR_INVALID << 24) | 4;
 // A GEMV instruction walks "items": one weight row, or a pair of rows whose
 // results are combined in the epilogue (q/k/v RoPE pairs, gate/up pairs).
 // Each row contributes a K-long slice (the whole row, or one chunk of it).
+// A page holds `ipp` items laid out [row kind r][item].
 struct Geom {
   int K;      // columns of each row slice
   int R;      // rows per item (1 or 2)
   int ipp;    // items per page
-  int J;      // 256-column blocks per segment held by one warp
-  int nseg;   // segments per row slice (K / (256 * J))
 };
 
 #if defined(__CUDACC__)
@@ -112,22 +116,11 @@ MK_HD bool is_gemv(int op) {
          op == MK_OP_LMHEAD;
 }
 
-// Largest J in 1..8 dividing K/256 with J * B <= 8 (activation registers).
-MK_HD int pick_J(int K, int B) {
-  int blocks = K / 256;
-  int jmax = 8 / B;
-  for (int j = jmax; j >= 1; --j)
-    if (blocks % j == 0) return j;
-  return 1;
-}
-
-MK_HD Geom geom_of(int op, int H, int QD, int Fc, int B) {
+MK_HD Geom geom_of(int op, int H, int QD, int Fc) {
   Geom g;
   g.K = (op == MK_OP_OPROJ) ? QD : (op == MK_OP_DOWN ? Fc : H);
   g.R = (op == MK_OP_QKV || op == MK_OP_GATEUP) ? 2 : 1;
   g.ipp = kPageBytes / (g.R * g.K * 2);
-  g.J = pick_J(g.K, B);
-  g.nseg = g.K / (256 * g.J);
   return g;
 }
 

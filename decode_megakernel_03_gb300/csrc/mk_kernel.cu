@@ -33,14 +33,21 @@ namespace mk {
 struct Misc {
   uint64_t full[kMaxPages];
   uint64_t empty[kMaxPages];
-  uint64_t res_full[2];
-  uint64_t res_empty[2];
+  uint64_t res_full[kResBufs];
+  uint64_t res_empty[kResBufs];
   float red[2][kComputeWarps][kMaxBatch];  // RMSNorm partial sums, double-buffered
   int abort;
 };
 
 constexpr int kComputeThreads = kComputeWarps * 32;
 constexpr int kBarCompute = 1;
+
+// Index of this warp among the compute warps (all warps but loader and storer).
+__device__ __forceinline__ int compute_warp() {
+  const int w = threadIdx.x >> 5;
+  return w < kLoaderWarp ? w : (w < kStorerWarp ? w - 1 : w - 2);
+}
+__device__ __forceinline__ int compute_tid() { return compute_warp() * 32 + (threadIdx.x & 31); }
 
 __device__ __forceinline__ void compute_bar() { named_bar(kBarCompute, kComputeThreads); }
 
@@ -96,74 +103,146 @@ __device__ __noinline__ bool wait_counter(const Params& p, Misc* m, int ctr, int
   }
 }
 
+// Instruction descriptors are read-only for the whole launch: two 16-byte
+// loads through the non-coherent path. Every role fetches the next descriptor
+// while it works on the current one, so no role stalls on a dependent global
+// load at an instruction boundary.
+__device__ __forceinline__ Instr load_instr(const Instr* q) {
+  const uint4 a = __ldg(reinterpret_cast<const uint4*>(q));
+  const uint4 b = __ldg(reinterpret_cast<const uint4*>(q) + 1);
+  Instr in;
+  in.op = (int16_t)(a.x & 0xffffu);
+  in.layer = (int16_t)(a.x >> 16);
+  in.a0 = (int32_t)a.y;
+  in.a1 = (int32_t)a.z;
+  in.a2 = (int32_t)a.w;
+  in.wait_ctr = (int32_t)b.x;
+  in.wait_target = (int32_t)b.y;
+  in.sig_ctr = (int32_t)b.z;
+  in.sig_amount = (int32_t)b.w;
+  return in;
+}
+
 // ---------------------------------------------------------------------------
 // weight rows of a GEMV item
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ const uint16_t* row_src(const Params& p, const Instr& in, int item,
-                                                   int r) {
-  const LayerPtrs& L = p.layers[in.layer];
-  switch (in.op) {
-    case MK_OP_QKV: {
-      PairRows pr = pair_rows(item, p.G, p.D);
-      const uint16_t* W = pr.which == 0 ? L.wq : (pr.which == 1 ? L.wk : L.wv);
-      int row = pr.head * p.D + pr.i + r * (p.D / 2);
-      return W + (size_t)row * p.H;
-    }
-    case MK_OP_OPROJ:
-      return L.wo + (size_t)item * p.QD;
-    case MK_OP_GATEUP:
-      return (r == 0 ? L.wgate : L.wup) + (size_t)item * p.H;
-    case MK_OP_DOWN:
-      return L.wdown + (size_t)item * p.F + (size_t)in.a2 * p.Fc;
-    default:  // MK_OP_LMHEAD
-      return p.lm + (size_t)item * p.H;
+// The weight matrices of one instruction, read from the layer table once per
+// instruction so that per-row addresses are pure arithmetic.
+struct RowSrc {
+  const uint16_t* w[3];
+  int op, G, D, H, QD, F;
+};
+
+__device__ __forceinline__ RowSrc row_src_of(const Params& p, const Instr& in) {
+  RowSrc s;
+  s.op = in.op;
+  s.G = p.G;
+  s.D = p.D;
+  s.H = p.H;
+  s.QD = p.QD;
+  s.F = p.F;
+  s.w[0] = s.w[1] = s.w[2] = nullptr;
+  if (in.op == MK_OP_LMHEAD) {
+    s.w[0] = p.lm;
+    return s;
   }
+  const LayerPtrs* L = p.layers + in.layer;
+  switch (in.op) {
+    case MK_OP_QKV: s.w[0] = L->wq; s.w[1] = L->wk; s.w[2] = L->wv; break;
+    case MK_OP_OPROJ: s.w[0] = L->wo; break;
+    case MK_OP_GATEUP: s.w[0] = L->wgate; s.w[1] = L->wup; break;
+    default: s.w[0] = L->wdown + (size_t)in.a2 * p.Fc; break;  // MK_OP_DOWN: chunk a2
+  }
+  return s;
 }
 
 // ---------------------------------------------------------------------------
 // loader role
 // ---------------------------------------------------------------------------
 
+// Issues the bulk copies of one page: items [i0, i1) of the instruction, laid
+// out [row kind r][item]. Rows are affine in the item (row = base + item *
+// stride) except for q/k/v pairs, which are affine within one head; runs of
+// rows that follow each other in memory go out as one copy.
+__device__ __forceinline__ void issue_page(const Params& p, const Instr& in, const Geom& g,
+                                           const RowSrc& rs, int i0, int i1, uint8_t* dst,
+                                           uint64_t* bar, uint64_t pol) {
+  const uint32_t row_bytes = (uint32_t)g.K * 2u;
+  if (in.op == MK_OP_QKV) {
+    // pair j holds rows (head*D + i, head*D + i + D/2); consecutive pairs of one
+    // head are consecutive rows, so a page splits at most at head boundaries
+    const int half = p.D / 2;
+    for (int r = 0; r < 2; ++r) {
+      int it = i0;
+      while (it < i1) {
+        const PairRows pr = pair_rows(in.a0 + it, p.G, p.D);
+        const int n = min(i1 - it, half - pr.i);
+        const uint16_t* src = rs.w[pr.which] + (size_t)(pr.head * p.D + pr.i + r * half) * p.H;
+        bulk_g2s_hint(dst, src, row_bytes * (uint32_t)n, bar, pol);
+        dst += row_bytes * (uint32_t)n;
+        it += n;
+      }
+    }
+    return;
+  }
+  // OPROJ / GATEUP / DOWN / LMHEAD: row of item j = w[r] + j * stride
+  const size_t stride = in.op == MK_OP_OPROJ ? (size_t)p.QD : (in.op == MK_OP_DOWN ? (size_t)p.F : (size_t)p.H);
+  for (int r = 0; r < g.R; ++r) {
+    const uint16_t* src = rs.w[r] + (size_t)(in.a0 + i0) * stride;
+    if (stride * 2 == row_bytes) {  // whole rows: one contiguous run
+      bulk_g2s_hint(dst, src, row_bytes * (uint32_t)(i1 - i0), bar, pol);
+      dst += row_bytes * (uint32_t)(i1 - i0);
+    } else {  // row slices (down-projection chunks): one copy per row
+      for (int it = i0; it < i1; ++it) {
+        bulk_g2s_hint(dst, src, row_bytes, bar, pol);
+        dst += row_bytes;
+        src += stride;
+      }
+    }
+  }
+}
+
 __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, const Instr* q, int n) {
   const int lane = threadIdx.x & 31;
   if (lane != 0) return;
   const uint64_t pol = policy_evict_first();
-  uint32_t page_cnt = 0;
+  uint32_t page_cnt = 0;  // pages issued
+  int slot = 0;           // page_cnt % n_pages
+  uint32_t round = 0;     // page_cnt / n_pages
   bool ok = true;
+  Instr nxt = n > 0 ? load_instr(q) : Instr{};
   for (int i = 0; i < n && ok; ++i) {
-    const Instr in = q[i];
+    const Instr in = nxt;
+    if (i + 1 < n) nxt = load_instr(q + i + 1);
     if (!is_gemv(in.op)) continue;
-    const Geom g = geom_of(in.op, p.H, p.QD, p.Fc, p.B);
+    const Geom g = geom_of(in.op, p.H, p.QD, p.Fc);
     const int items = in.a1 - in.a0;
-    const int npages = (items + g.ipp - 1) / g.ipp;
     const uint32_t row_bytes = (uint32_t)g.K * 2u;
-    for (int pg = 0; pg < npages; ++pg, ++page_cnt) {
-      const int slot = (int)(page_cnt % (uint32_t)p.n_pages);
-      const uint32_t round = page_cnt / (uint32_t)p.n_pages;
+    const RowSrc rs = row_src_of(p, in);
+    for (int i0 = 0; i0 < items; i0 += g.ipp) {
       if (!wait_mbar(p, m, &m->empty[slot], (round & 1u) ^ 1u, kErrTimeoutPage)) {
         ok = false;
         break;
       }
-      const int i0 = pg * g.ipp;
       const int i1 = min(items, i0 + g.ipp);
       mbar_arrive_expect_tx(&m->full[slot], (uint32_t)((i1 - i0) * g.R) * row_bytes);
-      uint8_t* dst = smem + (size_t)slot * kPageBytes;
-      for (int it = i0; it < i1; ++it)
-        for (int r = 0; r < g.R; ++r) {
-          bulk_g2s_hint(dst, row_src(p, in, in.a0 + it, r), row_bytes, &m->full[slot], pol);
-          dst += row_bytes;
-        }
+      issue_page(p, in, g, rs, i0, i1, smem + (size_t)slot * kPageBytes, &m->full[slot], pol);
+      ++page_cnt;
+      if (++slot == p.n_pages) {
+        slot = 0;
+        ++round;
+      }
     }
   }
   if (!ok) {
     // drain: every issued copy must land before the CTA's shared memory goes away
     const uint32_t first = page_cnt > (uint32_t)p.n_pages ? page_cnt - p.n_pages : 0u;
     for (uint32_t k = first; k < page_cnt; ++k) {
-      const int slot = (int)(k % (uint32_t)p.n_pages);
+      const int sl = (int)(k % (uint32_t)p.n_pages);
       const uint32_t par = (k / (uint32_t)p.n_pages) & 1u;
       const uint64_t t0 = globaltimer();
-      while (!mbar_try_wait(&m->full[slot], par)) {
+      while (!mbar_try_wait(&m->full[sl], par)) {
         if (globaltimer() - t0 > p.timeout_ns) break;
       }
     }
@@ -187,27 +266,39 @@ __device__ __forceinline__ int act_kind(int op) {
   }
 }
 
+struct InvScale {
+  float v[kMaxBatch];  // 1/rms per sequence (1 for activations without a norm)
+};
+
 struct Staged {
   int key_x = -1;     // what the x buffer holds
   int key_h = -1;     // what the h buffer holds
   int stage_cnt = 0;  // parity of the RMSNorm partial-sum buffer
-  float inv[kMaxBatch];
+  InvScale inv_x;     // scale of the x buffer's contents
 };
 
 __device__ __forceinline__ int act_key(int kind, int layer, int chunk) {
   return (kind << 20) | (layer << 4) | chunk;
 }
 
+__device__ __forceinline__ const uint16_t* norm_weight(const Params& p, int kind, int layer) {
+  if (kind == kActAttnNorm) return p.layers[layer].attn_norm;
+  if (kind == kActMlpNorm) return p.layers[layer].mlp_norm;
+  if (kind == kActFinalNorm) return p.final_norm;
+  return nullptr;
+}
+
 // Stages the activation vector(s) of `kind` for all B sequences into the x or
-// h buffer; for the RMSNorm kinds also computes 1/rms per sequence.
-__device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, Staged& st, int kind, int layer,
-                      int chunk) {
-  const int tid = threadIdx.x;  // 0..255 within the compute warps
+// h buffer. For the RMSNorm kinds the buffer holds x * w (the gain already
+// applied) and 1/rms(x) per sequence is returned in st.inv_x.
+__device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, Staged& st, int kind,
+                                      int layer, int chunk) {
+  const int tid = compute_tid();  // 0..kComputeThreads-1
   const int warp = tid >> 5, lane = tid & 31;
   const bool to_h = kind == kActH;
   float* dst = reinterpret_cast<float*>(smem + (to_h ? p.off_h : p.off_x));
   const int K = kind == kActAttnOut ? p.QD : (to_h ? p.Fc : p.H);
-  const bool norm = kind == kActAttnNorm || kind == kActMlpNorm || kind == kActFinalNorm;
+  const uint16_t* normw = norm_weight(p, kind, layer);
   const int par = st.stage_cnt & 1;
   compute_bar();  // everyone is done reading the buffer's previous contents
   for (int b = 0; b < p.B; ++b) {
@@ -225,22 +316,32 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
         else src = p.h + (size_t)b * p.F + (size_t)chunk * p.Fc;
         v = __ldcg(reinterpret_cast<const float4*>(src + c));
       }
-      *reinterpret_cast<float4*>(dst + (size_t)b * K + c) = v;
       ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+      if (normw) {
+        const uint2 wv = __ldg(reinterpret_cast<const uint2*>(normw + c));
+        v.x *= bf_lo(wv.x);
+        v.y *= bf_hi(wv.x);
+        v.z *= bf_lo(wv.y);
+        v.w *= bf_hi(wv.y);
+      }
+      *reinterpret_cast<float4*>(dst + (size_t)b * K + c) = v;
     }
-    if (norm) {
+    if (normw) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
       if (lane == 0) m->red[par][warp][b] = ss;
     }
   }
   compute_bar();
-  if (norm) {
-    for (int b = 0; b < p.B; ++b) {
-      float s = 0.f;
+  InvScale inv;
 #pragma unroll
-      for (int w = 0; w < kComputeWarps; ++w) s += m->red[par][w][b];
-      st.inv[b] = rsqrtf(s / (float)p.H + p.eps);
+  for (int b = 0; b < kMaxBatch; ++b) {
+    inv.v[b] = 1.f;
+    if (normw && b < p.B) {
+      float sum = 0.f;
+#pragma unroll
+      for (int w = 0; w < kComputeWarps; ++w) sum += m->red[par][w][b];
+      inv.v[b] = rsqrtf(sum / (float)p.H + p.eps);
     }
   }
   st.stage_cnt++;
@@ -250,124 +351,212 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
     if (p.alias_xh) st.key_x = -1;
   } else {
     st.key_x = key;
+    st.inv_x = inv;
     if (p.alias_xh) st.key_h = -1;
   }
 }
 
 // ---------------------------------------------------------------------------
-// compute role: GEMV pieces
+// compute role: GEMV pages
 // ---------------------------------------------------------------------------
-// A "piece" is (item, row of the item, segment): one warp dots one 256*J-long
-// segment of one weight row with the matching activations of all B sequences.
-// Lane l holds columns seg*256J + j*256 + l*8 + e (e < 8) in registers, so each
-// j reads 512 contiguous bytes of the page per warp. Pieces are dealt to warps
-// round-robin; every warp walks every page in order (wait full -> its pieces
-// -> arrive empty) so a page is released as soon as all warps are past it.
+// Each compute warp owns whole pages, dealt round-robin over the CTA's page
+// stream, and dots every row of its page with the activations of all B
+// sequences: lane l covers columns j*256 + l*8 .. +8 of each 256-column block,
+// i.e. every block is one 512-byte contiguous read of the row per warp. Four
+// rows are in flight at once (two accumulator chains each) for ILP. With one
+// sequence and rows of at most 2048 columns the activations sit in registers;
+// otherwise they are read from the staged buffer block by block.
 
-// J (256-column blocks per warp segment) is a runtime value <= JM = 8 / B;
-// the loops below are unrolled to JM and predicated on J so the activation
-// registers stay statically indexed and one body serves every row length.
-template <int B>
-__device__ __forceinline__ void load_act(float (&a)[B][64 / B], int J, const float* buf, int K,
-                                         int seg, const uint16_t* normw, const float* inv,
-                                         int lane) {
-  constexpr int JM = 8 / B;
+__device__ __forceinline__ void warp_sum4(float (&v)[4]) {
 #pragma unroll
-  for (int j = 0; j < JM; ++j) {
-    if (j < J) {
-      const int col = seg * 256 * J + j * 256 + lane * 8;
-      float w8[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
-      if (normw) {
-        const uint4 wv = __ldg(reinterpret_cast<const uint4*>(normw + col));
-        w8[0] = bf_lo(wv.x); w8[1] = bf_hi(wv.x); w8[2] = bf_lo(wv.y); w8[3] = bf_hi(wv.y);
-        w8[4] = bf_lo(wv.z); w8[5] = bf_hi(wv.z); w8[6] = bf_lo(wv.w); w8[7] = bf_hi(wv.w);
+  for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] += __shfl_xor_sync(0xffffffffu, v[q], o);
+  }
+}
+
+// B == 1, K <= 2048: activations a[j*8 + e] in registers. NR rows of the
+// page starting at `rows` (NR <= 4); row q's result goes to out[q * stride]
+// ... or to outq[q] when given per-row destinations.
+template <int NB>
+__device__ __forceinline__ void rows4_reg(const uint8_t* rows, int n_rows, int row_bytes,
+                                          int nblk, const float (&a)[64], float* const (&dst)[4],
+                                          int lane) {
+  float acc[4][2];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) acc[q][0] = acc[q][1] = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (NB == 8 || j < nblk) {
+      uint4 w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        w[q] = (NB == 8 || q < n_rows)
+                   ? *reinterpret_cast<const uint4*>(rows + (size_t)q * row_bytes + j * 512 + lane * 16)
+                   : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float& c = acc[q][j & 1];
+        c = fmaf(bf_lo(w[q].x), a[j * 8 + 0], c);
+        c = fmaf(bf_hi(w[q].x), a[j * 8 + 1], c);
+        c = fmaf(bf_lo(w[q].y), a[j * 8 + 2], c);
+        c = fmaf(bf_hi(w[q].y), a[j * 8 + 3], c);
+        c = fmaf(bf_lo(w[q].z), a[j * 8 + 4], c);
+        c = fmaf(bf_hi(w[q].z), a[j * 8 + 5], c);
+        c = fmaf(bf_lo(w[q].w), a[j * 8 + 6], c);
+        c = fmaf(bf_hi(w[q].w), a[j * 8 + 7], c);
       }
+    }
+  }
+  float v[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) v[q] = acc[q][0] + acc[q][1];
+  warp_sum4(v);
+  if (lane < 4 && lane < n_rows) {
+    float mine = v[0];
+#pragma unroll
+    for (int q = 1; q < 4; ++q) mine = lane == q ? v[q] : mine;
+    *dst[lane] = mine;
+  }
+}
+
+// any B, any K: activations read block by block from the staged buffer
+template <int B>
+__device__ __forceinline__ void page_rows_smem(const uint8_t* page, int n_rows, int row_bytes,
+                                               int nblk, const float* act, int K,
+                                               const InvScale& inv, float* out_row0,
+                                               int out_stride, int lane) {
+  constexpr int RG = B <= 2 ? 4 : (B == 4 ? 2 : 1);
+  for (int r0 = 0; r0 < n_rows; r0 += RG) {
+    float acc[RG][B];
+#pragma unroll
+    for (int q = 0; q < RG; ++q)
+#pragma unroll
+      for (int b = 0; b < B; ++b) acc[q][b] = 0.f;
+    for (int j = 0; j < nblk; ++j) {
+      float x[B][8];
 #pragma unroll
       for (int b = 0; b < B; ++b) {
-        const float4 x0 = *reinterpret_cast<const float4*>(buf + (size_t)b * K + col);
-        const float4 x1 = *reinterpret_cast<const float4*>(buf + (size_t)b * K + col + 4);
-        const float sc = normw ? inv[b] : 1.f;
-        a[b][j * 8 + 0] = x0.x * sc * w8[0];
-        a[b][j * 8 + 1] = x0.y * sc * w8[1];
-        a[b][j * 8 + 2] = x0.z * sc * w8[2];
-        a[b][j * 8 + 3] = x0.w * sc * w8[3];
-        a[b][j * 8 + 4] = x1.x * sc * w8[4];
-        a[b][j * 8 + 5] = x1.y * sc * w8[5];
-        a[b][j * 8 + 6] = x1.z * sc * w8[6];
-        a[b][j * 8 + 7] = x1.w * sc * w8[7];
+        const float* src = act + (size_t)b * K + j * 256 + lane * 8;
+        const float4 x0 = *reinterpret_cast<const float4*>(src);
+        const float4 x1 = *reinterpret_cast<const float4*>(src + 4);
+        const float s = inv.v[b];
+        x[b][0] = x0.x * s; x[b][1] = x0.y * s; x[b][2] = x0.z * s; x[b][3] = x0.w * s;
+        x[b][4] = x1.x * s; x[b][5] = x1.y * s; x[b][6] = x1.z * s; x[b][7] = x1.w * s;
       }
-    } else {
 #pragma unroll
-      for (int b = 0; b < B; ++b)
+      for (int q = 0; q < RG; ++q) {
+        if (r0 + q < n_rows) {
+          const uint4 w =
+              *reinterpret_cast<const uint4*>(page + (size_t)(r0 + q) * row_bytes + j * 512 + lane * 16);
+          const float wf[8] = {bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y),
+                               bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w)};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) a[b][j * 8 + e] = 0.f;
+          for (int e = 0; e < 8; ++e)
+#pragma unroll
+            for (int b = 0; b < B; ++b) acc[q][b] = fmaf(wf[e], x[b][e], acc[q][b]);
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < RG; ++q) {
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[q][b] += __shfl_xor_sync(0xffffffffu, acc[q][b], o);
+      }
+      if (lane == 0 && r0 + q < n_rows) {
+#pragma unroll
+        for (int b = 0; b < B; ++b) out_row0[(size_t)(r0 + q) * out_stride + b] = acc[q][b];
+      }
     }
   }
 }
 
 template <int B>
 __device__ __forceinline__ void gemv_run(const Params& p, Misc* m, uint8_t* smem, const Instr& in,
-                                         const Geom& g, const float* act, const uint16_t* normw,
-                                         const float* inv, float* res, uint32_t page_base) {
-  constexpr int JM = 8 / B;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int J = g.J;
+                                         const Geom& g, const float* act, const InvScale& inv,
+                                         float* res, uint32_t page_base) {
+  const int warp = compute_warp(), lane = threadIdx.x & 31;
   const int items = in.a1 - in.a0;
   const int npages = (items + g.ipp - 1) / g.ipp;
-  const int ppi = g.R * g.nseg;  // pieces per item
-  const int npieces = items * ppi;
   const int row_bytes = g.K * 2;
-  float a[B][64 / B];
-  int loaded = -1;
-  int piece = warp;
-  for (int pg = 0; pg < npages; ++pg) {
-    const uint32_t pc = page_base + (uint32_t)pg;
-    const int slot = (int)(pc % (uint32_t)p.n_pages);
-    const bool ok = wait_mbar(p, m, &m->full[slot], (pc / (uint32_t)p.n_pages) & 1u,
-                              kErrTimeoutPage);
-    const int piece_end = min(npieces, (pg + 1) * g.ipp * ppi);
-    const uint8_t* page = smem + (size_t)slot * kPageBytes;
-    for (; piece < piece_end; piece += kComputeWarps) {
-      if (!ok) continue;
-      const int item = piece / ppi;
-      const int rr = piece - item * ppi;
-      const int r = rr / g.nseg;
-      const int seg = rr - r * g.nseg;
-      if (seg != loaded) {
-        load_act<B>(a, J, act, g.K, seg, normw, inv, lane);
-        loaded = seg;
-      }
-      const uint8_t* rowp =
-          page + (size_t)((item - pg * g.ipp) * g.R + r) * row_bytes + (size_t)seg * J * 512;
-      uint4 wv[JM];
+  const int nblk = g.K / 256;
+  const bool in_regs = B == 1 && nblk <= 8;
+  float a[64];
+  bool loaded = false;
+  // the pages of this warp: global page index congruent to the warp index.
+  // n_pages is a multiple of kComputeWarps, so every slot this warp waits on
+  // was last used by this warp's own previous page (already consumed): the
+  // parity wait below cannot alias an older phase.
+  int pg = (int)(((uint32_t)warp + kComputeWarps - page_base % kComputeWarps) % kComputeWarps);
+  // slot and phase of this warp's first page, then advanced incrementally
+  const uint32_t pc0 = page_base + (uint32_t)pg;
+  int slot = (int)(pc0 % (uint32_t)p.n_pages);
+  uint32_t round = pc0 / (uint32_t)p.n_pages;
+  for (; pg < npages; pg += kComputeWarps) {
+    const bool ok = wait_mbar(p, m, &m->full[slot], round & 1u, kErrTimeoutPage);
+    if (ok) {
+      const int n_in = min(g.ipp, items - pg * g.ipp);  // items on this page
+      const uint8_t* page = smem + (size_t)slot * kPageBytes;
+      // page row pr = r * n_in + k holds row r of item pg*ipp + k; its result
+      // goes to res[((item * R) + r) * B + b]
+      const int n_rows = n_in * g.R;
+      float* const res_page = res + (size_t)(pg * g.ipp) * g.R * B;
+      if (in_regs) {
+        if (!loaded) {
 #pragma unroll
-      for (int j = 0; j < JM; ++j)
-        wv[j] = j < J ? *reinterpret_cast<const uint4*>(rowp + j * 512 + lane * 16)
-                      : make_uint4(0, 0, 0, 0);
-      float acc[B];
+          for (int j = 0; j < 8; ++j) {
+            if (j < nblk) {
+              const float* src = act + j * 256 + lane * 8;
+              const float4 x0 = *reinterpret_cast<const float4*>(src);
+              const float4 x1 = *reinterpret_cast<const float4*>(src + 4);
+              const float s = inv.v[0];
+              a[j * 8 + 0] = x0.x * s; a[j * 8 + 1] = x0.y * s; a[j * 8 + 2] = x0.z * s;
+              a[j * 8 + 3] = x0.w * s; a[j * 8 + 4] = x1.x * s; a[j * 8 + 5] = x1.y * s;
+              a[j * 8 + 6] = x1.z * s; a[j * 8 + 7] = x1.w * s;
+            } else {
 #pragma unroll
-      for (int b = 0; b < B; ++b) acc[b] = 0.f;
+              for (int e = 0; e < 8; ++e) a[j * 8 + e] = 0.f;
+            }
+          }
+          loaded = true;
+        }
+        if (nblk == 8 && n_rows == 4) {
+          // the common full page of 2048-column rows: 4 items (R = 1) or 2
+          // pairs (R = 2), no division on this path
+          float* dst[4];
 #pragma unroll
-      for (int j = 0; j < JM; ++j) {
-        const float wf[8] = {bf_lo(wv[j].x), bf_hi(wv[j].x), bf_lo(wv[j].y), bf_hi(wv[j].y),
-                             bf_lo(wv[j].z), bf_hi(wv[j].z), bf_lo(wv[j].w), bf_hi(wv[j].w)};
+          for (int q = 0; q < 4; ++q) {
+            const int r = g.R == 1 ? 0 : (q >> 1), k = g.R == 1 ? q : (q & 1);
+            dst[q] = res_page + ((size_t)k * g.R + r) * B;
+          }
+          rows4_reg<8>(page, 4, row_bytes, 8, a, dst, lane);
+        } else {
+          for (int r0 = 0; r0 < n_rows; r0 += 4) {
+            float* dst[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-#pragma unroll
-          for (int b = 0; b < B; ++b) acc[b] = fmaf(wf[e], a[b][j * 8 + e], acc[b]);
-      }
-#pragma unroll
-      for (int b = 0; b < B; ++b) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], o);
-      }
-      if (lane == 0) {
-#pragma unroll
-        for (int b = 0; b < B; ++b) res[(size_t)piece * B + b] = acc[b];
+            for (int q = 0; q < 4; ++q) {
+              const int pr = min(r0 + q, n_rows - 1);
+              const int r = pr / n_in, k = pr - r * n_in;
+              dst[q] = res_page + ((size_t)k * g.R + r) * B;
+            }
+            rows4_reg<0>(page + (size_t)r0 * row_bytes, n_rows - r0, row_bytes, nblk, a, dst, lane);
+          }
+        }
+      } else {
+        for (int r = 0; r < g.R; ++r)
+          page_rows_smem<B>(page + (size_t)r * n_in * row_bytes, n_in, row_bytes, nblk, act, g.K,
+                            inv, res_page + (size_t)r * B, g.R * B, lane);
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&m->empty[slot]);
+    slot += kComputeWarps;
+    if (slot >= p.n_pages) {
+      slot -= p.n_pages;
+      ++round;
+    }
   }
 }
 
@@ -397,7 +586,7 @@ template <int D, int GH>
 __device__ __forceinline__ void attn_partial(const Params& p, uint8_t* smem, const Instr& in, int h0) {
   constexpr int LPT = D / 8;       // lanes per key row
   constexpr int TPI = 32 / LPT;    // keys per warp load
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = compute_warp(), lane = threadIdx.x & 31;
   const int b = in.a0, g = in.a1, pidx = in.a2 >> 16, P = in.a2 & 0xffff;
   const int len = p.pos[b] + 1;
   const int t0 = (int)((long)pidx * len / P), t1 = (int)((long)(pidx + 1) * len / P);
@@ -503,7 +692,7 @@ __device__ __forceinline__ void attn_partial(const Params& p, uint8_t* smem, con
     }
   }
   compute_bar();
-  const int tid = threadIdx.x;
+  const int tid = compute_tid();
   for (int idx = tid; idx < GH * D; idx += kComputeThreads) {
     const int h = idx / D, d = idx - h * D;
     float M = -INFINITY;
@@ -545,7 +734,7 @@ __device__ void attn_unit(const Params& p, uint8_t* smem, const Instr& in) {
 template <int D>
 __device__ __forceinline__ void attn_reduce(const Params& p, const Instr& in) {
   constexpr int PL = D / 32;  // dims per lane
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = compute_warp(), lane = threadIdx.x & 31;
   const int b = in.a0, g = in.a1, P = in.a2;
   for (int hl = warp; hl < p.G; hl += kComputeWarps) {
     const int h = g * p.G + hl;
@@ -579,14 +768,16 @@ __device__ __forceinline__ void attn_reduce(const Params& p, const Instr& in) {
 template <int B>
 __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Instr* q, int n,
                              int qbase) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = compute_warp(), lane = threadIdx.x & 31;
   Staged st;
   uint32_t page_cnt = 0;
   int known_ctr = -1, known_tgt = 0;
+  Instr nxt = n > 0 ? load_instr(q) : Instr{};
   for (int i = 0; i < n; ++i) {
-    const Instr in = q[i];
-    const int buf = i & 1;
-    const uint32_t rpar = ((uint32_t)i >> 1) & 1u;
+    const Instr in = nxt;
+    if (i + 1 < n) nxt = load_instr(q + i + 1);
+    const int buf = i % kResBufs;
+    const uint32_t rpar = ((uint32_t)i / kResBufs) & 1u;
     uint64_t t_start = 0, t_ready = 0;
     const bool tracing = p.trace != nullptr && warp == 0 && lane == 0;
     if (tracing) t_start = globaltimer();
@@ -609,14 +800,12 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
       const int key = act_key(kind, in.layer, chunk);
       const bool to_h = kind == kActH;
       if ((to_h ? st.key_h : st.key_x) != key) stage(p, m, smem, st, kind, in.layer, chunk);
-      const Geom g = geom_of(in.op, p.H, p.QD, p.Fc, p.B);
+      const Geom g = geom_of(in.op, p.H, p.QD, p.Fc);
       const float* act = reinterpret_cast<const float*>(smem + (to_h ? p.off_h : p.off_x));
-      const LayerPtrs& L = p.layers[in.layer];
-      const uint16_t* normw = kind == kActAttnNorm ? L.attn_norm
-                              : kind == kActMlpNorm ? L.mlp_norm
-                              : kind == kActFinalNorm ? p.final_norm
-                                                      : nullptr;
-      gemv_run<B>(p, m, smem, in, g, act, normw, st.inv, res, page_cnt);
+      InvScale one;
+#pragma unroll
+      for (int b = 0; b < kMaxBatch; ++b) one.v[b] = 1.f;
+      gemv_run<B>(p, m, smem, in, g, act, to_h ? one : st.inv_x, res, page_cnt);
       page_cnt += (uint32_t)((in.a1 - in.a0 + g.ipp - 1) / g.ipp);
     } else if (in.op == MK_OP_ATTN) {
       st.key_x = -1;  // the staging area becomes scratch
@@ -638,15 +827,15 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
     if (tracing) {
       const int rec = p.trace_base + qbase + i;
       if (rec < p.trace_cap) {
-        mk_trace_record r;
-        r.sm = blockIdx.x;
-        r.index = (uint32_t)i;
-        r.op = in.op;
-        r.layer = in.layer;
-        r.t_start = t_start;
-        r.t_ready = t_ready;
-        r.t_end = globaltimer();
-        p.trace[rec] = r;
+        // field by field: the storer writes t_stored of the same record
+        mk_trace_record* r = p.trace + rec;
+        r->sm = blockIdx.x;
+        r->index = (uint32_t)i;
+        r->op = in.op;
+        r->layer = in.layer;
+        r->t_start = t_start;
+        r->t_ready = t_ready;
+        r->t_end = globaltimer();
       }
     }
   }
@@ -660,7 +849,7 @@ __device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
 
 __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const float* res) {
   const int lane = threadIdx.x & 31;
-  const Geom g = geom_of(in.op, p.H, p.QD, p.Fc, p.B);
+  const Geom g = geom_of(in.op, p.H, p.QD, p.Fc);
   const int items = in.a1 - in.a0;
   const int B = p.B;
   const LayerPtrs& L = p.layers[in.layer];
@@ -668,8 +857,7 @@ __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const
     const int j = in.a0 + it;
     for (int b = 0; b < B; ++b) {
       float v[2] = {0.f, 0.f};
-      for (int r = 0; r < g.R; ++r)
-        for (int s = 0; s < g.nseg; ++s) v[r] += res[((size_t)(it * g.R + r) * g.nseg + s) * B + b];
+      for (int r = 0; r < g.R; ++r) v[r] = res[((size_t)it * g.R + r) * B + b];
       switch (in.op) {
         case MK_OP_QKV: {
           const PairRows pr = pair_rows(j, p.G, p.D);
@@ -719,22 +907,32 @@ __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const
 
 __device__ void storer_role(const Params& p, Misc* m, uint8_t* smem, const Instr* q, int n) {
   const int lane = threadIdx.x & 31;
+  Instr nxt = n > 0 ? load_instr(q) : Instr{};
   for (int i = 0; i < n; ++i) {
-    const Instr in = q[i];
-    const int buf = i & 1;
-    const uint32_t par = ((uint32_t)i >> 1) & 1u;
+    const Instr in = nxt;
+    if (i + 1 < n) nxt = load_instr(q + i + 1);
+    const int buf = i % kResBufs;
+    const uint32_t par = ((uint32_t)i / kResBufs) & 1u;
     const bool ok = wait_mbar(p, m, &m->res_full[buf], par, kErrTimeoutRes);
     if (ok && !aborted(m)) {
       const float* res = reinterpret_cast<const float*>(smem + p.off_res) + (size_t)buf * p.res_floats;
       if (is_gemv(in.op)) epilogue(p, in, res);
       if (in.sig_ctr >= 0) {
-        __threadfence();
+        // the warp barrier orders the other lanes' stores (and, through the
+        // result mbarrier, the compute warps' stores) before lane 0's
+        // release-add, which publishes them at GPU scope
         __syncwarp();
         if (lane == 0) red_release_add(p.ctr + in.sig_ctr, in.sig_amount);
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&m->res_empty[buf]);
+    if (lane == 0) {
+      mbar_arrive(&m->res_empty[buf]);
+      if (p.trace) {
+        const int rec = p.trace_base + (int)(q - p.instrs) + i;
+        if (rec < p.trace_cap) p.trace[rec].t_stored = globaltimer();
+      }
+    }
   }
 }
 
@@ -749,9 +947,9 @@ __global__ void __launch_bounds__(kThreads, 1) interp_kernel(const __grid_consta
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.n_pages; ++i) {
       mbar_init(&m->full[i], 1);
-      mbar_init(&m->empty[i], kComputeWarps);
+      mbar_init(&m->empty[i], 1);  // the page's owner warp releases it
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kResBufs; ++i) {
       mbar_init(&m->res_full[i], kComputeWarps);
       mbar_init(&m->res_empty[i], 1);
     }

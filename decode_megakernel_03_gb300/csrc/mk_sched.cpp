@@ -26,7 +26,7 @@ std::string check_shape(const Shape& s) {
     std::snprintf(buf, sizeof buf, "unsupported configuration: %s", what);
     return std::string(buf);
   };
-  if (s.L < 1 || s.L > 255) return bad("n_layers must be in 1..255");
+  if (s.L < 1 || s.L > kMaxLayers) return bad("n_layers must be in 1..64");
   if (s.H < 256 || s.H % 256 || s.H > 4096) return bad("hidden must be a multiple of 256 in 256..4096");
   if (s.D != 64 && s.D != 128) return bad("head_dim must be 64 or 128");
   if (s.nh < 1 || s.nkv < 1 || s.nh % s.nkv) return bad("n_heads must be a multiple of n_kv_heads");

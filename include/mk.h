@@ -140,13 +140,16 @@ int mk_debug_inject_unsatisfiable_wait(mk_handle* h, int enable);
    buffer needs at least as many records as the schedule has instructions
    (mk_schedule_build reports that count). Records past `capacity` are dropped.
    Pass NULL to disable. The idle gap between two instructions of one SM is
-   t_start(next) - t_end(prev); the dependency stall is t_ready - t_start. */
+   t_start(next) - t_end(prev); the dependency stall is t_ready - t_start. The
+   storer fills t_stored after the compute warps' record, so read the buffer
+   only after the step has completed. */
 typedef struct {
   uint32_t sm, index;       /* SM and position in its queue */
   int32_t op, layer;        /* MK_OP_* and layer (-1 for the LM head) */
   uint64_t t_start;         /* compute warps start the instruction */
   uint64_t t_ready;         /* its counter wait (if any) is satisfied */
   uint64_t t_end;           /* compute warps finish it */
+  uint64_t t_stored;        /* the storer has published it (counter bumped) */
 } mk_trace_record;
 int mk_set_trace(mk_handle* h, mk_trace_record* dev_buf, int capacity);
 
