@@ -269,7 +269,12 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
   int xh = p.alias_xh ? std::max(p.x_floats, p.h_floats) : p.x_floats + p.h_floats;
   xh = std::max(xh, att_scratch);
   xh = (xh + 3) / 4 * 4;
-  const int fixed = xh * 4 + kResBufs * p.res_floats * 4 + ((misc_bytes() + 127) / 128) * 128;
+  // every SM's down-projection rows form one contiguous range of at most
+  // ceil(H / n_sm) rows, so row j can keep its chunk sum at slot j % dacc_rows
+  p.dacc_rows = (s.H + h->n_sm - 1) / h->n_sm;
+  const int dacc_bytes = (p.dacc_rows * B * 4 + 15) / 16 * 16;
+  const int fixed = xh * 4 + kResBufs * p.res_floats * 4 + dacc_bytes +
+                    ((misc_bytes() + 127) / 128) * 128;
   // A page slot is always owned by compute warp (slot % kComputeWarps): with
   // the slot count a multiple of the warp count, page k and page k + n_pages
   // (same slot) have the same owner, which consumes them in order, so no warp
@@ -282,7 +287,8 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
   p.off_x = n_pages * kPageBytes;
   p.off_h = p.alias_xh ? p.off_x : p.off_x + p.x_floats * 4;
   p.off_res = p.off_x + xh * 4;
-  p.off_misc = p.off_res + kResBufs * p.res_floats * 4;
+  p.off_dacc = p.off_res + kResBufs * p.res_floats * 4;
+  p.off_misc = p.off_dacc + dacc_bytes;
   p.off_misc = (p.off_misc + 127) / 128 * 128;
   h->smem_bytes = p.off_misc + misc_bytes();
 

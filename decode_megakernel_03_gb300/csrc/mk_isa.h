@@ -81,6 +81,7 @@ struct Params {
   // shared-memory layout (bytes from the dynamic smem base)
   int n_pages;
   int off_x, off_h, off_res, off_misc;
+  int off_dacc, dacc_rows;     // down-projection chunk sums, row j at slot j % dacc_rows
   int x_floats, h_floats, res_floats;
   int alias_xh;                // x and h staging share one buffer
   // per step

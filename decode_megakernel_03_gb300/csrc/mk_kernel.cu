@@ -356,6 +356,29 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
   }
 }
 
+// One sequence, rows of at most 2048 columns: each compute warp copies the
+// staged vector into registers in the layout of the page dot products (lane
+// l, block j: columns j*256 + l*8 .. +8), scaled by 1/rms for the norms.
+__device__ __forceinline__ void load_regs(float (&a)[64], const float* act, float scale, int K) {
+  const int lane = threadIdx.x & 31;
+  const int nblk = K / 256;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j < nblk) {
+      const float* src = act + j * 256 + lane * 8;
+      const float4 x0 = *reinterpret_cast<const float4*>(src);
+      const float4 x1 = *reinterpret_cast<const float4*>(src + 4);
+      a[j * 8 + 0] = x0.x * scale; a[j * 8 + 1] = x0.y * scale;
+      a[j * 8 + 2] = x0.z * scale; a[j * 8 + 3] = x0.w * scale;
+      a[j * 8 + 4] = x1.x * scale; a[j * 8 + 5] = x1.y * scale;
+      a[j * 8 + 6] = x1.z * scale; a[j * 8 + 7] = x1.w * scale;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) a[j * 8 + e] = 0.f;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // compute role: GEMV pages
 // ---------------------------------------------------------------------------
@@ -473,18 +496,17 @@ __device__ __forceinline__ void page_rows_smem(const uint8_t* page, int n_rows, 
   }
 }
 
-template <int B>
+// kRegs: the activations are in the caller's registers a[] (B == 1, rows of at
+// most 2048 columns); otherwise they are read from the staged buffer `act`.
+template <int B, bool kRegs>
 __device__ __forceinline__ void gemv_run(const Params& p, Misc* m, uint8_t* smem, const Instr& in,
                                          const Geom& g, const float* act, const InvScale& inv,
-                                         float* res, uint32_t page_base) {
+                                         const float (&a)[64], float* res, uint32_t page_base) {
   const int warp = compute_warp(), lane = threadIdx.x & 31;
   const int items = in.a1 - in.a0;
   const int npages = (items + g.ipp - 1) / g.ipp;
   const int row_bytes = g.K * 2;
   const int nblk = g.K / 256;
-  const bool in_regs = B == 1 && nblk <= 8;
-  float a[64];
-  bool loaded = false;
   // the pages of this warp: global page index congruent to the warp index.
   // n_pages is a multiple of kComputeWarps, so every slot this warp waits on
   // was last used by this warp's own previous page (already consumed): the
@@ -503,25 +525,7 @@ __device__ __forceinline__ void gemv_run(const Params& p, Misc* m, uint8_t* smem
       // goes to res[((item * R) + r) * B + b]
       const int n_rows = n_in * g.R;
       float* const res_page = res + (size_t)(pg * g.ipp) * g.R * B;
-      if (in_regs) {
-        if (!loaded) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (j < nblk) {
-              const float* src = act + j * 256 + lane * 8;
-              const float4 x0 = *reinterpret_cast<const float4*>(src);
-              const float4 x1 = *reinterpret_cast<const float4*>(src + 4);
-              const float s = inv.v[0];
-              a[j * 8 + 0] = x0.x * s; a[j * 8 + 1] = x0.y * s; a[j * 8 + 2] = x0.z * s;
-              a[j * 8 + 3] = x0.w * s; a[j * 8 + 4] = x1.x * s; a[j * 8 + 5] = x1.y * s;
-              a[j * 8 + 6] = x1.z * s; a[j * 8 + 7] = x1.w * s;
-            } else {
-#pragma unroll
-              for (int e = 0; e < 8; ++e) a[j * 8 + e] = 0.f;
-            }
-          }
-          loaded = true;
-        }
+      if (kRegs) {
         if (nblk == 8 && n_rows == 4) {
           // the common full page of 2048-column rows: 4 items (R = 1) or 2
           // pairs (R = 2), no division on this path
@@ -770,6 +774,9 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
                              int qbase) {
   const int warp = compute_warp(), lane = threadIdx.x & 31;
   Staged st;
+  // per-warp activation registers (one sequence, rows <= 2048 columns),
+  // reloaded from the staged smem vector at every instruction
+  float ax[64];
   uint32_t page_cnt = 0;
   int known_ctr = -1, known_tgt = 0;
   Instr nxt = n > 0 ? load_instr(q) : Instr{};
@@ -792,6 +799,8 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
     if (tracing) t_ready = globaltimer();
     // 2. the result buffer this instruction hands to the storer must be free
     const bool res_ok = wait_mbar(p, m, &m->res_empty[buf], rpar ^ 1u, kErrTimeoutRes);
+    const uint64_t t_res = tracing ? globaltimer() : 0;
+    uint64_t t_staged = t_res;
     float* res = reinterpret_cast<float*>(smem + p.off_res) + (size_t)buf * p.res_floats;
 
     if (is_gemv(in.op)) {
@@ -799,13 +808,21 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
       const int chunk = in.op == MK_OP_DOWN ? in.a2 : 0;
       const int key = act_key(kind, in.layer, chunk);
       const bool to_h = kind == kActH;
-      if ((to_h ? st.key_h : st.key_x) != key) stage(p, m, smem, st, kind, in.layer, chunk);
       const Geom g = geom_of(in.op, p.H, p.QD, p.Fc);
+      const bool regs = B == 1 && g.K <= 2048;
+      const bool norm = kind == kActAttnNorm || kind == kActMlpNorm || kind == kActFinalNorm;
+      if ((to_h ? st.key_h : st.key_x) != key) stage(p, m, smem, st, kind, in.layer, chunk);
+      if (tracing) t_staged = globaltimer();
       const float* act = reinterpret_cast<const float*>(smem + (to_h ? p.off_h : p.off_x));
       InvScale one;
 #pragma unroll
       for (int b = 0; b < kMaxBatch; ++b) one.v[b] = 1.f;
-      gemv_run<B>(p, m, smem, in, g, act, to_h ? one : st.inv_x, res, page_cnt);
+      if (regs) {
+        load_regs(ax, act, norm ? st.inv_x.v[0] : 1.f, g.K);
+        gemv_run<B, true>(p, m, smem, in, g, act, one, ax, res, page_cnt);
+      } else {
+        gemv_run<B, false>(p, m, smem, in, g, act, to_h ? one : st.inv_x, ax, res, page_cnt);
+      }
       page_cnt += (uint32_t)((in.a1 - in.a0 + g.ipp - 1) / g.ipp);
     } else if (in.op == MK_OP_ATTN) {
       st.key_x = -1;  // the staging area becomes scratch
@@ -836,6 +853,8 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
         r->t_start = t_start;
         r->t_ready = t_ready;
         r->t_end = globaltimer();
+        r->res_wait_ns = (uint32_t)(t_res - t_ready);
+        r->stage_ns = (uint32_t)(t_staged - t_res);
       }
     }
   }
@@ -847,7 +866,8 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
 
 __device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
 
-__device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const float* res) {
+__device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const float* res,
+                                         float* dacc) {
   const int lane = threadIdx.x & 31;
   const Geom g = geom_of(in.op, p.H, p.QD, p.Fc);
   const int items = in.a1 - in.a0;
@@ -891,8 +911,9 @@ __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const
           p.h[(size_t)b * p.F + j] = silu(v[0]) * v[1];
           break;
         case MK_OP_DOWN: {
-          float* acc = p.dacc + (size_t)b * p.H + j;
-          float d = in.a2 == 0 ? v[0] : __ldcg(acc) + v[0];
+          // the chunks of row j run on this SM in order; their sum stays in smem
+          float* acc = dacc + (size_t)(j % p.dacc_rows) * B + b;
+          const float d = in.a2 == 0 ? v[0] : *acc + v[0];
           if (in.a2 == kChunks - 1) p.x[(size_t)b * p.H + j] = __ldcg(p.xa + (size_t)b * p.H + j) + d;
           else *acc = d;
           break;
@@ -905,8 +926,13 @@ __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const
   }
 }
 
+// The storer drains finished instructions in order: epilogue, then lane 0
+// publishes the instruction with a release-add on its counter. (Publishing
+// several instructions behind one fence was measured slower: it delays the
+// first counter of each batch, which sits on the critical path.)
 __device__ void storer_role(const Params& p, Misc* m, uint8_t* smem, const Instr* q, int n) {
   const int lane = threadIdx.x & 31;
+  float* dacc = reinterpret_cast<float*>(smem + p.off_dacc);
   Instr nxt = n > 0 ? load_instr(q) : Instr{};
   for (int i = 0; i < n; ++i) {
     const Instr in = nxt;
@@ -916,7 +942,7 @@ __device__ void storer_role(const Params& p, Misc* m, uint8_t* smem, const Instr
     const bool ok = wait_mbar(p, m, &m->res_full[buf], par, kErrTimeoutRes);
     if (ok && !aborted(m)) {
       const float* res = reinterpret_cast<const float*>(smem + p.off_res) + (size_t)buf * p.res_floats;
-      if (is_gemv(in.op)) epilogue(p, in, res);
+      if (is_gemv(in.op)) epilogue(p, in, res, dacc);
       if (in.sig_ctr >= 0) {
         // the warp barrier orders the other lanes' stores (and, through the
         // result mbarrier, the compute warps' stores) before lane 0's

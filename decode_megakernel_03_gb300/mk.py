@@ -61,7 +61,7 @@ INSTR_DTYPE = np.dtype([("op", "<i2"), ("layer", "<i2"), ("a0", "<i4"), ("a1", "
                         ("sig_ctr", "<i4"), ("sig_amount", "<i4")])
 TRACE_DTYPE = np.dtype([("sm", "<u4"), ("index", "<u4"), ("op", "<i4"), ("layer", "<i4"),
                         ("t_start", "<u8"), ("t_ready", "<u8"), ("t_end", "<u8"),
-                        ("t_stored", "<u8")])
+                        ("t_stored", "<u8"), ("res_wait_ns", "<u4"), ("stage_ns", "<u4")])
 
 _lib = None
 
@@ -206,7 +206,7 @@ class Decoder:
         _check(lib().mk_debug_inject_unsatisfiable_wait(self.h, int(bool(enable))), self.h)
 
     def set_trace(self, buf=None):
-        """buf: a torch uint8 CUDA tensor of n * 48 bytes, or None to disable."""
+        """buf: a torch uint8 CUDA tensor of n * 56 bytes, or None to disable."""
         if buf is None:
             _check(lib().mk_set_trace(self.h, None, 0), self.h)
         else:

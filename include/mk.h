@@ -150,6 +150,8 @@ typedef struct {
   uint64_t t_ready;         /* its counter wait (if any) is satisfied */
   uint64_t t_end;           /* compute warps finish it */
   uint64_t t_stored;        /* the storer has published it (counter bumped) */
+  uint32_t res_wait_ns;     /* compute warp 0: waiting for a free result buffer */
+  uint32_t stage_ns;        /* compute warp 0: staging the activations */
 } mk_trace_record;
 int mk_set_trace(mk_handle* h, mk_trace_record* dev_buf, int capacity);
 
