@@ -22,7 +22,8 @@ OP_QKV, OP_ATTN, OP_RED, OP_OPROJ, OP_GATEUP, OP_DOWN, OP_LMHEAD = range(1, 8)
 # exported entry points (the C-ABI surface declared in include/mk.h)
 EXPORTS = ("mk_create", "mk_decode_step", "mk_decode_step_multilaunch", "mk_get_status",
            "mk_destroy", "mk_last_error", "mk_read_counters", "mk_set_timeout",
-           "mk_debug_inject_unsatisfiable_wait", "mk_set_trace", "mk_schedule_build")
+           "mk_debug_inject_unsatisfiable_wait", "mk_set_trace", "mk_schedule_build",
+           "mk_decode_step_noalloc")
 
 
 class MkError(RuntimeError):
@@ -90,6 +91,9 @@ def lib():
                                         ctypes.POINTER(MkInstr), ctypes.c_int,
                                         ctypes.POINTER(ctypes.c_int), i32p, i32p, ctypes.c_int,
                                         ctypes.POINTER(ctypes.c_int)]
+        L.mk_decode_step_noalloc.argtypes = [ctypes.POINTER(MkConfig), ctypes.POINTER(MkWeights),
+                                             _vpp, _vpp, i32p, i32p, vp, vp, ctypes.c_char_p,
+                                             ctypes.c_size_t]
         _lib = L
     return _lib
 
@@ -138,6 +142,39 @@ def _stream_ptr(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _model_structs(shape, weights: dict, k_cache: list, v_cache: list, batch: int):
+    """ctypes mk_config / mk_weights / cache pointer arrays for torch tensors;
+    the last element keeps the host arrays alive."""
+    L = shape.n_layers
+    arrs = {}
+    for name in ("attn_norm", "wq", "wk", "wv", "wo", "mlp_norm", "wgate", "wup", "wdown"):
+        arrs[name] = (ctypes.c_void_p * L)(*[t.data_ptr() for t in weights[name]])
+    lm = weights.get("lm_head")
+    w = MkWeights(weights["embed"].data_ptr(), lm.data_ptr() if lm is not None else None,
+                  weights["final_norm"].data_ptr(),
+                  *[ctypes.cast(arrs[n], _vpp) for n in ("attn_norm", "wq", "wk", "wv", "wo",
+                                                         "mlp_norm", "wgate", "wup", "wdown")])
+    kc = (ctypes.c_void_p * L)(*[t.data_ptr() for t in k_cache])
+    vc = (ctypes.c_void_p * L)(*[t.data_ptr() for t in v_cache])
+    cfg = make_config(shape, batch, int(k_cache[0].shape[2]))
+    return cfg, w, kc, vc, (arrs, weights, k_cache, v_cache)
+
+
+def decode_step_noalloc(shape, weights: dict, k_cache: list, v_cache: list, batch: int, tokens,
+                        positions, logits, stream=None):
+    """mk_decode_step_noalloc: one decode step with no handle and no device
+    allocation (scratch in the library's static device array). Synchronous.
+    Returns (status code, message)."""
+    cfg, w, kc, vc, keep = _model_structs(shape, weights, k_cache, v_cache, batch)
+    msg = ctypes.create_string_buffer(512)
+    rc = lib().mk_decode_step_noalloc(ctypes.byref(cfg), ctypes.byref(w), ctypes.cast(kc, _vpp),
+                                      ctypes.cast(vc, _vpp), _i32(tokens), _i32(positions),
+                                      ctypes.c_void_p(logits.data_ptr()), _stream_ptr(stream),
+                                      msg, len(msg))
+    del keep
+    return rc, msg.value.decode()
 
 
 class Decoder:

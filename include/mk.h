@@ -195,6 +195,44 @@ int mk_schedule_build(const mk_config* cfg, int n_sm, const int32_t* positions,
                       int32_t* sm_offsets, int32_t* targets, int counter_capacity,
                       int* n_counters);
 
+/* ---- decode step without any allocation -------------------------------- */
+
+/* The pages have no counterpart of this call; it exists for callers that may
+   not allocate device memory: code running inside a memory pool or arena that
+   owns every device byte, plugins whose host forbids device allocations after
+   start-up, serving paths that must not take the allocator's locks or risk an
+   allocation failure.
+
+   Runs the same decode step as mk_decode_step (same kernel, same schedule,
+   same results) without a handle. All scratch -- activations, attention
+   partials, counters, error word, RoPE table and instruction queues -- lives
+   in ONE file-scope device array of 16 MiB that the library reserves on every
+   GPU that loads it, until the process exits. The call performs no cudaMalloc,
+   cudaFree, pinned-memory or other device allocation (host-side schedule
+   building uses ordinary heap memory).
+
+   cfg, w, k_cache, v_cache: as for mk_create (host structs and host arrays of
+   device pointers; the caches are updated in place). token_ids, positions:
+   host arrays of cfg->batch, as for mk_decode_step. logits_out: device fp32
+   [batch][vocab]. stream: cudaStream_t as void*. errmsg / errmsg_cap: optional
+   host buffer for a description of a failure (may be NULL / 0).
+
+   The first call on a device resolves the array's device address
+   (cudaGetSymbolAddress) and the device attributes; make that first call
+   before any stream capture on the device.
+   The call is synchronous: it waits for the step on `stream` and returns
+   MK_ERR_TIMEOUT if a device wait expired.
+   Every call shares the array and leaves its contents behind; each call
+   clears the counters and the error word itself. Calls that overlap on the
+   GPU (several streams or host threads) race on the array: serialise them.
+   Errors: MK_ERR_INVALID (bad or unsupported arguments, or a configuration
+   whose scratch exceeds the 16 MiB array, reported with the size it needs),
+   MK_ERR_CUDA, MK_ERR_TIMEOUT. */
+int mk_decode_step_noalloc(const mk_config* cfg, const mk_weights* w,
+                           void* const* k_cache, void* const* v_cache,
+                           const int32_t* token_ids, const int32_t* positions,
+                           float* logits_out, void* stream, char* errmsg, size_t errmsg_cap);
+
 #ifdef __cplusplus
 }
 #endif
