@@ -273,15 +273,7 @@ def run_gpu(args, wl):
         cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"{n} decode steps of {wl.name} ({dt:.1f} s, all host threads)"}
 
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "dram_traffic.json")
-    if os.path.exists(prof):
-        try:
-            d = json.load(open(prof))
-            if d.get("workload") == wl.name and d.get("kernel_rev") == KERNEL_REV:
-                traffic = d.get("bytes_per_launch")
-        except Exception:
-            traffic = None
+    traffic = recorded_traffic(wl.name)
 
     if rank == 0:
         clocks = clk.summary()
@@ -331,7 +323,36 @@ def run_gpu(args, wl):
         dist.destroy_process_group()
 
 
-KERNEL_REV = "r1"
+def kernel_sources_sha1() -> str:
+    """Hash of the CUDA/C++ sources of the decode kernel (any change to them
+    invalidates DRAM counters captured earlier)."""
+    import hashlib
+    d = os.path.join(ROOT, "decode_megakernel_03_gb300", "csrc")
+    h = hashlib.sha1()
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload: str):
+    """dram__bytes_read.sum + dram__bytes_write.sum of one megakernel launch,
+    from the ncu summary in profiles/, or None if it was taken on other
+    kernel sources or another workload."""
+    path = os.path.join(ROOT, "profiles", f"megakernel_{workload}_dram.txt")
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    for line in open(path):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("kernel_sources_sha1") != kernel_sources_sha1():
+        return None
+    try:
+        return float(kv["dram_bytes_read_per_launch"]) + float(kv["dram_bytes_write_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 def main():
