@@ -55,7 +55,7 @@ __device__ __forceinline__ bool aborted(const Misc* m) {
   return *reinterpret_cast<const volatile int*>(&m->abort) != 0;
 }
 
-__device__ __noinline__ void raise_error(const Params& p, Misc* m, int code) {
+__device__ __forceinline__ void raise_error(const Params& p, Misc* m, int code) {
   if (atomicCAS(p.err, 0, code) == 0 && p.err_host)
     *reinterpret_cast<volatile int*>(p.err_host) = code;  // lets the host see it without a sync
   *reinterpret_cast<volatile int*>(&m->abort) = 1;
@@ -83,7 +83,7 @@ __device__ __forceinline__ bool wait_mbar(const Params& p, Misc* m, uint64_t* ba
 }
 
 // Bounded wait for counter >= target (acquire). One thread polls.
-__device__ __noinline__ bool wait_counter(const Params& p, Misc* m, int ctr, int target) {
+__device__ __forceinline__ bool wait_counter(const Params& p, Misc* m, int ctr, int target) {
   const int* a = p.ctr + ctr;
   if (ld_acquire(a) >= target) return true;
   const uint64_t t0 = globaltimer();
@@ -132,6 +132,10 @@ __device__ __forceinline__ Instr load_instr(const Instr* q) {
 struct RowSrc {
   const uint16_t* w[3];
   int op, G, D, H, QD, F;
+  // w[i] without a dynamically indexed array (which would live in local memory)
+  __device__ __forceinline__ const uint16_t* at(int i) const {
+    return i == 0 ? w[0] : (i == 1 ? w[1] : w[2]);
+  }
 };
 
 __device__ __forceinline__ RowSrc row_src_of(const Params& p, const Instr& in) {
@@ -178,7 +182,7 @@ __device__ __forceinline__ void issue_page(const Params& p, const Instr& in, con
       while (it < i1) {
         const PairRows pr = pair_rows(in.a0 + it, p.G, p.D);
         const int n = min(i1 - it, half - pr.i);
-        const uint16_t* src = rs.w[pr.which] + (size_t)(pr.head * p.D + pr.i + r * half) * p.H;
+        const uint16_t* src = rs.at(pr.which) + (size_t)(pr.head * p.D + pr.i + r * half) * p.H;
         bulk_g2s_hint(dst, src, row_bytes * (uint32_t)n, bar, pol);
         dst += row_bytes * (uint32_t)n;
         it += n;
@@ -189,7 +193,7 @@ __device__ __forceinline__ void issue_page(const Params& p, const Instr& in, con
   // OPROJ / GATEUP / DOWN / LMHEAD: row of item j = w[r] + j * stride
   const size_t stride = in.op == MK_OP_OPROJ ? (size_t)p.QD : (in.op == MK_OP_DOWN ? (size_t)p.F : (size_t)p.H);
   for (int r = 0; r < g.R; ++r) {
-    const uint16_t* src = rs.w[r] + (size_t)(in.a0 + i0) * stride;
+    const uint16_t* src = rs.at(r) + (size_t)(in.a0 + i0) * stride;
     if (stride * 2 == row_bytes) {  // whole rows: one contiguous run
       bulk_g2s_hint(dst, src, row_bytes * (uint32_t)(i1 - i0), bar, pol);
       dst += row_bytes * (uint32_t)(i1 - i0);
@@ -398,12 +402,13 @@ __device__ __forceinline__ void warp_sum4(float (&v)[4]) {
   }
 }
 
-// B == 1, K <= 2048: activations a[j*8 + e] in registers. NR rows of the
-// page starting at `rows` (NR <= 4); row q's result goes to out[q * stride]
-// ... or to outq[q] when given per-row destinations.
+// B == 1, K <= 2048: activations a[j*8 + e] in registers. Rows 0..n_rows-1
+// (n_rows <= 4) of the page starting at `rows`; lane q < n_rows stores row
+// q's result to *dst (every lane passes its own row's destination, so no
+// array of pointers is needed).
 template <int NB>
 __device__ __forceinline__ void rows4_reg(const uint8_t* rows, int n_rows, int row_bytes,
-                                          int nblk, const float (&a)[64], float* const (&dst)[4],
+                                          int nblk, const float (&a)[64], float* dst,
                                           int lane) {
   float acc[4][2];
 #pragma unroll
@@ -439,7 +444,7 @@ __device__ __forceinline__ void rows4_reg(const uint8_t* rows, int n_rows, int r
     float mine = v[0];
 #pragma unroll
     for (int q = 1; q < 4; ++q) mine = lane == q ? v[q] : mine;
-    *dst[lane] = mine;
+    *dst = mine;
   }
 }
 
@@ -529,23 +534,15 @@ __device__ __forceinline__ void gemv_run(const Params& p, Misc* m, uint8_t* smem
         if (nblk == 8 && n_rows == 4) {
           // the common full page of 2048-column rows: 4 items (R = 1) or 2
           // pairs (R = 2), no division on this path
-          float* dst[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int r = g.R == 1 ? 0 : (q >> 1), k = g.R == 1 ? q : (q & 1);
-            dst[q] = res_page + ((size_t)k * g.R + r) * B;
-          }
-          rows4_reg<8>(page, 4, row_bytes, 8, a, dst, lane);
+          const int q = lane & 3;
+          const int r = g.R == 1 ? 0 : (q >> 1), k = g.R == 1 ? q : (q & 1);
+          rows4_reg<8>(page, 4, row_bytes, 8, a, res_page + ((size_t)k * g.R + r) * B, lane);
         } else {
           for (int r0 = 0; r0 < n_rows; r0 += 4) {
-            float* dst[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int pr = min(r0 + q, n_rows - 1);
-              const int r = pr / n_in, k = pr - r * n_in;
-              dst[q] = res_page + ((size_t)k * g.R + r) * B;
-            }
-            rows4_reg<0>(page + (size_t)r0 * row_bytes, n_rows - r0, row_bytes, nblk, a, dst, lane);
+            const int pr = min(r0 + (lane & 3), n_rows - 1);
+            const int r = pr / n_in, k = pr - r * n_in;
+            rows4_reg<0>(page + (size_t)r0 * row_bytes, n_rows - r0, row_bytes, nblk, a,
+                         res_page + ((size_t)k * g.R + r) * B, lane);
           }
         }
       } else {

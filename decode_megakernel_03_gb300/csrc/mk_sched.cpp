@@ -165,7 +165,10 @@ struct Builder {
       });
       steps.push_back(std::move(st));
     }
-    // 5-6. gate/up chunk c, then down chunk c-1
+    // 5-6. the four gate/up chunks, then the four down chunks: down chunk c
+    // waits only for gate/up chunk c (its own counter), which every SM
+    // finished several instructions earlier, so the down-projection rarely
+    // waits and its weights keep streaming
     auto gateup = [&](int c) {
       Step st{MK_OP_GATEUP, l, {}};
       spread(Fc, 0, rot_of(l, 2 + c), [&](int sm, int a, int b) {
@@ -184,12 +187,8 @@ struct Builder {
       });
       steps.push_back(std::move(st));
     };
-    gateup(0);
-    for (int c = 1; c < kChunks; ++c) {
-      gateup(c);
-      down(c - 1);
-    }
-    down(kChunks - 1);
+    for (int c = 0; c < kChunks; ++c) gateup(c);
+    for (int c = 0; c < kChunks; ++c) down(c);
   }
 
   void add_lm_head() {

@@ -280,13 +280,13 @@ def test_no_unordered_hazards(case):
 
 def test_chunked_down_waits_only_for_its_chunk():
     # the down-projection of chunk c waits for chunk c of h, not for the whole
-    # hidden state, and sits after the gate/up of chunk c+1 on every SM
+    # hidden state; every SM runs the four gate/up chunks before the down chunks
     ins, off, tg, sm = _plan(synth.LLAMA_1B, 1, 640, 152, [512])
     for s in range(152):
         q = ins[off[s]:off[s + 1]]
         l0 = q[q["layer"] == 0]
         seq = [(int(r["op"]), int(r["a2"])) for r in l0 if r["op"] in (mk.OP_GATEUP, mk.OP_DOWN)]
-        assert seq == [(5, 0), (5, 1), (6, 0), (5, 2), (6, 1), (5, 3), (6, 2), (6, 3)], seq
+        assert seq == [(5, 0), (5, 1), (5, 2), (5, 3), (6, 0), (6, 1), (6, 2), (6, 3)], seq
     dn = ins[ins["op"] == mk.OP_DOWN]
     gu = ins[ins["op"] == mk.OP_GATEUP]
     for c in range(4):
