@@ -305,30 +305,50 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
   const uint16_t* normw = norm_weight(p, kind, layer);
   const int par = st.stage_cnt & 1;
   compute_bar();  // everyone is done reading the buffer's previous contents
+  // every thread issues all of its loads of a pass before using any, so a
+  // pass costs one round trip to L2 (a 2048-wide vector is one pass)
+  constexpr int kU = 4;
+  constexpr int kPass = kComputeThreads * 4 * kU;  // columns per pass
   for (int b = 0; b < p.B; ++b) {
+    const bool from_embed = kind == kActAttnNorm && layer == 0;
+    const uint16_t* erow = p.embed + (size_t)p.tok[b] * p.H;
+    const float* src;
+    if (kind == kActAttnNorm || kind == kActFinalNorm) src = p.x + (size_t)b * p.H;
+    else if (kind == kActMlpNorm) src = p.xa + (size_t)b * p.H;
+    else if (kind == kActAttnOut) src = p.attn + (size_t)b * p.QD;
+    else src = p.h + (size_t)b * p.F + (size_t)chunk * p.Fc;
     float ss = 0.f;
-    for (int c = tid * 4; c < K; c += kComputeThreads * 4) {
-      float4 v;
-      if (kind == kActAttnNorm && layer == 0) {
-        const uint2 e = *reinterpret_cast<const uint2*>(p.embed + (size_t)p.tok[b] * p.H + c);
-        v = make_float4(bf_lo(e.x), bf_hi(e.x), bf_lo(e.y), bf_hi(e.y));
-      } else {
-        const float* src;
-        if (kind == kActAttnNorm || kind == kActFinalNorm) src = p.x + (size_t)b * p.H;
-        else if (kind == kActMlpNorm) src = p.xa + (size_t)b * p.H;
-        else if (kind == kActAttnOut) src = p.attn + (size_t)b * p.QD;
-        else src = p.h + (size_t)b * p.F + (size_t)chunk * p.Fc;
-        v = __ldcg(reinterpret_cast<const float4*>(src + c));
+    for (int c0 = tid * 4; c0 < K; c0 += kPass) {
+      float4 v[kU];
+      uint2 wv[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int c = c0 + u * kComputeThreads * 4;
+        if (c < K) {
+          if (from_embed) {
+            const uint2 e = *reinterpret_cast<const uint2*>(erow + c);
+            v[u] = make_float4(bf_lo(e.x), bf_hi(e.x), bf_lo(e.y), bf_hi(e.y));
+          } else {
+            v[u] = __ldcg(reinterpret_cast<const float4*>(src + c));
+          }
+          if (normw) wv[u] = __ldg(reinterpret_cast<const uint2*>(normw + c));
+        }
       }
-      ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-      if (normw) {
-        const uint2 wv = __ldg(reinterpret_cast<const uint2*>(normw + c));
-        v.x *= bf_lo(wv.x);
-        v.y *= bf_hi(wv.x);
-        v.z *= bf_lo(wv.y);
-        v.w *= bf_hi(wv.y);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int c = c0 + u * kComputeThreads * 4;
+        if (c < K) {
+          float4 x = v[u];
+          ss += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+          if (normw) {
+            x.x *= bf_lo(wv[u].x);
+            x.y *= bf_hi(wv[u].x);
+            x.z *= bf_lo(wv[u].y);
+            x.w *= bf_hi(wv[u].y);
+          }
+          *reinterpret_cast<float4*>(dst + (size_t)b * K + c) = x;
+        }
       }
-      *reinterpret_cast<float4*>(dst + (size_t)b * K + c) = v;
     }
     if (normw) {
 #pragma unroll
@@ -863,28 +883,85 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
 
 __device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
 
+// What an epilogue reads from global memory, loaded by the storer while the
+// compute warps still work on the instruction: the RoPE (cos, sin) of the
+// q/k/v pairs, and the residual rows of the o-projection and of the last
+// down-projection chunk. Lane l holds items l and l + 32 (at most 64 items).
+template <int B>
+struct EpiPre {
+  float2 v[2][B];
+};
+
+template <int B>
+__device__ __forceinline__ void epilogue_prefetch(const Params& p, Misc* m, const Instr& in,
+                                                  EpiPre<B>& pre) {
+  const int lane = threadIdx.x & 31;
+  const int items = in.a1 - in.a0;
+  const bool resid = in.op == MK_OP_OPROJ || (in.op == MK_OP_DOWN && in.a2 == kChunks - 1);
+  if (in.op == MK_OP_QKV) {
+    const int half = p.D / 2;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int it = lane + 32 * k;
+      if (it < items) {
+        const PairRows pr = pair_rows(in.a0 + it, p.G, p.D);
+        if (pr.which < 2) {
+#pragma unroll
+          for (int b = 0; b < B; ++b) pre.v[k][b] = __ldg(p.rope + (size_t)p.pos[b] * half + pr.i);
+        }
+      }
+    }
+  } else if (resid) {
+    const bool from_embed = in.op == MK_OP_OPROJ && in.layer == 0;
+    if (!from_embed && !p.no_waits && in.wait_ctr >= 0) {
+      // the residual rows were written by other SMs before the instruction's
+      // input counter completed: acquire that counter (the compute warps
+      // wait on it too) before reading them
+      bool ok = true;
+      if (lane == 0) ok = wait_counter(p, m, in.wait_ctr, in.wait_target);
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) return;
+    }
+    const float* src = in.op == MK_OP_DOWN ? p.xa : p.x;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int it = lane + 32 * k;
+      if (it < items) {
+        const int j = in.a0 + it;
+#pragma unroll
+        for (int b = 0; b < B; ++b)
+          pre.v[k][b].x = from_embed ? bf16f(p.embed[(size_t)p.tok[b] * p.H + j])
+                                     : __ldcg(src + (size_t)b * p.H + j);
+      }
+    }
+  }
+}
+
+template <int B>
 __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const float* res,
-                                         float* dacc) {
+                                         float* dacc, const EpiPre<B>& pre) {
   const int lane = threadIdx.x & 31;
   const Geom g = geom_of(in.op, p.H, p.QD, p.Fc);
   const int items = in.a1 - in.a0;
-  const int B = p.B;
   const LayerPtrs& L = p.layers[in.layer];
-  for (int it = lane; it < items; it += 32) {
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int it = lane + 32 * k;
+    if (it >= items) continue;
     const int j = in.a0 + it;
+#pragma unroll
     for (int b = 0; b < B; ++b) {
-      float v[2] = {0.f, 0.f};
-      for (int r = 0; r < g.R; ++r) v[r] = res[((size_t)it * g.R + r) * B + b];
+      const float v0 = res[((size_t)it * g.R) * B + b];
+      const float v1 = g.R == 2 ? res[((size_t)it * g.R + 1) * B + b] : 0.f;
       switch (in.op) {
         case MK_OP_QKV: {
           const PairRows pr = pair_rows(j, p.G, p.D);
           const int pos = p.pos[b];
           const int half = p.D / 2;
-          float o0 = v[0], o1 = v[1];
+          float o0 = v0, o1 = v1;
           if (pr.which < 2) {
-            const float2 cs = p.rope[(size_t)pos * half + pr.i];
-            o0 = v[0] * cs.x - v[1] * cs.y;
-            o1 = v[1] * cs.x + v[0] * cs.y;
+            const float2 cs = pre.v[k][b];
+            o0 = v0 * cs.x - v1 * cs.y;
+            o1 = v1 * cs.x + v0 * cs.y;
           }
           if (pr.which == 0) {
             float* qd = p.q + (size_t)b * p.QD + (size_t)pr.head * p.D + pr.i;
@@ -898,25 +975,22 @@ __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const
           }
           break;
         }
-        case MK_OP_OPROJ: {
-          const float base = in.layer == 0 ? bf16f(p.embed[(size_t)p.tok[b] * p.H + j])
-                                           : __ldcg(p.x + (size_t)b * p.H + j);
-          p.xa[(size_t)b * p.H + j] = base + v[0];
+        case MK_OP_OPROJ:
+          p.xa[(size_t)b * p.H + j] = pre.v[k][b].x + v0;
           break;
-        }
         case MK_OP_GATEUP:
-          p.h[(size_t)b * p.F + j] = silu(v[0]) * v[1];
+          p.h[(size_t)b * p.F + j] = silu(v0) * v1;
           break;
         case MK_OP_DOWN: {
           // the chunks of row j run on this SM in order; their sum stays in smem
           float* acc = dacc + (size_t)(j % p.dacc_rows) * B + b;
-          const float d = in.a2 == 0 ? v[0] : *acc + v[0];
-          if (in.a2 == kChunks - 1) p.x[(size_t)b * p.H + j] = __ldcg(p.xa + (size_t)b * p.H + j) + d;
+          const float d = in.a2 == 0 ? v0 : *acc + v0;
+          if (in.a2 == kChunks - 1) p.x[(size_t)b * p.H + j] = pre.v[k][b].x + d;
           else *acc = d;
           break;
         }
         default:  // MK_OP_LMHEAD
-          p.logits[(size_t)b * p.V + j] = v[0];
+          p.logits[(size_t)b * p.V + j] = v0;
           break;
       }
     }
@@ -924,9 +998,12 @@ __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const
 }
 
 // The storer drains finished instructions in order: epilogue, then lane 0
-// publishes the instruction with a release-add on its counter. (Publishing
-// several instructions behind one fence was measured slower: it delays the
-// first counter of each batch, which sits on the critical path.)
+// publishes the instruction with a release-add on its counter. What the
+// epilogue needs from global memory is fetched before waiting for the compute
+// warps, so the epilogue itself touches only registers and shared memory.
+// (Publishing several instructions behind one fence was measured slower: it
+// delays the first counter of each batch, which sits on the critical path.)
+template <int B>
 __device__ void storer_role(const Params& p, Misc* m, uint8_t* smem, const Instr* q, int n) {
   const int lane = threadIdx.x & 31;
   float* dacc = reinterpret_cast<float*>(smem + p.off_dacc);
@@ -936,10 +1013,12 @@ __device__ void storer_role(const Params& p, Misc* m, uint8_t* smem, const Instr
     if (i + 1 < n) nxt = load_instr(q + i + 1);
     const int buf = i % kResBufs;
     const uint32_t par = ((uint32_t)i / kResBufs) & 1u;
+    EpiPre<B> pre;
+    if (is_gemv(in.op) && !aborted(m)) epilogue_prefetch<B>(p, m, in, pre);
     const bool ok = wait_mbar(p, m, &m->res_full[buf], par, kErrTimeoutRes);
     if (ok && !aborted(m)) {
       const float* res = reinterpret_cast<const float*>(smem + p.off_res) + (size_t)buf * p.res_floats;
-      if (is_gemv(in.op)) epilogue(p, in, res, dacc);
+      if (is_gemv(in.op)) epilogue<B>(p, in, res, dacc, pre);
       if (in.sig_ctr >= 0) {
         // the warp barrier orders the other lanes' stores (and, through the
         // result mbarrier, the compute warps' stores) before lane 0's
@@ -990,7 +1069,7 @@ __global__ void __launch_bounds__(kThreads, 1) interp_kernel(const __grid_consta
   const Instr* q = p.instrs + q0;
   const int warp = threadIdx.x >> 5;
   if (warp == kLoaderWarp) loader_role(p, m, smem, q, n);
-  else if (warp == kStorerWarp) storer_role(p, m, smem, q, n);
+  else if (warp == kStorerWarp) storer_role<B>(p, m, smem, q, n);
   else compute_role<B>(p, m, smem, q, n, q0);
 }
 
