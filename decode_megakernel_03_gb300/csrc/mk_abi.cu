@@ -257,40 +257,14 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
     ce = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device);
   if (ce != cudaSuccess) return cuda_fail(nullptr, ce, "cudaDeviceGetAttribute");
 
-  // ---- shared-memory layout: pages | x staging | h staging | results | misc
+  // ---- shared-memory layout
   const int B = s.B;
-  const int item_cap = item_cap_for(s);
   Params& p = h->base;
-  p.x_floats = B * std::max(s.H, s.QD());
-  p.h_floats = B * s.Fc();
-  p.alias_xh = B > 1 ? 1 : 0;
-  p.res_floats = item_cap * 2 * B;
-  int att_scratch = kComputeWarps * s.G() * (s.D + 2);
-  int xh = p.alias_xh ? std::max(p.x_floats, p.h_floats) : p.x_floats + p.h_floats;
-  xh = std::max(xh, att_scratch);
-  xh = (xh + 3) / 4 * 4;
-  // every SM's down-projection rows form one contiguous range of at most
-  // ceil(H / n_sm) rows, so row j can keep its chunk sum at slot j % dacc_rows
-  p.dacc_rows = (s.H + h->n_sm - 1) / h->n_sm;
-  const int dacc_bytes = (p.dacc_rows * B * 4 + 15) / 16 * 16;
-  const int fixed = xh * 4 + kResBufs * p.res_floats * 4 + dacc_bytes +
-                    ((misc_bytes() + 127) / 128) * 128;
-  // A page slot is always owned by compute warp (slot % kComputeWarps): with
-  // the slot count a multiple of the warp count, page k and page k + n_pages
-  // (same slot) have the same owner, which consumes them in order, so no warp
-  // can wait on a slot two mbarrier phases ahead of its contents.
-  int n_pages = std::min(kMaxPages, (optin - fixed) / kPageBytes);
-  n_pages -= n_pages % kComputeWarps;
-  if (n_pages < kComputeWarps)
-    return fail(nullptr, MK_ERR_INVALID, "configuration leaves too few shared-memory pages");
-  p.n_pages = n_pages;
-  p.off_x = n_pages * kPageBytes;
-  p.off_h = p.alias_xh ? p.off_x : p.off_x + p.x_floats * 4;
-  p.off_res = p.off_x + xh * 4;
-  p.off_dacc = p.off_res + kResBufs * p.res_floats * 4;
-  p.off_misc = p.off_dacc + dacc_bytes;
-  p.off_misc = (p.off_misc + 127) / 128 * 128;
-  h->smem_bytes = p.off_misc + misc_bytes();
+  {
+    std::string why;
+    h->smem_bytes = smem_layout(s, h->n_sm, optin, misc_bytes(), &p, &why);
+    if (!h->smem_bytes) return fail(nullptr, MK_ERR_INVALID, why);
+  }
 
   // ---- model constants
   p.L = s.L; p.H = s.H; p.nh = s.nh; p.nkv = s.nkv; p.D = s.D; p.F = s.F; p.V = s.V;

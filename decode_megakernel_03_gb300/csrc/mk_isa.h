@@ -84,6 +84,8 @@ struct Params {
   int off_dacc, dacc_rows;     // down-projection chunk sums, row j at slot j % dacc_rows
   int x_floats, h_floats, res_floats;
   int alias_xh;                // x and h staging share one buffer
+  int h_ring;                  // one sequence: the loader fetches each down-projection
+                               // chunk of h into one of two h slots (at off_h)
   // per step
   int tok[kMaxBatch];
   int pos[kMaxBatch];

@@ -35,6 +35,8 @@ struct Misc {
   uint64_t empty[kMaxPages];
   uint64_t res_full[kResBufs];
   uint64_t res_empty[kResBufs];
+  uint64_t hfull[2];   // h ring: the loader's copy of a down-projection chunk landed
+  uint64_t hempty[2];  // h ring: every compute warp has read the slot
   float red[2][kComputeWarps][kMaxBatch];  // RMSNorm partial sums, double-buffered
   int abort;
 };
@@ -214,12 +216,33 @@ __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, const Instr
   uint32_t page_cnt = 0;  // pages issued
   int slot = 0;           // page_cnt % n_pages
   uint32_t round = 0;     // page_cnt / n_pages
+  uint32_t h_cnt = 0;     // h chunks copied into the h ring
   bool ok = true;
   Instr nxt = n > 0 ? load_instr(q) : Instr{};
   for (int i = 0; i < n && ok; ++i) {
     const Instr in = nxt;
     if (i + 1 < n) nxt = load_instr(q + i + 1);
     if (!is_gemv(in.op)) continue;
+    if (p.h_ring && in.op == MK_OP_DOWN) {
+      // one sequence: fetch the chunk of h this down-projection reads into the
+      // next h slot, once its counter says gate/up chunk a2 is complete. In
+      // the queue the down chunks follow all four gate/up chunks, so the wait
+      // is short, and it sits before weight pages that are not needed yet.
+      const int k = (int)(h_cnt & 1u);
+      if (!wait_mbar(p, m, &m->hempty[k], ((h_cnt >> 1) & 1u) ^ 1u, kErrTimeoutRes)) {
+        ok = false;
+        break;
+      }
+      if (!p.no_waits && in.wait_ctr >= 0 && !wait_counter(p, m, in.wait_ctr, in.wait_target)) {
+        ok = false;
+        break;
+      }
+      fence_proxy_async_global();  // the acquire above, then the bulk copy's reads
+      const uint32_t bytes = (uint32_t)p.Fc * 4u;
+      mbar_arrive_expect_tx(&m->hfull[k], bytes);
+      bulk_g2s(smem + p.off_h + (size_t)k * bytes, p.h + (size_t)in.a2 * p.Fc, bytes, &m->hfull[k]);
+      ++h_cnt;
+    }
     const Geom g = geom_of(in.op, p.H, p.QD, p.Fc);
     const int items = in.a1 - in.a0;
     const uint32_t row_bytes = (uint32_t)g.K * 2u;
@@ -241,6 +264,12 @@ __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, const Instr
   }
   if (!ok) {
     // drain: every issued copy must land before the CTA's shared memory goes away
+    for (uint32_t k = h_cnt > 2u ? h_cnt - 2u : 0u; k < h_cnt; ++k) {
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(&m->hfull[k & 1u], (k >> 1) & 1u)) {
+        if (globaltimer() - t0 > p.timeout_ns) break;
+      }
+    }
     const uint32_t first = page_cnt > (uint32_t)p.n_pages ? page_cnt - p.n_pages : 0u;
     for (uint32_t k = first; k < page_cnt; ++k) {
       const int sl = (int)(k % (uint32_t)p.n_pages);
@@ -795,6 +824,7 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
   // reloaded from the staged smem vector at every instruction
   float ax[64];
   uint32_t page_cnt = 0;
+  uint32_t h_cnt = 0;  // down-projection chunks taken from the h ring
   int known_ctr = -1, known_tgt = 0;
   Instr nxt = n > 0 ? load_instr(q) : Instr{};
   for (int i = 0; i < n; ++i) {
@@ -805,8 +835,10 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
     uint64_t t_start = 0, t_ready = 0;
     const bool tracing = p.trace != nullptr && warp == 0 && lane == 0;
     if (tracing) t_start = globaltimer();
+    // the loader fetched this down-projection chunk of h (after its counter)
+    const bool from_ring = p.h_ring && in.op == MK_OP_DOWN;
     // 1. dependency: one thread polls, the other compute warps meet it at a barrier
-    if (!p.no_waits && in.wait_ctr >= 0 &&
+    if (!from_ring && !p.no_waits && in.wait_ctr >= 0 &&
         !(in.wait_ctr == known_ctr && in.wait_target <= known_tgt)) {
       if (warp == 0 && lane == 0) wait_counter(p, m, in.wait_ctr, in.wait_target);
       compute_bar();
@@ -828,14 +860,26 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
       const Geom g = geom_of(in.op, p.H, p.QD, p.Fc);
       const bool regs = B == 1 && g.K <= 2048;
       const bool norm = kind == kActAttnNorm || kind == kActMlpNorm || kind == kActFinalNorm;
-      if ((to_h ? st.key_h : st.key_x) != key) stage(p, m, smem, st, kind, in.layer, chunk);
+      const float* act;
+      if (from_ring) {
+        const int k = (int)(h_cnt & 1u);
+        wait_mbar(p, m, &m->hfull[k], (h_cnt >> 1) & 1u, kErrTimeoutRes);
+        act = reinterpret_cast<const float*>(smem + p.off_h) + (size_t)k * p.Fc;
+      } else {
+        if ((to_h ? st.key_h : st.key_x) != key) stage(p, m, smem, st, kind, in.layer, chunk);
+        act = reinterpret_cast<const float*>(smem + (to_h ? p.off_h : p.off_x));
+      }
       if (tracing) t_staged = globaltimer();
-      const float* act = reinterpret_cast<const float*>(smem + (to_h ? p.off_h : p.off_x));
       InvScale one;
 #pragma unroll
       for (int b = 0; b < kMaxBatch; ++b) one.v[b] = 1.f;
       if (regs) {
         load_regs(ax, act, norm ? st.inv_x.v[0] : 1.f, g.K);
+        if (from_ring) {  // the slot is in registers now
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&m->hempty[h_cnt & 1u]);
+          ++h_cnt;
+        }
         gemv_run<B, true>(p, m, smem, in, g, act, one, ax, res, page_cnt);
       } else {
         gemv_run<B, false>(p, m, smem, in, g, act, to_h ? one : st.inv_x, ax, res, page_cnt);
@@ -1054,6 +1098,10 @@ __global__ void __launch_bounds__(kThreads, 1) interp_kernel(const __grid_consta
     for (int i = 0; i < kResBufs; ++i) {
       mbar_init(&m->res_full[i], kComputeWarps);
       mbar_init(&m->res_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&m->hfull[i], 1);               // the loader's expect-tx arrival
+      mbar_init(&m->hempty[i], kComputeWarps);  // every compute warp
     }
     m->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");

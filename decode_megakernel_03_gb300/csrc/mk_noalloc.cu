@@ -229,30 +229,9 @@ extern "C" int mk_decode_step_noalloc(const mk_config* cfg, const mk_weights* w,
     p.tok[b] = b < B ? token_ids[b] : 0;
     p.pos[b] = b < B ? positions[b] : 0;
   }
-  // shared-memory layout: pages | x staging | h staging | results | chunk sums | misc
-  const int item_cap = item_cap_for(s);
-  p.x_floats = B * std::max(s.H, s.QD());
-  p.h_floats = B * s.Fc();
-  p.alias_xh = B > 1 ? 1 : 0;
-  p.res_floats = item_cap * 2 * B;
-  int xh = p.alias_xh ? std::max(p.x_floats, p.h_floats) : p.x_floats + p.h_floats;
-  xh = std::max(xh, kComputeWarps * s.G() * (s.D + 2));
-  xh = (xh + 3) / 4 * 4;
-  p.dacc_rows = (s.H + ds->n_sm - 1) / ds->n_sm;
-  const int dacc_bytes = (p.dacc_rows * B * 4 + 15) / 16 * 16;
-  const int fixed = xh * 4 + kResBufs * p.res_floats * 4 + dacc_bytes +
-                    ((misc_bytes() + 127) / 128) * 128;
-  int n_pages = std::min(kMaxPages, (ds->optin - fixed) / kPageBytes);
-  n_pages -= n_pages % kComputeWarps;
-  if (n_pages < kComputeWarps)
-    return set_error(errmsg, errmsg_cap, "configuration leaves too few shared-memory pages");
-  p.n_pages = n_pages;
-  p.off_x = n_pages * kPageBytes;
-  p.off_h = p.alias_xh ? p.off_x : p.off_x + p.x_floats * 4;
-  p.off_res = p.off_x + xh * 4;
-  p.off_dacc = p.off_res + kResBufs * p.res_floats * 4;
-  p.off_misc = (p.off_dacc + dacc_bytes + 127) / 128 * 128;
-  const int smem_bytes = p.off_misc + misc_bytes();
+  // shared-memory layout (the same rules as mk_create)
+  const int smem_bytes = smem_layout(s, ds->n_sm, ds->optin, misc_bytes(), &p, &why);
+  if (!smem_bytes) return set_error(errmsg, errmsg_cap, why.c_str());
 
   // ---- uploads, clears, launch: no allocation anywhere below
   std::vector<float2> rope((size_t)s.S * (s.D / 2));

@@ -114,6 +114,12 @@ __device__ __forceinline__ int ld_volatile(const int* p) {
   return v;
 }
 
+// orders this thread's earlier generic-proxy accesses (an acquire) before its
+// later async-proxy accesses of global memory (a bulk copy)
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_acq_rel_gpu() {
   asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }

@@ -287,4 +287,55 @@ bool build_plan(const Shape& s, int n_sm, const int* parts, Plan* out, std::stri
   return true;
 }
 
+int smem_layout(const Shape& s, int n_sm, int optin, int misc_bytes, Params* p, std::string* why) {
+  // pages | x staging | h staging (one buffer, or two ring slots) | results |
+  // down-projection chunk sums | barriers; the attention scratch reuses the
+  // staging area
+  const int B = s.B;
+  p->x_floats = B * std::max(s.H, s.QD());
+  p->h_floats = B * s.Fc();
+  p->alias_xh = B > 1 ? 1 : 0;
+  p->res_floats = item_cap_for(s) * 2 * B;
+  // every SM's down-projection rows form one contiguous range of at most
+  // ceil(H / n_sm) rows, so row j can keep its chunk sum at slot j % dacc_rows
+  p->dacc_rows = (s.H + n_sm - 1) / n_sm;
+  const int dacc_bytes = (p->dacc_rows * B * 4 + 15) / 16 * 16;
+  const int att_scratch = kComputeWarps * s.G() * (s.D + 2);
+  auto staging_floats = [&](int ring) {
+    int xh = p->alias_xh ? std::max(p->x_floats, p->h_floats)
+                         : p->x_floats + (ring ? 2 : 1) * p->h_floats;
+    xh = std::max(xh, att_scratch);
+    return (xh + 3) / 4 * 4;
+  };
+  // A page slot is always owned by compute warp (slot % kComputeWarps): with
+  // the slot count a multiple of the warp count, page k and page k + n_pages
+  // (same slot) have the same owner, which consumes them in order, so no warp
+  // can wait on a slot two mbarrier phases ahead of its contents.
+  auto pages_for = [&](int ring) {
+    const int fixed = staging_floats(ring) * 4 + kResBufs * p->res_floats * 4 + dacc_bytes +
+                      ((misc_bytes + 127) / 128) * 128;
+    int n = std::min(kMaxPages, (optin - fixed) / kPageBytes);
+    return n - n % kComputeWarps;
+  };
+  // the h ring serves the one-sequence register path (chunks of at most 2048
+  // columns) and is used only when it costs no page; the attention scratch
+  // must stay inside the x part of the staging area, clear of the h slots
+  // (the loader may fill them while attention runs)
+  int ring = B == 1 && s.Fc() <= 2048 && att_scratch <= p->x_floats ? 1 : 0;
+  if (ring && pages_for(1) < pages_for(0)) ring = 0;
+  const int n_pages = pages_for(ring);
+  if (n_pages < kComputeWarps) {
+    if (why) *why = "configuration leaves too few shared-memory pages";
+    return 0;
+  }
+  p->h_ring = ring;
+  p->n_pages = n_pages;
+  p->off_x = n_pages * kPageBytes;
+  p->off_h = p->alias_xh ? p->off_x : p->off_x + p->x_floats * 4;
+  p->off_res = p->off_x + staging_floats(ring) * 4;
+  p->off_dacc = p->off_res + kResBufs * p->res_floats * 4;
+  p->off_misc = (p->off_dacc + dacc_bytes + 127) / 128 * 128;
+  return p->off_misc + misc_bytes;
+}
+
 }  // namespace mk

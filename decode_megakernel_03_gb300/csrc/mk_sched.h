@@ -65,4 +65,11 @@ int item_cap_for(const Shape& s);
 
 bool build_plan(const Shape& s, int n_sm, const int* parts, Plan* out, std::string* why);
 
+// Shared-memory layout of the interpreter for this shape: fills the n_pages,
+// off_*, *_floats, alias_xh, h_ring and dacc_rows fields of p and returns the
+// dynamic shared memory size in bytes, or 0 (with *why set) when fewer than
+// kComputeWarps pages fit in `optin` bytes. misc_bytes is the size of the
+// kernel's barrier block.
+int smem_layout(const Shape& s, int n_sm, int optin, int misc_bytes, Params* p, std::string* why);
+
 }  // namespace mk
