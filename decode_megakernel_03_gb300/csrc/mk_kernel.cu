@@ -459,9 +459,11 @@ template <int NB>
 __device__ __forceinline__ void rows4_reg(const uint8_t* rows, int n_rows, int row_bytes,
                                           int nblk, const float (&a)[64], float* dst,
                                           int lane) {
-  float acc[4][2];
+  // two accumulator chains per row, each a packed pair of fp32 lanes (even
+  // and odd columns), so one fma.rn.f32x2 covers two weights
+  unsigned long long acc[4][2];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) acc[q][0] = acc[q][1] = 0.f;
+  for (int q = 0; q < 4; ++q) acc[q][0] = acc[q][1] = 0ull;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     if (NB == 8 || j < nblk) {
@@ -473,21 +475,20 @@ __device__ __forceinline__ void rows4_reg(const uint8_t* rows, int n_rows, int r
                    : make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        float& c = acc[q][j & 1];
-        c = fmaf(bf_lo(w[q].x), a[j * 8 + 0], c);
-        c = fmaf(bf_hi(w[q].x), a[j * 8 + 1], c);
-        c = fmaf(bf_lo(w[q].y), a[j * 8 + 2], c);
-        c = fmaf(bf_hi(w[q].y), a[j * 8 + 3], c);
-        c = fmaf(bf_lo(w[q].z), a[j * 8 + 4], c);
-        c = fmaf(bf_hi(w[q].z), a[j * 8 + 5], c);
-        c = fmaf(bf_lo(w[q].w), a[j * 8 + 6], c);
-        c = fmaf(bf_hi(w[q].w), a[j * 8 + 7], c);
+        const uint32_t ws[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          ffma2(acc[q][j & 1], pack2(bf_lo(ws[e]), bf_hi(ws[e])),
+                pack2(a[j * 8 + 2 * e], a[j * 8 + 2 * e + 1]));
       }
     }
   }
   float v[4];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) v[q] = acc[q][0] + acc[q][1];
+  for (int q = 0; q < 4; ++q) {
+    const float2 x = unpack2(acc[q][0]), y = unpack2(acc[q][1]);
+    v[q] = (x.x + x.y) + (y.x + y.y);
+  }
   warp_sum4(v);
   if (lane < 4 && lane < n_rows) {
     float mine = v[0];

@@ -156,6 +156,25 @@ __device__ __forceinline__ float4 lds128f(const void* p) {
   return v;
 }
 
+// ---- packed two-lane fp32 arithmetic (sm_100 and later) --------------------
+// A float2 held in one 64-bit register pair; fma.rn.f32x2 performs two fp32
+// fused multiply-adds per instruction, each rounded like fmaf.
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 unpack2(unsigned long long v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return make_float2(lo, hi);
+}
+// acc = a * b + acc, lane by lane
+__device__ __forceinline__ void ffma2(unsigned long long& acc, unsigned long long a,
+                                      unsigned long long b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+
 // bf16 pair in a 32-bit word -> two floats (exact widening)
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
