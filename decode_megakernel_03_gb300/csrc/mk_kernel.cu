@@ -587,6 +587,15 @@ __device__ __forceinline__ void gemv_run(const Params& p, Misc* m, uint8_t* smem
           const int q = lane & 3;
           const int r = g.R == 1 ? 0 : (q >> 1), k = g.R == 1 ? q : (q & 1);
           rows4_reg<8>(page, 4, row_bytes, 8, a, res_page + ((size_t)k * g.R + r) * B, lane);
+        } else if (nblk == 8 && n_rows < 4) {
+          // the short last page of an instruction: the same full-page code
+          // dots all four row slots (the ones past n_rows hold an earlier
+          // page's rows, stay inside the slot and are never stored). The
+          // generic path below was measured far slower, and this page is
+          // usually the instruction's last to finish.
+          const int pr = min(lane & 3, n_rows - 1);
+          const int r = pr / n_in, k = pr - r * n_in;
+          rows4_reg<8>(page, n_rows, row_bytes, 8, a, res_page + ((size_t)k * g.R + r) * B, lane);
         } else {
           for (int r0 = 0; r0 < n_rows; r0 += 4) {
             const int pr = min(r0 + (lane & 3), n_rows - 1);
