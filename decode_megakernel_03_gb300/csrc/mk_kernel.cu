@@ -610,8 +610,10 @@ __device__ __forceinline__ void gemv_run(const Params& p, Misc* m, uint8_t* smem
                             inv, res_page + (size_t)r * B, g.R * B, lane);
       }
     }
+    // a page whose copy has not landed (after an abort) is never handed back,
+    // so the loader cannot start a second copy into a slot still being filled
     __syncwarp();
-    if (lane == 0) mbar_arrive(&m->empty[slot]);
+    if (lane == 0 && ok) mbar_arrive(&m->empty[slot]);
     slot += kComputeWarps;
     if (slot >= p.n_pages) {
       slot -= p.n_pages;
@@ -871,9 +873,10 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
       const bool regs = B == 1 && g.K <= 2048;
       const bool norm = kind == kActAttnNorm || kind == kActMlpNorm || kind == kActFinalNorm;
       const float* act;
+      bool h_got = false;
       if (from_ring) {
         const int k = (int)(h_cnt & 1u);
-        wait_mbar(p, m, &m->hfull[k], (h_cnt >> 1) & 1u, kErrTimeoutRes);
+        h_got = wait_mbar(p, m, &m->hfull[k], (h_cnt >> 1) & 1u, kErrTimeoutRes);
         act = reinterpret_cast<const float*>(smem + p.off_h) + (size_t)k * p.Fc;
       } else {
         if ((to_h ? st.key_h : st.key_x) != key) stage(p, m, smem, st, kind, in.layer, chunk);
@@ -885,9 +888,11 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
       for (int b = 0; b < kMaxBatch; ++b) one.v[b] = 1.f;
       if (regs) {
         load_regs(ax, act, norm ? st.inv_x.v[0] : 1.f, g.K);
-        if (from_ring) {  // the slot is in registers now
+        if (from_ring) {
+          // the slot is in registers now (a copy that has not landed, after an
+          // abort, keeps its slot: the loader must not start another into it)
           __syncwarp();
-          if (lane == 0) mbar_arrive(&m->hempty[h_cnt & 1u]);
+          if (lane == 0 && h_got) mbar_arrive(&m->hempty[h_cnt & 1u]);
           ++h_cnt;
         }
         gemv_run<B, true>(p, m, smem, in, g, act, one, ax, res, page_cnt);
