@@ -11,12 +11,9 @@
 #include <vector>
 
 #include "mk_isa.h"
+#include "mk_kernels.h"
 #include "mk_sched.h"
 
-namespace mk {
-const void* kernel_for_batch(int B);
-int misc_bytes();
-}  // namespace mk
 
 using namespace mk;
 
@@ -46,6 +43,7 @@ struct mk_handle {
   int device = 0;
   int n_sm = 0;
   int smem_bytes = 0;
+  const void* fn = nullptr;  // the interpreter instantiation this handle launches
   Params base{};          // launch parameters without the per-step fields
   void* d_scratch = nullptr;
   float2* d_rope = nullptr;
@@ -349,9 +347,10 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
     lp[l].kc = static_cast<uint16_t*>(k_cache[l]);
     lp[l].vc = static_cast<uint16_t*>(v_cache[l]);
   }
+  h->fn = kernel_for(B, s.D, s.G(), false);
   ce = cudaMemcpy(h->d_rope, rope.data(), sizeof(float2) * rope.size(), cudaMemcpyHostToDevice);
   if (ce == cudaSuccess)
-    ce = cudaFuncSetAttribute(kernel_for_batch(B), cudaFuncAttributeMaxDynamicSharedMemorySize,
+    ce = cudaFuncSetAttribute(h->fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               h->smem_bytes);
   if (ce != cudaSuccess) {
     cudaFree(h->d_scratch);
@@ -386,6 +385,15 @@ int mk_set_trace(mk_handle* h, mk_trace_record* buf, int capacity) {
   return MK_OK;
 }
 
+int mk_debug_use_generic_kernel(mk_handle* h, int enable) {
+  if (!h) return MK_ERR_INVALID;
+  const Shape& s = h->shape;
+  const void* fn = kernel_for(s.B, s.D, s.G(), enable != 0);
+  MK_CUDA(h, cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, h->smem_bytes));
+  h->fn = fn;
+  return MK_OK;
+}
+
 int mk_debug_inject_unsatisfiable_wait(mk_handle* h, int enable) {
   if (!h) return MK_ERR_INVALID;
   h->inject = enable ? 1 : 0;
@@ -409,7 +417,7 @@ int mk_decode_step(mk_handle* h, const int32_t* tok, const int32_t* pos, float* 
   p.no_waits = 0;
   p.trace_base = 0;
   void* args[] = {&p};
-  cudaError_t ce = cudaLaunchCooperativeKernel(kernel_for_batch(h->shape.B), dim3(h->n_sm),
+  cudaError_t ce = cudaLaunchCooperativeKernel(h->fn, dim3(h->n_sm),
                                                dim3(kThreads), args, (size_t)h->smem_bytes,
                                                static_cast<cudaStream_t>(stream));
   if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaLaunchCooperativeKernel");
@@ -433,7 +441,7 @@ int mk_decode_step_multilaunch(mk_handle* h, const int32_t* tok, const int32_t* 
   p.no_waits = 1;
   p.trace = nullptr;
   p.trace_cap = 0;
-  const void* fn = kernel_for_batch(h->shape.B);
+  const void* fn = h->fn;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t nph = e->plan.phases.size();
   std::vector<Params> ps(nph, p);

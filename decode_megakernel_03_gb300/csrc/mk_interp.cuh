@@ -1,0 +1,1152 @@
+// The decode interpreter: one persistent CTA per SM walks its pre-planned
+// instruction queue ("3 · L'interpréteur sur GPU", §3.2). Every instruction is
+// split over three warp roles that walk the same queue independently:
+//
+//   loader  (1 warp)   streams the instruction's bf16 weight rows into 16 KB
+//                      shared-memory pages with bulk asynchronous copies; it
+//                      waits only for free pages, never for counters, so the
+//                      next instruction's weights load while the current one
+//                      still waits or computes (§3.3, the page allocator);
+//   compute (6 warps)  waits for the instruction's input counter, stages the
+//                      activations, and runs the dot products / attention;
+//                      each page is handed back as soon as it has been read;
+//   storer  (1 warp)   applies the epilogue (RoPE + KV append, residual adds,
+//                      SiLU, chunk accumulation), writes the outputs, then
+//                      fences and bumps the output counter with release
+//                      semantics (§3.4, counters in global memory).
+//
+// The same kernel also serves the multi-launch comparison build: launched once
+// per (layer, instruction type) with counter waits switched off, kernel
+// boundaries order the work instead.
+//
+// Every wait (counter, page, result buffer) is bounded by a %globaltimer
+// deadline; on expiry the kernel records MK_ERR_TIMEOUT in the error word,
+// the other CTAs notice it and all of them drain their copies and return.
+//
+// The kernel is a template over the batch B and, optionally, the head
+// dimension DS and the q-heads per kv-head GS (0: read from the parameters
+// at run time). An interpreter that carries every attention variant is about
+// twice the size of one specialised to its model's shape, and the SM's
+// instruction cache cannot hold it: the code of the instructions that run
+// together (loader, staging, pages, attention, epilogues) must fit, or the
+// warps stall on instruction fetches that queue behind the weight stream.
+// This header is included by the translation units that instantiate it.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "mk_isa.h"
+#include "mk_ptx.cuh"
+
+namespace mk {
+
+struct Misc {
+  uint64_t full[kMaxPages];
+  uint64_t empty[kMaxPages];
+  uint64_t res_full[kResBufs];
+  uint64_t res_empty[kResBufs];
+  uint64_t hfull[2];   // h ring: the loader's copy of a down-projection chunk landed
+  uint64_t hempty[2];  // h ring: every compute warp has read the slot
+  float red[2][kComputeWarps][kMaxBatch];  // RMSNorm partial sums, double-buffered
+  int abort;
+};
+
+constexpr int kComputeThreads = kComputeWarps * 32;
+constexpr int kBarCompute = 1;
+
+// Index of this warp among the compute warps (all warps but loader and storer).
+__device__ __forceinline__ int compute_warp() {
+  const int w = threadIdx.x >> 5;
+  return w < kLoaderWarp ? w : (w < kStorerWarp ? w - 1 : w - 2);
+}
+__device__ __forceinline__ int compute_tid() { return compute_warp() * 32 + (threadIdx.x & 31); }
+
+__device__ __forceinline__ void compute_bar() { named_bar(kBarCompute, kComputeThreads); }
+
+__device__ __forceinline__ bool aborted(const Misc* m) {
+  return *reinterpret_cast<const volatile int*>(&m->abort) != 0;
+}
+
+__device__ __forceinline__ void raise_error(const Params& p, Misc* m, int code) {
+  if (atomicCAS(p.err, 0, code) == 0 && p.err_host)
+    *reinterpret_cast<volatile int*>(p.err_host) = code;  // lets the host see it without a sync
+  *reinterpret_cast<volatile int*>(&m->abort) = 1;
+}
+
+// Bounded mbarrier wait. Returns false (without waiting) once the CTA aborts.
+__device__ __forceinline__ bool wait_mbar(const Params& p, Misc* m, uint64_t* bar,
+                                          uint32_t parity, int code) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15) == 0) {
+      if (aborted(m)) return false;
+      if (ld_volatile(p.err) != 0) {
+        *reinterpret_cast<volatile int*>(&m->abort) = 1;
+        return false;
+      }
+      if (globaltimer() - t0 > p.timeout_ns) {
+        raise_error(p, m, code);
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait for counter >= target (acquire). One thread polls.
+__device__ __forceinline__ bool wait_counter(const Params& p, Misc* m, int ctr, int target) {
+  const int* a = p.ctr + ctr;
+  if (ld_acquire(a) >= target) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (ld_acquire(a) >= target) return true;
+    if ((it & 7) == 0) {
+      if (aborted(m)) return false;
+      if (ld_volatile(p.err) != 0) {
+        *reinterpret_cast<volatile int*>(&m->abort) = 1;
+        return false;
+      }
+      if (globaltimer() - t0 > p.timeout_ns) {
+        raise_error(p, m, kErrTimeoutCounter);
+        return false;
+      }
+    }
+  }
+}
+
+// Instruction descriptors are read-only for the whole launch: two 16-byte
+// loads through the non-coherent path. Every role fetches the next descriptor
+// while it works on the current one, so no role stalls on a dependent global
+// load at an instruction boundary.
+__device__ __forceinline__ Instr load_instr(const Instr* q) {
+  const uint4 a = __ldg(reinterpret_cast<const uint4*>(q));
+  const uint4 b = __ldg(reinterpret_cast<const uint4*>(q) + 1);
+  Instr in;
+  in.op = (int16_t)(a.x & 0xffffu);
+  in.layer = (int16_t)(a.x >> 16);
+  in.a0 = (int32_t)a.y;
+  in.a1 = (int32_t)a.z;
+  in.a2 = (int32_t)a.w;
+  in.wait_ctr = (int32_t)b.x;
+  in.wait_target = (int32_t)b.y;
+  in.sig_ctr = (int32_t)b.z;
+  in.sig_amount = (int32_t)b.w;
+  return in;
+}
+
+// ---------------------------------------------------------------------------
+// weight rows of a GEMV item
+// ---------------------------------------------------------------------------
+
+// The weight matrices of one instruction, read from the layer table once per
+// instruction so that per-row addresses are pure arithmetic.
+struct RowSrc {
+  const uint16_t* w[3];
+  int op, G, D, H, QD, F;
+  // w[i] without a dynamically indexed array (which would live in local memory)
+  __device__ __forceinline__ const uint16_t* at(int i) const {
+    return i == 0 ? w[0] : (i == 1 ? w[1] : w[2]);
+  }
+};
+
+__device__ __forceinline__ RowSrc row_src_of(const Params& p, const Instr& in) {
+  RowSrc s;
+  s.op = in.op;
+  s.G = p.G;
+  s.D = p.D;
+  s.H = p.H;
+  s.QD = p.QD;
+  s.F = p.F;
+  s.w[0] = s.w[1] = s.w[2] = nullptr;
+  if (in.op == MK_OP_LMHEAD) {
+    s.w[0] = p.lm;
+    return s;
+  }
+  const LayerPtrs* L = p.layers + in.layer;
+  switch (in.op) {
+    case MK_OP_QKV: s.w[0] = L->wq; s.w[1] = L->wk; s.w[2] = L->wv; break;
+    case MK_OP_OPROJ: s.w[0] = L->wo; break;
+    case MK_OP_GATEUP: s.w[0] = L->wgate; s.w[1] = L->wup; break;
+    default: s.w[0] = L->wdown + (size_t)in.a2 * p.Fc; break;  // MK_OP_DOWN: chunk a2
+  }
+  return s;
+}
+
+// ---------------------------------------------------------------------------
+// loader role
+// ---------------------------------------------------------------------------
+
+// Issues the bulk copies of one page: items [i0, i1) of the instruction, laid
+// out [row kind r][item]. Rows are affine in the item (row = base + item *
+// stride) except for q/k/v pairs, which are affine within one head; runs of
+// rows that follow each other in memory go out as one copy.
+__device__ __forceinline__ void issue_page(const Params& p, const Instr& in, const Geom& g,
+                                           const RowSrc& rs, int i0, int i1, uint8_t* dst,
+                                           uint64_t* bar, uint64_t pol) {
+  const uint32_t row_bytes = (uint32_t)g.K * 2u;
+  if (in.op == MK_OP_QKV) {
+    // pair j holds rows (head*D + i, head*D + i + D/2); consecutive pairs of one
+    // head are consecutive rows, so a page splits at most at head boundaries
+    const int half = p.D / 2;
+    for (int r = 0; r < 2; ++r) {
+      int it = i0;
+      while (it < i1) {
+        const PairRows pr = pair_rows(in.a0 + it, p.G, p.D);
+        const int n = min(i1 - it, half - pr.i);
+        const uint16_t* src = rs.at(pr.which) + (size_t)(pr.head * p.D + pr.i + r * half) * p.H;
+        bulk_g2s_hint(dst, src, row_bytes * (uint32_t)n, bar, pol);
+        dst += row_bytes * (uint32_t)n;
+        it += n;
+      }
+    }
+    return;
+  }
+  // OPROJ / GATEUP / DOWN / LMHEAD: row of item j = w[r] + j * stride
+  const size_t stride = in.op == MK_OP_OPROJ ? (size_t)p.QD : (in.op == MK_OP_DOWN ? (size_t)p.F : (size_t)p.H);
+  for (int r = 0; r < g.R; ++r) {
+    const uint16_t* src = rs.at(r) + (size_t)(in.a0 + i0) * stride;
+    if (stride * 2 == row_bytes) {  // whole rows: one contiguous run
+      bulk_g2s_hint(dst, src, row_bytes * (uint32_t)(i1 - i0), bar, pol);
+      dst += row_bytes * (uint32_t)(i1 - i0);
+    } else {  // row slices (down-projection chunks): one copy per row
+      for (int it = i0; it < i1; ++it) {
+        bulk_g2s_hint(dst, src, row_bytes, bar, pol);
+        dst += row_bytes;
+        src += stride;
+      }
+    }
+  }
+}
+
+static __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, const Instr* q, int n) {
+  const int lane = threadIdx.x & 31;
+  if (lane != 0) return;
+  const uint64_t pol = policy_evict_first();
+  uint32_t page_cnt = 0;  // pages issued
+  int slot = 0;           // page_cnt % n_pages
+  uint32_t round = 0;     // page_cnt / n_pages
+  uint32_t h_cnt = 0;     // h chunks copied into the h ring
+  bool ok = true;
+  Instr nxt = n > 0 ? load_instr(q) : Instr{};
+  for (int i = 0; i < n && ok; ++i) {
+    const Instr in = nxt;
+    if (i + 1 < n) nxt = load_instr(q + i + 1);
+    if (!is_gemv(in.op)) continue;
+    if (p.h_ring && in.op == MK_OP_DOWN) {
+      // one sequence: fetch the chunk of h this down-projection reads into the
+      // next h slot, once its counter says gate/up chunk a2 is complete. In
+      // the queue the down chunks follow all four gate/up chunks, so the wait
+      // is short, and it sits before weight pages that are not needed yet.
+      const int k = (int)(h_cnt & 1u);
+      if (!wait_mbar(p, m, &m->hempty[k], ((h_cnt >> 1) & 1u) ^ 1u, kErrTimeoutRes)) {
+        ok = false;
+        break;
+      }
+      if (!p.no_waits && in.wait_ctr >= 0 && !wait_counter(p, m, in.wait_ctr, in.wait_target)) {
+        ok = false;
+        break;
+      }
+      fence_proxy_async_global();  // the acquire above, then the bulk copy's reads
+      const uint32_t bytes = (uint32_t)p.Fc * 4u;
+      mbar_arrive_expect_tx(&m->hfull[k], bytes);
+      bulk_g2s(smem + p.off_h + (size_t)k * bytes, p.h + (size_t)in.a2 * p.Fc, bytes, &m->hfull[k]);
+      ++h_cnt;
+    }
+    const Geom g = geom_of(in.op, p.H, p.QD, p.Fc);
+    const int items = in.a1 - in.a0;
+    const uint32_t row_bytes = (uint32_t)g.K * 2u;
+    const RowSrc rs = row_src_of(p, in);
+    for (int i0 = 0; i0 < items; i0 += g.ipp) {
+      if (!wait_mbar(p, m, &m->empty[slot], (round & 1u) ^ 1u, kErrTimeoutPage)) {
+        ok = false;
+        break;
+      }
+      const int i1 = min(items, i0 + g.ipp);
+      mbar_arrive_expect_tx(&m->full[slot], (uint32_t)((i1 - i0) * g.R) * row_bytes);
+      issue_page(p, in, g, rs, i0, i1, smem + (size_t)slot * kPageBytes, &m->full[slot], pol);
+      ++page_cnt;
+      if (++slot == p.n_pages) {
+        slot = 0;
+        ++round;
+      }
+    }
+  }
+  if (!ok) {
+    // drain: every issued copy must land before the CTA's shared memory goes away
+    for (uint32_t k = h_cnt > 2u ? h_cnt - 2u : 0u; k < h_cnt; ++k) {
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(&m->hfull[k & 1u], (k >> 1) & 1u)) {
+        if (globaltimer() - t0 > p.timeout_ns) break;
+      }
+    }
+    const uint32_t first = page_cnt > (uint32_t)p.n_pages ? page_cnt - p.n_pages : 0u;
+    for (uint32_t k = first; k < page_cnt; ++k) {
+      const int sl = (int)(k % (uint32_t)p.n_pages);
+      const uint32_t par = (k / (uint32_t)p.n_pages) & 1u;
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(&m->full[sl], par)) {
+        if (globaltimer() - t0 > p.timeout_ns) break;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// compute role: activation staging
+// ---------------------------------------------------------------------------
+
+enum ActKind { kActNone = 0, kActAttnNorm, kActMlpNorm, kActFinalNorm, kActAttnOut, kActH };
+
+__device__ __forceinline__ int act_kind(int op) {
+  switch (op) {
+    case MK_OP_QKV: return kActAttnNorm;
+    case MK_OP_OPROJ: return kActAttnOut;
+    case MK_OP_GATEUP: return kActMlpNorm;
+    case MK_OP_DOWN: return kActH;
+    case MK_OP_LMHEAD: return kActFinalNorm;
+    default: return kActNone;
+  }
+}
+
+struct InvScale {
+  float v[kMaxBatch];  // 1/rms per sequence (1 for activations without a norm)
+};
+
+struct Staged {
+  int key_x = -1;     // what the x buffer holds
+  int key_h = -1;     // what the h buffer holds
+  int stage_cnt = 0;  // parity of the RMSNorm partial-sum buffer
+  InvScale inv_x;     // scale of the x buffer's contents
+};
+
+__device__ __forceinline__ int act_key(int kind, int layer, int chunk) {
+  return (kind << 20) | (layer << 4) | chunk;
+}
+
+__device__ __forceinline__ const uint16_t* norm_weight(const Params& p, int kind, int layer) {
+  if (kind == kActAttnNorm) return p.layers[layer].attn_norm;
+  if (kind == kActMlpNorm) return p.layers[layer].mlp_norm;
+  if (kind == kActFinalNorm) return p.final_norm;
+  return nullptr;
+}
+
+// Stages the activation vector(s) of `kind` for all B sequences into the x or
+// h buffer. For the RMSNorm kinds the buffer holds x * w (the gain already
+// applied) and 1/rms(x) per sequence is returned in st.inv_x.
+__device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, Staged& st, int kind,
+                                      int layer, int chunk) {
+  const int tid = compute_tid();  // 0..kComputeThreads-1
+  const int warp = tid >> 5, lane = tid & 31;
+  const bool to_h = kind == kActH;
+  float* dst = reinterpret_cast<float*>(smem + (to_h ? p.off_h : p.off_x));
+  const int K = kind == kActAttnOut ? p.QD : (to_h ? p.Fc : p.H);
+  const uint16_t* normw = norm_weight(p, kind, layer);
+  const int par = st.stage_cnt & 1;
+  compute_bar();  // everyone is done reading the buffer's previous contents
+  // every thread issues all of its loads of a pass before using any, so a
+  // pass costs one round trip to L2 (a 2048-wide vector is one pass)
+  constexpr int kU = 4;
+  constexpr int kPass = kComputeThreads * 4 * kU;  // columns per pass
+  for (int b = 0; b < p.B; ++b) {
+    const bool from_embed = kind == kActAttnNorm && layer == 0;
+    const uint16_t* erow = p.embed + (size_t)p.tok[b] * p.H;
+    const float* src;
+    if (kind == kActAttnNorm || kind == kActFinalNorm) src = p.x + (size_t)b * p.H;
+    else if (kind == kActMlpNorm) src = p.xa + (size_t)b * p.H;
+    else if (kind == kActAttnOut) src = p.attn + (size_t)b * p.QD;
+    else src = p.h + (size_t)b * p.F + (size_t)chunk * p.Fc;
+    float ss = 0.f;
+    for (int c0 = tid * 4; c0 < K; c0 += kPass) {
+      float4 v[kU];
+      uint2 wv[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int c = c0 + u * kComputeThreads * 4;
+        if (c < K) {
+          if (from_embed) {
+            const uint2 e = *reinterpret_cast<const uint2*>(erow + c);
+            v[u] = make_float4(bf_lo(e.x), bf_hi(e.x), bf_lo(e.y), bf_hi(e.y));
+          } else {
+            v[u] = __ldcg(reinterpret_cast<const float4*>(src + c));
+          }
+          if (normw) wv[u] = __ldg(reinterpret_cast<const uint2*>(normw + c));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int c = c0 + u * kComputeThreads * 4;
+        if (c < K) {
+          float4 x = v[u];
+          ss += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+          if (normw) {
+            x.x *= bf_lo(wv[u].x);
+            x.y *= bf_hi(wv[u].x);
+            x.z *= bf_lo(wv[u].y);
+            x.w *= bf_hi(wv[u].y);
+          }
+          *reinterpret_cast<float4*>(dst + (size_t)b * K + c) = x;
+        }
+      }
+    }
+    if (normw) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) m->red[par][warp][b] = ss;
+    }
+  }
+  compute_bar();
+  InvScale inv;
+#pragma unroll
+  for (int b = 0; b < kMaxBatch; ++b) {
+    inv.v[b] = 1.f;
+    if (normw && b < p.B) {
+      float sum = 0.f;
+#pragma unroll
+      for (int w = 0; w < kComputeWarps; ++w) sum += m->red[par][w][b];
+      inv.v[b] = rsqrtf(sum / (float)p.H + p.eps);
+    }
+  }
+  st.stage_cnt++;
+  const int key = act_key(kind, layer, chunk);
+  if (to_h) {
+    st.key_h = key;
+    if (p.alias_xh) st.key_x = -1;
+  } else {
+    st.key_x = key;
+    st.inv_x = inv;
+    if (p.alias_xh) st.key_h = -1;
+  }
+}
+
+// One sequence, rows of at most 2048 columns: each compute warp copies the
+// staged vector into registers in the layout of the page dot products (lane
+// l, block j: columns j*256 + l*8 .. +8), scaled by 1/rms for the norms.
+__device__ __forceinline__ void load_regs(float (&a)[64], const float* act, float scale, int K) {
+  const int lane = threadIdx.x & 31;
+  const int nblk = K / 256;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j < nblk) {
+      const float* src = act + j * 256 + lane * 8;
+      const float4 x0 = *reinterpret_cast<const float4*>(src);
+      const float4 x1 = *reinterpret_cast<const float4*>(src + 4);
+      a[j * 8 + 0] = x0.x * scale; a[j * 8 + 1] = x0.y * scale;
+      a[j * 8 + 2] = x0.z * scale; a[j * 8 + 3] = x0.w * scale;
+      a[j * 8 + 4] = x1.x * scale; a[j * 8 + 5] = x1.y * scale;
+      a[j * 8 + 6] = x1.z * scale; a[j * 8 + 7] = x1.w * scale;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) a[j * 8 + e] = 0.f;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// compute role: GEMV pages
+// ---------------------------------------------------------------------------
+// Each compute warp owns whole pages, dealt round-robin over the CTA's page
+// stream, and dots every row of its page with the activations of all B
+// sequences: lane l covers columns j*256 + l*8 .. +8 of each 256-column block,
+// i.e. every block is one 512-byte contiguous read of the row per warp. Four
+// rows are in flight at once (two accumulator chains each) for ILP. With one
+// sequence and rows of at most 2048 columns the activations sit in registers;
+// otherwise they are read from the staged buffer block by block.
+
+__device__ __forceinline__ void warp_sum4(float (&v)[4]) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] += __shfl_xor_sync(0xffffffffu, v[q], o);
+  }
+}
+
+// B == 1, K <= 2048: activations a[j*8 + e] in registers. Rows 0..n_rows-1
+// (n_rows <= 4) of the page starting at `rows`; lane q < n_rows stores row
+// q's result to *dst (every lane passes its own row's destination, so no
+// array of pointers is needed).
+template <int NB>
+__device__ __forceinline__ void rows4_reg(const uint8_t* rows, int n_rows, int row_bytes,
+                                          int nblk, const float (&a)[64], float* dst,
+                                          int lane) {
+  // two accumulator chains per row, each a packed pair of fp32 lanes (even
+  // and odd columns), so one fma.rn.f32x2 covers two weights
+  unsigned long long acc[4][2];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) acc[q][0] = acc[q][1] = 0ull;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (NB == 8 || j < nblk) {
+      uint4 w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        w[q] = (NB == 8 || q < n_rows)
+                   ? *reinterpret_cast<const uint4*>(rows + (size_t)q * row_bytes + j * 512 + lane * 16)
+                   : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t ws[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          ffma2(acc[q][j & 1], pack2(bf_lo(ws[e]), bf_hi(ws[e])),
+                pack2(a[j * 8 + 2 * e], a[j * 8 + 2 * e + 1]));
+      }
+    }
+  }
+  float v[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 x = unpack2(acc[q][0]), y = unpack2(acc[q][1]);
+    v[q] = (x.x + x.y) + (y.x + y.y);
+  }
+  warp_sum4(v);
+  if (lane < 4 && lane < n_rows) {
+    float mine = v[0];
+#pragma unroll
+    for (int q = 1; q < 4; ++q) mine = lane == q ? v[q] : mine;
+    *dst = mine;
+  }
+}
+
+// any B, any K: activations read block by block from the staged buffer
+template <int B>
+__device__ __forceinline__ void page_rows_smem(const uint8_t* page, int n_rows, int row_bytes,
+                                               int nblk, const float* act, int K,
+                                               const InvScale& inv, float* out_row0,
+                                               int out_stride, int lane) {
+  constexpr int RG = B <= 2 ? 4 : (B == 4 ? 2 : 1);
+  for (int r0 = 0; r0 < n_rows; r0 += RG) {
+    float acc[RG][B];
+#pragma unroll
+    for (int q = 0; q < RG; ++q)
+#pragma unroll
+      for (int b = 0; b < B; ++b) acc[q][b] = 0.f;
+    for (int j = 0; j < nblk; ++j) {
+      float x[B][8];
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const float* src = act + (size_t)b * K + j * 256 + lane * 8;
+        const float4 x0 = *reinterpret_cast<const float4*>(src);
+        const float4 x1 = *reinterpret_cast<const float4*>(src + 4);
+        const float s = inv.v[b];
+        x[b][0] = x0.x * s; x[b][1] = x0.y * s; x[b][2] = x0.z * s; x[b][3] = x0.w * s;
+        x[b][4] = x1.x * s; x[b][5] = x1.y * s; x[b][6] = x1.z * s; x[b][7] = x1.w * s;
+      }
+#pragma unroll
+      for (int q = 0; q < RG; ++q) {
+        if (r0 + q < n_rows) {
+          const uint4 w =
+              *reinterpret_cast<const uint4*>(page + (size_t)(r0 + q) * row_bytes + j * 512 + lane * 16);
+          const float wf[8] = {bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y),
+                               bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w)};
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+#pragma unroll
+            for (int b = 0; b < B; ++b) acc[q][b] = fmaf(wf[e], x[b][e], acc[q][b]);
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < RG; ++q) {
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[q][b] += __shfl_xor_sync(0xffffffffu, acc[q][b], o);
+      }
+      if (lane == 0 && r0 + q < n_rows) {
+#pragma unroll
+        for (int b = 0; b < B; ++b) out_row0[(size_t)(r0 + q) * out_stride + b] = acc[q][b];
+      }
+    }
+  }
+}
+
+// kRegs: the activations are in the caller's registers a[] (B == 1, rows of at
+// most 2048 columns); otherwise they are read from the staged buffer `act`.
+template <int B, bool kRegs>
+__device__ __forceinline__ void gemv_run(const Params& p, Misc* m, uint8_t* smem, const Instr& in,
+                                         const Geom& g, const float* act, const InvScale& inv,
+                                         const float (&a)[64], float* res, uint32_t page_base) {
+  const int warp = compute_warp(), lane = threadIdx.x & 31;
+  const int items = in.a1 - in.a0;
+  const int npages = (items + g.ipp - 1) / g.ipp;
+  const int row_bytes = g.K * 2;
+  const int nblk = g.K / 256;
+  // the pages of this warp: global page index congruent to the warp index.
+  // n_pages is a multiple of kComputeWarps, so every slot this warp waits on
+  // was last used by this warp's own previous page (already consumed): the
+  // parity wait below cannot alias an older phase.
+  int pg = (int)(((uint32_t)warp + kComputeWarps - page_base % kComputeWarps) % kComputeWarps);
+  // slot and phase of this warp's first page, then advanced incrementally
+  const uint32_t pc0 = page_base + (uint32_t)pg;
+  int slot = (int)(pc0 % (uint32_t)p.n_pages);
+  uint32_t round = pc0 / (uint32_t)p.n_pages;
+  for (; pg < npages; pg += kComputeWarps) {
+    const bool ok = wait_mbar(p, m, &m->full[slot], round & 1u, kErrTimeoutPage);
+    if (ok) {
+      const int n_in = min(g.ipp, items - pg * g.ipp);  // items on this page
+      const uint8_t* page = smem + (size_t)slot * kPageBytes;
+      // page row pr = r * n_in + k holds row r of item pg*ipp + k; its result
+      // goes to res[((item * R) + r) * B + b]
+      const int n_rows = n_in * g.R;
+      float* const res_page = res + (size_t)(pg * g.ipp) * g.R * B;
+      if (kRegs) {
+        if (nblk == 8) {
+          // pages of 2048-column rows, full or the short last page of an
+          // instruction: one call site of the full-page code (a second copy
+          // costs instruction-cache space). It dots all four row slots; on a
+          // short page the ones past n_rows hold an earlier page's rows, stay
+          // inside the slot and are never stored.
+          const int pr = min(lane & 3, n_rows - 1);
+          const int r = pr / n_in, k = pr - r * n_in;
+          rows4_reg<8>(page, n_rows, row_bytes, 8, a, res_page + ((size_t)k * g.R + r) * B, lane);
+        } else {
+          for (int r0 = 0; r0 < n_rows; r0 += 4) {
+            const int pr = min(r0 + (lane & 3), n_rows - 1);
+            const int r = pr / n_in, k = pr - r * n_in;
+            rows4_reg<0>(page + (size_t)r0 * row_bytes, n_rows - r0, row_bytes, nblk, a,
+                         res_page + ((size_t)k * g.R + r) * B, lane);
+          }
+        }
+      } else {
+        for (int r = 0; r < g.R; ++r)
+          page_rows_smem<B>(page + (size_t)r * n_in * row_bytes, n_in, row_bytes, nblk, act, g.K,
+                            inv, res_page + (size_t)r * B, g.R * B, lane);
+      }
+    }
+    // a page whose copy has not landed (after an abort) is never handed back,
+    // so the loader cannot start a second copy into a slot still being filled
+    __syncwarp();
+    if (lane == 0 && ok) mbar_arrive(&m->empty[slot]);
+    slot += kComputeWarps;
+    if (slot >= p.n_pages) {
+      slot -= p.n_pages;
+      ++round;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// compute role: split-KV attention partial (instruction 2)
+// ---------------------------------------------------------------------------
+// Unit (b, g, p): the G q-heads of kv-head g over keys [t0, t1) of sequence b.
+// A key row of D bf16 is read by D/8 lanes with one 16-byte load each, so a
+// warp covers 256/D keys per load; per (lane group, head) an online softmax
+// keeps (m, l, o) in the log2 domain (q is pre-scaled by log2(e)/sqrt(D)).
+// Warps combine through shared memory and write (o, m, l) for the partition.
+
+__device__ __forceinline__ void softmax_merge(float& m, float& l, float* o, float m2, float l2,
+                                              const float* o2) {
+  const float M = fmaxf(m, m2);
+  if (M == -INFINITY) return;
+  const float s1 = exp2f(m - M), s2 = exp2f(m2 - M);
+  l = l * s1 + l2 * s2;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) o[e] = o[e] * s1 + o2[e] * s2;
+  m = M;
+}
+
+// GH heads per pass (G = 8 runs two passes over the same keys, which the
+// second pass finds in L2).
+template <int D, int GH>
+__device__ __forceinline__ void attn_partial(const Params& p, uint8_t* smem, const Instr& in, int h0) {
+  constexpr int LPT = D / 8;       // lanes per key row
+  constexpr int TPI = 32 / LPT;    // keys per warp load
+  const int warp = compute_warp(), lane = threadIdx.x & 31;
+  const int b = in.a0, g = in.a1, pidx = in.a2 >> 16, P = in.a2 & 0xffff;
+  const int len = p.pos[b] + 1;
+  const int t0 = (int)((long)pidx * len / P), t1 = (int)((long)(pidx + 1) * len / P);
+  const int sub = lane % LPT, ti = lane / LPT;
+  const LayerPtrs& L = p.layers[in.layer];
+  const size_t kvbase = ((size_t)b * p.nkv + g) * (size_t)p.S * D;
+  const uint16_t* Kc = L.kc + kvbase;
+  const uint16_t* Vc = L.vc + kvbase;
+  const float qscale = 1.4426950408889634f * rsqrtf((float)D);
+
+  float qf[GH][8], o[GH][8], mm[GH], ll[GH];
+#pragma unroll
+  for (int h = 0; h < GH; ++h) {
+    const float* qs = p.q + (size_t)b * p.QD + (size_t)(g * p.G + h0 + h) * D + sub * 8;
+    const float4 a0 = __ldcg(reinterpret_cast<const float4*>(qs));
+    const float4 a1 = __ldcg(reinterpret_cast<const float4*>(qs + 4));
+    qf[h][0] = a0.x * qscale; qf[h][1] = a0.y * qscale; qf[h][2] = a0.z * qscale;
+    qf[h][3] = a0.w * qscale; qf[h][4] = a1.x * qscale; qf[h][5] = a1.y * qscale;
+    qf[h][6] = a1.z * qscale; qf[h][7] = a1.w * qscale;
+    mm[h] = -INFINITY;
+    ll[h] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[h][e] = 0.f;
+  }
+
+  constexpr int U = 2;  // key rows in flight per lane
+  const int stride = kComputeWarps * TPI;
+  for (int base = t0 + warp * TPI; base < t1; base += U * stride) {
+    uint4 kv[U], vv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int t = base + u * stride + ti;
+      if (t < t1) {
+        kv[u] = __ldcg(reinterpret_cast<const uint4*>(Kc + (size_t)t * D + sub * 8));
+        vv[u] = __ldcg(reinterpret_cast<const uint4*>(Vc + (size_t)t * D + sub * 8));
+      } else {
+        kv[u] = make_uint4(0, 0, 0, 0);
+        vv[u] = make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const bool valid = base + u * stride + ti < t1;
+      float s[GH];
+#pragma unroll
+      for (int h = 0; h < GH; ++h) {
+        float acc = qf[h][0] * bf_lo(kv[u].x);
+        acc = fmaf(qf[h][1], bf_hi(kv[u].x), acc);
+        acc = fmaf(qf[h][2], bf_lo(kv[u].y), acc);
+        acc = fmaf(qf[h][3], bf_hi(kv[u].y), acc);
+        acc = fmaf(qf[h][4], bf_lo(kv[u].z), acc);
+        acc = fmaf(qf[h][5], bf_hi(kv[u].z), acc);
+        acc = fmaf(qf[h][6], bf_lo(kv[u].w), acc);
+        acc = fmaf(qf[h][7], bf_hi(kv[u].w), acc);
+        s[h] = acc;
+      }
+#pragma unroll
+      for (int off = 1; off < LPT; off <<= 1)
+#pragma unroll
+        for (int h = 0; h < GH; ++h) s[h] += __shfl_xor_sync(0xffffffffu, s[h], off);
+      if (valid) {
+        const float vf[8] = {bf_lo(vv[u].x), bf_hi(vv[u].x), bf_lo(vv[u].y), bf_hi(vv[u].y),
+                             bf_lo(vv[u].z), bf_hi(vv[u].z), bf_lo(vv[u].w), bf_hi(vv[u].w)};
+#pragma unroll
+        for (int h = 0; h < GH; ++h) {
+          const float mn = fmaxf(mm[h], s[h]);
+          const float sc = exp2f(mm[h] - mn);
+          const float pe = exp2f(s[h] - mn);
+          ll[h] = ll[h] * sc + pe;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pe, vf[e], o[h][e] * sc);
+          mm[h] = mn;
+        }
+      }
+    }
+  }
+  // merge the key groups of the warp (lanes with the same `sub`)
+#pragma unroll
+  for (int off = LPT; off < 32; off <<= 1) {
+#pragma unroll
+    for (int h = 0; h < GH; ++h) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, mm[h], off);
+      const float l2 = __shfl_xor_sync(0xffffffffu, ll[h], off);
+      float o2[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o2[e] = __shfl_xor_sync(0xffffffffu, o[h][e], off);
+      softmax_merge(mm[h], ll[h], o[h], m2, l2, o2);
+    }
+  }
+  // scratch [warp][h][D + 2] in the activation staging area
+  float* scr = reinterpret_cast<float*>(smem + p.off_x);
+  compute_bar();  // previous readers of the staging area are done
+  if (ti == 0) {
+#pragma unroll
+    for (int h = 0; h < GH; ++h) {
+      float* sp = scr + ((size_t)warp * GH + h) * (D + 2);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sp[sub * 8 + e] = o[h][e];
+      if (sub == 0) {
+        sp[D] = mm[h];
+        sp[D + 1] = ll[h];
+      }
+    }
+  }
+  compute_bar();
+  const int tid = compute_tid();
+  for (int idx = tid; idx < GH * D; idx += kComputeThreads) {
+    const int h = idx / D, d = idx - h * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kComputeWarps; ++w) M = fmaxf(M, scr[((size_t)w * GH + h) * (D + 2) + D]);
+    float acc = 0.f, den = 0.f;
+#pragma unroll
+    for (int w = 0; w < kComputeWarps; ++w) {
+      const float* sp = scr + ((size_t)w * GH + h) * (D + 2);
+      const float wt = sp[D] == -INFINITY ? 0.f : exp2f(sp[D] - M);
+      acc = fmaf(wt, sp[d], acc);
+      den = fmaf(wt, sp[D + 1], den);
+    }
+    float* dst = p.part + (((size_t)b * p.nh + g * p.G + h0 + h) * kMaxPartitions + pidx) * (D + 2);
+    dst[d] = acc;
+    if (d == 0) {
+      dst[D] = M;
+      dst[D + 1] = den;
+    }
+  }
+}
+
+// GS > 0: the q-heads per kv-head are fixed at compile time (one variant)
+template <int D, int GS>
+__device__ void attn_unit(const Params& p, uint8_t* smem, const Instr& in) {
+  if constexpr (GS == 1 || GS == 2 || GS == 4) {
+    attn_partial<D, GS>(p, smem, in, 0);
+  } else if constexpr (GS > 4) {
+    for (int h0 = 0; h0 < GS; h0 += 4) attn_partial<D, 4>(p, smem, in, h0);
+  } else {
+    switch (p.G) {
+      case 1: attn_partial<D, 1>(p, smem, in, 0); break;
+      case 2: attn_partial<D, 2>(p, smem, in, 0); break;
+      case 4: attn_partial<D, 4>(p, smem, in, 0); break;
+      default:
+        for (int h0 = 0; h0 < p.G; h0 += 4) attn_partial<D, 4>(p, smem, in, h0);
+        break;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// compute role: attention partial reduction (instruction 3)
+// ---------------------------------------------------------------------------
+
+template <int D>
+__device__ __forceinline__ void attn_reduce(const Params& p, const Instr& in) {
+  constexpr int PL = D / 32;  // dims per lane
+  const int warp = compute_warp(), lane = threadIdx.x & 31;
+  const int b = in.a0, g = in.a1, P = in.a2;
+  for (int hl = warp; hl < p.G; hl += kComputeWarps) {
+    const int h = g * p.G + hl;
+    const float* base = p.part + ((size_t)b * p.nh + h) * kMaxPartitions * (D + 2);
+    float M = -INFINITY;
+    for (int k = lane; k < P; k += 32) M = fmaxf(M, __ldcg(base + (size_t)k * (D + 2) + D));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float acc[PL], den = 0.f;
+#pragma unroll
+    for (int e = 0; e < PL; ++e) acc[e] = 0.f;
+    for (int k = 0; k < P; ++k) {
+      const float* s = base + (size_t)k * (D + 2);
+      const float mk = __ldcg(s + D);
+      const float wt = mk == -INFINITY ? 0.f : exp2f(mk - M);
+      den = fmaf(wt, __ldcg(s + D + 1), den);
+#pragma unroll
+      for (int e = 0; e < PL; ++e) acc[e] = fmaf(wt, __ldcg(s + lane * PL + e), acc[e]);
+    }
+    const float inv = 1.f / den;
+    float* dst = p.attn + (size_t)b * p.QD + (size_t)h * D + lane * PL;
+#pragma unroll
+    for (int e = 0; e < PL; ++e) dst[e] = acc[e] * inv;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// compute role: the instruction loop
+// ---------------------------------------------------------------------------
+
+template <int B, int DS, int GS>
+__device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Instr* q, int n,
+                             int qbase) {
+  const int warp = compute_warp(), lane = threadIdx.x & 31;
+  Staged st;
+  // per-warp activation registers (one sequence, rows <= 2048 columns),
+  // reloaded from the staged smem vector at every instruction
+  float ax[64];
+  uint32_t page_cnt = 0;
+  uint32_t h_cnt = 0;  // down-projection chunks taken from the h ring
+  int known_ctr = -1, known_tgt = 0;
+  Instr nxt = n > 0 ? load_instr(q) : Instr{};
+  for (int i = 0; i < n; ++i) {
+    const Instr in = nxt;
+    if (i + 1 < n) nxt = load_instr(q + i + 1);
+    const int buf = i % kResBufs;
+    const uint32_t rpar = ((uint32_t)i / kResBufs) & 1u;
+    uint64_t t_start = 0, t_ready = 0;
+    const bool tracing = p.trace != nullptr && warp == 0 && lane == 0;
+    if (tracing) t_start = globaltimer();
+    // the loader fetched this down-projection chunk of h (after its counter)
+    const bool from_ring = p.h_ring && in.op == MK_OP_DOWN;
+    // 1. dependency: one thread polls, the other compute warps meet it at a barrier
+    if (!from_ring && !p.no_waits && in.wait_ctr >= 0 &&
+        !(in.wait_ctr == known_ctr && in.wait_target <= known_tgt)) {
+      if (warp == 0 && lane == 0) wait_counter(p, m, in.wait_ctr, in.wait_target);
+      compute_bar();
+      known_ctr = in.wait_ctr;
+      known_tgt = in.wait_target;
+    }
+    if (tracing) t_ready = globaltimer();
+    // 2. the result buffer this instruction hands to the storer must be free
+    const bool res_ok = wait_mbar(p, m, &m->res_empty[buf], rpar ^ 1u, kErrTimeoutRes);
+    const uint64_t t_res = tracing ? globaltimer() : 0;
+    uint64_t t_staged = t_res;
+    float* res = reinterpret_cast<float*>(smem + p.off_res) + (size_t)buf * p.res_floats;
+
+    if (is_gemv(in.op)) {
+      const int kind = act_kind(in.op);
+      const int chunk = in.op == MK_OP_DOWN ? in.a2 : 0;
+      const int key = act_key(kind, in.layer, chunk);
+      const bool to_h = kind == kActH;
+      const Geom g = geom_of(in.op, p.H, p.QD, p.Fc);
+      const bool regs = B == 1 && g.K <= 2048;
+      const bool norm = kind == kActAttnNorm || kind == kActMlpNorm || kind == kActFinalNorm;
+      const float* act;
+      bool h_got = false;
+      if (from_ring) {
+        const int k = (int)(h_cnt & 1u);
+        h_got = wait_mbar(p, m, &m->hfull[k], (h_cnt >> 1) & 1u, kErrTimeoutRes);
+        act = reinterpret_cast<const float*>(smem + p.off_h) + (size_t)k * p.Fc;
+      } else {
+        if ((to_h ? st.key_h : st.key_x) != key) stage(p, m, smem, st, kind, in.layer, chunk);
+        act = reinterpret_cast<const float*>(smem + (to_h ? p.off_h : p.off_x));
+      }
+      if (tracing) t_staged = globaltimer();
+      InvScale one;
+#pragma unroll
+      for (int b = 0; b < kMaxBatch; ++b) one.v[b] = 1.f;
+      if (regs) {
+        load_regs(ax, act, norm ? st.inv_x.v[0] : 1.f, g.K);
+        if (from_ring) {
+          // the slot is in registers now (a copy that has not landed, after an
+          // abort, keeps its slot: the loader must not start another into it)
+          __syncwarp();
+          if (lane == 0 && h_got) mbar_arrive(&m->hempty[h_cnt & 1u]);
+          ++h_cnt;
+        }
+        gemv_run<B, true>(p, m, smem, in, g, act, one, ax, res, page_cnt);
+      } else {
+        gemv_run<B, false>(p, m, smem, in, g, act, to_h ? one : st.inv_x, ax, res, page_cnt);
+      }
+      page_cnt += (uint32_t)((in.a1 - in.a0 + g.ipp - 1) / g.ipp);
+    } else if (in.op == MK_OP_ATTN) {
+      st.key_x = -1;  // the staging area becomes scratch
+      st.key_h = -1;
+      // runs even after an abort: its loads stay in bounds and its barriers
+      // must be met by every compute warp
+      if constexpr (DS > 0) attn_unit<DS, GS>(p, smem, in);
+      else if (p.D == 64) attn_unit<64, GS>(p, smem, in);
+      else attn_unit<128, GS>(p, smem, in);
+    } else if (in.op == MK_OP_RED) {
+      if (!aborted(m)) {
+        if constexpr (DS > 0) attn_reduce<DS>(p, in);
+        else if (p.D == 64) attn_reduce<64>(p, in);
+        else attn_reduce<128>(p, in);
+      }
+    }
+    (void)res_ok;
+    // 3. hand the instruction to the storer
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&m->res_full[buf]);
+    if (tracing) {
+      const int rec = p.trace_base + qbase + i;
+      if (rec < p.trace_cap) {
+        // field by field: the storer writes t_stored of the same record
+        mk_trace_record* r = p.trace + rec;
+        r->sm = blockIdx.x;
+        r->index = (uint32_t)i;
+        r->op = in.op;
+        r->layer = in.layer;
+        r->t_start = t_start;
+        r->t_ready = t_ready;
+        r->t_end = globaltimer();
+        r->res_wait_ns = (uint32_t)(t_res - t_ready);
+        r->stage_ns = (uint32_t)(t_staged - t_res);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// storer role
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
+
+// What an epilogue reads from global memory, loaded by the storer while the
+// compute warps still work on the instruction: the RoPE (cos, sin) of the
+// q/k/v pairs, and the residual rows of the o-projection and of the last
+// down-projection chunk. Lane l holds items l and l + 32 (at most 64 items).
+template <int B>
+struct EpiPre {
+  float2 v[2][B];
+};
+
+template <int B>
+__device__ __forceinline__ void epilogue_prefetch(const Params& p, Misc* m, const Instr& in,
+                                                  EpiPre<B>& pre) {
+  const int lane = threadIdx.x & 31;
+  const int items = in.a1 - in.a0;
+  const bool resid = in.op == MK_OP_OPROJ || (in.op == MK_OP_DOWN && in.a2 == kChunks - 1);
+  if (in.op == MK_OP_QKV) {
+    const int half = p.D / 2;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int it = lane + 32 * k;
+      if (it < items) {
+        const PairRows pr = pair_rows(in.a0 + it, p.G, p.D);
+        if (pr.which < 2) {
+#pragma unroll
+          for (int b = 0; b < B; ++b) pre.v[k][b] = __ldg(p.rope + (size_t)p.pos[b] * half + pr.i);
+        }
+      }
+    }
+  } else if (resid) {
+    const bool from_embed = in.op == MK_OP_OPROJ && in.layer == 0;
+    if (!from_embed && !p.no_waits && in.wait_ctr >= 0) {
+      // the residual rows were written by other SMs before the instruction's
+      // input counter completed: acquire that counter (the compute warps
+      // wait on it too) before reading them
+      bool ok = true;
+      if (lane == 0) ok = wait_counter(p, m, in.wait_ctr, in.wait_target);
+      if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) return;
+    }
+    const float* src = in.op == MK_OP_DOWN ? p.xa : p.x;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int it = lane + 32 * k;
+      if (it < items) {
+        const int j = in.a0 + it;
+#pragma unroll
+        for (int b = 0; b < B; ++b)
+          pre.v[k][b].x = from_embed ? bf16f(p.embed[(size_t)p.tok[b] * p.H + j])
+                                     : __ldcg(src + (size_t)b * p.H + j);
+      }
+    }
+  }
+}
+
+template <int B>
+__device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const float* res,
+                                         float* dacc, const EpiPre<B>& pre) {
+  const int lane = threadIdx.x & 31;
+  const Geom g = geom_of(in.op, p.H, p.QD, p.Fc);
+  const int items = in.a1 - in.a0;
+  const LayerPtrs& L = p.layers[in.layer];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int it = lane + 32 * k;
+    if (it >= items) continue;
+    const int j = in.a0 + it;
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const float v0 = res[((size_t)it * g.R) * B + b];
+      const float v1 = g.R == 2 ? res[((size_t)it * g.R + 1) * B + b] : 0.f;
+      switch (in.op) {
+        case MK_OP_QKV: {
+          const PairRows pr = pair_rows(j, p.G, p.D);
+          const int pos = p.pos[b];
+          const int half = p.D / 2;
+          float o0 = v0, o1 = v1;
+          if (pr.which < 2) {
+            const float2 cs = pre.v[k][b];
+            o0 = v0 * cs.x - v1 * cs.y;
+            o1 = v1 * cs.x + v0 * cs.y;
+          }
+          if (pr.which == 0) {
+            float* qd = p.q + (size_t)b * p.QD + (size_t)pr.head * p.D + pr.i;
+            qd[0] = o0;
+            qd[half] = o1;
+          } else {
+            uint16_t* c = (pr.which == 1 ? L.kc : L.vc) +
+                          (((size_t)b * p.nkv + pr.head) * p.S + pos) * p.D + pr.i;
+            c[0] = __bfloat16_as_ushort(__float2bfloat16_rn(o0));
+            c[half] = __bfloat16_as_ushort(__float2bfloat16_rn(o1));
+          }
+          break;
+        }
+        case MK_OP_OPROJ:
+          p.xa[(size_t)b * p.H + j] = pre.v[k][b].x + v0;
+          break;
+        case MK_OP_GATEUP:
+          p.h[(size_t)b * p.F + j] = silu(v0) * v1;
+          break;
+        case MK_OP_DOWN: {
+          // the chunks of row j run on this SM in order; their sum stays in smem
+          float* acc = dacc + (size_t)(j % p.dacc_rows) * B + b;
+          const float d = in.a2 == 0 ? v0 : *acc + v0;
+          if (in.a2 == kChunks - 1) p.x[(size_t)b * p.H + j] = pre.v[k][b].x + d;
+          else *acc = d;
+          break;
+        }
+        default:  // MK_OP_LMHEAD
+          p.logits[(size_t)b * p.V + j] = v0;
+          break;
+      }
+    }
+  }
+}
+
+// The storer drains finished instructions in order: epilogue, then lane 0
+// publishes the instruction with a release-add on its counter. What the
+// epilogue needs from global memory is fetched before waiting for the compute
+// warps, so the epilogue itself touches only registers and shared memory.
+// (Publishing several instructions behind one fence was measured slower: it
+// delays the first counter of each batch, which sits on the critical path.)
+template <int B>
+__device__ void storer_role(const Params& p, Misc* m, uint8_t* smem, const Instr* q, int n) {
+  const int lane = threadIdx.x & 31;
+  float* dacc = reinterpret_cast<float*>(smem + p.off_dacc);
+  Instr nxt = n > 0 ? load_instr(q) : Instr{};
+  for (int i = 0; i < n; ++i) {
+    const Instr in = nxt;
+    if (i + 1 < n) nxt = load_instr(q + i + 1);
+    const int buf = i % kResBufs;
+    const uint32_t par = ((uint32_t)i / kResBufs) & 1u;
+    EpiPre<B> pre;
+    if (is_gemv(in.op) && !aborted(m)) epilogue_prefetch<B>(p, m, in, pre);
+    const bool ok = wait_mbar(p, m, &m->res_full[buf], par, kErrTimeoutRes);
+    if (ok && !aborted(m)) {
+      const float* res = reinterpret_cast<const float*>(smem + p.off_res) + (size_t)buf * p.res_floats;
+      if (is_gemv(in.op)) epilogue<B>(p, in, res, dacc, pre);
+      if (in.sig_ctr >= 0) {
+        // the warp barrier orders the other lanes' stores (and, through the
+        // result mbarrier, the compute warps' stores) before lane 0's
+        // release-add, which publishes them at GPU scope
+        __syncwarp();
+        if (lane == 0) red_release_add(p.ctr + in.sig_ctr, in.sig_amount);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(&m->res_empty[buf]);
+      if (p.trace) {
+        const int rec = p.trace_base + (int)(q - p.instrs) + i;
+        if (rec < p.trace_cap) p.trace[rec].t_stored = globaltimer();
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+
+template <int B, int DS, int GS>
+__global__ void __launch_bounds__(kThreads, 1) interp_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Misc* m = reinterpret_cast<Misc*>(smem + p.off_misc);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < p.n_pages; ++i) {
+      mbar_init(&m->full[i], 1);
+      mbar_init(&m->empty[i], 1);  // the page's owner warp releases it
+    }
+    for (int i = 0; i < kResBufs; ++i) {
+      mbar_init(&m->res_full[i], kComputeWarps);
+      mbar_init(&m->res_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&m->hfull[i], 1);               // the loader's expect-tx arrival
+      mbar_init(&m->hempty[i], kComputeWarps);  // every compute warp
+    }
+    m->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  // counters are zero before the launch that uses them (§3.4): this launch
+  // clears the set the next step will use
+  if (p.ctr_zero)
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.n_ctr; i += gridDim.x * blockDim.x)
+      p.ctr_zero[i] = 0;
+  __syncthreads();
+  const int q0 = p.sm_off[blockIdx.x];
+  const int n = p.sm_off[blockIdx.x + 1] - q0;
+  const Instr* q = p.instrs + q0;
+  const int warp = threadIdx.x >> 5;
+  if (warp == kLoaderWarp) loader_role(p, m, smem, q, n);
+  else if (warp == kStorerWarp) storer_role<B>(p, m, smem, q, n);
+  else compute_role<B, DS, GS>(p, m, smem, q, n, q0);
+}
+
+}  // namespace mk

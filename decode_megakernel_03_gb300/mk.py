@@ -23,7 +23,7 @@ OP_QKV, OP_ATTN, OP_RED, OP_OPROJ, OP_GATEUP, OP_DOWN, OP_LMHEAD = range(1, 8)
 EXPORTS = ("mk_create", "mk_decode_step", "mk_decode_step_multilaunch", "mk_get_status",
            "mk_destroy", "mk_last_error", "mk_read_counters", "mk_set_timeout",
            "mk_debug_inject_unsatisfiable_wait", "mk_set_trace", "mk_schedule_build",
-           "mk_decode_step_noalloc")
+           "mk_decode_step_noalloc", "mk_debug_use_generic_kernel")
 
 
 class MkError(RuntimeError):
@@ -86,6 +86,7 @@ def lib():
         L.mk_read_counters.argtypes = [vp, i32p, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
         L.mk_set_timeout.argtypes = [vp, ctypes.c_uint64]
         L.mk_debug_inject_unsatisfiable_wait.argtypes = [vp, ctypes.c_int]
+        L.mk_debug_use_generic_kernel.argtypes = [vp, ctypes.c_int]
         L.mk_set_trace.argtypes = [vp, vp, ctypes.c_int]
         L.mk_schedule_build.argtypes = [ctypes.POINTER(MkConfig), ctypes.c_int, i32p,
                                         ctypes.POINTER(MkInstr), ctypes.c_int,
@@ -238,6 +239,10 @@ class Decoder:
 
     def set_timeout(self, ns: int):
         _check(lib().mk_set_timeout(self.h, int(ns)), self.h)
+
+    def use_generic_kernel(self, enable: bool):
+        """Test hook: launch the instantiation that reads the head shape at run time."""
+        _check(lib().mk_debug_use_generic_kernel(self.h, int(bool(enable))), self.h)
 
     def inject_unsatisfiable_wait(self, enable: bool):
         _check(lib().mk_debug_inject_unsatisfiable_wait(self.h, int(bool(enable))), self.h)

@@ -133,6 +133,12 @@ int mk_set_timeout(mk_handle* h, uint64_t timeout_ns);
    MK_ERR_TIMEOUT (device waits are bounded; nothing faults). */
 int mk_debug_inject_unsatisfiable_wait(mk_handle* h, int enable);
 
+/* Test-only: with `enable` non-zero the handle launches the interpreter
+   instantiation that reads the head dimension and q-heads per kv-head at run
+   time, instead of one specialised to the model's head shape (the default
+   whenever the library has one). Both compute the same results. */
+int mk_debug_use_generic_kernel(mk_handle* h, int enable);
+
 /* Per-instruction trace. When dev_buf (device memory holding `capacity`
    mk_trace_record) is non-NULL, the compute warps of every SM write one record
    per instruction they run, timestamped with %globaltimer; record k belongs to

@@ -82,27 +82,29 @@ def test_tiny_decode_from_empty_cache_matches_full_forward():
 
 
 @pytest.mark.parametrize("shape_name", ["tiny", "llama1b"])
-def test_multilaunch_and_graph_are_bit_identical(shape_name):
+def test_multilaunch_graph_and_generic_kernel_are_bit_identical(shape_name):
     wl = synth.WORKLOADS[shape_name]
     ctx = (200,) if shape_name == "tiny" else wl.ctx
     cap = 256 if shape_name == "tiny" else wl.capacity
     toks = synth.step_tokens(wl)
     outs = {}
     caches = {}
-    for mode in ("mega", "multi", "graph"):
+    for mode in ("mega", "multi", "graph", "generic"):
         pair = Pair(wl.shape, 1, cap, ctx=ctx)
+        if mode == "generic":  # the instantiation that reads the head shape at run time
+            pair.dec.use_generic_kernel(True)
         res = []
         for s in range(3):
-            res.append(pair.gpu_step([int(toks[s, 0])], [ctx[0] + s], mode=mode))
+            res.append(pair.gpu_step([int(toks[s, 0])], [ctx[0] + s], mode="mega" if mode == "generic" else mode))
         outs[mode] = np.stack(res)
         caches[mode] = [bf16_bits(t) for t in pair.kc + pair.vc]
         if mode == "mega":
             counters_match(pair, [ctx[0] + 2])
         pair.close()
-    np.testing.assert_array_equal(outs["mega"], outs["multi"])
-    np.testing.assert_array_equal(outs["mega"], outs["graph"])
-    for a, b in zip(caches["mega"], caches["multi"]):
-        np.testing.assert_array_equal(a, b)
+    for other in ("multi", "graph", "generic"):
+        np.testing.assert_array_equal(outs["mega"], outs[other])
+        for a, b in zip(caches["mega"], caches[other]):
+            np.testing.assert_array_equal(a, b)
 
 
 @pytest.mark.parametrize("name,steps", [("llama1b", 3), ("llama1b_ctx8k", 2), ("llama8b", 2),
