@@ -232,6 +232,33 @@ static __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, cons
   for (int i = 0; i < n && ok; ++i) {
     const Instr in = nxt;
     if (i + 1 < n) nxt = load_instr(q + i + 1);
+    if (in.op == MK_OP_ATTN) {
+      // the unit's cached keys, K and V rows of kpp keys per page; they do
+      // not depend on this step's outputs, so they stream in while the unit
+      // still waits for its queries
+      const AttnSpan sp = attn_span(p.pos[in.a0], in.a2 >> 16, in.a2 & 0xffff, p.D);
+      const LayerPtrs& L = p.layers[in.layer];
+      const size_t kvbase = ((size_t)in.a0 * p.nkv + in.a1) * (size_t)p.S * p.D;
+      for (int pg = 0; pg < sp.npages; ++pg) {
+        if (!wait_mbar(p, m, &m->empty[slot], (round & 1u) ^ 1u, kErrTimeoutPage)) {
+          ok = false;
+          break;
+        }
+        const int k0 = sp.t0 + pg * sp.kpp;
+        const int nk = min(sp.kpp, sp.nc - pg * sp.kpp);
+        const uint32_t bytes = (uint32_t)nk * (uint32_t)p.D * 2u;
+        uint8_t* dst = smem + (size_t)slot * kPageBytes;
+        mbar_arrive_expect_tx(&m->full[slot], 2u * bytes);
+        bulk_g2s_hint(dst, L.kc + kvbase + (size_t)k0 * p.D, bytes, &m->full[slot], pol);
+        bulk_g2s_hint(dst + kPageBytes / 2, L.vc + kvbase + (size_t)k0 * p.D, bytes, &m->full[slot], pol);
+        ++page_cnt;
+        if (++slot == p.n_pages) {
+          slot = 0;
+          ++round;
+        }
+      }
+      continue;
+    }
     if (!is_gemv(in.op)) continue;
     if (p.h_ring && in.op == MK_OP_DOWN) {
       // one sequence: fetch the chunk of h this down-projection reads into the
@@ -617,7 +644,7 @@ __device__ __forceinline__ void gemv_run(const Params& p, Misc* m, uint8_t* smem
     // a page whose copy has not landed (after an abort) is never handed back,
     // so the loader cannot start a second copy into a slot still being filled
     __syncwarp();
-    if (lane == 0 && ok) mbar_arrive(&m->empty[slot]);
+    if (lane == 0 && ok) mbar_arrive_cnt(&m->empty[slot], kComputeWarps);
     slot += kComputeWarps;
     if (slot >= p.n_pages) {
       slot -= p.n_pages;
@@ -646,23 +673,76 @@ __device__ __forceinline__ void softmax_merge(float& m, float& l, float* o, floa
   m = M;
 }
 
-// GH heads per pass (G = 8 runs two passes over the same keys, which the
-// second pass finds in L2).
+// One key per lane group: its scores against the GH heads (a key row of D
+// bf16 is spread over D/8 lanes, 16 bytes each), then the online-softmax
+// update of (m, l, o) in the log2 domain. Lane groups whose key is not valid
+// only take part in the shuffles.
 template <int D, int GH>
-__device__ __forceinline__ void attn_partial(const Params& p, uint8_t* smem, const Instr& in, int h0) {
+__device__ __forceinline__ void attn_key(const float (&qf)[GH][8], float (&o)[GH][8],
+                                         float (&mm)[GH], float (&ll)[GH], const uint4 kv,
+                                         const uint4 vv, bool valid) {
+  constexpr int LPT = D / 8;
+  float s[GH];
+#pragma unroll
+  for (int h = 0; h < GH; ++h) {
+    float acc = qf[h][0] * bf_lo(kv.x);
+    acc = fmaf(qf[h][1], bf_hi(kv.x), acc);
+    acc = fmaf(qf[h][2], bf_lo(kv.y), acc);
+    acc = fmaf(qf[h][3], bf_hi(kv.y), acc);
+    acc = fmaf(qf[h][4], bf_lo(kv.z), acc);
+    acc = fmaf(qf[h][5], bf_hi(kv.z), acc);
+    acc = fmaf(qf[h][6], bf_lo(kv.w), acc);
+    acc = fmaf(qf[h][7], bf_hi(kv.w), acc);
+    s[h] = acc;
+  }
+#pragma unroll
+  for (int off = 1; off < LPT; off <<= 1)
+#pragma unroll
+    for (int h = 0; h < GH; ++h) s[h] += __shfl_xor_sync(0xffffffffu, s[h], off);
+  if (valid) {
+    const float vf[8] = {bf_lo(vv.x), bf_hi(vv.x), bf_lo(vv.y), bf_hi(vv.y),
+                         bf_lo(vv.z), bf_hi(vv.z), bf_lo(vv.w), bf_hi(vv.w)};
+#pragma unroll
+    for (int h = 0; h < GH; ++h) {
+      const float mn = fmaxf(mm[h], s[h]);
+      const float sc = exp2f(mm[h] - mn);
+      const float pe = exp2f(s[h] - mn);
+      ll[h] = ll[h] * sc + pe;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pe, vf[e], o[h][e] * sc);
+      mm[h] = mn;
+    }
+  }
+}
+
+// GH heads per pass. The unit's cached keys arrive in shared-memory pages
+// (attn_span) that every compute warp reads: warp w takes keys w*TPI + ti,
+// + kComputeWarps*TPI, ... of each page, and releases the page after its
+// last pass (G = 8 runs two passes of four heads over the same pages). The
+// new key comes from the cache in global memory after the counter wait.
+template <int D, int GH>
+__device__ __forceinline__ void attn_partial(const Params& p, Misc* m, uint8_t* smem, const Instr& in,
+                                             int h0, uint32_t page_base, bool release) {
   constexpr int LPT = D / 8;       // lanes per key row
   constexpr int TPI = 32 / LPT;    // keys per warp load
   const int warp = compute_warp(), lane = threadIdx.x & 31;
   const int b = in.a0, g = in.a1, pidx = in.a2 >> 16, P = in.a2 & 0xffff;
-  const int len = p.pos[b] + 1;
-  const int t0 = (int)((long)pidx * len / P), t1 = (int)((long)(pidx + 1) * len / P);
+  const int pos = p.pos[b];
+  const AttnSpan sp = attn_span(pos, pidx, P, D);
   const int sub = lane % LPT, ti = lane / LPT;
-  const LayerPtrs& L = p.layers[in.layer];
-  const size_t kvbase = ((size_t)b * p.nkv + g) * (size_t)p.S * D;
-  const uint16_t* Kc = L.kc + kvbase;
-  const uint16_t* Vc = L.vc + kvbase;
   const float qscale = 1.4426950408889634f * rsqrtf((float)D);
 
+  // the new key (in the unit's range), written by this step's QKV instruction
+  // (its counter wait ordered that write before this read): key group 0 of
+  // warp 0 takes it, its loads issued together with the queries'
+  const bool new_here = warp == 0 && sp.t0 <= pos && pos < sp.t1;
+  uint4 kn = make_uint4(0, 0, 0, 0), vn = kn;
+  if (new_here) {
+    const LayerPtrs& L = p.layers[in.layer];
+    const size_t row = (((size_t)b * p.nkv + g) * (size_t)p.S + pos) * D + sub * 8;
+    kn = __ldcg(reinterpret_cast<const uint4*>(L.kc + row));
+    vn = __ldcg(reinterpret_cast<const uint4*>(L.vc + row));
+  }
   float qf[GH][8], o[GH][8], mm[GH], ll[GH];
 #pragma unroll
   for (int h = 0; h < GH; ++h) {
@@ -677,57 +757,35 @@ __device__ __forceinline__ void attn_partial(const Params& p, uint8_t* smem, con
 #pragma unroll
     for (int e = 0; e < 8; ++e) o[h][e] = 0.f;
   }
+  if (new_here) attn_key<D, GH>(qf, o, mm, ll, kn, vn, ti == 0);
 
-  constexpr int U = 2;  // key rows in flight per lane
-  const int stride = kComputeWarps * TPI;
-  for (int base = t0 + warp * TPI; base < t1; base += U * stride) {
-    uint4 kv[U], vv[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int t = base + u * stride + ti;
-      if (t < t1) {
-        kv[u] = __ldcg(reinterpret_cast<const uint4*>(Kc + (size_t)t * D + sub * 8));
-        vv[u] = __ldcg(reinterpret_cast<const uint4*>(Vc + (size_t)t * D + sub * 8));
-      } else {
-        kv[u] = make_uint4(0, 0, 0, 0);
-        vv[u] = make_uint4(0, 0, 0, 0);
+  uint32_t pc = page_base;
+  for (int pg = 0; pg < sp.npages; ++pg, ++pc) {
+    const int slot = (int)(pc % (uint32_t)p.n_pages);
+    // Only the slot's owner warp (slot % kComputeWarps, the warp that
+    // consumes every GEMV page of this slot) waits on its barrier: it has seen
+    // every earlier fill of the slot, so its parity wait cannot mistake an
+    // older phase for this one. The other warps meet it at a barrier.
+    if (warp == slot % kComputeWarps)
+      wait_mbar(p, m, &m->full[slot], (pc / (uint32_t)p.n_pages) & 1u, kErrTimeoutPage);
+    compute_bar();
+    const bool ok = !aborted(m);
+    if (ok) {
+      const uint8_t* kp = smem + (size_t)slot * kPageBytes;
+      const uint8_t* vp = kp + kPageBytes / 2;
+      const int nk = min(sp.kpp, sp.nc - pg * sp.kpp);
+      for (int j0 = warp * TPI; j0 < nk; j0 += kComputeWarps * TPI) {
+        const int j = j0 + ti;
+        const bool valid = j < nk;
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        const uint4 kv = valid ? lds128(kp + (size_t)j * D * 2 + sub * 16) : z;
+        const uint4 vv = valid ? lds128(vp + (size_t)j * D * 2 + sub * 16) : z;
+        attn_key<D, GH>(qf, o, mm, ll, kv, vv, valid);
       }
     }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const bool valid = base + u * stride + ti < t1;
-      float s[GH];
-#pragma unroll
-      for (int h = 0; h < GH; ++h) {
-        float acc = qf[h][0] * bf_lo(kv[u].x);
-        acc = fmaf(qf[h][1], bf_hi(kv[u].x), acc);
-        acc = fmaf(qf[h][2], bf_lo(kv[u].y), acc);
-        acc = fmaf(qf[h][3], bf_hi(kv[u].y), acc);
-        acc = fmaf(qf[h][4], bf_lo(kv[u].z), acc);
-        acc = fmaf(qf[h][5], bf_hi(kv[u].z), acc);
-        acc = fmaf(qf[h][6], bf_lo(kv[u].w), acc);
-        acc = fmaf(qf[h][7], bf_hi(kv[u].w), acc);
-        s[h] = acc;
-      }
-#pragma unroll
-      for (int off = 1; off < LPT; off <<= 1)
-#pragma unroll
-        for (int h = 0; h < GH; ++h) s[h] += __shfl_xor_sync(0xffffffffu, s[h], off);
-      if (valid) {
-        const float vf[8] = {bf_lo(vv[u].x), bf_hi(vv[u].x), bf_lo(vv[u].y), bf_hi(vv[u].y),
-                             bf_lo(vv[u].z), bf_hi(vv[u].z), bf_lo(vv[u].w), bf_hi(vv[u].w)};
-#pragma unroll
-        for (int h = 0; h < GH; ++h) {
-          const float mn = fmaxf(mm[h], s[h]);
-          const float sc = exp2f(mm[h] - mn);
-          const float pe = exp2f(s[h] - mn);
-          ll[h] = ll[h] * sc + pe;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pe, vf[e], o[h][e] * sc);
-          mm[h] = mn;
-        }
-      }
-    }
+    // a page whose copy has not landed (after an abort) is never released
+    __syncwarp();
+    if (release && lane == 0 && ok) mbar_arrive(&m->empty[slot]);
   }
   // merge the key groups of the warp (lanes with the same `sub`)
 #pragma unroll
@@ -781,20 +839,22 @@ __device__ __forceinline__ void attn_partial(const Params& p, uint8_t* smem, con
   }
 }
 
-// GS > 0: the q-heads per kv-head are fixed at compile time (one variant)
+// GS > 0: the q-heads per kv-head are fixed at compile time (one variant).
+// page_base: the unit's first page in this SM's page stream.
 template <int D, int GS>
-__device__ void attn_unit(const Params& p, uint8_t* smem, const Instr& in) {
+__device__ void attn_unit(const Params& p, Misc* m, uint8_t* smem, const Instr& in, uint32_t page_base) {
   if constexpr (GS == 1 || GS == 2 || GS == 4) {
-    attn_partial<D, GS>(p, smem, in, 0);
+    attn_partial<D, GS>(p, m, smem, in, 0, page_base, true);
   } else if constexpr (GS > 4) {
-    for (int h0 = 0; h0 < GS; h0 += 4) attn_partial<D, 4>(p, smem, in, h0);
+    for (int h0 = 0; h0 < GS; h0 += 4) attn_partial<D, 4>(p, m, smem, in, h0, page_base, h0 + 4 >= GS);
   } else {
     switch (p.G) {
-      case 1: attn_partial<D, 1>(p, smem, in, 0); break;
-      case 2: attn_partial<D, 2>(p, smem, in, 0); break;
-      case 4: attn_partial<D, 4>(p, smem, in, 0); break;
+      case 1: attn_partial<D, 1>(p, m, smem, in, 0, page_base, true); break;
+      case 2: attn_partial<D, 2>(p, m, smem, in, 0, page_base, true); break;
+      case 4: attn_partial<D, 4>(p, m, smem, in, 0, page_base, true); break;
       default:
-        for (int h0 = 0; h0 < p.G; h0 += 4) attn_partial<D, 4>(p, smem, in, h0);
+        for (int h0 = 0; h0 < p.G; h0 += 4)
+          attn_partial<D, 4>(p, m, smem, in, h0, page_base, h0 + 4 >= p.G);
         break;
     }
   }
@@ -916,9 +976,10 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
       st.key_h = -1;
       // runs even after an abort: its loads stay in bounds and its barriers
       // must be met by every compute warp
-      if constexpr (DS > 0) attn_unit<DS, GS>(p, smem, in);
-      else if (p.D == 64) attn_unit<64, GS>(p, smem, in);
-      else attn_unit<128, GS>(p, smem, in);
+      if constexpr (DS > 0) attn_unit<DS, GS>(p, m, smem, in, page_cnt);
+      else if (p.D == 64) attn_unit<64, GS>(p, m, smem, in, page_cnt);
+      else attn_unit<128, GS>(p, m, smem, in, page_cnt);
+      page_cnt += (uint32_t)attn_span(p.pos[in.a0], in.a2 >> 16, in.a2 & 0xffff, p.D).npages;
     } else if (in.op == MK_OP_RED) {
       if (!aborted(m)) {
         if constexpr (DS > 0) attn_reduce<DS>(p, in);
@@ -1121,7 +1182,9 @@ __global__ void __launch_bounds__(kThreads, 1) interp_kernel(const __grid_consta
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.n_pages; ++i) {
       mbar_init(&m->full[i], 1);
-      mbar_init(&m->empty[i], 1);  // the page's owner warp releases it
+      // a GEMV page's owner warp releases it with all kComputeWarps arrivals;
+      // an attention page is released by every compute warp, one each
+      mbar_init(&m->empty[i], kComputeWarps);
     }
     for (int i = 0; i < kResBufs; ++i) {
       mbar_init(&m->res_full[i], kComputeWarps);

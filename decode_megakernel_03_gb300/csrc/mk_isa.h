@@ -127,6 +127,34 @@ MK_HD Geom geom_of(int op, int H, int QD, int Fc) {
   return g;
 }
 
+// One split-KV attention unit: keys [t0, t1) of the keys 0..pos of its
+// sequence, partition pidx of P (the host picks P; the device recomputes the
+// range from the exact position). The new key (pos), whose k/v row this step
+// writes, is read from the cache after the unit's counter wait; the other
+// nc = |[t0, min(t1, pos))| keys are cached already and stream through
+// shared-memory pages ahead of that wait, kpp keys per page: K rows in the
+// page's first half, V rows in its second.
+struct AttnSpan {
+  int t0, t1;   // the unit's keys
+  int nc;       // cached keys [t0, t0 + nc), all below pos
+  int kpp;      // keys per page
+  int npages;   // pages of cached keys
+};
+
+MK_HD AttnSpan attn_span(int pos, int pidx, int P, int D) {
+  const int len = pos + 1;
+  AttnSpan s;
+  // 32-bit arithmetic (the host checks kv_capacity * kMaxPartitions < 2^31);
+  // a 64-bit division would cost far more code and time
+  s.t0 = pidx * len / P;
+  s.t1 = (pidx + 1) * len / P;
+  const int end = s.t1 < pos ? s.t1 : pos;
+  s.nc = end > s.t0 ? end - s.t0 : 0;
+  s.kpp = kPageBytes / (4 * D);
+  s.npages = (s.nc + s.kpp - 1) / s.kpp;
+  return s;
+}
+
 // q/k/v row pairs are numbered group-major: for kv-head g, the G q-heads of the
 // group, then k-head g, then v-head g; inside a head, pair i holds rows i and
 // i + D/2 (the rotate-half RoPE partners).

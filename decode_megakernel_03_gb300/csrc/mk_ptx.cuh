@@ -35,6 +35,16 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   (void)state;
 }
 
+// `count` arrivals at once
+__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t count) {
+  uint64_t state;
+  asm volatile("mbarrier.arrive.shared::cta.b64 %0, [%1], %2;"
+               : "=l"(state)
+               : "r"(smem_u32(bar)), "r"(count)
+               : "memory");
+  (void)state;
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   uint64_t state;
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 %0, [%1], %2;"

@@ -37,6 +37,7 @@ std::string check_shape(const Shape& s) {
   if (s.V < 1) return bad("vocab must be positive");
   if (s.B != 1 && s.B != 2 && s.B != 4 && s.B != 8) return bad("batch must be 1, 2, 4 or 8");
   if (s.S < 1) return bad("kv_capacity must be positive");
+  if ((long)s.S * kMaxPartitions >= (1L << 31)) return bad("kv_capacity must be below 2^31 / 64");
   return std::string();
 }
 
