@@ -301,6 +301,8 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
   p.xa = reinterpret_cast<float*>(base + offs[1]);
   p.q = reinterpret_cast<float*>(base + offs[2]);
   p.part = reinterpret_cast<float*>(base + offs[3]);
+  // (m, l) after the o rows, in the same piece
+  p.part_ml = p.part + (size_t)B * s.nh * kMaxPartitions * s.D;
   p.attn = reinterpret_cast<float*>(base + offs[4]);
   p.h = reinterpret_cast<float*>(base + offs[5]);
   p.dacc = reinterpret_cast<float*>(base + offs[6]);

@@ -446,6 +446,97 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
   }
 }
 
+// One sequence: the O-projection's input, every head's attention output,
+// reduced from the split-KV partials as it is staged (the reduction
+// instruction fused into the O-projection). Thread t takes the 4-dimension
+// column groups t + i * kComputeThreads (i < kG), so the LPH lanes of a warp
+// that cover one head's columns form an aligned group. Per round of kR
+// partitions every load is issued first: each lane the o of its groups for
+// the round's partitions, and the (m, l) of one partition of its head, which
+// the head's lanes then share by shuffles; weights e^(m_k - M) rescale online
+// across rounds. P: partitions per head.
+template <int D>
+__device__ __forceinline__ void stage_attn_fused(const Params& p, uint8_t* smem, Staged& st,
+                                                 int layer, int P) {
+  constexpr int kG = 1;  // column groups per thread per pass (768 columns: smaller code, as fast)
+  constexpr int kR = 6;  // partitions per round
+  constexpr int LPH = D / 4 < 32 ? D / 4 : 32;  // lanes covering one head
+  const int tid = compute_tid(), lane = threadIdx.x & 31;
+  const int lead = lane & ~(LPH - 1);
+  float* dst = reinterpret_cast<float*>(smem + p.off_x);
+  compute_bar();  // everyone is done reading the buffer's previous contents
+  for (int q0 = tid; q0 * 4 < p.QD; q0 += kComputeThreads * kG) {
+    float M[kG], den[kG];
+    float4 acc[kG];
+#pragma unroll
+    for (int i = 0; i < kG; ++i) {
+      M[i] = -INFINITY;
+      den[i] = 0.f;
+      acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int k0 = 0; k0 < P; k0 += kR) {
+      float4 o[kG][kR];
+      float2 ml[kG];
+#pragma unroll
+      for (int i = 0; i < kG; ++i) {
+        const int c = (q0 + i * kComputeThreads) * 4;  // the whole warp agrees on c < QD
+        if (c < p.QD) {
+          const int h = c / D;
+          const float* ob = p.part + ((size_t)h * kMaxPartitions + k0) * D + (c - h * D);
+#pragma unroll
+          for (int k = 0; k < kR; ++k)
+            if (k0 + k < P) o[i][k] = __ldcg(reinterpret_cast<const float4*>(ob + (size_t)k * D));
+          const int kk = k0 + (lane & (LPH - 1));
+          ml[i] = kk < P && (lane & (LPH - 1)) < kR
+                      ? __ldcg(reinterpret_cast<const float2*>(p.part_ml + ((size_t)h * kMaxPartitions + kk) * 2))
+                      : make_float2(-INFINITY, 0.f);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kG; ++i) {
+        const int c = (q0 + i * kComputeThreads) * 4;
+        if (c >= p.QD) continue;  // warp-uniform
+        float mr = ml[i].x;
+#pragma unroll
+        for (int off = 1; off < LPH; off <<= 1) mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, off));
+        const float Mn = fmaxf(M[i], mr);
+        const float sc = M[i] == -INFINITY ? 0.f : fast_exp2(M[i] - Mn);
+        den[i] *= sc;
+        acc[i].x *= sc; acc[i].y *= sc; acc[i].z *= sc; acc[i].w *= sc;
+#pragma unroll
+        for (int k = 0; k < kR; ++k) {
+          const float mk = __shfl_sync(0xffffffffu, ml[i].x, lead | k);
+          const float lk = __shfl_sync(0xffffffffu, ml[i].y, lead | k);
+          if (k0 + k < P && mk != -INFINITY) {
+            const float w = fast_exp2(mk - Mn);
+            den[i] = fmaf(w, lk, den[i]);
+            acc[i].x = fmaf(w, o[i][k].x, acc[i].x);
+            acc[i].y = fmaf(w, o[i][k].y, acc[i].y);
+            acc[i].z = fmaf(w, o[i][k].z, acc[i].z);
+            acc[i].w = fmaf(w, o[i][k].w, acc[i].w);
+          }
+        }
+        M[i] = Mn;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kG; ++i) {
+      const int c = (q0 + i * kComputeThreads) * 4;
+      if (c < p.QD) {
+        const float inv = 1.f / den[i];
+        *reinterpret_cast<float4*>(dst + c) =
+            make_float4(acc[i].x * inv, acc[i].y * inv, acc[i].z * inv, acc[i].w * inv);
+      }
+    }
+  }
+  compute_bar();
+  st.stage_cnt++;
+  st.key_x = act_key(kActAttnOut, layer, 0);
+#pragma unroll
+  for (int b = 0; b < kMaxBatch; ++b) st.inv_x.v[b] = 1.f;
+  if (p.alias_xh) st.key_h = -1;
+}
+
 // One sequence, rows of at most 2048 columns: each compute warp copies the
 // staged vector into registers in the layout of the page dot products (lane
 // l, block j: columns j*256 + l*8 .. +8), scaled by 1/rms for the norms.
@@ -666,7 +757,7 @@ __device__ __forceinline__ void softmax_merge(float& m, float& l, float* o, floa
                                               const float* o2) {
   const float M = fmaxf(m, m2);
   if (M == -INFINITY) return;
-  const float s1 = exp2f(m - M), s2 = exp2f(m2 - M);
+  const float s1 = fast_exp2(m - M), s2 = fast_exp2(m2 - M);
   l = l * s1 + l2 * s2;
 #pragma unroll
   for (int e = 0; e < 8; ++e) o[e] = o[e] * s1 + o2[e] * s2;
@@ -705,8 +796,8 @@ __device__ __forceinline__ void attn_key(const float (&qf)[GH][8], float (&o)[GH
 #pragma unroll
     for (int h = 0; h < GH; ++h) {
       const float mn = fmaxf(mm[h], s[h]);
-      const float sc = exp2f(mm[h] - mn);
-      const float pe = exp2f(s[h] - mn);
+      const float sc = fast_exp2(mm[h] - mn);
+      const float pe = fast_exp2(s[h] - mn);
       ll[h] = ll[h] * sc + pe;
 #pragma unroll
       for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pe, vf[e], o[h][e] * sc);
@@ -826,15 +917,15 @@ __device__ __forceinline__ void attn_partial(const Params& p, Misc* m, uint8_t* 
 #pragma unroll
     for (int w = 0; w < kComputeWarps; ++w) {
       const float* sp = scr + ((size_t)w * GH + h) * (D + 2);
-      const float wt = sp[D] == -INFINITY ? 0.f : exp2f(sp[D] - M);
+      const float wt = sp[D] == -INFINITY ? 0.f : fast_exp2(sp[D] - M);
       acc = fmaf(wt, sp[d], acc);
       den = fmaf(wt, sp[D + 1], den);
     }
-    float* dst = p.part + (((size_t)b * p.nh + g * p.G + h0 + h) * kMaxPartitions + pidx) * (D + 2);
-    dst[d] = acc;
+    const size_t row = ((size_t)b * p.nh + g * p.G + h0 + h) * kMaxPartitions + pidx;
+    p.part[row * D + d] = acc;
     if (d == 0) {
-      dst[D] = M;
-      dst[D + 1] = den;
+      p.part_ml[row * 2] = M;
+      p.part_ml[row * 2 + 1] = den;
     }
   }
 }
@@ -871,19 +962,20 @@ __device__ __forceinline__ void attn_reduce(const Params& p, const Instr& in) {
   const int b = in.a0, g = in.a1, P = in.a2;
   for (int hl = warp; hl < p.G; hl += kComputeWarps) {
     const int h = g * p.G + hl;
-    const float* base = p.part + ((size_t)b * p.nh + h) * kMaxPartitions * (D + 2);
+    const float* base = p.part + ((size_t)b * p.nh + h) * kMaxPartitions * D;
+    const float* ml = p.part_ml + ((size_t)b * p.nh + h) * kMaxPartitions * 2;
     float M = -INFINITY;
-    for (int k = lane; k < P; k += 32) M = fmaxf(M, __ldcg(base + (size_t)k * (D + 2) + D));
+    for (int k = lane; k < P; k += 32) M = fmaxf(M, __ldcg(ml + 2 * k));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float acc[PL], den = 0.f;
 #pragma unroll
     for (int e = 0; e < PL; ++e) acc[e] = 0.f;
     for (int k = 0; k < P; ++k) {
-      const float* s = base + (size_t)k * (D + 2);
-      const float mk = __ldcg(s + D);
-      const float wt = mk == -INFINITY ? 0.f : exp2f(mk - M);
-      den = fmaf(wt, __ldcg(s + D + 1), den);
+      const float* s = base + (size_t)k * D;
+      const float mk = __ldcg(ml + 2 * k);
+      const float wt = mk == -INFINITY ? 0.f : fast_exp2(mk - M);
+      den = fmaf(wt, __ldcg(ml + 2 * k + 1), den);
 #pragma unroll
       for (int e = 0; e < PL; ++e) acc[e] = fmaf(wt, __ldcg(s + lane * PL + e), acc[e]);
     }
@@ -950,7 +1042,18 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
         h_got = wait_mbar(p, m, &m->hfull[k], (h_cnt >> 1) & 1u, kErrTimeoutRes);
         act = reinterpret_cast<const float*>(smem + p.off_h) + (size_t)k * p.Fc;
       } else {
-        if ((to_h ? st.key_h : st.key_x) != key) stage(p, m, smem, st, kind, in.layer, chunk);
+        if ((to_h ? st.key_h : st.key_x) != key) {
+          bool staged = false;
+          if constexpr (B == 1) {  // one sequence: the O-projection reduces while staging
+            if (kind == kActAttnOut && p.fused_red) {
+              if constexpr (DS > 0) stage_attn_fused<DS>(p, smem, st, in.layer, in.a2);
+              else if (p.D == 64) stage_attn_fused<64>(p, smem, st, in.layer, in.a2);
+              else stage_attn_fused<128>(p, smem, st, in.layer, in.a2);
+              staged = true;
+            }
+          }
+          if (!staged) stage(p, m, smem, st, kind, in.layer, chunk);
+        }
         act = reinterpret_cast<const float*>(smem + (to_h ? p.off_h : p.off_x));
       }
       if (tracing) t_staged = globaltimer();
@@ -981,7 +1084,9 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
       else attn_unit<128, GS>(p, m, smem, in, page_cnt);
       page_cnt += (uint32_t)attn_span(p.pos[in.a0], in.a2 >> 16, in.a2 & 0xffff, p.D).npages;
     } else if (in.op == MK_OP_RED) {
-      if (!aborted(m)) {
+      // the reduction instruction runs only with several sequences (one
+      // sequence reduces in the O-projection's staging)
+      if constexpr (B > 1) if (!aborted(m)) {
         if constexpr (DS > 0) attn_reduce<DS>(p, in);
         else if (p.D == 64) attn_reduce<64>(p, in);
         else attn_reduce<128>(p, in);

@@ -61,7 +61,8 @@ struct Params {
   float* x;      // [B][H] residual stream between layers
   float* xa;     // [B][H] residual after the attention block
   float* q;      // [B][nh*D] rotated queries
-  float* part;   // [B][nh][kMaxPartitions][D + 2] attention partials (o, m, l)
+  float* part;   // [B][nh][kMaxPartitions][D] attention partials: o
+  float* part_ml; // [B][nh][kMaxPartitions][2] attention partials: (m, l)
   float* attn;   // [B][nh*D] reduced attention output
   float* h;      // [B][F] SwiGLU hidden state
   float* dacc;   // [B][H] down-projection partial sums across chunks
@@ -84,6 +85,8 @@ struct Params {
   int off_dacc, dacc_rows;     // down-projection chunk sums, row j at slot j % dacc_rows
   int x_floats, h_floats, res_floats;
   int alias_xh;                // x and h staging share one buffer
+  int fused_red;               // one sequence: the O-projection's staging reduces the
+                               // attention partials itself (no reduction instruction)
   int h_ring;                  // one sequence: the loader fetches each down-projection
                                // chunk of h into one of two h slots (at off_h)
   // per step

@@ -185,6 +185,15 @@ __device__ __forceinline__ void ffma2(unsigned long long& acc, unsigned long lon
   asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
 }
 
+// 2^x with the hardware approximation (ex2.approx.ftz: relative error below
+// 2^-22; results below the normal range flush to zero). Softmax weights
+// 2^(m - M) with m <= M need nothing more.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // bf16 pair in a 32-bit word -> two floats (exact widening)
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }

@@ -3,7 +3,7 @@
 // The queues of all SMs are cut from ONE global order of the step:
 //
 //   for each layer l:
-//     QKV(l)  ATTN(l)  RED(l)  OPROJ(l)
+//     QKV(l)  ATTN(l)  RED(l)  OPROJ(l)   (one sequence: no RED; OPROJ reduces)
 //     GATEUP(l,0)  GATEUP(l,1) DOWN(l,0)  GATEUP(l,2) DOWN(l,1)  ...  DOWN(l,3)
 //   LMHEAD
 //
@@ -52,8 +52,12 @@ void choose_partitions(const Shape& s, int n_sm, const int* positions, int* part
     work += bucket[b] * s.nkv;
   }
   // about one partition per SM over all (sequence, kv-head) pairs, and at
-  // least 64 keys per partition so each stays worth a queue entry
-  long per = std::max<long>(64, (work + n_sm - 1) / std::max(1, n_sm));
+  // least 64 keys per partition so each stays worth a queue entry. With one
+  // sequence the O-projection reduces the partials while staging, so fewer,
+  // longer partitions (at least 128 keys: two pages) keep that cheap; the
+  // keys stream through pages ahead of the unit, so a longer one costs little
+  const long min_keys = fused_reduction(s) ? 128 : 64;
+  long per = std::max<long>(min_keys, (work + n_sm - 1) / std::max(1, n_sm));
   for (int b = 0; b < kMaxBatch; ++b) parts[b] = 0;
   for (int b = 0; b < s.B; ++b) {
     long p = (bucket[b] + per - 1) / per;
@@ -120,6 +124,7 @@ struct Builder {
 
   void add_layer(int l, const int* parts, int rot) {
     const int H = s.H, G = s.G(), Fc = s.Fc();
+    const bool fused = fused_reduction(s);
     const int ppg = s.pairs_per_group();
     // 1. RMSNorm + QKV + RoPE + KV append
     {
@@ -141,12 +146,13 @@ struct Builder {
           for (int p = 0; p < parts[b]; ++p, ++k) {
             int sm = (rot + k) % n_sm;
             st.items.push_back({sm, make(MK_OP_ATTN, l, b, g, (p << 16) | parts[b], cm.qkv(l, g),
-                                         ppg, cm.att(l, b, g), 1)});
+                                         ppg, fused ? cm.red(l) : cm.att(l, b, g), 1)});
           }
       steps.push_back(std::move(st));
     }
-    // 3. attention reduction: one unit per (sequence, kv-head)
-    {
+    // 3. attention reduction: one unit per (sequence, kv-head); one sequence:
+    // none, the O-projection reduces while staging
+    if (!fused) {
       Step st{MK_OP_RED, l, {}};
       int k = 0;
       for (int b = 0; b < s.B; ++b)
@@ -160,9 +166,11 @@ struct Builder {
     // 4. O-projection + residual
     {
       Step st{MK_OP_OPROJ, l, {}};
+      // fused: a2 = partitions per head, and the wait is for every unit
+      const int red_target = fused ? s.nkv * parts[0] : s.B * s.nkv;
       spread(H, 0, rot_of(l, 1), [&](int sm, int a, int b) {
-        st.items.push_back({sm, make(MK_OP_OPROJ, l, a, b, 0, cm.red(l), s.B * s.nkv, cm.omid(l),
-                                     b - a)});
+        st.items.push_back({sm, make(MK_OP_OPROJ, l, a, b, fused ? parts[0] : 0, cm.red(l),
+                                     red_target, cm.omid(l), b - a)});
       });
       steps.push_back(std::move(st));
     }
@@ -296,6 +304,7 @@ int smem_layout(const Shape& s, int n_sm, int optin, int misc_bytes, Params* p, 
   p->x_floats = B * std::max(s.H, s.QD());
   p->h_floats = B * s.Fc();
   p->alias_xh = B > 1 ? 1 : 0;
+  p->fused_red = fused_reduction(s) ? 1 : 0;
   p->res_floats = item_cap_for(s) * 2 * B;
   // every SM's down-projection rows form one contiguous range of at most
   // ceil(H / n_sm) rows, so row j can keep its chunk sum at slot j % dacc_rows

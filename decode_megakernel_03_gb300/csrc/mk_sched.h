@@ -59,6 +59,10 @@ std::string check_shape(const Shape& s);
 // position.
 void choose_partitions(const Shape& s, int n_sm, const int* positions, int* parts);
 
+// One sequence: the O-projection reduces the attention partials while it
+// stages its input (no reduction instruction between them).
+inline bool fused_reduction(const Shape& s) { return s.B == 1; }
+
 // Items (rows or row pairs) per GEMV instruction, bounded by the result
 // buffer the storer drains.
 int item_cap_for(const Shape& s);

@@ -22,6 +22,12 @@ def _lib():
     mkbuild.build()
 
 
+def _fused(B):
+    """One sequence: no reduction instruction; the O-projection reduces the
+    attention partials while it stages its input."""
+    return B == 1
+
+
 def _plan(shape, B, S, n_sm, pos):
     ins, off, tg = mk.schedule(shape, B, S, n_sm, pos)
     sm = np.zeros(len(ins), dtype=np.int64)
@@ -79,12 +85,19 @@ def test_every_output_produced_exactly_once(case):
             assert r[0][0] == c * Fc and r[-1][1] == (c + 1) * Fc
             _check_partition([(a - c * Fc, b - c * Fc) for a, b in r], Fc)
             _check_partition(_ranges(ins, (op == mk.OP_DOWN) & (layer == l) & (ins["a2"] == c)), H)
-        # attention: each (b, g) has partitions 0..P-1 once, and one reduction with that P
+        # attention: each (b, g) has partitions 0..P-1 once, and its reduction
+        # (a reduction instruction, or every O-projection unit) uses that P
         att = ins[(op == mk.OP_ATTN) & (layer == l)]
-        red = ins[(op == mk.OP_RED) & (layer == l)]
+        if _fused(B):
+            assert not np.any((op == mk.OP_RED) & (layer == l))
+            o = ins[(op == mk.OP_OPROJ) & (layer == l)]
+            assert len(set(int(x) for x in o["a2"])) == 1
+            red = [(0, g, int(o["a2"][0])) for g in range(shape.n_kv_heads)]
+        else:
+            red = [(int(r["a0"]), int(r["a1"]), int(r["a2"]))
+                   for r in ins[(op == mk.OP_RED) & (layer == l)]]
         assert len(red) == B * shape.n_kv_heads
-        for r in red:
-            b, g, P = int(r["a0"]), int(r["a1"]), int(r["a2"])
+        for b, g, P in red:
             mine = att[(att["a0"] == b) & (att["a1"] == g)]
             assert sorted(int(x) >> 16 for x in mine["a2"]) == list(range(P))
             assert all((int(x) & 0xFFFF) == P for x in mine["a2"])
@@ -106,7 +119,7 @@ def test_counter_targets(case):
     np.testing.assert_array_equal(sums, tg)
     w = ins["wait_ctr"] >= 0
     np.testing.assert_array_equal(ins["wait_target"][w], tg[ins["wait_ctr"][w]])
-    assert np.all(tg > 0), "every counter is produced"
+    assert np.all(tg[ins["wait_ctr"][w]] > 0), "every awaited counter is produced"
 
 
 def _simulate(ins, off, tg, n_sm, pick):
@@ -228,7 +241,10 @@ def _accesses(ins, shape, B):
             R |= {("part", a0, a1, p) for p in range(a2)}
             W.add(("attn", a0, a1))
         elif op == mk.OP_OPROJ:
-            R |= {("attn", b, g) for b in range(B) for g in range(nkv)}
+            if _fused(B):  # reduces every head's partitions while staging
+                R |= {("part", 0, g, p) for g in range(nkv) for p in range(a2)}
+            else:
+                R |= {("attn", b, g) for b in range(B) for g in range(nkv)}
             if l > 0:
                 R |= {("x", k) for k in range(a0, a1)}
             W |= {("xa", k) for k in range(a0, a1)}
