@@ -309,7 +309,9 @@ def run_gpu(args, wl):
                 "megakernel_p90_us": float(np.percentile(per_mega, 90)) * 1e3,
                 "multilaunch_us": multi_ms * 1e3,
                 "multilaunch_graph_us": graph_ms * 1e3,
-                "multilaunch_launches_per_step": 6 * shape.n_layers + 1,
+                # per layer QKV, attention, (reduction,) O-projection, gate/up,
+                # down; one sequence has no reduction instruction
+                "multilaunch_launches_per_step": (5 if wl.batch == 1 else 6) * shape.n_layers + 1,
                 "recovered_overhead_vs_multilaunch": (multi_ms - ms) / (multi_ms - t_min_ms),
                 "recovered_overhead_vs_graph": (graph_ms - ms) / (graph_ms - t_min_ms),
                 "overhead_megakernel": (ms - t_min_ms) / ms,
