@@ -349,7 +349,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
     lp[l].kc = static_cast<uint16_t*>(k_cache[l]);
     lp[l].vc = static_cast<uint16_t*>(v_cache[l]);
   }
-  h->fn = kernel_for(B, s.D, s.G(), false);
+  h->fn = kernel_for(s, false);
   ce = cudaMemcpy(h->d_rope, rope.data(), sizeof(float2) * rope.size(), cudaMemcpyHostToDevice);
   if (ce == cudaSuccess)
     ce = cudaFuncSetAttribute(h->fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -390,7 +390,7 @@ int mk_set_trace(mk_handle* h, mk_trace_record* buf, int capacity) {
 int mk_debug_use_generic_kernel(mk_handle* h, int enable) {
   if (!h) return MK_ERR_INVALID;
   const Shape& s = h->shape;
-  const void* fn = kernel_for(s.B, s.D, s.G(), enable != 0);
+  const void* fn = kernel_for(s, enable != 0);
   MK_CUDA(h, cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, h->smem_bytes));
   h->fn = fn;
   return MK_OK;

@@ -25,7 +25,9 @@
 //
 // The kernel is a template over the batch B and, optionally, the head
 // dimension DS and the q-heads per kv-head GS (0: read from the parameters
-// at run time). An interpreter that carries every attention variant is about
+// at run time), and KW: 2048 when every GEMV row (hidden, n_heads*head_dim
+// and ffn/4 columns) is 2048 wide, so only the full-page register path is
+// compiled (0: any width). An interpreter that carries every attention variant is about
 // twice the size of one specialised to its model's shape, and the SM's
 // instruction cache cannot hold it: the code of the instructions that run
 // together (loader, staging, pages, attention, epilogues) must fit, or the
@@ -681,7 +683,8 @@ __device__ __forceinline__ void page_rows_smem(const uint8_t* page, int n_rows, 
 
 // kRegs: the activations are in the caller's registers a[] (B == 1, rows of at
 // most 2048 columns); otherwise they are read from the staged buffer `act`.
-template <int B, bool kRegs>
+// KW == 2048: every row is 2048 wide (only the full-page code is compiled).
+template <int B, bool kRegs, int KW>
 __device__ __forceinline__ void gemv_run(const Params& p, Misc* m, uint8_t* smem, const Instr& in,
                                          const Geom& g, const float* act, const InvScale& inv,
                                          const float (&a)[64], float* res, uint32_t page_base) {
@@ -709,7 +712,7 @@ __device__ __forceinline__ void gemv_run(const Params& p, Misc* m, uint8_t* smem
       const int n_rows = n_in * g.R;
       float* const res_page = res + (size_t)(pg * g.ipp) * g.R * B;
       if (kRegs) {
-        if (nblk == 8) {
+        if (KW == 2048 || nblk == 8) {
           // pages of 2048-column rows, full or the short last page of an
           // instruction: one call site of the full-page code (a second copy
           // costs instruction-cache space). It dots all four row slots; on a
@@ -718,7 +721,7 @@ __device__ __forceinline__ void gemv_run(const Params& p, Misc* m, uint8_t* smem
           const int pr = min(lane & 3, n_rows - 1);
           const int r = pr / n_in, k = pr - r * n_in;
           rows4_reg<8>(page, n_rows, row_bytes, 8, a, res_page + ((size_t)k * g.R + r) * B, lane);
-        } else {
+        } else if constexpr (KW == 0) {
           for (int r0 = 0; r0 < n_rows; r0 += 4) {
             const int pr = min(r0 + (lane & 3), n_rows - 1);
             const int r = pr / n_in, k = pr - r * n_in;
@@ -990,7 +993,7 @@ __device__ __forceinline__ void attn_reduce(const Params& p, const Instr& in) {
 // compute role: the instruction loop
 // ---------------------------------------------------------------------------
 
-template <int B, int DS, int GS>
+template <int B, int DS, int GS, int KW>
 __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Instr* q, int n,
                              int qbase) {
   const int warp = compute_warp(), lane = threadIdx.x & 31;
@@ -1069,9 +1072,10 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
           if (lane == 0 && h_got) mbar_arrive(&m->hempty[h_cnt & 1u]);
           ++h_cnt;
         }
-        gemv_run<B, true>(p, m, smem, in, g, act, one, ax, res, page_cnt);
+        gemv_run<B, true, KW>(p, m, smem, in, g, act, one, ax, res, page_cnt);
       } else {
-        gemv_run<B, false>(p, m, smem, in, g, act, to_h ? one : st.inv_x, ax, res, page_cnt);
+        if constexpr (KW == 0)
+          gemv_run<B, false, KW>(p, m, smem, in, g, act, to_h ? one : st.inv_x, ax, res, page_cnt);
       }
       page_cnt += (uint32_t)((in.a1 - in.a0 + g.ipp - 1) / g.ipp);
     } else if (in.op == MK_OP_ATTN) {
@@ -1280,7 +1284,7 @@ __device__ void storer_role(const Params& p, Misc* m, uint8_t* smem, const Instr
 // the kernel
 // ---------------------------------------------------------------------------
 
-template <int B, int DS, int GS>
+template <int B, int DS, int GS, int KW>
 __global__ void __launch_bounds__(kThreads, 1) interp_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Misc* m = reinterpret_cast<Misc*>(smem + p.off_misc);
@@ -1314,7 +1318,7 @@ __global__ void __launch_bounds__(kThreads, 1) interp_kernel(const __grid_consta
   const int warp = threadIdx.x >> 5;
   if (warp == kLoaderWarp) loader_role(p, m, smem, q, n);
   else if (warp == kStorerWarp) storer_role<B>(p, m, smem, q, n);
-  else compute_role<B, DS, GS>(p, m, smem, q, n, q0);
+  else compute_role<B, DS, GS, KW>(p, m, smem, q, n, q0);
 }
 
 }  // namespace mk

@@ -3,12 +3,13 @@
 // and eight sequences with the Llama-3.2-1B head shape.
 #include "mk_interp.cuh"
 #include "mk_kernels.h"
+#include "mk_sched.h"
 
 namespace mk {
 
-const void* kernel_fixed_b(int B, int D, int G) {
-  if (B == 1 && D == 128 && G == 4) return reinterpret_cast<const void*>(&interp_kernel<1, 128, 4>);
-  if (B == 8 && D == 64 && G == 4) return reinterpret_cast<const void*>(&interp_kernel<8, 64, 4>);
+const void* kernel_fixed_b(const Shape& s) {
+  if (s.B == 1 && s.D == 128 && s.G() == 4) return reinterpret_cast<const void*>(&interp_kernel<1, 128, 4, 0>);
+  if (s.B == 8 && s.D == 64 && s.G() == 4) return reinterpret_cast<const void*>(&interp_kernel<8, 64, 4, 0>);
   return nullptr;
 }
 

@@ -240,7 +240,7 @@ extern "C" int mk_decode_step_noalloc(const mk_config* cfg, const mk_weights* w,
       rope[(size_t)pos * (s.D / 2) + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
     }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const void* fn = kernel_for(B, s.D, s.G(), false);
+  const void* fn = kernel_for(s, false);
   // pageable-source copies are staged by the driver before they return, so
   // the host vectors may go out of scope right after the calls
   ce = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
