@@ -363,65 +363,95 @@ __device__ __forceinline__ const uint16_t* norm_weight(const Params& p, int kind
 // Stages the activation vector(s) of `kind` for all B sequences into the x or
 // h buffer. For the RMSNorm kinds the buffer holds x * w (the gain already
 // applied) and 1/rms(x) per sequence is returned in st.inv_x.
+// Several sequences (B > 1): sequence b's row starts at word b * (K + 4), and
+// each group of four columns c .. c + 3 is stored in place as the bf16 split
+// v = hi + lo of its values, {hi(c, c+1), lo(c, c+1), hi(c+2, c+3),
+// lo(c+2, c+3)}: the A fragment of the tensor-core product (page_rows_mma).
+template <int B>
 __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, Staged& st, int kind,
                                       int layer, int chunk) {
+  constexpr bool kFrag = B > 1;
   const int tid = compute_tid();  // 0..kComputeThreads-1
   const int warp = tid >> 5, lane = tid & 31;
   const bool to_h = kind == kActH;
   float* dst = reinterpret_cast<float*>(smem + (to_h ? p.off_h : p.off_x));
   const int K = kind == kActAttnOut ? p.QD : (to_h ? p.Fc : p.H);
+  const int Ks = kFrag ? K + 4 : K;  // row stride of the buffer, in words
   const uint16_t* normw = norm_weight(p, kind, layer);
+  const bool from_embed = kind == kActAttnNorm && layer == 0;
+  // sequence b's source row: base + b * stride
+  const float* base;
+  size_t stride;
+  if (kind == kActAttnNorm || kind == kActFinalNorm) base = p.x, stride = p.H;
+  else if (kind == kActMlpNorm) base = p.xa, stride = p.H;
+  else if (kind == kActAttnOut) base = p.attn, stride = p.QD;
+  else base = p.h + (size_t)chunk * p.Fc, stride = p.F;
   const int par = st.stage_cnt & 1;
   compute_bar();  // everyone is done reading the buffer's previous contents
   // every thread issues all of its loads of a pass before using any, so a
-  // pass costs one round trip to L2 (a 2048-wide vector is one pass)
-  constexpr int kU = 4;
+  // pass costs one round trip to L2: 2048-wide vectors of all sequences at
+  // once
+  constexpr int kNB = B;
+  constexpr int kU = B == 1 ? 4 : 3;
   constexpr int kPass = kComputeThreads * 4 * kU;  // columns per pass
-  for (int b = 0; b < p.B; ++b) {
-    const bool from_embed = kind == kActAttnNorm && layer == 0;
-    const uint16_t* erow = p.embed + (size_t)p.tok[b] * p.H;
-    const float* src;
-    if (kind == kActAttnNorm || kind == kActFinalNorm) src = p.x + (size_t)b * p.H;
-    else if (kind == kActMlpNorm) src = p.xa + (size_t)b * p.H;
-    else if (kind == kActAttnOut) src = p.attn + (size_t)b * p.QD;
-    else src = p.h + (size_t)b * p.F + (size_t)chunk * p.Fc;
-    float ss = 0.f;
+  for (int b0 = 0; b0 < B; b0 += kNB) {
+    float ss[kNB];
+#pragma unroll
+    for (int bb = 0; bb < kNB; ++bb) ss[bb] = 0.f;
     for (int c0 = tid * 4; c0 < K; c0 += kPass) {
-      float4 v[kU];
+      float4 v[kNB][kU];
       uint2 wv[kU];
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
         const int c = c0 + u * kComputeThreads * 4;
         if (c < K) {
-          if (from_embed) {
-            const uint2 e = *reinterpret_cast<const uint2*>(erow + c);
-            v[u] = make_float4(bf_lo(e.x), bf_hi(e.x), bf_lo(e.y), bf_hi(e.y));
-          } else {
-            v[u] = __ldcg(reinterpret_cast<const float4*>(src + c));
-          }
           if (normw) wv[u] = __ldg(reinterpret_cast<const uint2*>(normw + c));
+#pragma unroll
+          for (int bb = 0; bb < kNB; ++bb) {
+            if (from_embed) {
+              const uint16_t* erow = p.embed + (size_t)p.tok[b0 + bb] * p.H;
+              const uint2 e = *reinterpret_cast<const uint2*>(erow + c);
+              v[bb][u] = make_float4(bf_lo(e.x), bf_hi(e.x), bf_lo(e.y), bf_hi(e.y));
+            } else {
+              v[bb][u] = __ldcg(reinterpret_cast<const float4*>(base + (b0 + bb) * stride + c));
+            }
+          }
         }
       }
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
         const int c = c0 + u * kComputeThreads * 4;
         if (c < K) {
-          float4 x = v[u];
-          ss += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
-          if (normw) {
-            x.x *= bf_lo(wv[u].x);
-            x.y *= bf_hi(wv[u].x);
-            x.z *= bf_lo(wv[u].y);
-            x.w *= bf_hi(wv[u].y);
+#pragma unroll
+          for (int bb = 0; bb < kNB; ++bb) {
+            float4 x = v[bb][u];
+            ss[bb] += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+            if (normw) {
+              x.x *= bf_lo(wv[u].x);
+              x.y *= bf_hi(wv[u].x);
+              x.z *= bf_lo(wv[u].y);
+              x.w *= bf_hi(wv[u].y);
+            }
+            float* d = dst + (size_t)(b0 + bb) * Ks + c;
+            if (kFrag) {
+              const uint32_t h01 = bf16x2_rn(x.x, x.y), h23 = bf16x2_rn(x.z, x.w);
+              const uint32_t l01 = bf16x2_rn(x.x - bf_lo(h01), x.y - bf_hi(h01));
+              const uint32_t l23 = bf16x2_rn(x.z - bf_lo(h23), x.w - bf_hi(h23));
+              *reinterpret_cast<uint4*>(d) = make_uint4(h01, l01, h23, l23);
+            } else {
+              *reinterpret_cast<float4*>(d) = x;
+            }
           }
-          *reinterpret_cast<float4*>(dst + (size_t)b * K + c) = x;
         }
       }
     }
     if (normw) {
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (lane == 0) m->red[par][warp][b] = ss;
+      for (int bb = 0; bb < kNB; ++bb) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss[bb] += __shfl_xor_sync(0xffffffffu, ss[bb], o);
+        if (lane == 0) m->red[par][warp][b0 + bb] = ss[bb];
+      }
     }
   }
   compute_bar();
@@ -429,7 +459,7 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
 #pragma unroll
   for (int b = 0; b < kMaxBatch; ++b) {
     inv.v[b] = 1.f;
-    if (normw && b < p.B) {
+    if (normw && b < B) {
       float sum = 0.f;
 #pragma unroll
       for (int w = 0; w < kComputeWarps; ++w) sum += m->red[par][w][b];
@@ -567,11 +597,15 @@ __device__ __forceinline__ void load_regs(float (&a)[64], const float* act, floa
 // ---------------------------------------------------------------------------
 // Each compute warp owns whole pages, dealt round-robin over the CTA's page
 // stream, and dots every row of its page with the activations of all B
-// sequences: lane l covers columns j*256 + l*8 .. +8 of each 256-column block,
-// i.e. every block is one 512-byte contiguous read of the row per warp. Four
-// rows are in flight at once (two accumulator chains each) for ILP. With one
-// sequence and rows of at most 2048 columns the activations sit in registers;
-// otherwise they are read from the staged buffer block by block.
+// sequences. One sequence runs on the CUDA cores: lane l covers columns
+// j*256 + l*8 .. +8 of each 256-column block, i.e. every block is one
+// 512-byte contiguous read of the row per warp, and four rows are in flight
+// at once (two accumulator chains each) for ILP; with rows of at most 2048
+// columns the activations sit in registers, otherwise they are read from the
+// staged buffer block by block. Several sequences run on the tensor cores
+// (page_rows_mma): there every weight meets B activations, which the FMA
+// pipes and the shared-memory reads of fp32 activations could not keep up
+// with at the weight stream's rate.
 
 __device__ __forceinline__ void warp_sum4(float (&v)[4]) {
 #pragma unroll
@@ -628,7 +662,7 @@ __device__ __forceinline__ void rows4_reg(const uint8_t* rows, int n_rows, int r
   }
 }
 
-// any B, any K: activations read block by block from the staged buffer
+// one sequence, any K: activations read block by block from the staged buffer
 template <int B>
 __device__ __forceinline__ void page_rows_smem(const uint8_t* page, int n_rows, int row_bytes,
                                                int nblk, const float* act, int K,
@@ -681,8 +715,73 @@ __device__ __forceinline__ void page_rows_smem(const uint8_t* page, int n_rows, 
   }
 }
 
+// Several sequences: the tensor-core product of a page's rows with the staged
+// activations of all B sequences. One mma.sync m16n8k16 multiplies 16
+// activation rows (the bf16 hi parts of sequences 0..7 in rows 0..7, their lo
+// parts in rows 8..15) by 16 columns of 8 page rows, so hi and lo products add
+// up to an fp32-accurate dot product. The order of the 16 columns inside one
+// product is free as long as both operands follow it: step s takes column
+// pair tig from the columns P, P + 1 and pair tig + 4 from P + 2, P + 3, with
+// P = 32 (s / 2) + 8 tig + 4 (s % 2). Then one 16-byte load of a page row
+// feeds two steps, and the 16 staged bytes at column P are exactly one A
+// fragment. Odd page rows load the two 64-byte halves of a 64-column chunk
+// in swapped order, so that even and odd rows fall on disjoint banks; the
+// staged rows are padded by 4 words for the same reason.
+template <int B>
+__device__ __forceinline__ void page_rows_mma(const uint8_t* page, int n_rows, int row_bytes,
+                                              int K, const uint32_t* act, const InvScale& inv,
+                                              float* res_page, int n_in, int R, int lane) {
+  const int grp = lane >> 2, tig = lane & 3, odd = grp & 1;
+  // lanes past the last sequence repeat it; their product rows are not stored
+  const uint32_t* arow = act + (size_t)min(grp, B - 1) * (K + 4) + 8 * tig;
+  float sc = inv.v[0];
+#pragma unroll
+  for (int b = 1; b < B; ++b) sc = grp == b ? inv.v[b] : sc;
+  for (int r0 = 0; r0 < n_rows; r0 += 8) {
+    const int nv = min(8, n_rows - r0);
+    // B column grp = page row r0 + grp; lanes past the valid rows repeat a
+    // valid row of the same parity, i.e. another lane's addresses
+    const int rr = grp < nv ? grp : (nv > 1 ? odd : 0);
+    const uint8_t* w0 = page + (size_t)(r0 + rr) * row_bytes + 16 * tig + 64 * odd;
+    const uint8_t* w1 = page + (size_t)(r0 + rr) * row_bytes + 16 * tig + 64 * (odd ^ 1);
+    // four accumulator chains; plain loads, so that the compiler can issue
+    // the next chunks' loads ahead of this chunk's products
+    float d[4][4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) d[q][0] = d[q][1] = d[q][2] = d[q][3] = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < K; c += 64) {
+      const uint4 wa = *reinterpret_cast<const uint4*>(w0 + 2 * c);
+      const uint4 wb = *reinterpret_cast<const uint4*>(w1 + 2 * c);
+      const uint4 a0 = *reinterpret_cast<const uint4*>(arow + c);
+      const uint4 a1 = *reinterpret_cast<const uint4*>(arow + c + 4);
+      const uint4 a2 = *reinterpret_cast<const uint4*>(arow + c + 32);
+      const uint4 a3 = *reinterpret_cast<const uint4*>(arow + c + 36);
+      const uint4 wl = odd ? wb : wa;  // columns c + 8 tig .. + 7
+      const uint4 wh = odd ? wa : wb;  // columns c + 32 + 8 tig .. + 7
+      mma_bf16_16816(d[0], a0, wl.x, wl.y);
+      mma_bf16_16816(d[1], a1, wl.z, wl.w);
+      mma_bf16_16816(d[2], a2, wh.x, wh.y);
+      mma_bf16_16816(d[3], a3, wh.z, wh.w);
+    }
+    if (grp < B) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int pr = 2 * tig + e;
+        if (pr < nv) {
+          const int row = r0 + pr, r = row / n_in, k = row - r * n_in;
+          const float hi = (d[0][e] + d[1][e]) + (d[2][e] + d[3][e]);
+          const float lo = (d[0][2 + e] + d[1][2 + e]) + (d[2][2 + e] + d[3][2 + e]);
+          res_page[((size_t)k * R + r) * B + grp] = (hi + lo) * sc;
+        }
+      }
+    }
+  }
+}
+
 // kRegs: the activations are in the caller's registers a[] (B == 1, rows of at
-// most 2048 columns); otherwise they are read from the staged buffer `act`.
+// most 2048 columns); otherwise they are read from the staged buffer `act`
+// (fp32 for one sequence, tensor-core fragments for several).
 // KW == 2048: every row is 2048 wide (only the full-page code is compiled).
 template <int B, bool kRegs, int KW>
 __device__ __forceinline__ void gemv_run(const Params& p, Misc* m, uint8_t* smem, const Instr& in,
@@ -729,6 +828,9 @@ __device__ __forceinline__ void gemv_run(const Params& p, Misc* m, uint8_t* smem
                          res_page + ((size_t)k * g.R + r) * B, lane);
           }
         }
+      } else if constexpr (B > 1) {
+        page_rows_mma<B>(page, n_rows, row_bytes, g.K, reinterpret_cast<const uint32_t*>(act), inv,
+                         res_page, n_in, g.R, lane);
       } else {
         for (int r = 0; r < g.R; ++r)
           page_rows_smem<B>(page + (size_t)r * n_in * row_bytes, n_in, row_bytes, nblk, act, g.K,
@@ -809,6 +911,7 @@ __device__ __forceinline__ void attn_key(const float (&qf)[GH][8], float (&o)[GH
   }
 }
 
+
 // GH heads per pass. The unit's cached keys arrive in shared-memory pages
 // (attn_span) that every compute warp reads: warp w takes keys w*TPI + ti,
 // + kComputeWarps*TPI, ... of each page, and releases the page after its
@@ -868,10 +971,10 @@ __device__ __forceinline__ void attn_partial(const Params& p, Misc* m, uint8_t* 
       const uint8_t* kp = smem + (size_t)slot * kPageBytes;
       const uint8_t* vp = kp + kPageBytes / 2;
       const int nk = min(sp.kpp, sp.nc - pg * sp.kpp);
+      const uint4 z = make_uint4(0, 0, 0, 0);
       for (int j0 = warp * TPI; j0 < nk; j0 += kComputeWarps * TPI) {
         const int j = j0 + ti;
         const bool valid = j < nk;
-        const uint4 z = make_uint4(0, 0, 0, 0);
         const uint4 kv = valid ? lds128(kp + (size_t)j * D * 2 + sub * 16) : z;
         const uint4 vv = valid ? lds128(vp + (size_t)j * D * 2 + sub * 16) : z;
         attn_key<D, GH>(qf, o, mm, ll, kv, vv, valid);
@@ -1055,7 +1158,7 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
               staged = true;
             }
           }
-          if (!staged) stage(p, m, smem, st, kind, in.layer, chunk);
+          if (!staged) stage<B>(p, m, smem, st, kind, in.layer, chunk);
         }
         act = reinterpret_cast<const float*>(smem + (to_h ? p.off_h : p.off_x));
       }
@@ -1264,9 +1367,15 @@ __device__ void storer_role(const Params& p, Misc* m, uint8_t* smem, const Instr
       if (in.sig_ctr >= 0) {
         // the warp barrier orders the other lanes' stores (and, through the
         // result mbarrier, the compute warps' stores) before lane 0's
-        // release-add, which publishes them at GPU scope
+        // release-add, which publishes them at GPU scope. No instruction
+        // waits for the LM head's logits (the end of the kernel publishes
+        // them), so its count goes out without the release, whose fence
+        // would wait for this SM's weight copies in flight.
         __syncwarp();
-        if (lane == 0) red_release_add(p.ctr + in.sig_ctr, in.sig_amount);
+        if (lane == 0) {
+          if (in.op == MK_OP_LMHEAD) red_relaxed_add(p.ctr + in.sig_ctr, in.sig_amount);
+          else red_release_add(p.ctr + in.sig_ctr, in.sig_amount);
+        }
       }
     }
     __syncwarp();

@@ -194,6 +194,28 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// ---- warp-level tensor-core product (several sequences) -----------------------
+// D(16x8, fp32) += A(16x16, bf16, row-major) * B(16x8, bf16, column-major).
+// Lane l = 4 * grp + tig holds A rows grp and grp + 8 at the column pairs
+// 2 * tig and 2 * tig + 8 (a.x, a.y, a.z, a.w = (grp, 2tig), (grp + 8, 2tig),
+// (grp, 2tig + 8), (grp + 8, 2tig + 8)), B column grp at the row pairs 2 * tig
+// (b0) and 2 * tig + 8 (b1), and D rows grp (d[0], d[1]) and grp + 8 (d[2],
+// d[3]) at the columns 2 * tig and 2 * tig + 1.
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint4& a, uint32_t b0,
+                                               uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
+}
+
+// two floats -> bf16 pair (round to nearest even), lo in the low half
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // bf16 pair in a 32-bit word -> two floats (exact widening)
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }

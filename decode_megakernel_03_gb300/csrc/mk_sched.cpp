@@ -57,8 +57,36 @@ void choose_partitions(const Shape& s, int n_sm, const int* positions, int* part
   // longer partitions (at least 128 keys: two pages) keep that cheap; the
   // keys stream through pages ahead of the unit, so a longer one costs little
   const long min_keys = fused_reduction(s) ? 128 : 64;
-  long per = std::max<long>(min_keys, (work + n_sm - 1) / std::max(1, n_sm));
   for (int b = 0; b < kMaxBatch; ++b) parts[b] = 0;
+  if (!fused_reduction(s)) {
+    // several sequences: at most one unit per SM over all (sequence,
+    // kv-head, partition) triples (a second unit on some SMs would double
+    // their attention time), dealt one partition at a time to the sequence
+    // with the most keys per partition, since the longest unit bounds the
+    // layer; no partition drops below min_keys
+    const long budget = std::max<long>(s.B, n_sm / std::max(1, s.nkv));
+    long total = s.B;
+    for (int b = 0; b < s.B; ++b) parts[b] = 1;
+    while (total < budget) {
+      int best = -1;
+      long best_num = 0, best_den = 1;  // keys per partition, as a fraction
+      for (int b = 0; b < s.B; ++b) {
+        const long len = (long)positions[b] + 1;
+        if (parts[b] >= kMaxPartitions || parts[b] >= len) continue;
+        if (bucket[b] / (parts[b] + 1) < min_keys) continue;
+        if (best < 0 || bucket[b] * best_den > best_num * parts[b]) {
+          best = b;
+          best_num = bucket[b];
+          best_den = parts[b];
+        }
+      }
+      if (best < 0) break;
+      ++parts[best];
+      ++total;
+    }
+    return;
+  }
+  long per = std::max<long>(min_keys, (work + n_sm - 1) / std::max(1, n_sm));
   for (int b = 0; b < s.B; ++b) {
     long p = (bucket[b] + per - 1) / per;
     long len = (long)positions[b] + 1;
@@ -301,8 +329,11 @@ int smem_layout(const Shape& s, int n_sm, int optin, int misc_bytes, Params* p, 
   // down-projection chunk sums | barriers; the attention scratch reuses the
   // staging area
   const int B = s.B;
-  p->x_floats = B * std::max(s.H, s.QD());
-  p->h_floats = B * s.Fc();
+  // several sequences: each staged row is padded by 4 words (bank spread of
+  // the tensor-core fragments)
+  const int pad = B > 1 ? 4 : 0;
+  p->x_floats = B * (std::max(s.H, s.QD()) + pad);
+  p->h_floats = B * (s.Fc() + pad);
   p->alias_xh = B > 1 ? 1 : 0;
   p->fused_red = fused_reduction(s) ? 1 : 0;
   p->res_floats = item_cap_for(s) * 2 * B;
