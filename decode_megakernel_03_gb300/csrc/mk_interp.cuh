@@ -852,207 +852,237 @@ __device__ __forceinline__ void gemv_run(const Params& p, Misc* m, uint8_t* smem
 // ---------------------------------------------------------------------------
 // compute role: split-KV attention partial (instruction 2)
 // ---------------------------------------------------------------------------
-// Unit (b, g, p): the G q-heads of kv-head g over keys [t0, t1) of sequence b.
-// A key row of D bf16 is read by D/8 lanes with one 16-byte load each, so a
-// warp covers 256/D keys per load; per (lane group, head) an online softmax
-// keeps (m, l, o) in the log2 domain (q is pre-scaled by log2(e)/sqrt(D)).
-// Warps combine through shared memory and write (o, m, l) for the partition.
+// Unit (b, g, p): the G <= 8 q-heads of kv-head g over keys [t0, t1) of
+// sequence b, on the tensor cores. Every compute warp takes whole pages of the
+// unit (the pages it owns in the SM's page stream, as for GEMV pages) and
+// keeps its own online softmax in the log2 domain (q is pre-scaled by
+// log2(e)/sqrt(D)):
+//   scores   S = Q K^T, one mma.sync per 16 dimensions and 8 keys: rows
+//            0..7 the bf16 hi parts of the queries, rows 8..15 their lo
+//            parts (query rows past G repeat the last one), the dimensions
+//            in the permuted order of the GEMV products, so that one 16-byte
+//            load of a key row feeds two steps;
+//   weights  p = 2^(s - m), split into bf16 hi and lo the same way: the score
+//            fragments of two 8-key blocks are exactly the A fragment of a
+//            16-key step of
+//   output   O += P V, V read transposed from the page with ldmatrix.
+// The hi and lo rows add up at the end, and the warps' (o, m, l) combine
+// through shared memory in a fixed order. The new key (position pos, written
+// by this step's QKV instruction after the pages were fetched) starts the
+// softmax of the warp that takes the unit's first page: a single key's
+// partial is (o, m, l) = (v, q.k, 1); its k and v rows load from global
+// memory together with the queries.
 
-__device__ __forceinline__ void softmax_merge(float& m, float& l, float* o, float m2, float l2,
-                                              const float* o2) {
-  const float M = fmaxf(m, m2);
-  if (M == -INFINITY) return;
-  const float s1 = fast_exp2(m - M), s2 = fast_exp2(m2 - M);
-  l = l * s1 + l2 * s2;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) o[e] = o[e] * s1 + o2[e] * s2;
-  m = M;
+__device__ __forceinline__ uint4 split_hi_lo(float a, float b, float c, float d) {
+  const uint32_t h01 = bf16x2_rn(a, b), h23 = bf16x2_rn(c, d);
+  return make_uint4(h01, bf16x2_rn(a - bf_lo(h01), b - bf_hi(h01)), h23,
+                    bf16x2_rn(c - bf_lo(h23), d - bf_hi(h23)));
 }
 
-// One key per lane group: its scores against the GH heads (a key row of D
-// bf16 is spread over D/8 lanes, 16 bytes each), then the online-softmax
-// update of (m, l, o) in the log2 domain. Lane groups whose key is not valid
-// only take part in the shuffles.
-template <int D, int GH>
-__device__ __forceinline__ void attn_key(const float (&qf)[GH][8], float (&o)[GH][8],
-                                         float (&mm)[GH], float (&ll)[GH], const uint4 kv,
-                                         const uint4 vv, bool valid) {
-  constexpr int LPT = D / 8;
-  float s[GH];
-#pragma unroll
-  for (int h = 0; h < GH; ++h) {
-    float acc = qf[h][0] * bf_lo(kv.x);
-    acc = fmaf(qf[h][1], bf_hi(kv.x), acc);
-    acc = fmaf(qf[h][2], bf_lo(kv.y), acc);
-    acc = fmaf(qf[h][3], bf_hi(kv.y), acc);
-    acc = fmaf(qf[h][4], bf_lo(kv.z), acc);
-    acc = fmaf(qf[h][5], bf_hi(kv.z), acc);
-    acc = fmaf(qf[h][6], bf_lo(kv.w), acc);
-    acc = fmaf(qf[h][7], bf_hi(kv.w), acc);
-    s[h] = acc;
-  }
-#pragma unroll
-  for (int off = 1; off < LPT; off <<= 1)
-#pragma unroll
-    for (int h = 0; h < GH; ++h) s[h] += __shfl_xor_sync(0xffffffffu, s[h], off);
-  if (valid) {
-    const float vf[8] = {bf_lo(vv.x), bf_hi(vv.x), bf_lo(vv.y), bf_hi(vv.y),
-                         bf_lo(vv.z), bf_hi(vv.z), bf_lo(vv.w), bf_hi(vv.w)};
-#pragma unroll
-    for (int h = 0; h < GH; ++h) {
-      const float mn = fmaxf(mm[h], s[h]);
-      const float sc = fast_exp2(mm[h] - mn);
-      const float pe = fast_exp2(s[h] - mn);
-      ll[h] = ll[h] * sc + pe;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o[h][e] = fmaf(pe, vf[e], o[h][e] * sc);
-      mm[h] = mn;
-    }
-  }
-}
-
-
-// GH heads per pass. The unit's cached keys arrive in shared-memory pages
-// (attn_span) that every compute warp reads: warp w takes keys w*TPI + ti,
-// + kComputeWarps*TPI, ... of each page, and releases the page after its
-// last pass (G = 8 runs two passes of four heads over the same pages). The
-// new key comes from the cache in global memory after the counter wait.
-template <int D, int GH>
-__device__ __forceinline__ void attn_partial(const Params& p, Misc* m, uint8_t* smem, const Instr& in,
-                                             int h0, uint32_t page_base, bool release) {
-  constexpr int LPT = D / 8;       // lanes per key row
-  constexpr int TPI = 32 / LPT;    // keys per warp load
+template <int D>
+__device__ void attn_unit(const Params& p, Misc* m, uint8_t* smem, const Instr& in,
+                          uint32_t page_base) {
+  constexpr int KS = D / 16;                   // product steps over the head dimension
+  constexpr int NB = D / 8;                    // 8-column blocks of the output
+  constexpr int KPP = kPageBytes / (4 * D);    // keys per page (K, then V)
+  constexpr int NKB = KPP / 8;                 // 8-key blocks per page
   const int warp = compute_warp(), lane = threadIdx.x & 31;
+  const int grp = lane >> 2, tig = lane & 3, odd = grp & 1;
   const int b = in.a0, g = in.a1, pidx = in.a2 >> 16, P = in.a2 & 0xffff;
-  const int pos = p.pos[b];
+  const int G = p.G, pos = p.pos[b];
   const AttnSpan sp = attn_span(pos, pidx, P, D);
-  const int sub = lane % LPT, ti = lane / LPT;
   const float qscale = 1.4426950408889634f * rsqrtf((float)D);
+  const float* qhead = p.q + (size_t)b * p.QD + (size_t)g * G * D;
 
-  // the new key (in the unit's range), written by this step's QKV instruction
-  // (its counter wait ordered that write before this read): key group 0 of
-  // warp 0 takes it, its loads issued together with the queries'
-  const bool new_here = warp == 0 && sp.t0 <= pos && pos < sp.t1;
-  uint4 kn = make_uint4(0, 0, 0, 0), vn = kn;
+  // this warp's pages are the unit's pages r0, r0 + kComputeWarps, ... (it
+  // owns the slots congruent to its index; n_pages is a multiple of
+  // kComputeWarps, see gemv_run). The residue r0, not the warp, names the
+  // warp's share in the combination, so that the result does not depend on
+  // where the unit starts in the SM's page stream.
+  const int r0 = (int)(((uint32_t)warp + kComputeWarps - page_base % kComputeWarps) % kComputeWarps);
+  // the new key, if in this unit, goes with share 0: k row as the B fragment
+  // of key column 0 (lanes grp == 0), v columns 8 nb + 2 tig, +1 of every lane
+  const bool new_here = r0 == 0 && sp.t0 <= pos && pos < sp.t1;
+  uint4 kn[D / 64][2];
+  uint32_t vn[NB];
   if (new_here) {
     const LayerPtrs& L = p.layers[in.layer];
-    const size_t row = (((size_t)b * p.nkv + g) * (size_t)p.S + pos) * D + sub * 8;
-    kn = __ldcg(reinterpret_cast<const uint4*>(L.kc + row));
-    vn = __ldcg(reinterpret_cast<const uint4*>(L.vc + row));
-  }
-  float qf[GH][8], o[GH][8], mm[GH], ll[GH];
+    const size_t row = (((size_t)b * p.nkv + g) * (size_t)p.S + pos) * D;
 #pragma unroll
-  for (int h = 0; h < GH; ++h) {
-    const float* qs = p.q + (size_t)b * p.QD + (size_t)(g * p.G + h0 + h) * D + sub * 8;
-    const float4 a0 = __ldcg(reinterpret_cast<const float4*>(qs));
-    const float4 a1 = __ldcg(reinterpret_cast<const float4*>(qs + 4));
-    qf[h][0] = a0.x * qscale; qf[h][1] = a0.y * qscale; qf[h][2] = a0.z * qscale;
-    qf[h][3] = a0.w * qscale; qf[h][4] = a1.x * qscale; qf[h][5] = a1.y * qscale;
-    qf[h][6] = a1.z * qscale; qf[h][7] = a1.w * qscale;
-    mm[h] = -INFINITY;
-    ll[h] = 0.f;
+    for (int j2 = 0; j2 < D / 64; ++j2) {
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      kn[j2][0] = grp == 0 ? __ldcg(reinterpret_cast<const uint4*>(L.kc + row + 64 * j2 + 8 * tig)) : z;
+      kn[j2][1] = grp == 0 ? __ldcg(reinterpret_cast<const uint4*>(L.kc + row + 64 * j2 + 32 + 8 * tig)) : z;
+    }
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o[h][e] = 0.f;
+    for (int nb = 0; nb < NB; ++nb)
+      vn[nb] = __ldcg(reinterpret_cast<const unsigned int*>(L.vc + row + 8 * nb + 2 * tig));
   }
-  if (new_here) attn_key<D, GH>(qf, o, mm, ll, kn, vn, ti == 0);
+  // query fragments of head min(grp, G - 1): step s covers dimensions
+  // 32 (s / 2) + 8 tig + 4 (s % 2) .. + 3
+  uint4 qa[KS];
+  {
+    const float* qs = qhead + (size_t)min(grp, G - 1) * D + 8 * tig;
+#pragma unroll
+    for (int j = 0; j < KS / 2; ++j) {
+      const float4 x0 = __ldcg(reinterpret_cast<const float4*>(qs + 32 * j));
+      const float4 x1 = __ldcg(reinterpret_cast<const float4*>(qs + 32 * j + 4));
+      qa[2 * j] = split_hi_lo(x0.x * qscale, x0.y * qscale, x0.z * qscale, x0.w * qscale);
+      qa[2 * j + 1] = split_hi_lo(x1.x * qscale, x1.y * qscale, x1.z * qscale, x1.w * qscale);
+    }
+  }
+  float mrow = -INFINITY;  // running maximum of head grp (equal in the group's 4 lanes)
+  float lsum = 0.f;        // this lane's share of the running sum
+  float o[NB][4];          // rows grp (hi weights) and grp + 8 (lo), columns 8 nb + 2 tig, +1
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb) o[nb][0] = o[nb][1] = o[nb][2] = o[nb][3] = 0.f;
+  if (new_here) {
+    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j2 = 0; j2 < D / 64; ++j2) {
+      mma_bf16_16816(d0, qa[4 * j2], kn[j2][0].x, kn[j2][0].y);
+      mma_bf16_16816(d1, qa[4 * j2 + 1], kn[j2][0].z, kn[j2][0].w);
+      mma_bf16_16816(d0, qa[4 * j2 + 2], kn[j2][1].x, kn[j2][1].y);
+      mma_bf16_16816(d1, qa[4 * j2 + 3], kn[j2][1].z, kn[j2][1].w);
+    }
+    // key column 0 sits in lane 4 grp of the group
+    mrow = __shfl_sync(0xffffffffu, (d0[0] + d1[0]) + (d0[2] + d1[2]), lane & ~3);
+    lsum = tig == 0 ? 1.f : 0.f;
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      o[nb][0] = bf_lo(vn[nb]);
+      o[nb][1] = bf_hi(vn[nb]);
+    }
+  }
 
-  uint32_t pc = page_base;
-  for (int pg = 0; pg < sp.npages; ++pg, ++pc) {
-    const int slot = (int)(pc % (uint32_t)p.n_pages);
-    // Only the slot's owner warp (slot % kComputeWarps, the warp that
-    // consumes every GEMV page of this slot) waits on its barrier: it has seen
-    // every earlier fill of the slot, so its parity wait cannot mistake an
-    // older phase for this one. The other warps meet it at a barrier.
-    if (warp == slot % kComputeWarps)
-      wait_mbar(p, m, &m->full[slot], (pc / (uint32_t)p.n_pages) & 1u, kErrTimeoutPage);
-    compute_bar();
-    const bool ok = !aborted(m);
+  int pg = r0;
+  const uint32_t pc0 = page_base + (uint32_t)pg;
+  int slot = (int)(pc0 % (uint32_t)p.n_pages);
+  uint32_t round = pc0 / (uint32_t)p.n_pages;
+  for (; pg < sp.npages; pg += kComputeWarps) {
+    // the products need the whole warp: the lanes agree on the page
+    const bool ok =
+        __all_sync(0xffffffffu, wait_mbar(p, m, &m->full[slot], round & 1u, kErrTimeoutPage));
     if (ok) {
       const uint8_t* kp = smem + (size_t)slot * kPageBytes;
       const uint8_t* vp = kp + kPageBytes / 2;
-      const int nk = min(sp.kpp, sp.nc - pg * sp.kpp);
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      for (int j0 = warp * TPI; j0 < nk; j0 += kComputeWarps * TPI) {
-        const int j = j0 + ti;
-        const bool valid = j < nk;
-        const uint4 kv = valid ? lds128(kp + (size_t)j * D * 2 + sub * 16) : z;
-        const uint4 vv = valid ? lds128(vp + (size_t)j * D * 2 + sub * 16) : z;
-        attn_key<D, GH>(qf, o, mm, ll, kv, vv, valid);
+      const int nk = min(KPP, sp.nc - pg * KPP);
+      float sc[NKB][2];
+#pragma unroll
+      for (int kb = 0; kb < NKB; ++kb) {
+        sc[kb][0] = sc[kb][1] = -INFINITY;
+        if (kb * 8 < nk) {
+          // key kb*8 + grp is column grp; odd keys load the two 64-byte halves
+          // of each 128-byte stretch swapped (disjoint banks)
+          const uint8_t* kr = kp + (size_t)(kb * 8 + grp) * (D * 2) + 16 * tig;
+          float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int j2 = 0; j2 < D / 64; ++j2) {
+            const uint4 x = *reinterpret_cast<const uint4*>(kr + 128 * j2 + 64 * odd);
+            const uint4 y = *reinterpret_cast<const uint4*>(kr + 128 * j2 + 64 * (odd ^ 1));
+            const uint4 wl = odd ? y : x, wh = odd ? x : y;
+            mma_bf16_16816(d0, qa[4 * j2], wl.x, wl.y);
+            mma_bf16_16816(d1, qa[4 * j2 + 1], wl.z, wl.w);
+            mma_bf16_16816(d0, qa[4 * j2 + 2], wh.x, wh.y);
+            mma_bf16_16816(d1, qa[4 * j2 + 3], wh.z, wh.w);
+          }
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            if (kb * 8 + 2 * tig + e < nk) sc[kb][e] = (d0[e] + d1[e]) + (d0[2 + e] + d1[2 + e]);
+        }
+      }
+      // online softmax over the page (every page holds at least one key)
+      float mx = -INFINITY;
+#pragma unroll
+      for (int kb = 0; kb < NKB; ++kb) mx = fmaxf(mx, fmaxf(sc[kb][0], sc[kb][1]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float mnew = fmaxf(mrow, mx);
+      const float alpha = fast_exp2(mrow - mnew);
+      mrow = mnew;
+      lsum *= alpha;
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[nb][e] *= alpha;
+#pragma unroll
+      for (int kb = 0; kb < NKB; ++kb)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          sc[kb][e] = fast_exp2(sc[kb][e] - mnew);  // -inf (no key): 0
+          lsum += sc[kb][e];
+        }
+      // O += P V, 16 keys per step; V blocks of 8 keys x 8 columns transposed
+      // by ldmatrix (lane l addresses row l % 8 of block l / 8). Rows past the
+      // page's keys hold whatever the slot held before (possibly not a finite
+      // number): their halves of the B fragments are zeroed, since a zero
+      // weight would not cancel them.
+#pragma unroll
+      for (int t = 0; t < NKB / 2; ++t) {
+        if (16 * t < nk) {
+          const uint4 pa = split_hi_lo(sc[2 * t][0], sc[2 * t][1], sc[2 * t + 1][0], sc[2 * t + 1][1]);
+          const uint8_t* vr = vp + (size_t)(16 * t + (lane & 7)) * (D * 2) + 16 * (lane >> 3);
+          const int k0 = 16 * t + 2 * tig;  // this lane's keys: k0, k0 + 1, k0 + 8, k0 + 9
+          const uint32_t m0 = (k0 < nk ? 0xffffu : 0u) | (k0 + 1 < nk ? 0xffff0000u : 0u);
+          const uint32_t m1 = (k0 + 8 < nk ? 0xffffu : 0u) | (k0 + 9 < nk ? 0xffff0000u : 0u);
+#pragma unroll
+          for (int nq = 0; nq < NB / 4; ++nq) {
+            uint32_t b0[4], b1[4];
+            ldsm_x4_trans(b0, vr + 64 * nq);                  // keys 16t .. +7
+            ldsm_x4_trans(b1, vr + 64 * nq + 8 * (D * 2));    // keys 16t + 8 .. +15
+#pragma unroll
+            for (int i = 0; i < 4; ++i) mma_bf16_16816(o[4 * nq + i], pa, b0[i] & m0, b1[i] & m1);
+          }
+        }
       }
     }
-    // a page whose copy has not landed (after an abort) is never released
+    // a page whose copy has not landed (after an abort) is never handed back
     __syncwarp();
-    if (release && lane == 0 && ok) mbar_arrive(&m->empty[slot]);
-  }
-  // merge the key groups of the warp (lanes with the same `sub`)
-#pragma unroll
-  for (int off = LPT; off < 32; off <<= 1) {
-#pragma unroll
-    for (int h = 0; h < GH; ++h) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, mm[h], off);
-      const float l2 = __shfl_xor_sync(0xffffffffu, ll[h], off);
-      float o2[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) o2[e] = __shfl_xor_sync(0xffffffffu, o[h][e], off);
-      softmax_merge(mm[h], ll[h], o[h], m2, l2, o2);
+    if (lane == 0 && ok) mbar_arrive_cnt(&m->empty[slot], kComputeWarps);
+    slot += kComputeWarps;
+    if (slot >= p.n_pages) {
+      slot -= p.n_pages;
+      ++round;
     }
   }
-  // scratch [warp][h][D + 2] in the activation staging area
+  lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
+  lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+
+  // scratch [share][h][D + 2] in the activation staging area
   float* scr = reinterpret_cast<float*>(smem + p.off_x);
   compute_bar();  // previous readers of the staging area are done
-  if (ti == 0) {
+  if (grp < G) {
+    float* e = scr + ((size_t)r0 * G + grp) * (D + 2);
 #pragma unroll
-    for (int h = 0; h < GH; ++h) {
-      float* sp = scr + ((size_t)warp * GH + h) * (D + 2);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) sp[sub * 8 + e] = o[h][e];
-      if (sub == 0) {
-        sp[D] = mm[h];
-        sp[D + 1] = ll[h];
-      }
+    for (int nb = 0; nb < NB; ++nb) {
+      e[8 * nb + 2 * tig] = o[nb][0] + o[nb][2];
+      e[8 * nb + 2 * tig + 1] = o[nb][1] + o[nb][3];
+    }
+    if (tig == 0) {
+      e[D] = mrow;
+      e[D + 1] = lsum;
     }
   }
   compute_bar();
   const int tid = compute_tid();
-  for (int idx = tid; idx < GH * D; idx += kComputeThreads) {
+  for (int idx = tid; idx < G * D; idx += kComputeThreads) {
     const int h = idx / D, d = idx - h * D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kComputeWarps; ++w) M = fmaxf(M, scr[((size_t)w * GH + h) * (D + 2) + D]);
+    for (int w = 0; w < kComputeWarps; ++w) M = fmaxf(M, scr[((size_t)w * G + h) * (D + 2) + D]);
     float acc = 0.f, den = 0.f;
 #pragma unroll
     for (int w = 0; w < kComputeWarps; ++w) {
-      const float* sp = scr + ((size_t)w * GH + h) * (D + 2);
-      const float wt = sp[D] == -INFINITY ? 0.f : fast_exp2(sp[D] - M);
-      acc = fmaf(wt, sp[d], acc);
-      den = fmaf(wt, sp[D + 1], den);
+      const float* e = scr + ((size_t)w * G + h) * (D + 2);
+      const float wt = e[D] == -INFINITY ? 0.f : fast_exp2(e[D] - M);
+      acc = fmaf(wt, e[d], acc);
+      den = fmaf(wt, e[D + 1], den);
     }
-    const size_t row = ((size_t)b * p.nh + g * p.G + h0 + h) * kMaxPartitions + pidx;
-    p.part[row * D + d] = acc;
+    const size_t prow = ((size_t)b * p.nh + g * G + h) * kMaxPartitions + pidx;
+    p.part[prow * D + d] = acc;
     if (d == 0) {
-      p.part_ml[row * 2] = M;
-      p.part_ml[row * 2 + 1] = den;
-    }
-  }
-}
-
-// GS > 0: the q-heads per kv-head are fixed at compile time (one variant).
-// page_base: the unit's first page in this SM's page stream.
-template <int D, int GS>
-__device__ void attn_unit(const Params& p, Misc* m, uint8_t* smem, const Instr& in, uint32_t page_base) {
-  if constexpr (GS == 1 || GS == 2 || GS == 4) {
-    attn_partial<D, GS>(p, m, smem, in, 0, page_base, true);
-  } else if constexpr (GS > 4) {
-    for (int h0 = 0; h0 < GS; h0 += 4) attn_partial<D, 4>(p, m, smem, in, h0, page_base, h0 + 4 >= GS);
-  } else {
-    switch (p.G) {
-      case 1: attn_partial<D, 1>(p, m, smem, in, 0, page_base, true); break;
-      case 2: attn_partial<D, 2>(p, m, smem, in, 0, page_base, true); break;
-      case 4: attn_partial<D, 4>(p, m, smem, in, 0, page_base, true); break;
-      default:
-        for (int h0 = 0; h0 < p.G; h0 += 4)
-          attn_partial<D, 4>(p, m, smem, in, h0, page_base, h0 + 4 >= p.G);
-        break;
+      p.part_ml[prow * 2] = M;
+      p.part_ml[prow * 2 + 1] = den;
     }
   }
 }
@@ -1186,9 +1216,9 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
       st.key_h = -1;
       // runs even after an abort: its loads stay in bounds and its barriers
       // must be met by every compute warp
-      if constexpr (DS > 0) attn_unit<DS, GS>(p, m, smem, in, page_cnt);
-      else if (p.D == 64) attn_unit<64, GS>(p, m, smem, in, page_cnt);
-      else attn_unit<128, GS>(p, m, smem, in, page_cnt);
+      if constexpr (DS > 0) attn_unit<DS>(p, m, smem, in, page_cnt);
+      else if (p.D == 64) attn_unit<64>(p, m, smem, in, page_cnt);
+      else attn_unit<128>(p, m, smem, in, page_cnt);
       page_cnt += (uint32_t)attn_span(p.pos[in.a0], in.a2 >> 16, in.a2 & 0xffff, p.D).npages;
     } else if (in.op == MK_OP_RED) {
       // the reduction instruction runs only with several sequences (one

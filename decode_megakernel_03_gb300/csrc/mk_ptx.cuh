@@ -209,6 +209,15 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint4& a, ui
       : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
 }
 
+// four 8x8 blocks of 16-bit elements, transposed: lane l gives the address
+// of row l % 8 of block l / 8 (16 contiguous bytes); r[i] receives elements
+// (2 * tig, grp) and (2 * tig + 1, grp) of block i (lane = 4 * grp + tig)
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const void* row) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(row)));
+}
+
 // two floats -> bf16 pair (round to nearest even), lo in the low half
 __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
   uint32_t r;
