@@ -662,56 +662,46 @@ __device__ __forceinline__ void rows4_reg(const uint8_t* rows, int n_rows, int r
   }
 }
 
-// one sequence, any K: activations read block by block from the staged buffer
-template <int B>
-__device__ __forceinline__ void page_rows_smem(const uint8_t* page, int n_rows, int row_bytes,
-                                               int nblk, const float* act, int K,
-                                               const InvScale& inv, float* out_row0,
-                                               int out_stride, int lane) {
-  constexpr int RG = B <= 2 ? 4 : (B == 4 ? 2 : 1);
-  for (int r0 = 0; r0 < n_rows; r0 += RG) {
-    float acc[RG][B];
+// One sequence, rows wider than 2048 columns (a page holds at most three):
+// rows4_reg with the activations read from the staged buffer block by block,
+// each read serving every row of the page; the 1/rms scale multiplies the
+// sums. Lane q < n_rows stores row q's result to *dst.
+__device__ __forceinline__ void rows4_smem(const uint8_t* rows, int n_rows, int row_bytes,
+                                           int nblk, const float* act, float scale, float* dst,
+                                           int lane) {
+  unsigned long long acc[4][2];
 #pragma unroll
-    for (int q = 0; q < RG; ++q)
+  for (int q = 0; q < 4; ++q) acc[q][0] = acc[q][1] = 0ull;
+#pragma unroll 2
+  for (int j = 0; j < nblk; ++j) {
+    const float4 x0 = *reinterpret_cast<const float4*>(act + j * 256 + lane * 8);
+    const float4 x1 = *reinterpret_cast<const float4*>(act + j * 256 + lane * 8 + 4);
+    const unsigned long long a[4] = {pack2(x0.x, x0.y), pack2(x0.z, x0.w), pack2(x1.x, x1.y),
+                                     pack2(x1.z, x1.w)};
+    uint4 w[4];
 #pragma unroll
-      for (int b = 0; b < B; ++b) acc[q][b] = 0.f;
-    for (int j = 0; j < nblk; ++j) {
-      float x[B][8];
+    for (int q = 0; q < 4; ++q)
+      w[q] = q < n_rows ? *reinterpret_cast<const uint4*>(rows + (size_t)q * row_bytes + j * 512 + lane * 16)
+                        : make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int b = 0; b < B; ++b) {
-        const float* src = act + (size_t)b * K + j * 256 + lane * 8;
-        const float4 x0 = *reinterpret_cast<const float4*>(src);
-        const float4 x1 = *reinterpret_cast<const float4*>(src + 4);
-        const float s = inv.v[b];
-        x[b][0] = x0.x * s; x[b][1] = x0.y * s; x[b][2] = x0.z * s; x[b][3] = x0.w * s;
-        x[b][4] = x1.x * s; x[b][5] = x1.y * s; x[b][6] = x1.z * s; x[b][7] = x1.w * s;
-      }
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t ws[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
 #pragma unroll
-      for (int q = 0; q < RG; ++q) {
-        if (r0 + q < n_rows) {
-          const uint4 w =
-              *reinterpret_cast<const uint4*>(page + (size_t)(r0 + q) * row_bytes + j * 512 + lane * 16);
-          const float wf[8] = {bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y),
-                               bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w)};
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-#pragma unroll
-            for (int b = 0; b < B; ++b) acc[q][b] = fmaf(wf[e], x[b][e], acc[q][b]);
-        }
-      }
+      for (int e = 0; e < 4; ++e) ffma2(acc[q][j & 1], pack2(bf_lo(ws[e]), bf_hi(ws[e])), a[e]);
     }
+  }
+  float v[4];
 #pragma unroll
-    for (int q = 0; q < RG; ++q) {
+  for (int q = 0; q < 4; ++q) {
+    const float2 x = unpack2(acc[q][0]), y = unpack2(acc[q][1]);
+    v[q] = (x.x + x.y) + (y.x + y.y);
+  }
+  warp_sum4(v);
+  if (lane < 4 && lane < n_rows) {
+    float mine = v[0];
 #pragma unroll
-      for (int b = 0; b < B; ++b) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc[q][b] += __shfl_xor_sync(0xffffffffu, acc[q][b], o);
-      }
-      if (lane == 0 && r0 + q < n_rows) {
-#pragma unroll
-        for (int b = 0; b < B; ++b) out_row0[(size_t)(r0 + q) * out_stride + b] = acc[q][b];
-      }
-    }
+    for (int q = 1; q < 4; ++q) mine = lane == q ? v[q] : mine;
+    *dst = mine * scale;
   }
 }
 
@@ -832,9 +822,10 @@ __device__ __forceinline__ void gemv_run(const Params& p, Misc* m, uint8_t* smem
         page_rows_mma<B>(page, n_rows, row_bytes, g.K, reinterpret_cast<const uint32_t*>(act), inv,
                          res_page, n_in, g.R, lane);
       } else {
-        for (int r = 0; r < g.R; ++r)
-          page_rows_smem<B>(page + (size_t)r * n_in * row_bytes, n_in, row_bytes, nblk, act, g.K,
-                            inv, res_page + (size_t)r * B, g.R * B, lane);
+        const int pr = min(lane & 3, n_rows - 1);
+        const int r = pr / n_in, k = pr - r * n_in;
+        rows4_smem(page, n_rows, row_bytes, nblk, act, inv.v[0], res_page + ((size_t)k * g.R + r) * B,
+                   lane);
       }
     }
     // a page whose copy has not landed (after an abort) is never handed back,
