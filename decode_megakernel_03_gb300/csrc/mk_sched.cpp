@@ -92,6 +92,12 @@ void choose_partitions(const Shape& s, int n_sm, const int* positions, int* part
     long p = (bucket[b] + per - 1) / per;
     long len = (long)positions[b] + 1;
     p = std::min<long>(p, len);  // every partition keeps at least one key
+    // every SM's O-projection reduces all partitions of all heads while it
+    // stages (P x n_heads x head_dim floats per SM), so that cost grows with
+    // P while a unit's shrinks: at most 12 (measured on the 1B shape at 8192
+    // keys and the 8B shape at 2048: 852 -> 806 and 3637 -> 3532 us/step
+    // against the uncapped count; a cap of 8 was slower on both)
+    p = std::min<long>(p, 12);
     p = std::max<long>(1, std::min<long>(p, kMaxPartitions));
     parts[b] = (int)p;
   }
