@@ -1212,9 +1212,10 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
       else attn_unit<128>(p, m, smem, in, page_cnt);
       page_cnt += (uint32_t)attn_span(p.pos[in.a0], in.a2 >> 16, in.a2 & 0xffff, p.D).npages;
     } else if (in.op == MK_OP_RED) {
-      // the reduction instruction runs only with several sequences (one
-      // sequence reduces in the O-projection's staging)
-      if constexpr (B > 1) if (!aborted(m)) {
+      // the reduction instruction: several sequences, or one sequence with
+      // more than 2048 attention columns (the one-sequence kernel of head
+      // dimension 64 reduces in the O-projection's staging and omits it)
+      if constexpr (B > 1 || DS != 64) if (!aborted(m)) {
         if constexpr (DS > 0) attn_reduce<DS>(p, in);
         else if (p.D == 64) attn_reduce<64>(p, in);
         else attn_reduce<128>(p, in);

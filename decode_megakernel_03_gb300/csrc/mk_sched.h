@@ -60,8 +60,11 @@ std::string check_shape(const Shape& s);
 void choose_partitions(const Shape& s, int n_sm, const int* positions, int* parts);
 
 // One sequence: the O-projection reduces the attention partials while it
-// stages its input (no reduction instruction between them).
-inline bool fused_reduction(const Shape& s) { return s.B == 1; }
+// stages its input (no reduction instruction between them). Every SM then
+// reads all partitions of all heads (P x n_heads x head_dim floats), so
+// beyond 2048 attention columns the separate reduction instruction is
+// cheaper despite its extra hop (8B shape: 3520 -> 3478 us/step).
+inline bool fused_reduction(const Shape& s) { return s.B == 1 && s.QD() <= 2048; }
 
 // Items (rows or row pairs) per GEMV instruction, bounded by the result
 // buffer the storer drains.

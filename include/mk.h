@@ -99,8 +99,10 @@ int mk_decode_step(mk_handle* h, const int32_t* token_ids, const int32_t* positi
 /* The same step run as the multi-launch comparison build: the same
    instruction templates and the same per-SM work units, but one kernel per
    (layer, instruction type) — kernel boundaries instead of counter waits —
-   5 * n_layers + 1 launches with one sequence, 6 * n_layers + 1 with more. use_graph != 0 replays them as one CUDA
-   graph. Results are bit-identical to mk_decode_step. */
+   5 * n_layers + 1 launches with one sequence and at most 2048 attention
+   columns (n_heads * head_dim), 6 * n_layers + 1 otherwise (a separate
+   reduction instruction). use_graph != 0 replays them as one CUDA graph.
+   Results are bit-identical to mk_decode_step. */
 int mk_decode_step_multilaunch(mk_handle* h, const int32_t* token_ids,
                                const int32_t* positions, float* logits_out,
                                void* stream, int use_graph);

@@ -22,10 +22,11 @@ def _lib():
     mkbuild.build()
 
 
-def _fused(B):
-    """One sequence: no reduction instruction; the O-projection reduces the
-    attention partials while it stages its input."""
-    return B == 1
+def _fused(B, shape):
+    """One sequence with at most 2048 attention columns: no reduction
+    instruction; the O-projection reduces the attention partials while it
+    stages its input."""
+    return B == 1 and shape.n_heads * shape.head_dim <= 2048
 
 
 def _plan(shape, B, S, n_sm, pos):
@@ -88,7 +89,7 @@ def test_every_output_produced_exactly_once(case):
         # attention: each (b, g) has partitions 0..P-1 once, and its reduction
         # (a reduction instruction, or every O-projection unit) uses that P
         att = ins[(op == mk.OP_ATTN) & (layer == l)]
-        if _fused(B):
+        if _fused(B, shape):
             assert not np.any((op == mk.OP_RED) & (layer == l))
             o = ins[(op == mk.OP_OPROJ) & (layer == l)]
             assert len(set(int(x) for x in o["a2"])) == 1
@@ -241,7 +242,7 @@ def _accesses(ins, shape, B):
             R |= {("part", a0, a1, p) for p in range(a2)}
             W.add(("attn", a0, a1))
         elif op == mk.OP_OPROJ:
-            if _fused(B):  # reduces every head's partitions while staging
+            if _fused(B, shape):  # reduces every head's partitions while staging
                 R |= {("part", 0, g, p) for g in range(nkv) for p in range(a2)}
             else:
                 R |= {("attn", b, g) for b in range(B) for g in range(nkv)}
