@@ -50,6 +50,7 @@ struct mk_handle {
   int* d_ctr = nullptr;   // two counter sets
   int n_ctr = 0;
   int* d_err = nullptr;
+  unsigned long long* d_keys = nullptr;  // greedy decode: argmax keys [kMaxGreedySteps][B]
   int* h_err_mirror = nullptr;  // mapped pinned host memory the kernel writes on error
   std::vector<PlanEntry*> plans;
   unsigned long long use_clock = 0;
@@ -195,6 +196,8 @@ Params step_params(mk_handle* h, const int32_t* tok, const int32_t* pos, float* 
     p.pos[b] = b < h->shape.B ? pos[b] : 0;
   }
   p.logits = logits;
+  p.tok_keys = nullptr;
+  p.argmax_out = nullptr;
   const int set = (int)(h->steps & 1ull);
   p.ctr = h->d_ctr + (size_t)set * h->n_ctr;
   p.ctr_zero = h->d_ctr + (size_t)(set ^ 1) * h->n_ctr;
@@ -207,6 +210,12 @@ int check_sticky(mk_handle* h) {
   if (h->h_err_mirror && *reinterpret_cast<volatile int*>(h->h_err_mirror) != 0)
     return fail(h, MK_ERR_TIMEOUT, "an earlier step reported a device timeout; call mk_get_status");
   return MK_OK;
+}
+
+// greedy decode: argmax keys -> token ids
+__global__ void keys_to_tokens(const unsigned long long* keys, int n, int32_t* tokens) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) tokens[i] = key_token(keys[i]);
 }
 
 }  // namespace
@@ -287,6 +296,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
       sizeof(float2) * (size_t)s.S * (s.D / 2),                           // rope
       sizeof(int) * (size_t)2 * h->n_ctr,                                 // counters
       sizeof(int) * 64,                                                   // error word
+      sizeof(unsigned long long) * (size_t)MK_MAX_GREEDY_STEPS * B,      // argmax keys
   };
   const int npieces = sizeof(sizes) / sizeof(sizes[0]);
   size_t offs[npieces], total = 0;
@@ -309,6 +319,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
   h->d_rope = reinterpret_cast<float2*>(base + offs[7]);
   h->d_ctr = reinterpret_cast<int*>(base + offs[8]);
   h->d_err = reinterpret_cast<int*>(base + offs[9]);
+  h->d_keys = reinterpret_cast<unsigned long long*>(base + offs[10]);
   p.rope = h->d_rope;
   p.err = h->d_err;
   p.n_ctr = h->n_ctr;
@@ -425,6 +436,50 @@ int mk_decode_step(mk_handle* h, const int32_t* tok, const int32_t* pos, float* 
   if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaLaunchCooperativeKernel");
   h->cur_set = (int)(h->steps & 1ull);
   h->steps++;
+  return MK_OK;
+}
+
+int mk_decode_greedy(mk_handle* h, const int32_t* tok, const int32_t* pos, int n_steps,
+                     int32_t* tokens_out, float* logits, void* stream) {
+  if (!h) return MK_ERR_INVALID;
+  int rc = check_steps(h, tok, pos);
+  if (rc) return rc;
+  if (n_steps < 1 || n_steps > MK_MAX_GREEDY_STEPS)
+    return fail(h, MK_ERR_INVALID, "n_steps must be in [1, MK_MAX_GREEDY_STEPS]");
+  for (int b = 0; b < h->shape.B; ++b)
+    if (pos[b] + n_steps - 1 >= h->shape.S)
+      return fail(h, MK_ERR_INVALID, "positions + n_steps - 1 must be < kv_capacity");
+  if (!tokens_out || !aligned16(tokens_out))
+    return fail(h, MK_ERR_INVALID, "tokens_out must be 16-byte aligned");
+  if (!logits || !aligned16(logits)) return fail(h, MK_ERR_INVALID, "logits must be 16-byte aligned");
+  rc = check_sticky(h);
+  if (rc) return rc;
+  const int B = h->shape.B;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MK_CUDA(h, cudaMemsetAsync(h->d_keys, 0, sizeof(unsigned long long) * (size_t)n_steps * B, st));
+  int32_t ps[kMaxBatch];
+  for (int s = 0; s < n_steps; ++s) {
+    for (int b = 0; b < B; ++b) ps[b] = pos[b] + s;
+    PlanEntry* e = nullptr;
+    rc = get_plan(h, ps, &e);
+    if (rc) return rc;
+    Params p = step_params(h, tok, ps, logits);
+    p.tok_keys = s > 0 ? h->d_keys + (size_t)(s - 1) * B : nullptr;
+    p.argmax_out = h->d_keys + (size_t)s * B;
+    p.instrs = e->d_instrs;
+    p.sm_off = e->d_sm_off;
+    p.no_waits = 0;
+    p.trace_base = 0;
+    void* args[] = {&p};
+    cudaError_t ce = cudaLaunchCooperativeKernel(h->fn, dim3(h->n_sm), dim3(kThreads), args,
+                                                 (size_t)h->smem_bytes, st);
+    if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaLaunchCooperativeKernel");
+    h->cur_set = (int)(h->steps & 1ull);
+    h->steps++;
+  }
+  const int n = n_steps * B;
+  keys_to_tokens<<<(n + 255) / 256, 256, 0, st>>>(h->d_keys, n, tokens_out);
+  MK_CUDA(h, cudaGetLastError());
   return MK_OK;
 }
 

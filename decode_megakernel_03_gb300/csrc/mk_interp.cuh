@@ -349,6 +349,12 @@ struct Staged {
   InvScale inv_x;     // scale of the x buffer's contents
 };
 
+// the token of sequence b: from the parameters, or (greedy decode) from the
+// previous step's argmax
+__device__ __forceinline__ int token_of(const Params& p, int b) {
+  return p.tok_keys ? key_token(__ldcg(p.tok_keys + b)) : p.tok[b];
+}
+
 __device__ __forceinline__ int act_key(int kind, int layer, int chunk) {
   return (kind << 20) | (layer << 4) | chunk;
 }
@@ -409,7 +415,7 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
 #pragma unroll
           for (int bb = 0; bb < kNB; ++bb) {
             if (from_embed) {
-              const uint16_t* erow = p.embed + (size_t)p.tok[b0 + bb] * p.H;
+              const uint16_t* erow = p.embed + (size_t)token_of(p, b0 + bb) * p.H;
               const uint2 e = *reinterpret_cast<const uint2*>(erow + c);
               v[bb][u] = make_float4(bf_lo(e.x), bf_hi(e.x), bf_lo(e.y), bf_hi(e.y));
             } else {
@@ -1296,7 +1302,7 @@ __device__ __forceinline__ void epilogue_prefetch(const Params& p, Misc* m, cons
         const int j = in.a0 + it;
 #pragma unroll
         for (int b = 0; b < B; ++b)
-          pre.v[k][b].x = from_embed ? bf16f(p.embed[(size_t)p.tok[b] * p.H + j])
+          pre.v[k][b].x = from_embed ? bf16f(p.embed[(size_t)token_of(p, b) * p.H + j])
                                      : __ldcg(src + (size_t)b * p.H + j);
       }
     }
@@ -1360,6 +1366,32 @@ __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const
           p.logits[(size_t)b * p.V + j] = v0;
           break;
       }
+    }
+  }
+  if (in.op == MK_OP_LMHEAD && p.argmax_out) {
+    // greedy decode: the instruction's best row per sequence joins the
+    // step's argmax (atomicMax of order-preserving keys: any order of the
+    // SMs gives the same result)
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      unsigned long long best = 0ull;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int it = lane + 32 * k;
+        if (it < items) {
+          const uint32_t u = __float_as_uint(res[((size_t)it * g.R) * B + b]);
+          const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+          const unsigned long long key =
+              ((unsigned long long)ord << 32) | (0xffffffffu - (uint32_t)(in.a0 + it));
+          best = key > best ? key : best;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
+        best = o > best ? o : best;
+      }
+      if (lane == 0) atomicMax(p.argmax_out + b, best);
     }
   }
 }

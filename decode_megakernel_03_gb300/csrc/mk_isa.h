@@ -89,6 +89,12 @@ struct Params {
                                // attention partials itself (no reduction instruction)
   int h_ring;                  // one sequence: the loader fetches each down-projection
                                // chunk of h into one of two h slots (at off_h)
+  // greedy decode (both may be null): the previous step's argmax keys, read
+  // as this step's tokens instead of tok[]; this step's argmax keys, raised
+  // with atomicMax by the LM head (key = ordered(logit) << 32 | ~index, so the
+  // largest logit wins and the lowest index among equal ones)
+  const unsigned long long* tok_keys;
+  unsigned long long* argmax_out;
   // per step
   int tok[kMaxBatch];
   int pos[kMaxBatch];
@@ -116,6 +122,9 @@ struct Geom {
 #else
 #define MK_HD inline
 #endif
+
+// token id of a greedy-decode argmax key (Params::argmax_out)
+MK_HD int key_token(unsigned long long key) { return (int)(0xffffffffu - (uint32_t)key); }
 
 MK_HD bool is_gemv(int op) {
   return op == MK_OP_QKV || op == MK_OP_OPROJ || op == MK_OP_GATEUP || op == MK_OP_DOWN ||

@@ -23,7 +23,9 @@ OP_QKV, OP_ATTN, OP_RED, OP_OPROJ, OP_GATEUP, OP_DOWN, OP_LMHEAD = range(1, 8)
 EXPORTS = ("mk_create", "mk_decode_step", "mk_decode_step_multilaunch", "mk_get_status",
            "mk_destroy", "mk_last_error", "mk_read_counters", "mk_set_timeout",
            "mk_debug_inject_unsatisfiable_wait", "mk_set_trace", "mk_schedule_build",
-           "mk_decode_step_noalloc", "mk_debug_use_generic_kernel")
+           "mk_decode_step_noalloc", "mk_debug_use_generic_kernel", "mk_decode_greedy")
+
+MAX_GREEDY_STEPS = 1024  # MK_MAX_GREEDY_STEPS
 
 
 class MkError(RuntimeError):
@@ -79,6 +81,7 @@ def lib():
                                 ctypes.POINTER(vp)]
         L.mk_decode_step.argtypes = [vp, i32p, i32p, vp, vp]
         L.mk_decode_step_multilaunch.argtypes = [vp, i32p, i32p, vp, vp, ctypes.c_int]
+        L.mk_decode_greedy.argtypes = [vp, i32p, i32p, ctypes.c_int, vp, vp, vp]
         L.mk_get_status.argtypes = [vp, vp]
         L.mk_destroy.argtypes = [vp]
         L.mk_last_error.argtypes = [vp]
@@ -216,6 +219,16 @@ class Decoder:
     def step(self, tokens, positions, logits, stream=None) -> int:
         rc = lib().mk_decode_step(self.h, _i32(tokens), _i32(positions),
                                   ctypes.c_void_p(logits.data_ptr()), _stream_ptr(stream))
+        _check(rc, self.h)
+        return rc
+
+    def decode_greedy(self, tokens, positions, n_steps: int, tokens_out, logits,
+                      stream=None) -> int:
+        """mk_decode_greedy: n_steps greedy steps, the tokens fed back on the
+        device; tokens_out is a device int32 tensor of n_steps * batch."""
+        rc = lib().mk_decode_greedy(self.h, _i32(tokens), _i32(positions), int(n_steps),
+                                    ctypes.c_void_p(tokens_out.data_ptr()),
+                                    ctypes.c_void_p(logits.data_ptr()), _stream_ptr(stream))
         _check(rc, self.h)
         return rc
 

@@ -96,6 +96,24 @@ int mk_create(const mk_config* cfg, const mk_weights* w,
 int mk_decode_step(mk_handle* h, const int32_t* token_ids, const int32_t* positions,
                    float* logits_out, void* stream);
 
+/* Greedy decode of n_steps tokens per sequence in one call, the next token
+   fed back on the device (no host round trip between steps): step s
+   (0 <= s < n_steps) consumes token_ids[b] (s = 0, HOST) or the argmax of
+   step s - 1's logits (s > 0) at position positions[b] + s, appending its
+   k/v rows there as mk_decode_step does. The LM-head instruction fuses the
+   argmax (largest logit; the lowest token id among equal ones):
+   tokens_out[s * batch + b] (DEVICE int32, caller-owned, 16-byte aligned)
+   receives step s's argmax, logits_out (DEVICE fp32 [batch][vocab]) each
+   step's logits in turn, so the last step's remain. One interpreter launch
+   per step plus one small conversion launch, back to back on `stream`;
+   asynchronous. Returns MK_ERR_INVALID before launching when n_steps is
+   outside [1, MK_MAX_GREEDY_STEPS], a position + n_steps - 1 reaches
+   kv_capacity or a range check of mk_decode_step fails; otherwise as
+   mk_decode_step. */
+#define MK_MAX_GREEDY_STEPS 1024
+int mk_decode_greedy(mk_handle* h, const int32_t* token_ids, const int32_t* positions,
+                     int n_steps, int32_t* tokens_out, float* logits_out, void* stream);
+
 /* The same step run as the multi-launch comparison build: the same
    instruction templates and the same per-SM work units, but one kernel per
    (layer, instruction type) — kernel boundaries instead of counter waits —
