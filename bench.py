@@ -251,6 +251,24 @@ def run_gpu(args, wl):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / K
 
+    # greedy decode through mk_decode_greedy: 16 steps per call, each next
+    # token fed back on the device, the call's token ids read back to the host
+    g_steps = 16
+    g_calls = max(1, K // g_steps)
+    tok_dev = torch.empty(g_steps * wl.batch, dtype=torch.int32, device=dev)
+    tok_host = torch.empty(g_steps * wl.batch, dtype=torch.int32, pin_memory=True)
+    t0_, p0_ = tok_pos(0)
+    dec.decode_greedy(t0_, p0_, g_steps, tok_dev, logits)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(g_calls):
+        dec.decode_greedy(t0_, p0_, g_steps, tok_dev, logits)
+        tok_host.copy_(tok_dev, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert dec.status() == mk.MK_OK, dec.last_error()
+    greedy_ms = e0.elapsed_time(e1) / (g_calls * g_steps)
+
     ms = sum(per_mega) / K
     t_max = torch.tensor([ms], device=dev)
     if world > 1:
@@ -310,9 +328,8 @@ def run_gpu(args, wl):
                 "multilaunch_us": multi_ms * 1e3,
                 "multilaunch_graph_us": graph_ms * 1e3,
                 # per layer QKV, attention, (reduction,) O-projection, gate/up,
-                # down; one sequence has no reduction instruction
-                # one sequence with at most 2048 attention columns has no
-                # reduction instruction (the O-projection's staging reduces)
+                # down; one sequence with at most 2048 attention columns has
+                # no reduction instruction (the O-projection's staging reduces)
                 "multilaunch_launches_per_step":
                     (5 if wl.batch == 1 and shape.n_heads * shape.head_dim <= 2048 else 6)
                     * shape.n_layers + 1,
@@ -321,6 +338,8 @@ def run_gpu(args, wl):
                 "overhead_megakernel": (ms - t_min_ms) / ms,
                 "overhead_multilaunch": (multi_ms - t_min_ms) / multi_ms,
                 "wall_s_megakernel": wall_mega,
+                "greedy_us_per_step": greedy_ms * 1e3,
+                "greedy_steps_per_call": g_steps,
             },
         }
         print(json.dumps(line), flush=True)
