@@ -51,6 +51,10 @@ struct mk_handle {
   int n_ctr = 0;
   int* d_err = nullptr;
   unsigned long long* d_keys = nullptr;  // greedy decode: argmax keys [kMaxGreedySteps][B]
+  int kv_block = 0;       // paged KV cache: positions per block (0: contiguous caches)
+  int n_blocks = 0;       // paged KV cache: blocks in each layer's pool
+  int max_blocks = 0;     // paged KV cache: block-table entries per sequence
+  int* d_table = nullptr; // paged KV cache: the step's block table [B][max_blocks]
   int* h_err_mirror = nullptr;  // mapped pinned host memory the kernel writes on error
   std::vector<PlanEntry*> plans;
   unsigned long long use_clock = 0;
@@ -226,12 +230,17 @@ const char* mk_last_error(const mk_handle* h) {
   return h ? h->err.c_str() : g_create_error.c_str();
 }
 
-int mk_create(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
-              void* const* v_cache, mk_handle** out) {
+namespace {
+
+// mk_create and mk_create_paged (kv_block > 0: the caches are block pools)
+int create_impl(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
+                void* const* v_cache, int kv_block, int n_blocks, mk_handle** out) {
   if (!out) return fail(nullptr, MK_ERR_INVALID, "out is NULL");
   *out = nullptr;
   int rc = check_config(cfg, nullptr);
   if (rc) return rc;
+  if (kv_block < 0 || (kv_block > 0 && n_blocks < 1))
+    return fail(nullptr, MK_ERR_INVALID, "block_size must be >= 1 and n_blocks >= 1");
   if (!w || !k_cache || !v_cache) return fail(nullptr, MK_ERR_INVALID, "weights / caches NULL");
   const int L = cfg->n_layers;
   if (!w->embed || !w->final_norm || !w->attn_norm || !w->wq || !w->wk || !w->wv || !w->wo ||
@@ -255,6 +264,9 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
   std::unique_ptr<mk_handle> h(new mk_handle());
   h->cfg = *cfg;
   h->shape = shape_of(*cfg);
+  h->kv_block = kv_block;
+  h->n_blocks = n_blocks;
+  h->max_blocks = kv_block > 0 ? (cfg->kv_capacity + kv_block - 1) / kv_block : 0;
   const Shape& s = h->shape;
   cudaError_t ce = cudaGetDevice(&h->device);
   if (ce != cudaSuccess) return cuda_fail(nullptr, ce, "cudaGetDevice");
@@ -297,6 +309,7 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
       sizeof(int) * (size_t)2 * h->n_ctr,                                 // counters
       sizeof(int) * 64,                                                   // error word
       sizeof(unsigned long long) * (size_t)MK_MAX_GREEDY_STEPS * B,      // argmax keys
+      sizeof(int) * (size_t)B * std::max(1, h->max_blocks),               // block table
   };
   const int npieces = sizeof(sizes) / sizeof(sizes[0]);
   size_t offs[npieces], total = 0;
@@ -320,6 +333,10 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
   h->d_ctr = reinterpret_cast<int*>(base + offs[8]);
   h->d_err = reinterpret_cast<int*>(base + offs[9]);
   h->d_keys = reinterpret_cast<unsigned long long*>(base + offs[10]);
+  h->d_table = reinterpret_cast<int*>(base + offs[11]);
+  p.block_table = nullptr;  // set per step (paged handles)
+  p.max_blocks = h->max_blocks;
+  p.kv_block = kv_block;
   p.rope = h->d_rope;
   p.err = h->d_err;
   p.n_ctr = h->n_ctr;
@@ -373,6 +390,19 @@ int mk_create(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
   return MK_OK;
 }
 
+}  // namespace
+
+int mk_create(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
+              void* const* v_cache, mk_handle** out) {
+  return create_impl(cfg, w, k_cache, v_cache, 0, 0, out);
+}
+
+int mk_create_paged(const mk_config* cfg, const mk_weights* w, void* const* k_pool,
+                    void* const* v_pool, int block_size, int n_blocks, mk_handle** out) {
+  if (block_size < 1) return fail(nullptr, MK_ERR_INVALID, "block_size must be >= 1");
+  return create_impl(cfg, w, k_pool, v_pool, block_size, n_blocks, out);
+}
+
 int mk_destroy(mk_handle* h) {
   if (!h) return MK_OK;
   cudaDeviceSynchronize();
@@ -413,9 +443,49 @@ int mk_debug_inject_unsatisfiable_wait(mk_handle* h, int enable) {
   return MK_OK;
 }
 
+int mk_decode_step_paged(mk_handle* h, const int32_t* tok, const int32_t* pos,
+                         const int32_t* block_table, float* logits, void* stream) {
+  if (!h) return MK_ERR_INVALID;
+  if (h->kv_block == 0) return fail(h, MK_ERR_INVALID, "not a paged handle (mk_create_paged)");
+  int rc = check_steps(h, tok, pos);
+  if (rc) return rc;
+  if (!block_table) return fail(h, MK_ERR_INVALID, "block_table is NULL");
+  for (int b = 0; b < h->shape.B; ++b)
+    for (int i = 0; i <= pos[b] / h->kv_block; ++i) {
+      const int e = block_table[b * h->max_blocks + i];
+      if (e < 0 || e >= h->n_blocks)
+        return fail(h, MK_ERR_INVALID, "block_table entry out of range [0, n_blocks)");
+    }
+  if (!logits || !aligned16(logits)) return fail(h, MK_ERR_INVALID, "logits must be 16-byte aligned");
+  rc = check_sticky(h);
+  if (rc) return rc;
+  PlanEntry* e = nullptr;
+  rc = get_plan(h, pos, &e);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // pageable source: the copy has read the table when the call returns
+  MK_CUDA(h, cudaMemcpyAsync(h->d_table, block_table,
+                             sizeof(int) * (size_t)h->shape.B * h->max_blocks,
+                             cudaMemcpyHostToDevice, st));
+  Params p = step_params(h, tok, pos, logits);
+  p.block_table = h->d_table;
+  p.instrs = e->d_instrs;
+  p.sm_off = e->d_sm_off;
+  p.no_waits = 0;
+  p.trace_base = 0;
+  void* args[] = {&p};
+  cudaError_t ce = cudaLaunchCooperativeKernel(h->fn, dim3(h->n_sm), dim3(kThreads), args,
+                                               (size_t)h->smem_bytes, st);
+  if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaLaunchCooperativeKernel");
+  h->cur_set = (int)(h->steps & 1ull);
+  h->steps++;
+  return MK_OK;
+}
+
 int mk_decode_step(mk_handle* h, const int32_t* tok, const int32_t* pos, float* logits,
                    void* stream) {
   if (!h) return MK_ERR_INVALID;
+  if (h->kv_block) return fail(h, MK_ERR_INVALID, "paged handle: use mk_decode_step_paged");
   int rc = check_steps(h, tok, pos);
   if (rc) return rc;
   if (!logits || !aligned16(logits)) return fail(h, MK_ERR_INVALID, "logits must be 16-byte aligned");
@@ -442,6 +512,7 @@ int mk_decode_step(mk_handle* h, const int32_t* tok, const int32_t* pos, float* 
 int mk_decode_greedy(mk_handle* h, const int32_t* tok, const int32_t* pos, int n_steps,
                      int32_t* tokens_out, float* logits, void* stream) {
   if (!h) return MK_ERR_INVALID;
+  if (h->kv_block) return fail(h, MK_ERR_INVALID, "paged handle: greedy decode needs contiguous caches");
   int rc = check_steps(h, tok, pos);
   if (rc) return rc;
   if (n_steps < 1 || n_steps > MK_MAX_GREEDY_STEPS)
@@ -486,6 +557,7 @@ int mk_decode_greedy(mk_handle* h, const int32_t* tok, const int32_t* pos, int n
 int mk_decode_step_multilaunch(mk_handle* h, const int32_t* tok, const int32_t* pos,
                                float* logits, void* stream, int use_graph) {
   if (!h) return MK_ERR_INVALID;
+  if (h->kv_block) return fail(h, MK_ERR_INVALID, "paged handle: the multi-launch build needs contiguous caches");
   int rc = check_steps(h, tok, pos);
   if (rc) return rc;
   if (!logits || !aligned16(logits)) return fail(h, MK_ERR_INVALID, "logits must be 16-byte aligned");

@@ -175,6 +175,14 @@ __device__ __forceinline__ RowSrc row_src_of(const Params& p, const Instr& in) {
   return s;
 }
 
+// element offset of key/value row t of (sequence b, kv-head g) in a layer's
+// cache, contiguous or paged; rows of one block are contiguous
+__device__ __forceinline__ size_t kv_row(const Params& p, int b, int g, int t) {
+  if (!p.block_table) return (((size_t)b * p.nkv + g) * (size_t)p.S + t) * p.D;
+  const int blk = __ldg(p.block_table + b * p.max_blocks + t / p.kv_block);
+  return (((size_t)blk * p.nkv + g) * p.kv_block + t % p.kv_block) * p.D;
+}
+
 // ---------------------------------------------------------------------------
 // loader role
 // ---------------------------------------------------------------------------
@@ -240,7 +248,6 @@ static __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, cons
       // still waits for its queries
       const AttnSpan sp = attn_span(p.pos[in.a0], in.a2 >> 16, in.a2 & 0xffff, p.D);
       const LayerPtrs& L = p.layers[in.layer];
-      const size_t kvbase = ((size_t)in.a0 * p.nkv + in.a1) * (size_t)p.S * p.D;
       for (int pg = 0; pg < sp.npages; ++pg) {
         if (!wait_mbar(p, m, &m->empty[slot], (round & 1u) ^ 1u, kErrTimeoutPage)) {
           ok = false;
@@ -251,8 +258,17 @@ static __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, cons
         const uint32_t bytes = (uint32_t)nk * (uint32_t)p.D * 2u;
         uint8_t* dst = smem + (size_t)slot * kPageBytes;
         mbar_arrive_expect_tx(&m->full[slot], 2u * bytes);
-        bulk_g2s_hint(dst, L.kc + kvbase + (size_t)k0 * p.D, bytes, &m->full[slot], pol);
-        bulk_g2s_hint(dst + kPageBytes / 2, L.vc + kvbase + (size_t)k0 * p.D, bytes, &m->full[slot], pol);
+        // one copy per run of keys that are contiguous in the cache (a paged
+        // cache breaks runs at block boundaries)
+        for (int t = k0, off = 0; t < k0 + nk;) {
+          const int run = p.block_table ? min(k0 + nk - t, p.kv_block - t % p.kv_block) : nk;
+          const size_t row = kv_row(p, in.a0, in.a1, t);
+          const uint32_t rb = (uint32_t)run * (uint32_t)p.D * 2u;
+          bulk_g2s_hint(dst + off, L.kc + row, rb, &m->full[slot], pol);
+          bulk_g2s_hint(dst + kPageBytes / 2 + off, L.vc + row, rb, &m->full[slot], pol);
+          t += run;
+          off += (int)rb;
+        }
         ++page_cnt;
         if (++slot == p.n_pages) {
           slot = 0;
@@ -904,7 +920,7 @@ __device__ void attn_unit(const Params& p, Misc* m, uint8_t* smem, const Instr& 
   uint32_t vn[NB];
   if (new_here) {
     const LayerPtrs& L = p.layers[in.layer];
-    const size_t row = (((size_t)b * p.nkv + g) * (size_t)p.S + pos) * D;
+    const size_t row = kv_row(p, b, g, pos);
 #pragma unroll
     for (int j2 = 0; j2 < D / 64; ++j2) {
       const uint4 z = make_uint4(0, 0, 0, 0);
@@ -1341,8 +1357,7 @@ __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const
             qd[0] = o0;
             qd[half] = o1;
           } else {
-            uint16_t* c = (pr.which == 1 ? L.kc : L.vc) +
-                          (((size_t)b * p.nkv + pr.head) * p.S + pos) * p.D + pr.i;
+            uint16_t* c = (pr.which == 1 ? L.kc : L.vc) + kv_row(p, b, pr.head, pos) + pr.i;
             c[0] = __bfloat16_as_ushort(__float2bfloat16_rn(o0));
             c[half] = __bfloat16_as_ushort(__float2bfloat16_rn(o1));
           }

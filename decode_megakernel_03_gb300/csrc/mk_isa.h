@@ -89,6 +89,11 @@ struct Params {
                                // attention partials itself (no reduction instruction)
   int h_ring;                  // one sequence: the loader fetches each down-projection
                                // chunk of h into one of two h slots (at off_h)
+  // paged KV cache (block_table null: each layer's cache is [B][nkv][S][D]):
+  // each layer's pool is [n_blocks][nkv][kv_block][D]; position t of
+  // sequence b lives in block block_table[b * max_blocks + t / kv_block]
+  const int* block_table;
+  int max_blocks, kv_block;
   // greedy decode (both may be null): the previous step's argmax keys, read
   // as this step's tokens instead of tok[]; this step's argmax keys, raised
   // with atomicMax by the LM head (key = ordered(logit) << 32 | ~index, so the

@@ -23,7 +23,8 @@ OP_QKV, OP_ATTN, OP_RED, OP_OPROJ, OP_GATEUP, OP_DOWN, OP_LMHEAD = range(1, 8)
 EXPORTS = ("mk_create", "mk_decode_step", "mk_decode_step_multilaunch", "mk_get_status",
            "mk_destroy", "mk_last_error", "mk_read_counters", "mk_set_timeout",
            "mk_debug_inject_unsatisfiable_wait", "mk_set_trace", "mk_schedule_build",
-           "mk_decode_step_noalloc", "mk_debug_use_generic_kernel", "mk_decode_greedy")
+           "mk_decode_step_noalloc", "mk_debug_use_generic_kernel", "mk_decode_greedy",
+           "mk_create_paged", "mk_decode_step_paged")
 
 MAX_GREEDY_STEPS = 1024  # MK_MAX_GREEDY_STEPS
 
@@ -82,6 +83,9 @@ def lib():
         L.mk_decode_step.argtypes = [vp, i32p, i32p, vp, vp]
         L.mk_decode_step_multilaunch.argtypes = [vp, i32p, i32p, vp, vp, ctypes.c_int]
         L.mk_decode_greedy.argtypes = [vp, i32p, i32p, ctypes.c_int, vp, vp, vp]
+        L.mk_create_paged.argtypes = [ctypes.POINTER(MkConfig), ctypes.POINTER(MkWeights), _vpp,
+                                      _vpp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(vp)]
+        L.mk_decode_step_paged.argtypes = [vp, i32p, i32p, i32p, vp, vp]
         L.mk_get_status.argtypes = [vp, vp]
         L.mk_destroy.argtypes = [vp]
         L.mk_last_error.argtypes = [vp]
@@ -189,10 +193,14 @@ class Decoder:
     [B][nkv][S][D] bf16 CUDA tensors, updated in place by every step.
     """
 
-    def __init__(self, shape, weights: dict, k_cache: list, v_cache: list, batch: int):
+    def __init__(self, shape, weights: dict, k_cache: list, v_cache: list, batch: int,
+                 paged=None):
+        """paged = (block_size, n_blocks, kv_capacity): k_cache / v_cache are
+        block pools [n_blocks][nkv][block_size][D] (mk_create_paged), stepped
+        with step_paged."""
         self.shape = shape
         self.batch = batch
-        self.capacity = int(k_cache[0].shape[2])
+        self.capacity = int(k_cache[0].shape[2]) if paged is None else int(paged[2])
         L = shape.n_layers
         self._keep = (weights, k_cache, v_cache)
         arrs = {}
@@ -209,9 +217,14 @@ class Decoder:
         self._vc = (ctypes.c_void_p * L)(*[t.data_ptr() for t in v_cache])
         self.cfg = make_config(shape, batch, self.capacity)
         h = ctypes.c_void_p()
-        rc = lib().mk_create(ctypes.byref(self.cfg), ctypes.byref(self._w),
-                             ctypes.cast(self._kc, _vpp), ctypes.cast(self._vc, _vpp),
-                             ctypes.byref(h))
+        if paged is None:
+            rc = lib().mk_create(ctypes.byref(self.cfg), ctypes.byref(self._w),
+                                 ctypes.cast(self._kc, _vpp), ctypes.cast(self._vc, _vpp),
+                                 ctypes.byref(h))
+        else:
+            rc = lib().mk_create_paged(ctypes.byref(self.cfg), ctypes.byref(self._w),
+                                       ctypes.cast(self._kc, _vpp), ctypes.cast(self._vc, _vpp),
+                                       int(paged[0]), int(paged[1]), ctypes.byref(h))
         _check(rc, None)
         self.h = h
 
@@ -219,6 +232,17 @@ class Decoder:
     def step(self, tokens, positions, logits, stream=None) -> int:
         rc = lib().mk_decode_step(self.h, _i32(tokens), _i32(positions),
                                   ctypes.c_void_p(logits.data_ptr()), _stream_ptr(stream))
+        _check(rc, self.h)
+        return rc
+
+    def step_paged(self, tokens, positions, block_table, logits, stream=None) -> int:
+        """mk_decode_step_paged; block_table: int32 numpy array
+        [batch][ceil(kv_capacity / block_size)] on the host."""
+        tbl = np.ascontiguousarray(block_table, dtype=np.int32)
+        rc = lib().mk_decode_step_paged(self.h, _i32(tokens), _i32(positions),
+                                        tbl.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                        ctypes.c_void_p(logits.data_ptr()),
+                                        _stream_ptr(stream))
         _check(rc, self.h)
         return rc
 

@@ -83,6 +83,28 @@ typedef struct {
 int mk_create(const mk_config* cfg, const mk_weights* w,
               void* const* k_cache, void* const* v_cache, mk_handle** out);
 
+/* mk_create for a paged KV cache: k_pool[l] / v_pool[l] (DEVICE, bf16,
+   caller-owned, 16-byte aligned) are each layer's block pool
+   [n_blocks][n_kv_heads][block_size][head_dim]; position t of sequence b
+   lives in block block_table[b][t / block_size] of the table passed to
+   mk_decode_step_paged, at row t % block_size. config->kv_capacity bounds
+   the positions (block tables have ceil(kv_capacity / block_size) entries
+   per sequence). Such a handle takes mk_decode_step_paged only (not
+   mk_decode_step, mk_decode_greedy or the multi-launch build).
+   Errors: as mk_create, and MK_ERR_INVALID when block_size < 1 or
+   n_blocks < 1. */
+int mk_create_paged(const mk_config* cfg, const mk_weights* w, void* const* k_pool,
+                    void* const* v_pool, int block_size, int n_blocks, mk_handle** out);
+
+/* mk_decode_step for a paged handle. block_table: HOST int32
+   [batch][ceil(kv_capacity / block_size)], copied to the device by the call
+   (the caller may reuse it on return); the entries that cover positions
+   0..positions[b] must lie in [0, n_blocks) (MK_ERR_INVALID before any
+   launch otherwise); the step appends sequence b's k/v row at position
+   positions[b] into its block. Otherwise as mk_decode_step. */
+int mk_decode_step_paged(mk_handle* h, const int32_t* token_ids, const int32_t* positions,
+                         const int32_t* block_table, float* logits_out, void* stream);
+
 /* One decode step, ONE kernel launch (the persistent interpreter).
    token_ids, positions: HOST arrays of `batch` int32. Sequence b consumes
    token_ids[b] at position positions[b]: its new k/v row is written into slot
