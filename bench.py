@@ -269,6 +269,37 @@ def run_gpu(args, wl):
     assert dec.status() == mk.MK_OK, dec.last_error()
     greedy_ms = e0.elapsed_time(e1) / (g_calls * g_steps)
 
+    # the same steps on a paged KV cache: the caches' contents in pools of
+    # 16-position blocks in shuffled order, a host block table per step
+    bs = 16
+    mb = wl.capacity // bs
+    n_blocks = wl.batch * mb
+    perm = torch.randperm(n_blocks, generator=torch.Generator().manual_seed(7))
+    table = perm.view(wl.batch, mb).numpy().astype(np.int32)
+    def to_pool(c):
+        blocks = c[:, :, :mb * bs].reshape(wl.batch, shape.n_kv_heads, mb, bs, shape.head_dim)
+        blocks = blocks.permute(0, 2, 1, 3, 4).reshape(n_blocks, shape.n_kv_heads, bs,
+                                                       shape.head_dim)
+        pool = torch.empty_like(blocks)
+        pool[perm.to(dev)] = blocks
+        return pool
+    kp, vp = [to_pool(c) for c in kc], [to_pool(c) for c in vc]
+    dp = mk.Decoder(shape, w, kp, vp, wl.batch, paged=(bs, n_blocks, mb * bs))
+    for s in range(W):
+        t, p = tok_pos(s)
+        dp.step_paged(t, p, table, logits)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for s in range(K):
+        t, p = tok_pos(s)
+        dp.step_paged(t, p, table, logits)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert dp.status() == mk.MK_OK, dp.last_error()
+    paged_ms = e0.elapsed_time(e1) / K
+    dp.close()
+    del kp, vp
+
     ms = sum(per_mega) / K
     t_max = torch.tensor([ms], device=dev)
     if world > 1:
@@ -340,6 +371,8 @@ def run_gpu(args, wl):
                 "wall_s_megakernel": wall_mega,
                 "greedy_us_per_step": greedy_ms * 1e3,
                 "greedy_steps_per_call": g_steps,
+                "paged_kv_us_per_step": paged_ms * 1e3,
+                "paged_kv_block_size": bs,
             },
         }
         print(json.dumps(line), flush=True)

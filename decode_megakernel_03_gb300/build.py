@@ -18,7 +18,8 @@ ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libmk.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 
-SOURCES = ["mk_kernel.cu", "mk_kernel_fixed_a.cu", "mk_kernel_fixed_b.cu", "mk_abi.cu", "mk_sched.cpp",
+SOURCES = ["mk_kernel.cu", "mk_kernel_fixed_a.cu", "mk_kernel_fixed_b.cu", "mk_kernel_fx.cu",
+           "mk_abi.cu", "mk_sched.cpp",
            "mk_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]

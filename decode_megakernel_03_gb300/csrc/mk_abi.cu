@@ -44,6 +44,7 @@ struct mk_handle {
   int n_sm = 0;
   int smem_bytes = 0;
   const void* fn = nullptr;  // the interpreter instantiation this handle launches
+  const void* fn_fx = nullptr;  // the one with the paged-cache / greedy-decode code
   Params base{};          // launch parameters without the per-step fields
   void* d_scratch = nullptr;
   float2* d_rope = nullptr;
@@ -378,9 +379,13 @@ int create_impl(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
     lp[l].vc = static_cast<uint16_t*>(v_cache[l]);
   }
   h->fn = kernel_for(s, false);
+  h->fn_fx = kernel_features(s);
   ce = cudaMemcpy(h->d_rope, rope.data(), sizeof(float2) * rope.size(), cudaMemcpyHostToDevice);
   if (ce == cudaSuccess)
     ce = cudaFuncSetAttribute(h->fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              h->smem_bytes);
+  if (ce == cudaSuccess)
+    ce = cudaFuncSetAttribute(h->fn_fx, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               h->smem_bytes);
   if (ce != cudaSuccess) {
     cudaFree(h->d_scratch);
@@ -474,7 +479,7 @@ int mk_decode_step_paged(mk_handle* h, const int32_t* tok, const int32_t* pos,
   p.no_waits = 0;
   p.trace_base = 0;
   void* args[] = {&p};
-  cudaError_t ce = cudaLaunchCooperativeKernel(h->fn, dim3(h->n_sm), dim3(kThreads), args,
+  cudaError_t ce = cudaLaunchCooperativeKernel(h->fn_fx, dim3(h->n_sm), dim3(kThreads), args,
                                                (size_t)h->smem_bytes, st);
   if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaLaunchCooperativeKernel");
   h->cur_set = (int)(h->steps & 1ull);
@@ -542,7 +547,7 @@ int mk_decode_greedy(mk_handle* h, const int32_t* tok, const int32_t* pos, int n
     p.no_waits = 0;
     p.trace_base = 0;
     void* args[] = {&p};
-    cudaError_t ce = cudaLaunchCooperativeKernel(h->fn, dim3(h->n_sm), dim3(kThreads), args,
+    cudaError_t ce = cudaLaunchCooperativeKernel(h->fn_fx, dim3(h->n_sm), dim3(kThreads), args,
                                                  (size_t)h->smem_bytes, st);
     if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaLaunchCooperativeKernel");
     h->cur_set = (int)(h->steps & 1ull);

@@ -177,8 +177,11 @@ __device__ __forceinline__ RowSrc row_src_of(const Params& p, const Instr& in) {
 
 // element offset of key/value row t of (sequence b, kv-head g) in a layer's
 // cache, contiguous or paged; rows of one block are contiguous
+// FX: the interpreter is built with the paged-cache and greedy-decode code
+// (kernels without it carry none of that code: the instruction cache)
+template <int FX>
 __device__ __forceinline__ size_t kv_row(const Params& p, int b, int g, int t) {
-  if (!p.block_table) return (((size_t)b * p.nkv + g) * (size_t)p.S + t) * p.D;
+  if (!FX || !p.block_table) return (((size_t)b * p.nkv + g) * (size_t)p.S + t) * p.D;
   const int blk = __ldg(p.block_table + b * p.max_blocks + t / p.kv_block);
   return (((size_t)blk * p.nkv + g) * p.kv_block + t % p.kv_block) * p.D;
 }
@@ -229,6 +232,7 @@ __device__ __forceinline__ void issue_page(const Params& p, const Instr& in, con
   }
 }
 
+template <int FX>
 static __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, const Instr* q, int n) {
   const int lane = threadIdx.x & 31;
   if (lane != 0) return;
@@ -261,8 +265,8 @@ static __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, cons
         // one copy per run of keys that are contiguous in the cache (a paged
         // cache breaks runs at block boundaries)
         for (int t = k0, off = 0; t < k0 + nk;) {
-          const int run = p.block_table ? min(k0 + nk - t, p.kv_block - t % p.kv_block) : nk;
-          const size_t row = kv_row(p, in.a0, in.a1, t);
+          const int run = FX && p.block_table ? min(k0 + nk - t, p.kv_block - t % p.kv_block) : nk;
+          const size_t row = kv_row<FX>(p, in.a0, in.a1, t);
           const uint32_t rb = (uint32_t)run * (uint32_t)p.D * 2u;
           bulk_g2s_hint(dst + off, L.kc + row, rb, &m->full[slot], pol);
           bulk_g2s_hint(dst + kPageBytes / 2 + off, L.vc + row, rb, &m->full[slot], pol);
@@ -367,8 +371,9 @@ struct Staged {
 
 // the token of sequence b: from the parameters, or (greedy decode) from the
 // previous step's argmax
+template <int FX>
 __device__ __forceinline__ int token_of(const Params& p, int b) {
-  return p.tok_keys ? key_token(__ldcg(p.tok_keys + b)) : p.tok[b];
+  return FX && p.tok_keys ? key_token(__ldcg(p.tok_keys + b)) : p.tok[b];
 }
 
 __device__ __forceinline__ int act_key(int kind, int layer, int chunk) {
@@ -389,7 +394,7 @@ __device__ __forceinline__ const uint16_t* norm_weight(const Params& p, int kind
 // each group of four columns c .. c + 3 is stored in place as the bf16 split
 // v = hi + lo of its values, {hi(c, c+1), lo(c, c+1), hi(c+2, c+3),
 // lo(c+2, c+3)}: the A fragment of the tensor-core product (page_rows_mma).
-template <int B>
+template <int B, int FX>
 __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, Staged& st, int kind,
                                       int layer, int chunk) {
   constexpr bool kFrag = B > 1;
@@ -431,7 +436,7 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
 #pragma unroll
           for (int bb = 0; bb < kNB; ++bb) {
             if (from_embed) {
-              const uint16_t* erow = p.embed + (size_t)token_of(p, b0 + bb) * p.H;
+              const uint16_t* erow = p.embed + (size_t)token_of<FX>(p, b0 + bb) * p.H;
               const uint2 e = *reinterpret_cast<const uint2*>(erow + c);
               v[bb][u] = make_float4(bf_lo(e.x), bf_hi(e.x), bf_lo(e.y), bf_hi(e.y));
             } else {
@@ -892,7 +897,7 @@ __device__ __forceinline__ uint4 split_hi_lo(float a, float b, float c, float d)
                     bf16x2_rn(c - bf_lo(h23), d - bf_hi(h23)));
 }
 
-template <int D>
+template <int D, int FX>
 __device__ void attn_unit(const Params& p, Misc* m, uint8_t* smem, const Instr& in,
                           uint32_t page_base) {
   constexpr int KS = D / 16;                   // product steps over the head dimension
@@ -920,7 +925,7 @@ __device__ void attn_unit(const Params& p, Misc* m, uint8_t* smem, const Instr& 
   uint32_t vn[NB];
   if (new_here) {
     const LayerPtrs& L = p.layers[in.layer];
-    const size_t row = kv_row(p, b, g, pos);
+    const size_t row = kv_row<FX>(p, b, g, pos);
 #pragma unroll
     for (int j2 = 0; j2 < D / 64; ++j2) {
       const uint4 z = make_uint4(0, 0, 0, 0);
@@ -1139,7 +1144,7 @@ __device__ __forceinline__ void attn_reduce(const Params& p, const Instr& in) {
 // compute role: the instruction loop
 // ---------------------------------------------------------------------------
 
-template <int B, int DS, int GS, int KW>
+template <int B, int DS, int GS, int KW, int FX>
 __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Instr* q, int n,
                              int qbase) {
   const int warp = compute_warp(), lane = threadIdx.x & 31;
@@ -1201,7 +1206,7 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
               staged = true;
             }
           }
-          if (!staged) stage<B>(p, m, smem, st, kind, in.layer, chunk);
+          if (!staged) stage<B, FX>(p, m, smem, st, kind, in.layer, chunk);
         }
         act = reinterpret_cast<const float*>(smem + (to_h ? p.off_h : p.off_x));
       }
@@ -1229,9 +1234,9 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
       st.key_h = -1;
       // runs even after an abort: its loads stay in bounds and its barriers
       // must be met by every compute warp
-      if constexpr (DS > 0) attn_unit<DS>(p, m, smem, in, page_cnt);
-      else if (p.D == 64) attn_unit<64>(p, m, smem, in, page_cnt);
-      else attn_unit<128>(p, m, smem, in, page_cnt);
+      if constexpr (DS > 0) attn_unit<DS, FX>(p, m, smem, in, page_cnt);
+      else if (p.D == 64) attn_unit<64, FX>(p, m, smem, in, page_cnt);
+      else attn_unit<128, FX>(p, m, smem, in, page_cnt);
       page_cnt += (uint32_t)attn_span(p.pos[in.a0], in.a2 >> 16, in.a2 & 0xffff, p.D).npages;
     } else if (in.op == MK_OP_RED) {
       // the reduction instruction: several sequences, or one sequence with
@@ -1281,7 +1286,7 @@ struct EpiPre {
   float2 v[2][B];
 };
 
-template <int B>
+template <int B, int FX>
 __device__ __forceinline__ void epilogue_prefetch(const Params& p, Misc* m, const Instr& in,
                                                   EpiPre<B>& pre) {
   const int lane = threadIdx.x & 31;
@@ -1318,14 +1323,14 @@ __device__ __forceinline__ void epilogue_prefetch(const Params& p, Misc* m, cons
         const int j = in.a0 + it;
 #pragma unroll
         for (int b = 0; b < B; ++b)
-          pre.v[k][b].x = from_embed ? bf16f(p.embed[(size_t)token_of(p, b) * p.H + j])
+          pre.v[k][b].x = from_embed ? bf16f(p.embed[(size_t)token_of<FX>(p, b) * p.H + j])
                                      : __ldcg(src + (size_t)b * p.H + j);
       }
     }
   }
 }
 
-template <int B>
+template <int B, int FX>
 __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const float* res,
                                          float* dacc, const EpiPre<B>& pre) {
   const int lane = threadIdx.x & 31;
@@ -1357,7 +1362,7 @@ __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const
             qd[0] = o0;
             qd[half] = o1;
           } else {
-            uint16_t* c = (pr.which == 1 ? L.kc : L.vc) + kv_row(p, b, pr.head, pos) + pr.i;
+            uint16_t* c = (pr.which == 1 ? L.kc : L.vc) + kv_row<FX>(p, b, pr.head, pos) + pr.i;
             c[0] = __bfloat16_as_ushort(__float2bfloat16_rn(o0));
             c[half] = __bfloat16_as_ushort(__float2bfloat16_rn(o1));
           }
@@ -1383,7 +1388,7 @@ __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const
       }
     }
   }
-  if (in.op == MK_OP_LMHEAD && p.argmax_out) {
+  if (FX && in.op == MK_OP_LMHEAD && p.argmax_out) {
     // greedy decode: the instruction's best row per sequence joins the
     // step's argmax (atomicMax of order-preserving keys: any order of the
     // SMs gives the same result)
@@ -1417,7 +1422,7 @@ __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const
 // warps, so the epilogue itself touches only registers and shared memory.
 // (Publishing several instructions behind one fence was measured slower: it
 // delays the first counter of each batch, which sits on the critical path.)
-template <int B>
+template <int B, int FX>
 __device__ void storer_role(const Params& p, Misc* m, uint8_t* smem, const Instr* q, int n) {
   const int lane = threadIdx.x & 31;
   float* dacc = reinterpret_cast<float*>(smem + p.off_dacc);
@@ -1428,11 +1433,11 @@ __device__ void storer_role(const Params& p, Misc* m, uint8_t* smem, const Instr
     const int buf = i % kResBufs;
     const uint32_t par = ((uint32_t)i / kResBufs) & 1u;
     EpiPre<B> pre;
-    if (is_gemv(in.op) && !aborted(m)) epilogue_prefetch<B>(p, m, in, pre);
+    if (is_gemv(in.op) && !aborted(m)) epilogue_prefetch<B, FX>(p, m, in, pre);
     const bool ok = wait_mbar(p, m, &m->res_full[buf], par, kErrTimeoutRes);
     if (ok && !aborted(m)) {
       const float* res = reinterpret_cast<const float*>(smem + p.off_res) + (size_t)buf * p.res_floats;
-      if (is_gemv(in.op)) epilogue<B>(p, in, res, dacc, pre);
+      if (is_gemv(in.op)) epilogue<B, FX>(p, in, res, dacc, pre);
       if (in.sig_ctr >= 0) {
         // the warp barrier orders the other lanes' stores (and, through the
         // result mbarrier, the compute warps' stores) before lane 0's
@@ -1462,7 +1467,7 @@ __device__ void storer_role(const Params& p, Misc* m, uint8_t* smem, const Instr
 // the kernel
 // ---------------------------------------------------------------------------
 
-template <int B, int DS, int GS, int KW>
+template <int B, int DS, int GS, int KW, int FX>
 __global__ void __launch_bounds__(kThreads, 1) interp_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Misc* m = reinterpret_cast<Misc*>(smem + p.off_misc);
@@ -1494,9 +1499,9 @@ __global__ void __launch_bounds__(kThreads, 1) interp_kernel(const __grid_consta
   const int n = p.sm_off[blockIdx.x + 1] - q0;
   const Instr* q = p.instrs + q0;
   const int warp = threadIdx.x >> 5;
-  if (warp == kLoaderWarp) loader_role(p, m, smem, q, n);
-  else if (warp == kStorerWarp) storer_role<B>(p, m, smem, q, n);
-  else compute_role<B, DS, GS, KW>(p, m, smem, q, n, q0);
+  if (warp == kLoaderWarp) loader_role<FX>(p, m, smem, q, n);
+  else if (warp == kStorerWarp) storer_role<B, FX>(p, m, smem, q, n);
+  else compute_role<B, DS, GS, KW, FX>(p, m, smem, q, n, q0);
 }
 
 }  // namespace mk

@@ -8,10 +8,10 @@ namespace mk {
 
 const void* kernel_generic(int B) {
   switch (B) {
-    case 1: return reinterpret_cast<const void*>(&interp_kernel<1, 0, 0, 0>);
-    case 2: return reinterpret_cast<const void*>(&interp_kernel<2, 0, 0, 0>);
-    case 4: return reinterpret_cast<const void*>(&interp_kernel<4, 0, 0, 0>);
-    case 8: return reinterpret_cast<const void*>(&interp_kernel<8, 0, 0, 0>);
+    case 1: return reinterpret_cast<const void*>(&interp_kernel<1, 0, 0, 0, 0>);
+    case 2: return reinterpret_cast<const void*>(&interp_kernel<2, 0, 0, 0, 0>);
+    case 4: return reinterpret_cast<const void*>(&interp_kernel<4, 0, 0, 0, 0>);
+    case 8: return reinterpret_cast<const void*>(&interp_kernel<8, 0, 0, 0, 0>);
     default: return nullptr;
   }
 }

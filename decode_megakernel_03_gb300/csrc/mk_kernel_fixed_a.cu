@@ -10,8 +10,8 @@ namespace mk {
 
 const void* kernel_fixed_a(const Shape& s) {
   if (s.B == 1 && s.D == 64 && s.G() == 4 && s.H == 2048 && s.QD() == 2048 && s.Fc() == 2048)
-    return reinterpret_cast<const void*>(&interp_kernel<1, 64, 4, 2048>);
-  if (s.B == 1 && s.D == 64 && s.G() == 2) return reinterpret_cast<const void*>(&interp_kernel<1, 64, 2, 0>);
+    return reinterpret_cast<const void*>(&interp_kernel<1, 64, 4, 2048, 0>);
+  if (s.B == 1 && s.D == 64 && s.G() == 2) return reinterpret_cast<const void*>(&interp_kernel<1, 64, 2, 0, 0>);
   return nullptr;
 }
 

@@ -8,8 +8,8 @@
 namespace mk {
 
 const void* kernel_fixed_b(const Shape& s) {
-  if (s.B == 1 && s.D == 128 && s.G() == 4) return reinterpret_cast<const void*>(&interp_kernel<1, 128, 4, 0>);
-  if (s.B == 8 && s.D == 64 && s.G() == 4) return reinterpret_cast<const void*>(&interp_kernel<8, 64, 4, 0>);
+  if (s.B == 1 && s.D == 128 && s.G() == 4) return reinterpret_cast<const void*>(&interp_kernel<1, 128, 4, 0, 0>);
+  if (s.B == 8 && s.D == 64 && s.G() == 4) return reinterpret_cast<const void*>(&interp_kernel<8, 64, 4, 0, 0>);
   return nullptr;
 }
 

@@ -5,7 +5,10 @@ namespace mk {
 
 struct Shape;
 
-// interp_kernel<B, 0, 0, 0>: head dimension and q-heads per kv-head read at
+// interp_kernel<B, DS, GS, KW, FX>: batch, head dimension (0: read at run
+// time), q-heads per kv-head (0: run time), GEMV width (2048, or 0: any),
+// and FX = 1 for the build with the paged-cache and greedy-decode code.
+// interp_kernel<B, 0, 0, 0, 0>: head dimension and q-heads per kv-head read at
 // run time, any GEMV width (B = 1, 2, 4 or 8).
 const void* kernel_generic(int B);
 // Instantiations specialised to a model's shape, or nullptr when the shape
@@ -15,6 +18,9 @@ const void* kernel_fixed_b(const Shape& s);
 // The kernel a step of this shape runs: the specialised one when there is
 // one (unless `generic`), else the generic one.
 const void* kernel_for(const Shape& s, bool generic);
+// The instantiation with the paged-cache and greedy-decode code for this
+// shape (specialised for the Llama-1B shape at batch 1, else generic).
+const void* kernel_features(const Shape& s);
 // Size of the kernel's shared-memory barrier block.
 int misc_bytes();
 
