@@ -394,7 +394,9 @@ __device__ __forceinline__ const uint16_t* norm_weight(const Params& p, int kind
 // each group of four columns c .. c + 3 is stored in place as the bf16 split
 // v = hi + lo of its values, {hi(c, c+1), lo(c, c+1), hi(c+2, c+3),
 // lo(c+2, c+3)}: the A fragment of the tensor-core product (page_rows_mma).
-template <int B, int FX>
+// kWide: rows may be wider than 3072 columns (one sequence): six column groups
+// per thread, so that 4608 columns still take one L2 round trip
+template <int B, int FX, bool kWide>
 __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, Staged& st, int kind,
                                       int layer, int chunk) {
   constexpr bool kFrag = B > 1;
@@ -419,7 +421,7 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
   // pass costs one round trip to L2: 2048-wide vectors of all sequences at
   // once
   constexpr int kNB = B;
-  constexpr int kU = B == 1 ? 4 : 3;
+  constexpr int kU = B == 1 ? (kWide ? 6 : 4) : 3;
   constexpr int kPass = kComputeThreads * 4 * kU;  // columns per pass
   for (int b0 = 0; b0 < B; b0 += kNB) {
     float ss[kNB];
@@ -1206,7 +1208,7 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
               staged = true;
             }
           }
-          if (!staged) stage<B, FX>(p, m, smem, st, kind, in.layer, chunk);
+          if (!staged) stage<B, FX, (B == 1 && KW == 0)>(p, m, smem, st, kind, in.layer, chunk);
         }
         act = reinterpret_cast<const float*>(smem + (to_h ? p.off_h : p.off_x));
       }
