@@ -142,7 +142,8 @@ struct Builder {
   // goes to SM (k + rot) % n_sm: rotating per step moves the ranges that get
   // one item more around the SMs, so their totals over the step stay level.
   template <class F>
-  void spread(int n, int align, int rot, F emit) {
+  void spread(int n, int align, int rot, F emit, int item_cap = 0) {
+    const int cap = item_cap > 0 ? item_cap : this->cap;
     for (int k = 0; k < n_sm; ++k) {
       int sm = (k + rot) % n_sm;
       int lo = (int)((long)n * k / n_sm);
@@ -237,10 +238,13 @@ struct Builder {
 
   void add_lm_head() {
     Step st{MK_OP_LMHEAD, -1, {}};
+    // one row per item: twice the items of a row-pair instruction fit the
+    // result buffer, up to the 64 the storer's epilogue takes (fewer
+    // instructions for the longest GEMV of the step)
     spread(s.V, 0, rot_of(s.L, 0), [&](int sm, int a, int b) {
       st.items.push_back({sm, make(MK_OP_LMHEAD, s.L - 1, a, b, 0, cm.xout(s.L - 1), s.H, cm.lm(),
                                    b - a)});
-    });
+    }, std::min(64, 2 * cap));
     steps.push_back(std::move(st));
   }
 };
