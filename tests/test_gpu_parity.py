@@ -195,3 +195,29 @@ def test_unsatisfiable_wait_times_out_and_recovers():
     again = pair.gpu_step([3], [40])
     np.testing.assert_array_equal(again, good)
     pair.close()
+
+
+# shapes the workloads do not cover: 8 query heads per kv-head (the most the
+# tensor-core attention takes in one product), head_dim 128 with several
+# sequences, and a tied head on the generic kernels
+G8 = synth.ModelShape("g8", 2, 512, 8, 1, 64, 1024, 4096, tied=False, rope_theta=10000.0)
+D128 = synth.ModelShape("d128", 2, 512, 4, 2, 128, 1024, 4096, tied=True, rope_theta=10000.0)
+
+
+@pytest.mark.parametrize("shape,batch", [(G8, 1), (G8, 2), (G8, 8), (D128, 1), (D128, 2)])
+def test_other_head_shapes(shape, batch):
+    cap = 256
+    ctx = tuple(70 + 41 * b % 150 for b in range(batch))
+    pair = Pair(shape, batch, cap, ctx=ctx)
+    tally = Tally()
+    for s in range(2):
+        tok = [(13 * s + 7 * b + 1) % shape.vocab for b in range(batch)]
+        pos = [c + s for c in ctx]
+        bk = [bf16_bits(t) for t in pair.kc]
+        bv = [bf16_bits(t) for t in pair.vc]
+        got = pair.gpu_step(tok, pos)
+        want = pair.oracle_step(tok, pos)
+        tally.add(compare_logits(got, want))
+        check_kv_step(pair, pos, bk, bv)
+    print(shape.name, batch, tally.check())
+    pair.close()
