@@ -56,6 +56,13 @@ struct mk_handle {
   int n_blocks = 0;       // paged KV cache: blocks in each layer's pool
   int max_blocks = 0;     // paged KV cache: block-table entries per sequence
   int* d_table = nullptr; // paged KV cache: the step's block table [B][max_blocks]
+  int* d_ctr_steps = nullptr;  // counters of a several-step launch [kMaxLaunchSteps][n_ctr]
+  struct StepsPlan {
+    std::vector<int> key;  // steps, then each step's partition counts
+    Instr* d_instrs = nullptr;
+    int* d_sm_off = nullptr;
+  };
+  std::vector<StepsPlan> steps_plans;
   int* h_err_mirror = nullptr;  // mapped pinned host memory the kernel writes on error
   std::vector<PlanEntry*> plans;
   unsigned long long use_clock = 0;
@@ -217,6 +224,8 @@ int check_sticky(mk_handle* h) {
   return MK_OK;
 }
 
+static_assert(MK_MAX_STEPS_PER_LAUNCH == kMaxLaunchSteps, "steps per launch");
+
 // greedy decode: argmax keys -> token ids
 __global__ void keys_to_tokens(const unsigned long long* keys, int n, int32_t* tokens) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -311,6 +320,7 @@ int create_impl(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
       sizeof(int) * 64,                                                   // error word
       sizeof(unsigned long long) * (size_t)MK_MAX_GREEDY_STEPS * B,      // argmax keys
       sizeof(int) * (size_t)B * std::max(1, h->max_blocks),               // block table
+      sizeof(int) * (size_t)kMaxLaunchSteps * h->n_ctr,                   // several-step counters
   };
   const int npieces = sizeof(sizes) / sizeof(sizes[0]);
   size_t offs[npieces], total = 0;
@@ -335,6 +345,7 @@ int create_impl(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
   h->d_err = reinterpret_cast<int*>(base + offs[9]);
   h->d_keys = reinterpret_cast<unsigned long long*>(base + offs[10]);
   h->d_table = reinterpret_cast<int*>(base + offs[11]);
+  h->d_ctr_steps = reinterpret_cast<int*>(base + offs[12]);
   p.block_table = nullptr;  // set per step (paged handles)
   p.max_blocks = h->max_blocks;
   p.kv_block = kv_block;
@@ -412,6 +423,10 @@ int mk_destroy(mk_handle* h) {
   if (!h) return MK_OK;
   cudaDeviceSynchronize();
   for (PlanEntry* e : h->plans) free_plan(e);
+  for (auto& sp : h->steps_plans) {
+    cudaFree(sp.d_instrs);
+    cudaFree(sp.d_sm_off);
+  }
   cudaFree(h->d_scratch);
   if (h->h_err_mirror) cudaFreeHost(h->h_err_mirror);
   delete h;
@@ -553,6 +568,81 @@ int mk_decode_greedy(mk_handle* h, const int32_t* tok, const int32_t* pos, int n
     h->cur_set = (int)(h->steps & 1ull);
     h->steps++;
   }
+  const int n = n_steps * B;
+  keys_to_tokens<<<(n + 255) / 256, 256, 0, st>>>(h->d_keys, n, tokens_out);
+  MK_CUDA(h, cudaGetLastError());
+  return MK_OK;
+}
+
+int mk_decode_greedy_persistent(mk_handle* h, const int32_t* tok, const int32_t* pos,
+                                int n_steps, int32_t* tokens_out, float* logits, void* stream) {
+  if (!h) return MK_ERR_INVALID;
+  if (h->kv_block) return fail(h, MK_ERR_INVALID, "paged handle: greedy decode needs contiguous caches");
+  int rc = check_steps(h, tok, pos);
+  if (rc) return rc;
+  if (n_steps < 1 || n_steps > MK_MAX_STEPS_PER_LAUNCH)
+    return fail(h, MK_ERR_INVALID, "n_steps must be in [1, MK_MAX_STEPS_PER_LAUNCH]");
+  const int B = h->shape.B;
+  for (int b = 0; b < B; ++b)
+    if (pos[b] + n_steps - 1 >= h->shape.S)
+      return fail(h, MK_ERR_INVALID, "positions + n_steps - 1 must be < kv_capacity");
+  if (!tokens_out || !aligned16(tokens_out))
+    return fail(h, MK_ERR_INVALID, "tokens_out must be 16-byte aligned");
+  if (!logits || !aligned16(logits)) return fail(h, MK_ERR_INVALID, "logits must be 16-byte aligned");
+  rc = check_sticky(h);
+  if (rc) return rc;
+  // the plan: every step's partitions (cached by them)
+  std::vector<int> parts((size_t)n_steps * kMaxBatch, 0);
+  std::vector<int> key(1, n_steps);
+  for (int s = 0; s < n_steps; ++s) {
+    int32_t ps[kMaxBatch] = {0};
+    for (int b = 0; b < B; ++b) ps[b] = pos[b] + s;
+    choose_partitions(h->shape, h->n_sm, ps, parts.data() + (size_t)s * kMaxBatch);
+    key.insert(key.end(), parts.begin() + (size_t)s * kMaxBatch,
+               parts.begin() + (size_t)(s + 1) * kMaxBatch);
+  }
+  mk_handle::StepsPlan* sp = nullptr;
+  for (auto& c : h->steps_plans)
+    if (c.key == key) sp = &c;
+  if (!sp) {
+    Plan P;
+    std::string why;
+    if (!build_plan_steps(h->shape, h->n_sm, parts.data(), n_steps, &P, &why))
+      return fail(h, MK_ERR_INVALID, why);
+    if (h->steps_plans.size() >= 4) {
+      MK_CUDA(h, cudaDeviceSynchronize());
+      cudaFree(h->steps_plans.front().d_instrs);
+      cudaFree(h->steps_plans.front().d_sm_off);
+      h->steps_plans.erase(h->steps_plans.begin());
+    }
+    mk_handle::StepsPlan c;
+    c.key = key;
+    MK_CUDA(h, cudaMalloc(&c.d_instrs, sizeof(Instr) * std::max<size_t>(1, P.instrs.size())));
+    MK_CUDA(h, cudaMalloc(&c.d_sm_off, sizeof(int) * P.sm_off.size()));
+    MK_CUDA(h, cudaMemcpy(c.d_instrs, P.instrs.data(), sizeof(Instr) * P.instrs.size(),
+                          cudaMemcpyHostToDevice));
+    MK_CUDA(h, cudaMemcpy(c.d_sm_off, P.sm_off.data(), sizeof(int) * P.sm_off.size(),
+                          cudaMemcpyHostToDevice));
+    h->steps_plans.push_back(c);
+    sp = &h->steps_plans.back();
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MK_CUDA(h, cudaMemsetAsync(h->d_ctr_steps, 0, sizeof(int) * (size_t)n_steps * h->n_ctr, st));
+  MK_CUDA(h, cudaMemsetAsync(h->d_keys, 0, sizeof(unsigned long long) * (size_t)n_steps * B, st));
+  Params p = step_params(h, tok, pos, logits);
+  p.ctr = h->d_ctr_steps;
+  p.ctr_zero = nullptr;  // this launch's counters were cleared just above
+  p.n_ctr_step = h->n_ctr;
+  p.lm_ctr = CounterMap{h->shape.L, h->shape.nkv, B}.lm();
+  p.argmax_out = h->d_keys;
+  p.instrs = sp->d_instrs;
+  p.sm_off = sp->d_sm_off;
+  p.no_waits = 0;
+  p.trace_base = 0;
+  void* args[] = {&p};
+  cudaError_t ce = cudaLaunchCooperativeKernel(h->fn_fx, dim3(h->n_sm), dim3(kThreads), args,
+                                               (size_t)h->smem_bytes, st);
+  if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaLaunchCooperativeKernel");
   const int n = n_steps * B;
   keys_to_tokens<<<(n + 255) / 256, 256, 0, st>>>(h->d_keys, n, tokens_out);
   MK_CUDA(h, cudaGetLastError());

@@ -165,7 +165,7 @@ __device__ __forceinline__ RowSrc row_src_of(const Params& p, const Instr& in) {
     s.w[0] = p.lm;
     return s;
   }
-  const LayerPtrs* L = p.layers + in.layer;
+  const LayerPtrs* L = p.layers + layer_of(in);
   switch (in.op) {
     case MK_OP_QKV: s.w[0] = L->wq; s.w[1] = L->wk; s.w[2] = L->wv; break;
     case MK_OP_OPROJ: s.w[0] = L->wo; break;
@@ -241,6 +241,7 @@ static __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, cons
   int slot = 0;           // page_cnt % n_pages
   uint32_t round = 0;     // page_cnt / n_pages
   uint32_t h_cnt = 0;     // h chunks copied into the h ring
+  int acq_step = 0;       // greedy steps whose LM head this loader has acquired
   bool ok = true;
   Instr nxt = n > 0 ? load_instr(q) : Instr{};
   for (int i = 0; i < n && ok; ++i) {
@@ -250,8 +251,23 @@ static __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, cons
       // the unit's cached keys, K and V rows of kpp keys per page; they do
       // not depend on this step's outputs, so they stream in while the unit
       // still waits for its queries
-      const AttnSpan sp = attn_span(p.pos[in.a0], in.a2 >> 16, in.a2 & 0xffff, p.D);
-      const LayerPtrs& L = p.layers[in.layer];
+      const AttnSpan sp = attn_span(p.pos[in.a0] + step_of(in), in.a2 >> 16, in.a2 & 0xffff, p.D);
+      const LayerPtrs& L = p.layers[layer_of(in)];
+      if constexpr (FX) {
+        // keys written by an earlier step of this launch: every write of step
+        // s - 1 is ordered before its LM head's count (and the bulk copies
+        // below after this acquire)
+        const int st = step_of(in);
+        if (st > acq_step) {
+          if (!p.no_waits &&
+              !wait_counter(p, m, p.lm_ctr + (st - 1) * p.n_ctr_step, p.V)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();
+          acq_step = st;
+        }
+      }
       for (int pg = 0; pg < sp.npages; ++pg) {
         if (!wait_mbar(p, m, &m->empty[slot], (round & 1u) ^ 1u, kErrTimeoutPage)) {
           ok = false;
@@ -372,7 +388,8 @@ struct Staged {
 // the token of sequence b: from the parameters, or (greedy decode) from the
 // previous step's argmax
 template <int FX>
-__device__ __forceinline__ int token_of(const Params& p, int b) {
+__device__ __forceinline__ int token_of(const Params& p, int b, int step) {
+  if (FX && step > 0) return key_token(__ldcg(p.argmax_out + (size_t)(step - 1) * p.B + b));
   return FX && p.tok_keys ? key_token(__ldcg(p.tok_keys + b)) : p.tok[b];
 }
 
@@ -398,7 +415,7 @@ __device__ __forceinline__ const uint16_t* norm_weight(const Params& p, int kind
 // per thread, so that 4608 columns still take one L2 round trip
 template <int B, int FX, bool kWide>
 __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, Staged& st, int kind,
-                                      int layer, int chunk) {
+                                      int layer, int chunk, int key, int step) {
   constexpr bool kFrag = B > 1;
   const int tid = compute_tid();  // 0..kComputeThreads-1
   const int warp = tid >> 5, lane = tid & 31;
@@ -438,7 +455,7 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
 #pragma unroll
           for (int bb = 0; bb < kNB; ++bb) {
             if (from_embed) {
-              const uint16_t* erow = p.embed + (size_t)token_of<FX>(p, b0 + bb) * p.H;
+              const uint16_t* erow = p.embed + (size_t)token_of<FX>(p, b0 + bb, step) * p.H;
               const uint2 e = *reinterpret_cast<const uint2*>(erow + c);
               v[bb][u] = make_float4(bf_lo(e.x), bf_hi(e.x), bf_lo(e.y), bf_hi(e.y));
             } else {
@@ -496,7 +513,6 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
     }
   }
   st.stage_cnt++;
-  const int key = act_key(kind, layer, chunk);
   if (to_h) {
     st.key_h = key;
     if (p.alias_xh) st.key_x = -1;
@@ -518,7 +534,7 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
 // across rounds. P: partitions per head.
 template <int D>
 __device__ __forceinline__ void stage_attn_fused(const Params& p, uint8_t* smem, Staged& st,
-                                                 int layer, int P) {
+                                                 int layer, int P, int key) {
   constexpr int kG = 1;  // column groups per thread per pass (768 columns: smaller code, as fast)
   constexpr int kR = 6;  // partitions per round
   constexpr int LPH = D / 4 < 32 ? D / 4 : 32;  // lanes covering one head
@@ -592,7 +608,7 @@ __device__ __forceinline__ void stage_attn_fused(const Params& p, uint8_t* smem,
   }
   compute_bar();
   st.stage_cnt++;
-  st.key_x = act_key(kActAttnOut, layer, 0);
+  st.key_x = key;
 #pragma unroll
   for (int b = 0; b < kMaxBatch; ++b) st.inv_x.v[b] = 1.f;
   if (p.alias_xh) st.key_h = -1;
@@ -909,7 +925,7 @@ __device__ void attn_unit(const Params& p, Misc* m, uint8_t* smem, const Instr& 
   const int warp = compute_warp(), lane = threadIdx.x & 31;
   const int grp = lane >> 2, tig = lane & 3, odd = grp & 1;
   const int b = in.a0, g = in.a1, pidx = in.a2 >> 16, P = in.a2 & 0xffff;
-  const int G = p.G, pos = p.pos[b];
+  const int G = p.G, pos = p.pos[b] + step_of(in);
   const AttnSpan sp = attn_span(pos, pidx, P, D);
   const float qscale = 1.4426950408889634f * rsqrtf((float)D);
   const float* qhead = p.q + (size_t)b * p.QD + (size_t)g * G * D;
@@ -926,7 +942,7 @@ __device__ void attn_unit(const Params& p, Misc* m, uint8_t* smem, const Instr& 
   uint4 kn[D / 64][2];
   uint32_t vn[NB];
   if (new_here) {
-    const LayerPtrs& L = p.layers[in.layer];
+    const LayerPtrs& L = p.layers[layer_of(in)];
     const size_t row = kv_row<FX>(p, b, g, pos);
 #pragma unroll
     for (int j2 = 0; j2 < D / 64; ++j2) {
@@ -1202,13 +1218,15 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
           bool staged = false;
           if constexpr (B == 1) {  // one sequence: the O-projection reduces while staging
             if (kind == kActAttnOut && p.fused_red) {
-              if constexpr (DS > 0) stage_attn_fused<DS>(p, smem, st, in.layer, in.a2);
-              else if (p.D == 64) stage_attn_fused<64>(p, smem, st, in.layer, in.a2);
-              else stage_attn_fused<128>(p, smem, st, in.layer, in.a2);
+              if constexpr (DS > 0) stage_attn_fused<DS>(p, smem, st, layer_of(in), in.a2, key);
+              else if (p.D == 64) stage_attn_fused<64>(p, smem, st, layer_of(in), in.a2, key);
+              else stage_attn_fused<128>(p, smem, st, layer_of(in), in.a2, key);
               staged = true;
             }
           }
-          if (!staged) stage<B, FX, (B == 1 && KW == 0)>(p, m, smem, st, kind, in.layer, chunk);
+          if (!staged)
+            stage<B, FX, (B == 1 && KW == 0)>(p, m, smem, st, kind, layer_of(in), chunk, key,
+                                               step_of(in));
         }
         act = reinterpret_cast<const float*>(smem + (to_h ? p.off_h : p.off_x));
       }
@@ -1239,7 +1257,8 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
       if constexpr (DS > 0) attn_unit<DS, FX>(p, m, smem, in, page_cnt);
       else if (p.D == 64) attn_unit<64, FX>(p, m, smem, in, page_cnt);
       else attn_unit<128, FX>(p, m, smem, in, page_cnt);
-      page_cnt += (uint32_t)attn_span(p.pos[in.a0], in.a2 >> 16, in.a2 & 0xffff, p.D).npages;
+      page_cnt += (uint32_t)attn_span(p.pos[in.a0] + step_of(in), in.a2 >> 16, in.a2 & 0xffff, p.D)
+                      .npages;
     } else if (in.op == MK_OP_RED) {
       // the reduction instruction: several sequences, or one sequence with
       // more than 2048 attention columns (the one-sequence kernel of head
@@ -1303,12 +1322,13 @@ __device__ __forceinline__ void epilogue_prefetch(const Params& p, Misc* m, cons
         const PairRows pr = pair_rows(in.a0 + it, p.G, p.D);
         if (pr.which < 2) {
 #pragma unroll
-          for (int b = 0; b < B; ++b) pre.v[k][b] = __ldg(p.rope + (size_t)p.pos[b] * half + pr.i);
+          for (int b = 0; b < B; ++b)
+            pre.v[k][b] = __ldg(p.rope + (size_t)(p.pos[b] + step_of(in)) * half + pr.i);
         }
       }
     }
   } else if (resid) {
-    const bool from_embed = in.op == MK_OP_OPROJ && in.layer == 0;
+    const bool from_embed = in.op == MK_OP_OPROJ && layer_of(in) == 0;
     if (!from_embed && !p.no_waits && in.wait_ctr >= 0) {
       // the residual rows were written by other SMs before the instruction's
       // input counter completed: acquire that counter (the compute warps
@@ -1325,7 +1345,7 @@ __device__ __forceinline__ void epilogue_prefetch(const Params& p, Misc* m, cons
         const int j = in.a0 + it;
 #pragma unroll
         for (int b = 0; b < B; ++b)
-          pre.v[k][b].x = from_embed ? bf16f(p.embed[(size_t)token_of<FX>(p, b) * p.H + j])
+          pre.v[k][b].x = from_embed ? bf16f(p.embed[(size_t)token_of<FX>(p, b, step_of(in)) * p.H + j])
                                      : __ldcg(src + (size_t)b * p.H + j);
       }
     }
@@ -1338,7 +1358,7 @@ __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const
   const int lane = threadIdx.x & 31;
   const Geom g = geom_of(in.op, p.H, p.QD, p.Fc);
   const int items = in.a1 - in.a0;
-  const LayerPtrs& L = p.layers[in.layer];
+  const LayerPtrs& L = p.layers[layer_of(in)];
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     const int it = lane + 32 * k;
@@ -1351,7 +1371,7 @@ __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const
       switch (in.op) {
         case MK_OP_QKV: {
           const PairRows pr = pair_rows(j, p.G, p.D);
-          const int pos = p.pos[b];
+          const int pos = p.pos[b] + step_of(in);
           const int half = p.D / 2;
           float o0 = v0, o1 = v1;
           if (pr.which < 2) {
@@ -1413,7 +1433,7 @@ __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const
         const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
         best = o > best ? o : best;
       }
-      if (lane == 0) atomicMax(p.argmax_out + b, best);
+      if (lane == 0) atomicMax(p.argmax_out + (size_t)step_of(in) * B + b, best);
     }
   }
 }
@@ -1449,7 +1469,7 @@ __device__ void storer_role(const Params& p, Misc* m, uint8_t* smem, const Instr
         // would wait for this SM's weight copies in flight.
         __syncwarp();
         if (lane == 0) {
-          if (in.op == MK_OP_LMHEAD) red_relaxed_add(p.ctr + in.sig_ctr, in.sig_amount);
+          if (in.op == MK_OP_LMHEAD && !FX) red_relaxed_add(p.ctr + in.sig_ctr, in.sig_amount);
           else red_release_add(p.ctr + in.sig_ctr, in.sig_amount);
         }
       }

@@ -100,6 +100,11 @@ struct Params {
   // largest logit wins and the lowest index among equal ones)
   const unsigned long long* tok_keys;
   unsigned long long* argmax_out;
+  // several greedy steps in one launch (instructions carry their step,
+  // layer = step << 10 | layer): step s > 0 reads its token from
+  // argmax_out[(s - 1) * B + b]; counters of step s are offset by
+  // s * n_ctr_step; lm_ctr is the LM head's counter of step 0
+  int n_ctr_step, lm_ctr;
   // per step
   int tok[kMaxBatch];
   int pos[kMaxBatch];
@@ -127,6 +132,12 @@ struct Geom {
 #else
 #define MK_HD inline
 #endif
+
+// layer and greedy step of an instruction (Instr::layer = step << 10 | layer)
+constexpr int kStepShift = 10;
+constexpr int kMaxLaunchSteps = 32;
+MK_HD int layer_of(const Instr& in) { return in.layer & ((1 << kStepShift) - 1); }
+MK_HD int step_of(const Instr& in) { return (in.layer >> kStepShift) & (kMaxLaunchSteps - 1); }
 
 // token id of a greedy-decode argmax key (Params::argmax_out)
 MK_HD int key_token(unsigned long long key) { return (int)(0xffffffffu - (uint32_t)key); }

@@ -335,6 +335,50 @@ bool build_plan(const Shape& s, int n_sm, const int* parts, Plan* out, std::stri
   return true;
 }
 
+bool build_plan_steps(const Shape& s, int n_sm, const int* parts, int k, Plan* out,
+                      std::string* why) {
+  if (k < 1 || k > kMaxLaunchSteps) {
+    if (why) *why = "steps per launch out of range";
+    return false;
+  }
+  if (s.L > (1 << kStepShift)) {
+    if (why) *why = "too many layers for steps in one launch";
+    return false;
+  }
+  std::vector<Plan> pl(k);
+  for (int st = 0; st < k; ++st)
+    if (!build_plan(s, n_sm, parts + st * kMaxBatch, &pl[st], why)) return false;
+  const int nc = (int)pl[0].targets.size();  // counters per step
+  const CounterMap cm{s.L, s.nkv, s.B};
+  out->n_sm = n_sm;
+  for (int b = 0; b < kMaxBatch; ++b) out->parts[b] = pl[0].parts[b];
+  out->instrs.clear();
+  out->targets.clear();
+  out->phases.clear();
+  out->sm_off.assign(n_sm + 1, 0);
+  for (int st = 0; st < k; ++st)
+    out->targets.insert(out->targets.end(), pl[st].targets.begin(), pl[st].targets.end());
+  for (int sm = 0; sm < n_sm; ++sm) {
+    out->sm_off[sm] = (int)out->instrs.size();
+    for (int st = 0; st < k; ++st) {
+      for (int i = pl[st].sm_off[sm]; i < pl[st].sm_off[sm + 1]; ++i) {
+        Instr in = pl[st].instrs[i];
+        in.layer = (int16_t)(in.layer | (st << kStepShift));
+        if (in.wait_ctr >= 0) in.wait_ctr += st * nc;
+        if (in.sig_ctr >= 0) in.sig_ctr += st * nc;
+        if (st > 0 && in.op == MK_OP_QKV && layer_of(in) == 0) {
+          // the token is the previous step's argmax
+          in.wait_ctr = cm.lm() + (st - 1) * nc;
+          in.wait_target = pl[st - 1].targets[cm.lm()];
+        }
+        out->instrs.push_back(in);
+      }
+    }
+  }
+  out->sm_off[n_sm] = (int)out->instrs.size();
+  return true;
+}
+
 int smem_layout(const Shape& s, int n_sm, int optin, int misc_bytes, Params* p, std::string* why) {
   // pages | x staging | h staging (one buffer, or two ring slots) | results |
   // down-projection chunk sums | barriers; the attention scratch reuses the

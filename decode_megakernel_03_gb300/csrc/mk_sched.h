@@ -72,6 +72,15 @@ int item_cap_for(const Shape& s);
 
 bool build_plan(const Shape& s, int n_sm, const int* parts, Plan* out, std::string* why);
 
+// k greedy steps in one launch (1 <= k <= kMaxLaunchSteps): the plans of the
+// steps (parts: k rows of kMaxBatch partition counts), each SM's queues
+// concatenated in step order; instructions carry their step in the layer
+// field, counters of step s are offset by s times the per-step count, and
+// step s > 0's layer-0 QKV instructions wait for step s - 1's LM head (their
+// token is its argmax). No multi-launch phases.
+bool build_plan_steps(const Shape& s, int n_sm, const int* parts, int k, Plan* out,
+                      std::string* why);
+
 // Shared-memory layout of the interpreter for this shape: fills the n_pages,
 // off_*, *_floats, alias_xh, h_ring and dacc_rows fields of p and returns the
 // dynamic shared memory size in bytes, or 0 (with *why set) when fewer than

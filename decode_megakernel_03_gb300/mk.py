@@ -24,7 +24,9 @@ EXPORTS = ("mk_create", "mk_decode_step", "mk_decode_step_multilaunch", "mk_get_
            "mk_destroy", "mk_last_error", "mk_read_counters", "mk_set_timeout",
            "mk_debug_inject_unsatisfiable_wait", "mk_set_trace", "mk_schedule_build",
            "mk_decode_step_noalloc", "mk_debug_use_generic_kernel", "mk_decode_greedy",
-           "mk_create_paged", "mk_decode_step_paged")
+           "mk_create_paged", "mk_decode_step_paged", "mk_decode_greedy_persistent")
+
+MAX_STEPS_PER_LAUNCH = 32  # MK_MAX_STEPS_PER_LAUNCH
 
 MAX_GREEDY_STEPS = 1024  # MK_MAX_GREEDY_STEPS
 
@@ -86,6 +88,7 @@ def lib():
         L.mk_create_paged.argtypes = [ctypes.POINTER(MkConfig), ctypes.POINTER(MkWeights), _vpp,
                                       _vpp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(vp)]
         L.mk_decode_step_paged.argtypes = [vp, i32p, i32p, i32p, vp, vp]
+        L.mk_decode_greedy_persistent.argtypes = [vp, i32p, i32p, ctypes.c_int, vp, vp, vp]
         L.mk_get_status.argtypes = [vp, vp]
         L.mk_destroy.argtypes = [vp]
         L.mk_last_error.argtypes = [vp]
@@ -253,6 +256,16 @@ class Decoder:
         rc = lib().mk_decode_greedy(self.h, _i32(tokens), _i32(positions), int(n_steps),
                                     ctypes.c_void_p(tokens_out.data_ptr()),
                                     ctypes.c_void_p(logits.data_ptr()), _stream_ptr(stream))
+        _check(rc, self.h)
+        return rc
+
+    def decode_greedy_persistent(self, tokens, positions, n_steps: int, tokens_out, logits,
+                                 stream=None) -> int:
+        """mk_decode_greedy_persistent: n_steps greedy steps in one launch."""
+        rc = lib().mk_decode_greedy_persistent(self.h, _i32(tokens), _i32(positions),
+                                               int(n_steps), ctypes.c_void_p(tokens_out.data_ptr()),
+                                               ctypes.c_void_p(logits.data_ptr()),
+                                               _stream_ptr(stream))
         _check(rc, self.h)
         return rc
 

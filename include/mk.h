@@ -136,6 +136,18 @@ int mk_decode_step(mk_handle* h, const int32_t* token_ids, const int32_t* positi
 int mk_decode_greedy(mk_handle* h, const int32_t* token_ids, const int32_t* positions,
                      int n_steps, int32_t* tokens_out, float* logits_out, void* stream);
 
+/* mk_decode_greedy with all n_steps steps in ONE persistent launch: each
+   SM's queue holds the steps one after the other, every step with its own
+   counters; step s + 1's first layer waits on step s's LM head (its argmax
+   is the token), and each SM's loader acquires that count before it
+   prefetches cached keys an earlier step of the launch wrote. Arguments,
+   results and errors as mk_decode_greedy, with 1 <= n_steps <=
+   MK_MAX_STEPS_PER_LAUNCH. */
+#define MK_MAX_STEPS_PER_LAUNCH 32
+int mk_decode_greedy_persistent(mk_handle* h, const int32_t* token_ids, const int32_t* positions,
+                                int n_steps, int32_t* tokens_out, float* logits_out,
+                                void* stream);
+
 /* The same step run as the multi-launch comparison build: the same
    instruction templates and the same per-SM work units, but one kernel per
    (layer, instruction type) — kernel boundaries instead of counter waits —

@@ -53,6 +53,33 @@ def test_greedy_equals_host_argmax_loop(name, batch, n):
         np.testing.assert_array_equal(x, y)
 
 
+@pytest.mark.parametrize("name,batch,n", [("tiny", 1, 12), ("tiny", 4, 8), ("llama1b", 1, 4)])
+def test_one_launch_greedy_equals_greedy(name, batch, n):
+    """All steps in one persistent launch: the same tokens, final logits and
+    caches as one launch per step."""
+    wl = synth.WORKLOADS[name]
+    cap = 256 if name == "tiny" else wl.capacity
+    ctx = tuple(40 + 23 * b for b in range(batch)) if name == "tiny" else wl.ctx
+    t0 = int(synth.step_tokens(wl)[0][0])
+    tok = [(t0 + 17 * b) % wl.shape.vocab for b in range(batch)]
+    a = Pair(wl.shape, batch, cap, ctx=ctx)
+    want_tok, want_logits = _device_loop(a, tok, list(ctx), n)
+    caches_a = [bf16_bits(t) for t in a.kc + a.vc]
+    a.close()
+    b = Pair(wl.shape, batch, cap, ctx=ctx)
+    out = torch.zeros(n * batch, dtype=torch.int32, device="cuda")
+    b.dec.decode_greedy_persistent(tok, list(ctx), n, out, b.logits)
+    assert b.dec.status() == mk.MK_OK, b.dec.last_error()
+    got_tok = out.cpu().numpy().reshape(n, batch)
+    got_logits = b.logits.cpu().numpy().astype(np.float64)
+    caches_b = [bf16_bits(t) for t in b.kc + b.vc]
+    b.close()
+    np.testing.assert_array_equal(got_tok, want_tok)
+    np.testing.assert_array_equal(got_logits, want_logits)
+    for x, y in zip(caches_a, caches_b):
+        np.testing.assert_array_equal(x, y)
+
+
 def test_greedy_follows_the_oracle():
     """Tiny shape, two sequences: the device-fed tokens are the oracle's greedy
     tokens (compared until a step whose oracle top-1/top-2 margin is below
@@ -90,5 +117,9 @@ def test_greedy_rejects_bad_arguments():
     for n, pos in ((0, 20), (mk.MAX_GREEDY_STEPS + 1, 20), (10, 120)):
         with pytest.raises(mk.MkError) as e:
             pair.dec.decode_greedy([1], [pos], n, out, pair.logits)
+        assert e.value.code == mk.MK_ERR_INVALID
+    for n, pos in ((0, 20), (mk.MAX_STEPS_PER_LAUNCH + 1, 20), (10, 120)):
+        with pytest.raises(mk.MkError) as e:
+            pair.dec.decode_greedy_persistent([1], [pos], n, out, pair.logits)
         assert e.value.code == mk.MK_ERR_INVALID
     pair.close()
