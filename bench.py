@@ -268,6 +268,17 @@ def run_gpu(args, wl):
     torch.cuda.synchronize()
     assert dec.status() == mk.MK_OK, dec.last_error()
     greedy_ms = e0.elapsed_time(e1) / (g_calls * g_steps)
+    # the same 16 steps in one persistent launch per call
+    dec.decode_greedy_persistent(t0_, p0_, g_steps, tok_dev, logits)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(g_calls):
+        dec.decode_greedy_persistent(t0_, p0_, g_steps, tok_dev, logits)
+        tok_host.copy_(tok_dev, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert dec.status() == mk.MK_OK, dec.last_error()
+    greedy_one_ms = e0.elapsed_time(e1) / (g_calls * g_steps)
 
     # the same steps on a paged KV cache: the caches' contents in pools of
     # 16-position blocks in shuffled order, a host block table per step
@@ -371,6 +382,7 @@ def run_gpu(args, wl):
                 "wall_s_megakernel": wall_mega,
                 "greedy_us_per_step": greedy_ms * 1e3,
                 "greedy_steps_per_call": g_steps,
+                "greedy_one_launch_us_per_step": greedy_one_ms * 1e3,
                 "paged_kv_us_per_step": paged_ms * 1e3,
                 "paged_kv_block_size": bs,
             },
