@@ -19,7 +19,8 @@ const void* kernel_fixed_b(const Shape& s);
 // one (unless `generic`), else the generic one.
 const void* kernel_for(const Shape& s, bool generic);
 // The instantiation with the paged-cache and greedy-decode code for this
-// shape (specialised for the Llama-1B shape at batch 1 and 8, else generic).
+// shape (specialised for the Llama-1B shape at batch 1 and 8 and the Llama-8B
+// shape, else generic).
 const void* kernel_features(const Shape& s);
 // Size of the kernel's shared-memory barrier block.
 int misc_bytes();
