@@ -1130,26 +1130,52 @@ __device__ void attn_unit(const Params& p, Misc* m, uint8_t* smem, const Instr& 
 template <int D>
 __device__ __forceinline__ void attn_reduce(const Params& p, const Instr& in) {
   constexpr int PL = D / 32;  // dims per lane
+  constexpr int kU = 8;       // partitions whose o rows load together
   const int warp = compute_warp(), lane = threadIdx.x & 31;
   const int b = in.a0, g = in.a1, P = in.a2;
   for (int hl = warp; hl < p.G; hl += kComputeWarps) {
     const int h = g * p.G + hl;
     const float* base = p.part + ((size_t)b * p.nh + h) * kMaxPartitions * D;
     const float* ml = p.part_ml + ((size_t)b * p.nh + h) * kMaxPartitions * 2;
-    float M = -INFINITY;
-    for (int k = lane; k < P; k += 32) M = fmaxf(M, __ldcg(ml + 2 * k));
+    // lane k (and k + 32) holds partition k's (m, l); P <= kMaxPartitions = 64
+    float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
+    if (lane < P) {
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(ml + 2 * lane));
+      m0 = v.x;
+      l0 = v.y;
+    }
+    if (lane + 32 < P) {
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(ml + 2 * (lane + 32)));
+      m1 = v.x;
+      l1 = v.y;
+    }
+    float M = fmaxf(m0, m1);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float acc[PL], den = 0.f;
+    const float w0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M);
+    const float w1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M);
+    float den = w0 * l0 + w1 * l1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    float acc[PL];
 #pragma unroll
     for (int e = 0; e < PL; ++e) acc[e] = 0.f;
-    for (int k = 0; k < P; ++k) {
-      const float* s = base + (size_t)k * D;
-      const float mk = __ldcg(ml + 2 * k);
-      const float wt = mk == -INFINITY ? 0.f : fast_exp2(mk - M);
-      den = fmaf(wt, __ldcg(ml + 2 * k + 1), den);
+    for (int k0 = 0; k0 < P; k0 += kU) {
+      float o[kU][PL];
 #pragma unroll
-      for (int e = 0; e < PL; ++e) acc[e] = fmaf(wt, __ldcg(s + lane * PL + e), acc[e]);
+      for (int u = 0; u < kU; ++u)
+#pragma unroll
+        for (int e = 0; e < PL; ++e)
+          o[u][e] = k0 + u < P ? __ldcg(base + (size_t)(k0 + u) * D + lane * PL + e) : 0.f;
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int k = k0 + u;  // its weight sits in lane k % 32 of w0 (k < 32) or w1
+        const float wa = __shfl_sync(0xffffffffu, w0, k & 31);
+        const float wb = __shfl_sync(0xffffffffu, w1, k & 31);
+        const float wt = k < P ? (k < 32 ? wa : wb) : 0.f;
+#pragma unroll
+        for (int e = 0; e < PL; ++e) acc[e] = fmaf(wt, o[u][e], acc[e]);
+      }
     }
     const float inv = 1.f / den;
     float* dst = p.attn + (size_t)b * p.QD + (size_t)h * D + lane * PL;
