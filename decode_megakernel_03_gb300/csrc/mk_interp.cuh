@@ -175,6 +175,14 @@ __device__ __forceinline__ RowSrc row_src_of(const Params& p, const Instr& in) {
   return s;
 }
 
+// h ring slot and round of the n-th chunk (h_ring is 1 or 2 slots)
+__device__ __forceinline__ int ring_slot(const Params& p, uint32_t n) {
+  return p.h_ring == 2 ? (int)(n & 1u) : 0;
+}
+__device__ __forceinline__ uint32_t ring_round(const Params& p, uint32_t n) {
+  return p.h_ring == 2 ? n >> 1 : n;
+}
+
 // element offset of key/value row t of (sequence b, kv-head g) in a layer's
 // cache, contiguous or paged; rows of one block are contiguous
 // FX: the interpreter is built with the paged-cache and greedy-decode code
@@ -303,8 +311,8 @@ static __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, cons
       // next h slot, once its counter says gate/up chunk a2 is complete. In
       // the queue the down chunks follow all four gate/up chunks, so the wait
       // is short, and it sits before weight pages that are not needed yet.
-      const int k = (int)(h_cnt & 1u);
-      if (!wait_mbar(p, m, &m->hempty[k], ((h_cnt >> 1) & 1u) ^ 1u, kErrTimeoutRes)) {
+      const int k = ring_slot(p, h_cnt);
+      if (!wait_mbar(p, m, &m->hempty[k], (ring_round(p, h_cnt) & 1u) ^ 1u, kErrTimeoutRes)) {
         ok = false;
         break;
       }
@@ -339,9 +347,10 @@ static __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, cons
   }
   if (!ok) {
     // drain: every issued copy must land before the CTA's shared memory goes away
-    for (uint32_t k = h_cnt > 2u ? h_cnt - 2u : 0u; k < h_cnt; ++k) {
+    const uint32_t nslot = p.h_ring == 2 ? 2u : 1u;
+    for (uint32_t k = h_cnt > nslot ? h_cnt - nslot : 0u; k < h_cnt; ++k) {
       const uint64_t t0 = globaltimer();
-      while (!mbar_try_wait(&m->hfull[k & 1u], (k >> 1) & 1u)) {
+      while (!mbar_try_wait(&m->hfull[ring_slot(p, k)], ring_round(p, k) & 1u)) {
         if (globaltimer() - t0 > p.timeout_ns) break;
       }
     }
@@ -1236,9 +1245,26 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
       const float* act;
       bool h_got = false;
       if (from_ring) {
-        const int k = (int)(h_cnt & 1u);
-        h_got = wait_mbar(p, m, &m->hfull[k], (h_cnt >> 1) & 1u, kErrTimeoutRes);
+        const int k = ring_slot(p, h_cnt);
+        h_got = wait_mbar(p, m, &m->hfull[k], ring_round(p, h_cnt) & 1u, kErrTimeoutRes);
         act = reinterpret_cast<const float*>(smem + p.off_h) + (size_t)k * p.Fc;
+        if constexpr (B == 1 && KW == 0) {
+          if (g.K > 2048) {
+            // a wide chunk: copied into the x buffer (idle until the next
+            // layer restages it) and its slot handed back at once, so the
+            // loader fetches the next chunk while this one runs
+            float* xb = reinterpret_cast<float*>(smem + p.off_x);
+            compute_bar();  // the previous instruction's pages are read
+            for (int c = compute_tid() * 4; c < g.K; c += kComputeThreads * 4)
+              *reinterpret_cast<float4*>(xb + c) = *reinterpret_cast<const float4*>(act + c);
+            compute_bar();
+            __syncwarp();
+            if (lane == 0 && h_got) mbar_arrive(&m->hempty[k]);
+            ++h_cnt;
+            st.key_x = -1;
+            act = xb;
+          }
+        }
       } else {
         if ((to_h ? st.key_h : st.key_x) != key) {
           bool staged = false;
@@ -1266,7 +1292,7 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
           // the slot is in registers now (a copy that has not landed, after an
           // abort, keeps its slot: the loader must not start another into it)
           __syncwarp();
-          if (lane == 0 && h_got) mbar_arrive(&m->hempty[h_cnt & 1u]);
+          if (lane == 0 && h_got) mbar_arrive(&m->hempty[ring_slot(p, h_cnt)]);
           ++h_cnt;
         }
         gemv_run<B, true, KW>(p, m, smem, in, g, act, one, ax, res, page_cnt);

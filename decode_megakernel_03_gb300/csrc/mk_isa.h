@@ -88,7 +88,7 @@ struct Params {
   int fused_red;               // one sequence: the O-projection's staging reduces the
                                // attention partials itself (no reduction instruction)
   int h_ring;                  // one sequence: the loader fetches each down-projection
-                               // chunk of h into one of two h slots (at off_h)
+                               // chunk of h into one of h_ring slots (at off_h; 0: none)
   // paged KV cache (block_table null: each layer's cache is [B][nkv][S][D]):
   // each layer's pool is [n_blocks][nkv][kv_block][D]; position t of
   // sequence b lives in block block_table[b * max_blocks + t / kv_block]

@@ -399,7 +399,7 @@ int smem_layout(const Shape& s, int n_sm, int optin, int misc_bytes, Params* p, 
   const int att_scratch = kComputeWarps * s.G() * (s.D + 2);
   auto staging_floats = [&](int ring) {
     int xh = p->alias_xh ? std::max(p->x_floats, p->h_floats)
-                         : p->x_floats + (ring ? 2 : 1) * p->h_floats;
+                         : p->x_floats + std::max(1, ring) * p->h_floats;
     xh = std::max(xh, att_scratch);
     return (xh + 3) / 4 * 4;
   };
@@ -413,12 +413,18 @@ int smem_layout(const Shape& s, int n_sm, int optin, int misc_bytes, Params* p, 
     int n = std::min(kMaxPages, (optin - fixed) / kPageBytes);
     return n - n % kComputeWarps;
   };
-  // the h ring serves the one-sequence register path (chunks of at most 2048
-  // columns) and is used only when it costs no page; the attention scratch
-  // must stay inside the x part of the staging area, clear of the h slots
-  // (the loader may fill them while attention runs)
-  int ring = B == 1 && s.Fc() <= 2048 && att_scratch <= p->x_floats ? 1 : 0;
-  if (ring && pages_for(1) < pages_for(0)) ring = 0;
+  // the h ring (one sequence): two slots for chunks of at most 2048 columns
+  // (the register path takes a chunk out of its slot at once), one slot for
+  // wider chunks (copied into the idle x buffer at once); used only when it
+  // costs no page. The attention scratch must stay inside the x part of the
+  // staging area, clear of the h slots (the loader may fill them while
+  // attention runs).
+  int ring = 0;
+  if (B == 1 && att_scratch <= p->x_floats) {
+    if (s.Fc() <= 2048) ring = 2;
+    else if (s.Fc() <= p->x_floats) ring = 1;
+  }
+  if (ring && pages_for(ring) < pages_for(0)) ring = 0;
   const int n_pages = pages_for(ring);
   if (n_pages < kComputeWarps) {
     if (why) *why = "configuration leaves too few shared-memory pages";
