@@ -133,10 +133,43 @@ def cpu_oracle_rate(wl, w_host, target_s=12.0, max_steps=64):
     return n * wl.batch / dt, n, dt, threads
 
 
+def replica_env():
+    """(world, rank, local rank) from the launcher's environment; one rank
+    and no process group without torchrun."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's x. Replicas share no data, so the job
+    advances at the pace of its slowest replica: its step time is the max
+    of the ranks' step times. `device` holds the one-element reduction
+    tensor (a CUDA device under NCCL, the CPU under gloo)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(batch: int, world: int, ms_per_step: float) -> float:
+    """Whole-job tokens/s: every rank decodes `batch` sequences one token per
+    step, and a step of the job takes the slowest rank's time."""
+    return batch * world / (ms_per_step * 1e-3)
+
+
+def rank_barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
 def run_reference(args, wl):
-    rank = int(os.environ.get("RANK", "0"))
+    _, rank, _ = replica_env()
     if rank != 0:
-        return
+        return  # the reference arm runs on rank 0 alone
     from decode_megakernel_03_gb300 import synth
     w = synth.make_weights(wl.shape, seed=wl.weight_seed)
     w_host = synth.oracle_weights(w)
@@ -179,9 +212,7 @@ def run_gpu(args, wl):
     from decode_megakernel_03_gb300 import build as mkbuild
     from decode_megakernel_03_gb300 import mk, synth
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = replica_env()
     if world > 1:
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
@@ -209,8 +240,7 @@ def run_gpu(args, wl):
             else:
                 dec.step_multilaunch(t, p, logits, graph=(mode == "graph"))
         torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
+        rank_barrier(world)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(K)]
         torch.cuda.synchronize()
@@ -225,6 +255,7 @@ def run_gpu(args, wl):
             ev[s][1].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t_wall
+        rank_barrier(world)
         assert dec.status() == mk.MK_OK, dec.last_error()
         per = [a.elapsed_time(b) for a, b in ev]
         return per, wall
@@ -241,6 +272,7 @@ def run_gpu(args, wl):
         dec.step(t, p, logits)
         host_logits.copy_(logits, non_blocking=True)
     torch.cuda.synchronize()
+    rank_barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for s in range(K):
@@ -249,7 +281,8 @@ def run_gpu(args, wl):
         host_logits.copy_(logits, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / K
+    rank_barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K, world, dev)
 
     # greedy decode through mk_decode_greedy: 16 steps per call, each next
     # token fed back on the device, the call's token ids read back to the host
@@ -312,10 +345,7 @@ def run_gpu(args, wl):
     del kp, vp
 
     ms = sum(per_mega) / K
-    t_max = torch.tensor([ms], device=dev)
-    if world > 1:
-        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
-    ms_all = float(t_max.item())
+    ms_all = max_over_ranks(ms, world, dev)
 
     positions = [synth.step_positions(wl, s % wl.steps) for s in range(K)]
     wb, kvb = zip(*[algorithmic_bytes(shape, wl.batch, p) for p in positions])
@@ -339,7 +369,7 @@ def run_gpu(args, wl):
         clocks = clk.summary()
         line = {
             "metric": METRIC,
-            "value": wl.batch * world / (ms_all * 1e-3),
+            "value": job_rate(wl.batch, world, ms_all),
             "unit": "tokens/s",
             "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": ms_all,
@@ -358,7 +388,7 @@ def run_gpu(args, wl):
                          "algorithmic_bytes_per_step": bytes_step, "traffic": traffic,
                          "t_min_us": t_min_ms * 1e3},
             "cpu_baseline": cpu,
-            "e2e": {"value": wl.batch / (e2e_ms * 1e-3), "unit": "tokens/s",
+            "e2e": {"value": job_rate(wl.batch, world, e2e_ms), "unit": "tokens/s",
                     "h2d_bytes_per_step": 8 * wl.batch,
                     "d2h_bytes_per_step": 4 * wl.batch * shape.vocab},
             "gpu_launches": K,
