@@ -45,6 +45,11 @@ CASES = [
     (synth.LLAMA_1B, 1, 8256, 152, [8200]),
     (synth.LLAMA_8B, 1, 2112, 152, [2048]),
     (synth.LLAMA_1B, 8, 4160, 152, list(synth.WORKLOADS["llama1b_b8"].ctx)),
+    # four query heads per kv-head at batch 8, and head_dim 128 with a single kv-head
+    (synth.ModelShape("g4", 2, 512, 8, 2, 64, 1024, 4096, tied=False, rope_theta=1e4), 8, 256, 152,
+     [33 + 29 * b for b in range(8)]),
+    (synth.ModelShape("d128g4", 2, 512, 4, 1, 128, 1024, 4096, tied=True, rope_theta=5e5), 1, 256,
+     152, [33]),
 ]
 
 
