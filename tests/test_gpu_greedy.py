@@ -53,7 +53,8 @@ def test_greedy_equals_host_argmax_loop(name, batch, n):
         np.testing.assert_array_equal(x, y)
 
 
-@pytest.mark.parametrize("name,batch,n", [("tiny", 1, 12), ("tiny", 4, 8), ("llama1b", 1, 4)])
+@pytest.mark.parametrize("name,batch,n", [("tiny", 1, 12), ("tiny", 4, 8), ("llama1b", 1, 4),
+                                          ("tiny", 2, mk.MAX_STEPS_PER_LAUNCH)])
 def test_one_launch_greedy_equals_greedy(name, batch, n):
     """All steps in one persistent launch: the same tokens, final logits and
     caches as one launch per step."""
@@ -72,6 +73,27 @@ def test_one_launch_greedy_equals_greedy(name, batch, n):
     assert b.dec.status() == mk.MK_OK, b.dec.last_error()
     got_tok = out.cpu().numpy().reshape(n, batch)
     got_logits = b.logits.cpu().numpy().astype(np.float64)
+    caches_b = [bf16_bits(t) for t in b.kc + b.vc]
+    b.close()
+    np.testing.assert_array_equal(got_tok, want_tok)
+    np.testing.assert_array_equal(got_logits, want_logits)
+    for x, y in zip(caches_a, caches_b):
+        np.testing.assert_array_equal(x, y)
+
+
+def test_greedy_at_its_maximum_step_count():
+    """MAX_GREEDY_STEPS steps in one call, one sequence on the tiny shape:
+    the tokens, final logits and caches of a host argmax loop."""
+    wl = synth.WORKLOADS["tiny"]
+    n = mk.MAX_GREEDY_STEPS
+    ctx = (17,)
+    cap = ctx[0] + n + 15
+    a = Pair(wl.shape, 1, cap, ctx=ctx)
+    want_tok, want_logits = _host_loop(a, [9], list(ctx), n)
+    caches_a = [bf16_bits(t) for t in a.kc + a.vc]
+    a.close()
+    b = Pair(wl.shape, 1, cap, ctx=ctx)
+    got_tok, got_logits = _device_loop(b, [9], list(ctx), n)
     caches_b = [bf16_bits(t) for t in b.kc + b.vc]
     b.close()
     np.testing.assert_array_equal(got_tok, want_tok)
