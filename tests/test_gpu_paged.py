@@ -30,7 +30,11 @@ def _cache_from(pool, table, B, S, bs):
     return out
 
 
-@pytest.mark.parametrize("name,batch,bs,steps", [("tiny", 2, 16, 4), ("llama1b", 1, 32, 3)])
+# block sizes: one position per block (every key its own copy), sizes that do
+# not divide a 64-key page (runs break inside pages), and whole pages
+@pytest.mark.parametrize("name,batch,bs,steps", [("tiny", 2, 16, 4), ("llama1b", 1, 32, 3),
+                                                 ("tiny", 2, 1, 3), ("tiny", 2, 5, 3),
+                                                 ("tiny", 4, 48, 2)])
 def test_paged_matches_contiguous(name, batch, bs, steps):
     wl = synth.WORKLOADS[name]
     shape = wl.shape
