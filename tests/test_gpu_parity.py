@@ -81,25 +81,28 @@ def test_tiny_decode_from_empty_cache_matches_full_forward():
     pair.close()
 
 
-@pytest.mark.parametrize("shape_name", ["tiny", "llama1b"])
+@pytest.mark.parametrize("shape_name", ["tiny", "llama1b", "llama1b_b8"])
 def test_multilaunch_graph_and_generic_kernel_are_bit_identical(shape_name):
     wl = synth.WORKLOADS[shape_name]
     ctx = (200,) if shape_name == "tiny" else wl.ctx
     cap = 256 if shape_name == "tiny" else wl.capacity
+    batch = wl.batch
     toks = synth.step_tokens(wl)
     outs = {}
     caches = {}
     for mode in ("mega", "multi", "graph", "generic"):
-        pair = Pair(wl.shape, 1, cap, ctx=ctx)
+        pair = Pair(wl.shape, batch, cap, ctx=ctx)
         if mode == "generic":  # the instantiation that reads the head shape at run time
             pair.dec.use_generic_kernel(True)
         res = []
         for s in range(3):
-            res.append(pair.gpu_step([int(toks[s, 0])], [ctx[0] + s], mode="mega" if mode == "generic" else mode))
+            tok = [int(t) for t in toks[s][:batch]]
+            res.append(pair.gpu_step(tok, [c + s for c in ctx],
+                                     mode="mega" if mode == "generic" else mode))
         outs[mode] = np.stack(res)
         caches[mode] = [bf16_bits(t) for t in pair.kc + pair.vc]
         if mode == "mega":
-            counters_match(pair, [ctx[0] + 2])
+            counters_match(pair, [c + 2 for c in ctx])
         pair.close()
     for other in ("multi", "graph", "generic"):
         np.testing.assert_array_equal(outs["mega"], outs[other])
