@@ -308,13 +308,12 @@ int create_impl(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
   CounterMap cm{s.L, s.nkv, s.B};
   h->n_ctr = cm.count();
   size_t sizes[] = {
-      sizeof(float) * (size_t)B * s.H,                                    // x
+      sizeof(float) * (size_t)kChunks * B * s.H,                          // xpart
       sizeof(float) * (size_t)B * s.H,                                    // xa
       sizeof(float) * (size_t)B * s.QD(),                                 // q
       sizeof(float) * (size_t)B * s.nh * kMaxPartitions * (s.D + 2),      // part
       sizeof(float) * (size_t)B * s.QD(),                                 // attn
       sizeof(float) * (size_t)B * s.F,                                    // h
-      sizeof(float) * (size_t)B * s.H,                                    // dacc
       sizeof(float2) * (size_t)s.S * (s.D / 2),                           // rope
       sizeof(int) * (size_t)2 * h->n_ctr,                                 // counters
       sizeof(int) * 64,                                                   // error word
@@ -331,7 +330,7 @@ int create_impl(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
   ce = cudaMalloc(&h->d_scratch, total);
   if (ce != cudaSuccess) return cuda_fail(nullptr, ce, "cudaMalloc(scratch)");
   char* base = static_cast<char*>(h->d_scratch);
-  p.x = reinterpret_cast<float*>(base + offs[0]);
+  p.xpart = reinterpret_cast<float*>(base + offs[0]);
   p.xa = reinterpret_cast<float*>(base + offs[1]);
   p.q = reinterpret_cast<float*>(base + offs[2]);
   p.part = reinterpret_cast<float*>(base + offs[3]);
@@ -339,13 +338,12 @@ int create_impl(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
   p.part_ml = p.part + (size_t)B * s.nh * kMaxPartitions * s.D;
   p.attn = reinterpret_cast<float*>(base + offs[4]);
   p.h = reinterpret_cast<float*>(base + offs[5]);
-  p.dacc = reinterpret_cast<float*>(base + offs[6]);
-  h->d_rope = reinterpret_cast<float2*>(base + offs[7]);
-  h->d_ctr = reinterpret_cast<int*>(base + offs[8]);
-  h->d_err = reinterpret_cast<int*>(base + offs[9]);
-  h->d_keys = reinterpret_cast<unsigned long long*>(base + offs[10]);
-  h->d_table = reinterpret_cast<int*>(base + offs[11]);
-  h->d_ctr_steps = reinterpret_cast<int*>(base + offs[12]);
+  h->d_rope = reinterpret_cast<float2*>(base + offs[6]);
+  h->d_ctr = reinterpret_cast<int*>(base + offs[7]);
+  h->d_err = reinterpret_cast<int*>(base + offs[8]);
+  h->d_keys = reinterpret_cast<unsigned long long*>(base + offs[9]);
+  h->d_table = reinterpret_cast<int*>(base + offs[10]);
+  h->d_ctr_steps = reinterpret_cast<int*>(base + offs[11]);
   p.block_table = nullptr;  // set per step (paged handles)
   p.max_blocks = h->max_blocks;
   p.kv_block = kv_block;

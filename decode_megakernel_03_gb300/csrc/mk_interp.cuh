@@ -47,10 +47,10 @@ struct Misc {
   uint64_t empty[kMaxPages];
   uint64_t res_full[kResBufs];
   uint64_t res_empty[kResBufs];
-  uint64_t hfull[2];   // h ring: the loader's copy of a down-projection chunk landed
-  uint64_t hempty[2];  // h ring: every compute warp has read the slot
   float red[2][kComputeWarps][kMaxBatch];  // RMSNorm partial sums, double-buffered
   int abort;
+  int hold;       // queue index of the latency-critical instruction being computed (-1: none)
+  int published;  // instructions the storer has published (queue order)
 };
 
 constexpr int kComputeThreads = kComputeWarps * 32;
@@ -90,6 +90,45 @@ __device__ __forceinline__ bool wait_mbar(const Params& p, Misc* m, uint64_t* ba
       }
       if (globaltimer() - t0 > p.timeout_ns) {
         raise_error(p, m, code);
+        return false;
+      }
+    }
+  }
+}
+
+// Latency-critical instructions: the attention units, the O-projection and
+// the down-projection of the last chunk of h (the last to start), whose
+// outputs every SM's next hop waits for. While the compute warps run one of
+// them, the loader issues no copy for a later instruction: the storer's
+// release fence waits for the SM's bulk copies in flight, so with nothing new
+// in flight it publishes sooner (measured on the 1B shape: 698 -> 660
+// us/step; holding during the QKV instruction as well was slower, the pages
+// issued then are needed next). The ring is full during these hops anyway,
+// so the hold costs little bandwidth.
+__device__ __forceinline__ bool critical_op(const Instr& in) {
+  return in.op == MK_OP_ATTN || in.op == MK_OP_OPROJ ||
+         (in.op == MK_OP_DOWN && in.a2 == kChunks - 1);
+}
+
+// Loader: before issuing a copy for queue entry j, wait while an earlier
+// critical instruction is computing and not yet published (bounded).
+__device__ __forceinline__ bool hold_wait(const Params& p, Misc* m, int j) {
+  const volatile int* vh = &m->hold;
+  const volatile int* vp = &m->published;
+  int h = *vh;
+  if (h < 0 || j <= h || *vp > h) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    h = *vh;
+    if (h < 0 || j <= h || *vp > h) return true;
+    if ((it & 15) == 0) {
+      if (aborted(m)) return false;
+      if (ld_volatile(p.err) != 0) {
+        *reinterpret_cast<volatile int*>(&m->abort) = 1;
+        return false;
+      }
+      if (globaltimer() - t0 > p.timeout_ns) {
+        raise_error(p, m, kErrTimeoutPage);
         return false;
       }
     }
@@ -175,14 +214,6 @@ __device__ __forceinline__ RowSrc row_src_of(const Params& p, const Instr& in) {
   return s;
 }
 
-// h ring slot and round of the n-th chunk (h_ring is 1 or 2 slots)
-__device__ __forceinline__ int ring_slot(const Params& p, uint32_t n) {
-  return p.h_ring == 2 ? (int)(n & 1u) : 0;
-}
-__device__ __forceinline__ uint32_t ring_round(const Params& p, uint32_t n) {
-  return p.h_ring == 2 ? n >> 1 : n;
-}
-
 // element offset of key/value row t of (sequence b, kv-head g) in a layer's
 // cache, contiguous or paged; rows of one block are contiguous
 // FX: the interpreter is built with the paged-cache and greedy-decode code
@@ -248,13 +279,21 @@ static __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, cons
   uint32_t page_cnt = 0;  // pages issued
   int slot = 0;           // page_cnt % n_pages
   uint32_t round = 0;     // page_cnt / n_pages
-  uint32_t h_cnt = 0;     // h chunks copied into the h ring
   int acq_step = 0;       // greedy steps whose LM head this loader has acquired
   bool ok = true;
+  // trace: when this instruction's first and last copies went out
+  const int rec0 = p.trace_base + (int)(q - p.instrs);
+  auto trace_issue = [&](int i, uint64_t t_first) {
+    if (p.trace != nullptr && rec0 + i < p.trace_cap) {
+      p.trace[rec0 + i].t_issue_first = t_first;
+      p.trace[rec0 + i].t_issue_last = globaltimer();
+    }
+  };
   Instr nxt = n > 0 ? load_instr(q) : Instr{};
   for (int i = 0; i < n && ok; ++i) {
     const Instr in = nxt;
     if (i + 1 < n) nxt = load_instr(q + i + 1);
+    uint64_t t_first = 0;
     if (in.op == MK_OP_ATTN) {
       // the unit's cached keys, K and V rows of kpp keys per page; they do
       // not depend on this step's outputs, so they stream in while the unit
@@ -277,10 +316,12 @@ static __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, cons
         }
       }
       for (int pg = 0; pg < sp.npages; ++pg) {
-        if (!wait_mbar(p, m, &m->empty[slot], (round & 1u) ^ 1u, kErrTimeoutPage)) {
+        if (!wait_mbar(p, m, &m->empty[slot], (round & 1u) ^ 1u, kErrTimeoutPage) ||
+            !hold_wait(p, m, i)) {
           ok = false;
           break;
         }
+        if (pg == 0 && p.trace != nullptr) t_first = globaltimer();
         const int k0 = sp.t0 + pg * sp.kpp;
         const int nk = min(sp.kpp, sp.nc - pg * sp.kpp);
         const uint32_t bytes = (uint32_t)nk * (uint32_t)p.D * 2u;
@@ -303,39 +344,22 @@ static __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, cons
           ++round;
         }
       }
+      if (ok && sp.npages > 0) trace_issue(i, t_first);
       continue;
     }
     if (!is_gemv(in.op)) continue;
-    if (p.h_ring && in.op == MK_OP_DOWN) {
-      // one sequence: fetch the chunk of h this down-projection reads into the
-      // next h slot, once its counter says gate/up chunk a2 is complete. In
-      // the queue the down chunks follow all four gate/up chunks, so the wait
-      // is short, and it sits before weight pages that are not needed yet.
-      const int k = ring_slot(p, h_cnt);
-      if (!wait_mbar(p, m, &m->hempty[k], (ring_round(p, h_cnt) & 1u) ^ 1u, kErrTimeoutRes)) {
-        ok = false;
-        break;
-      }
-      if (!p.no_waits && in.wait_ctr >= 0 && !wait_counter(p, m, in.wait_ctr, in.wait_target)) {
-        ok = false;
-        break;
-      }
-      fence_proxy_async_global();  // the acquire above, then the bulk copy's reads
-      const uint32_t bytes = (uint32_t)p.Fc * 4u;
-      mbar_arrive_expect_tx(&m->hfull[k], bytes);
-      bulk_g2s(smem + p.off_h + (size_t)k * bytes, p.h + (size_t)in.a2 * p.Fc, bytes, &m->hfull[k]);
-      ++h_cnt;
-    }
     const Geom g = geom_of(in.op, p.H, p.QD, p.Fc);
     const int items = in.a1 - in.a0;
     const uint32_t row_bytes = (uint32_t)g.K * 2u;
     const RowSrc rs = row_src_of(p, in);
     for (int i0 = 0; i0 < items; i0 += g.ipp) {
-      if (!wait_mbar(p, m, &m->empty[slot], (round & 1u) ^ 1u, kErrTimeoutPage)) {
+      if (!wait_mbar(p, m, &m->empty[slot], (round & 1u) ^ 1u, kErrTimeoutPage) ||
+          !hold_wait(p, m, i)) {
         ok = false;
         break;
       }
       const int i1 = min(items, i0 + g.ipp);
+      if (i0 == 0 && p.trace != nullptr) t_first = globaltimer();
       mbar_arrive_expect_tx(&m->full[slot], (uint32_t)((i1 - i0) * g.R) * row_bytes);
       issue_page(p, in, g, rs, i0, i1, smem + (size_t)slot * kPageBytes, &m->full[slot], pol);
       ++page_cnt;
@@ -344,16 +368,10 @@ static __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, cons
         ++round;
       }
     }
+    if (ok && items > 0) trace_issue(i, t_first);
   }
   if (!ok) {
     // drain: every issued copy must land before the CTA's shared memory goes away
-    const uint32_t nslot = p.h_ring == 2 ? 2u : 1u;
-    for (uint32_t k = h_cnt > nslot ? h_cnt - nslot : 0u; k < h_cnt; ++k) {
-      const uint64_t t0 = globaltimer();
-      while (!mbar_try_wait(&m->hfull[ring_slot(p, k)], ring_round(p, k) & 1u)) {
-        if (globaltimer() - t0 > p.timeout_ns) break;
-      }
-    }
     const uint32_t first = page_cnt > (uint32_t)p.n_pages ? page_cnt - p.n_pages : 0u;
     for (uint32_t k = first; k < page_cnt; ++k) {
       const int sl = (int)(k % (uint32_t)p.n_pages);
@@ -413,9 +431,92 @@ __device__ __forceinline__ const uint16_t* norm_weight(const Params& p, int kind
   return nullptr;
 }
 
+// One pass of the staging over sequences [b0, b0 + NB): NS source rows per
+// sequence are added left to right (NS = 5: the previous layer's output x =
+// xa + its four down-projection shares; NS = 1: one row), the RMSNorm gain is
+// applied, and the result is stored in the staging layout. Every thread
+// issues all of its loads of a column pass before using any, so a pass costs
+// one L2 round trip. Returns the sums of squares per sequence in ss.
+template <int B, int NS, int NB, int KU, int FX>
+__device__ __forceinline__ void stage_pass(const Params& p, float* dst, int K, int Ks,
+                                           const uint16_t* normw, bool from_embed,
+                                           const float* base, size_t stride, int b0, int step,
+                                           float (&ss)[NB]) {
+  constexpr bool kFrag = B > 1;
+  constexpr int kPass = kComputeThreads * 4 * KU;  // columns per pass
+  const int tid = compute_tid();
+  const size_t cs = (size_t)p.B * p.H;  // distance between two down-projection shares
+#pragma unroll
+  for (int bb = 0; bb < NB; ++bb) ss[bb] = 0.f;
+  for (int c0 = tid * 4; c0 < K; c0 += kPass) {
+    float4 v[NS][NB][KU];
+    uint2 wv[KU];
+#pragma unroll
+    for (int u = 0; u < KU; ++u) {
+      const int c = c0 + u * kComputeThreads * 4;
+      if (c < K) {
+        if (normw) wv[u] = __ldg(reinterpret_cast<const uint2*>(normw + c));
+#pragma unroll
+        for (int bb = 0; bb < NB; ++bb) {
+          if (b0 + bb >= B) continue;
+          if (from_embed) {
+            const uint16_t* erow = p.embed + (size_t)token_of<FX>(p, b0 + bb, step) * p.H;
+            const uint2 e = *reinterpret_cast<const uint2*>(erow + c);
+            v[0][bb][u] = make_float4(bf_lo(e.x), bf_hi(e.x), bf_lo(e.y), bf_hi(e.y));
+          } else {
+#pragma unroll
+            for (int sidx = 0; sidx < NS; ++sidx) {
+              const float* src = sidx == 0 ? base : p.xpart + (size_t)(sidx - 1) * cs;
+              v[sidx][bb][u] = __ldcg(reinterpret_cast<const float4*>(src + (b0 + bb) * stride + c));
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < KU; ++u) {
+      const int c = c0 + u * kComputeThreads * 4;
+      if (c < K) {
+#pragma unroll
+        for (int bb = 0; bb < NB; ++bb) {
+          if (b0 + bb >= B) continue;
+          float4 x = v[0][bb][u];
+          if (!from_embed) {
+#pragma unroll
+            for (int sidx = 1; sidx < NS; ++sidx) {
+              x.x += v[sidx][bb][u].x;
+              x.y += v[sidx][bb][u].y;
+              x.z += v[sidx][bb][u].z;
+              x.w += v[sidx][bb][u].w;
+            }
+          }
+          ss[bb] += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+          if (normw) {
+            x.x *= bf_lo(wv[u].x);
+            x.y *= bf_hi(wv[u].x);
+            x.z *= bf_lo(wv[u].y);
+            x.w *= bf_hi(wv[u].y);
+          }
+          float* d = dst + (size_t)(b0 + bb) * Ks + c;
+          if (kFrag) {
+            const uint32_t h01 = bf16x2_rn(x.x, x.y), h23 = bf16x2_rn(x.z, x.w);
+            const uint32_t l01 = bf16x2_rn(x.x - bf_lo(h01), x.y - bf_hi(h01));
+            const uint32_t l23 = bf16x2_rn(x.z - bf_lo(h23), x.w - bf_hi(h23));
+            *reinterpret_cast<uint4*>(d) = make_uint4(h01, l01, h23, l23);
+          } else {
+            *reinterpret_cast<float4*>(d) = x;
+          }
+        }
+      }
+    }
+  }
+}
+
 // Stages the activation vector(s) of `kind` for all B sequences into the x or
 // h buffer. For the RMSNorm kinds the buffer holds x * w (the gain already
-// applied) and 1/rms(x) per sequence is returned in st.inv_x.
+// applied) and 1/rms(x) per sequence is returned in st.inv_x. The RMSNorm
+// inputs of layer l > 0 and of the LM head are the previous layer's output,
+// x = xa + the four down-projection shares, summed here.
 // Several sequences (B > 1): sequence b's row starts at word b * (K + 4), and
 // each group of four columns c .. c + 3 is stored in place as the bf16 split
 // v = hi + lo of its values, {hi(c, c+1), lo(c, c+1), hi(c+2, c+3),
@@ -434,78 +535,43 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
   const int Ks = kFrag ? K + 4 : K;  // row stride of the buffer, in words
   const uint16_t* normw = norm_weight(p, kind, layer);
   const bool from_embed = kind == kActAttnNorm && layer == 0;
+  // x = xa + the four down-projection shares of the previous layer
+  const bool sum_x = (kind == kActAttnNorm && layer > 0) || kind == kActFinalNorm;
   // sequence b's source row: base + b * stride
   const float* base;
   size_t stride;
-  if (kind == kActAttnNorm || kind == kActFinalNorm) base = p.x, stride = p.H;
-  else if (kind == kActMlpNorm) base = p.xa, stride = p.H;
+  if (sum_x || kind == kActMlpNorm) base = p.xa, stride = p.H;
   else if (kind == kActAttnOut) base = p.attn, stride = p.QD;
   else base = p.h + (size_t)chunk * p.Fc, stride = p.F;
   const int par = st.stage_cnt & 1;
   compute_bar();  // everyone is done reading the buffer's previous contents
-  // every thread issues all of its loads of a pass before using any, so a
-  // pass costs one round trip to L2: 2048-wide vectors of all sequences at
-  // once
-  constexpr int kNB = B;
-  constexpr int kU = B == 1 ? (kWide ? 6 : 4) : 3;
-  constexpr int kPass = kComputeThreads * 4 * kU;  // columns per pass
-  for (int b0 = 0; b0 < B; b0 += kNB) {
-    float ss[kNB];
+  // one sequence: four (six if wide) column groups per thread and pass; with
+  // five sources, four. Several sequences: all of them and three groups per
+  // pass; with five sources, two sequences and two groups (register budget)
+  constexpr int kNB1 = B, kU1 = B == 1 ? (kWide ? 6 : 4) : 3;
+  constexpr int kNB5 = B == 1 ? 1 : 2, kU5 = B == 1 && !kWide ? 2 : 1;
+  if (sum_x) {
+    for (int b0 = 0; b0 < B; b0 += kNB5) {
+      float ss[kNB5];
+      stage_pass<B, 5, kNB5, kU5, FX>(p, dst, K, Ks, normw, false, base, stride, b0, step, ss);
+      if (normw) {
 #pragma unroll
-    for (int bb = 0; bb < kNB; ++bb) ss[bb] = 0.f;
-    for (int c0 = tid * 4; c0 < K; c0 += kPass) {
-      float4 v[kNB][kU];
-      uint2 wv[kU];
+        for (int bb = 0; bb < kNB5; ++bb) {
 #pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int c = c0 + u * kComputeThreads * 4;
-        if (c < K) {
-          if (normw) wv[u] = __ldg(reinterpret_cast<const uint2*>(normw + c));
-#pragma unroll
-          for (int bb = 0; bb < kNB; ++bb) {
-            if (from_embed) {
-              const uint16_t* erow = p.embed + (size_t)token_of<FX>(p, b0 + bb, step) * p.H;
-              const uint2 e = *reinterpret_cast<const uint2*>(erow + c);
-              v[bb][u] = make_float4(bf_lo(e.x), bf_hi(e.x), bf_lo(e.y), bf_hi(e.y));
-            } else {
-              v[bb][u] = __ldcg(reinterpret_cast<const float4*>(base + (b0 + bb) * stride + c));
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int c = c0 + u * kComputeThreads * 4;
-        if (c < K) {
-#pragma unroll
-          for (int bb = 0; bb < kNB; ++bb) {
-            float4 x = v[bb][u];
-            ss[bb] += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
-            if (normw) {
-              x.x *= bf_lo(wv[u].x);
-              x.y *= bf_hi(wv[u].x);
-              x.z *= bf_lo(wv[u].y);
-              x.w *= bf_hi(wv[u].y);
-            }
-            float* d = dst + (size_t)(b0 + bb) * Ks + c;
-            if (kFrag) {
-              const uint32_t h01 = bf16x2_rn(x.x, x.y), h23 = bf16x2_rn(x.z, x.w);
-              const uint32_t l01 = bf16x2_rn(x.x - bf_lo(h01), x.y - bf_hi(h01));
-              const uint32_t l23 = bf16x2_rn(x.z - bf_lo(h23), x.w - bf_hi(h23));
-              *reinterpret_cast<uint4*>(d) = make_uint4(h01, l01, h23, l23);
-            } else {
-              *reinterpret_cast<float4*>(d) = x;
-            }
-          }
+          for (int o = 16; o > 0; o >>= 1) ss[bb] += __shfl_xor_sync(0xffffffffu, ss[bb], o);
+          if (lane == 0 && b0 + bb < B) m->red[par][warp][b0 + bb] = ss[bb];
         }
       }
     }
+  } else {
+    float ss[kNB1];
+    stage_pass<B, 1, kNB1, kU1, FX>(p, dst, K, Ks, normw, from_embed, base, stride, 0, step, ss);
     if (normw) {
 #pragma unroll
-      for (int bb = 0; bb < kNB; ++bb) {
+      for (int bb = 0; bb < kNB1; ++bb) {
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) ss[bb] += __shfl_xor_sync(0xffffffffu, ss[bb], o);
-        if (lane == 0) m->red[par][warp][b0 + bb] = ss[bb];
+        if (lane == 0) m->red[par][warp][bb] = ss[bb];
       }
     }
   }
@@ -830,7 +896,8 @@ __device__ __forceinline__ void page_rows_mma(const uint8_t* page, int n_rows, i
 template <int B, bool kRegs, int KW>
 __device__ __forceinline__ void gemv_run(const Params& p, Misc* m, uint8_t* smem, const Instr& in,
                                          const Geom& g, const float* act, const InvScale& inv,
-                                         const float (&a)[64], float* res, uint32_t page_base) {
+                                         const float (&a)[64], float* res, uint32_t page_base,
+                                         uint64_t& pwait) {
   const int warp = compute_warp(), lane = threadIdx.x & 31;
   const int items = in.a1 - in.a0;
   const int npages = (items + g.ipp - 1) / g.ipp;
@@ -846,7 +913,9 @@ __device__ __forceinline__ void gemv_run(const Params& p, Misc* m, uint8_t* smem
   int slot = (int)(pc0 % (uint32_t)p.n_pages);
   uint32_t round = pc0 / (uint32_t)p.n_pages;
   for (; pg < npages; pg += kComputeWarps) {
+    const uint64_t tw = p.trace != nullptr ? globaltimer() : 0;
     const bool ok = wait_mbar(p, m, &m->full[slot], round & 1u, kErrTimeoutPage);
+    if (p.trace != nullptr) pwait += globaltimer() - tw;
     if (ok) {
       const int n_in = min(g.ipp, items - pg * g.ipp);  // items on this page
       const uint8_t* page = smem + (size_t)slot * kPageBytes;
@@ -926,7 +995,7 @@ __device__ __forceinline__ uint4 split_hi_lo(float a, float b, float c, float d)
 
 template <int D, int FX>
 __device__ void attn_unit(const Params& p, Misc* m, uint8_t* smem, const Instr& in,
-                          uint32_t page_base) {
+                          uint32_t page_base, uint64_t& pwait) {
   constexpr int KS = D / 16;                   // product steps over the head dimension
   constexpr int NB = D / 8;                    // 8-column blocks of the output
   constexpr int KPP = kPageBytes / (4 * D);    // keys per page (K, then V)
@@ -1006,8 +1075,10 @@ __device__ void attn_unit(const Params& p, Misc* m, uint8_t* smem, const Instr& 
   uint32_t round = pc0 / (uint32_t)p.n_pages;
   for (; pg < sp.npages; pg += kComputeWarps) {
     // the products need the whole warp: the lanes agree on the page
+    const uint64_t tw = p.trace != nullptr ? globaltimer() : 0;
     const bool ok =
         __all_sync(0xffffffffu, wait_mbar(p, m, &m->full[slot], round & 1u, kErrTimeoutPage));
+    if (p.trace != nullptr) pwait += globaltimer() - tw;
     if (ok) {
       const uint8_t* kp = smem + (size_t)slot * kPageBytes;
       const uint8_t* vp = kp + kPageBytes / 2;
@@ -1206,7 +1277,6 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
   // reloaded from the staged smem vector at every instruction
   float ax[64];
   uint32_t page_cnt = 0;
-  uint32_t h_cnt = 0;  // down-projection chunks taken from the h ring
   int known_ctr = -1, known_tgt = 0;
   Instr nxt = n > 0 ? load_instr(q) : Instr{};
   for (int i = 0; i < n; ++i) {
@@ -1214,13 +1284,13 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
     if (i + 1 < n) nxt = load_instr(q + i + 1);
     const int buf = i % kResBufs;
     const uint32_t rpar = ((uint32_t)i / kResBufs) & 1u;
-    uint64_t t_start = 0, t_ready = 0;
+    uint64_t t_start = 0, t_ready = 0, pwait = 0;
     const bool tracing = p.trace != nullptr && warp == 0 && lane == 0;
     if (tracing) t_start = globaltimer();
-    // the loader fetched this down-projection chunk of h (after its counter)
-    const bool from_ring = p.h_ring && in.op == MK_OP_DOWN;
+    if (warp == 0 && lane == 0 && critical_op(in))
+      *reinterpret_cast<volatile int*>(&m->hold) = i;
     // 1. dependency: one thread polls, the other compute warps meet it at a barrier
-    if (!from_ring && !p.no_waits && in.wait_ctr >= 0 &&
+    if (!p.no_waits && in.wait_ctr >= 0 &&
         !(in.wait_ctr == known_ctr && in.wait_target <= known_tgt)) {
       if (warp == 0 && lane == 0) wait_counter(p, m, in.wait_ctr, in.wait_target);
       compute_bar();
@@ -1243,29 +1313,7 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
       const bool regs = B == 1 && g.K <= 2048;
       const bool norm = kind == kActAttnNorm || kind == kActMlpNorm || kind == kActFinalNorm;
       const float* act;
-      bool h_got = false;
-      if (from_ring) {
-        const int k = ring_slot(p, h_cnt);
-        h_got = wait_mbar(p, m, &m->hfull[k], ring_round(p, h_cnt) & 1u, kErrTimeoutRes);
-        act = reinterpret_cast<const float*>(smem + p.off_h) + (size_t)k * p.Fc;
-        if constexpr (B == 1 && KW == 0) {
-          if (g.K > 2048) {
-            // a wide chunk: copied into the x buffer (idle until the next
-            // layer restages it) and its slot handed back at once, so the
-            // loader fetches the next chunk while this one runs
-            float* xb = reinterpret_cast<float*>(smem + p.off_x);
-            compute_bar();  // the previous instruction's pages are read
-            for (int c = compute_tid() * 4; c < g.K; c += kComputeThreads * 4)
-              *reinterpret_cast<float4*>(xb + c) = *reinterpret_cast<const float4*>(act + c);
-            compute_bar();
-            __syncwarp();
-            if (lane == 0 && h_got) mbar_arrive(&m->hempty[k]);
-            ++h_cnt;
-            st.key_x = -1;
-            act = xb;
-          }
-        }
-      } else {
+      {
         if ((to_h ? st.key_h : st.key_x) != key) {
           bool staged = false;
           if constexpr (B == 1) {  // one sequence: the O-projection reduces while staging
@@ -1288,17 +1336,11 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
       for (int b = 0; b < kMaxBatch; ++b) one.v[b] = 1.f;
       if (regs) {
         load_regs(ax, act, norm ? st.inv_x.v[0] : 1.f, g.K);
-        if (from_ring) {
-          // the slot is in registers now (a copy that has not landed, after an
-          // abort, keeps its slot: the loader must not start another into it)
-          __syncwarp();
-          if (lane == 0 && h_got) mbar_arrive(&m->hempty[ring_slot(p, h_cnt)]);
-          ++h_cnt;
-        }
-        gemv_run<B, true, KW>(p, m, smem, in, g, act, one, ax, res, page_cnt);
+        gemv_run<B, true, KW>(p, m, smem, in, g, act, one, ax, res, page_cnt, pwait);
       } else {
         if constexpr (KW == 0)
-          gemv_run<B, false, KW>(p, m, smem, in, g, act, to_h ? one : st.inv_x, ax, res, page_cnt);
+          gemv_run<B, false, KW>(p, m, smem, in, g, act, to_h ? one : st.inv_x, ax, res, page_cnt,
+                                  pwait);
       }
       page_cnt += (uint32_t)((in.a1 - in.a0 + g.ipp - 1) / g.ipp);
     } else if (in.op == MK_OP_ATTN) {
@@ -1306,9 +1348,9 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
       st.key_h = -1;
       // runs even after an abort: its loads stay in bounds and its barriers
       // must be met by every compute warp
-      if constexpr (DS > 0) attn_unit<DS, FX>(p, m, smem, in, page_cnt);
-      else if (p.D == 64) attn_unit<64, FX>(p, m, smem, in, page_cnt);
-      else attn_unit<128, FX>(p, m, smem, in, page_cnt);
+      if constexpr (DS > 0) attn_unit<DS, FX>(p, m, smem, in, page_cnt, pwait);
+      else if (p.D == 64) attn_unit<64, FX>(p, m, smem, in, page_cnt, pwait);
+      else attn_unit<128, FX>(p, m, smem, in, page_cnt, pwait);
       page_cnt += (uint32_t)attn_span(p.pos[in.a0] + step_of(in), in.a2 >> 16, in.a2 & 0xffff, p.D)
                       .npages;
     } else if (in.op == MK_OP_RED) {
@@ -1339,6 +1381,7 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
         r->t_end = globaltimer();
         r->res_wait_ns = (uint32_t)(t_res - t_ready);
         r->stage_ns = (uint32_t)(t_staged - t_res);
+        r->page_wait_ns = (uint32_t)pwait;
       }
     }
   }
@@ -1352,8 +1395,9 @@ __device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
 
 // What an epilogue reads from global memory, loaded by the storer while the
 // compute warps still work on the instruction: the RoPE (cos, sin) of the
-// q/k/v pairs, and the residual rows of the o-projection and of the last
-// down-projection chunk. Lane l holds items l and l + 32 (at most 64 items).
+// q/k/v pairs, and the residual rows of the o-projection (the previous
+// layer's output x = xa + its four down-projection shares, or the embedding
+// row). Lane l holds items l and l + 32 (at most 64 items).
 template <int B>
 struct EpiPre {
   float2 v[2][B];
@@ -1364,7 +1408,7 @@ __device__ __forceinline__ void epilogue_prefetch(const Params& p, Misc* m, cons
                                                   EpiPre<B>& pre) {
   const int lane = threadIdx.x & 31;
   const int items = in.a1 - in.a0;
-  const bool resid = in.op == MK_OP_OPROJ || (in.op == MK_OP_DOWN && in.a2 == kChunks - 1);
+  const bool resid = in.op == MK_OP_OPROJ;
   if (in.op == MK_OP_QKV) {
     const int half = p.D / 2;
 #pragma unroll
@@ -1389,16 +1433,23 @@ __device__ __forceinline__ void epilogue_prefetch(const Params& p, Misc* m, cons
       if (lane == 0) ok = wait_counter(p, m, in.wait_ctr, in.wait_target);
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) return;
     }
-    const float* src = in.op == MK_OP_DOWN ? p.xa : p.x;
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       const int it = lane + 32 * k;
       if (it < items) {
         const int j = in.a0 + it;
 #pragma unroll
-        for (int b = 0; b < B; ++b)
-          pre.v[k][b].x = from_embed ? bf16f(p.embed[(size_t)token_of<FX>(p, b, step_of(in)) * p.H + j])
-                                     : __ldcg(src + (size_t)b * p.H + j);
+        for (int b = 0; b < B; ++b) {
+          if (from_embed) {
+            pre.v[k][b].x = bf16f(p.embed[(size_t)token_of<FX>(p, b, step_of(in)) * p.H + j]);
+          } else {
+            const size_t o = (size_t)b * p.H + j, cs = (size_t)p.B * p.H;
+            const float x0 = __ldcg(p.xa + o), x1 = __ldcg(p.xpart + o),
+                        x2 = __ldcg(p.xpart + cs + o), x3 = __ldcg(p.xpart + 2 * cs + o),
+                        x4 = __ldcg(p.xpart + 3 * cs + o);
+            pre.v[k][b].x = x0 + x1 + x2 + x3 + x4;
+          }
+        }
       }
     }
   }
@@ -1406,7 +1457,7 @@ __device__ __forceinline__ void epilogue_prefetch(const Params& p, Misc* m, cons
 
 template <int B, int FX>
 __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const float* res,
-                                         float* dacc, const EpiPre<B>& pre) {
+                                         const EpiPre<B>& pre) {
   const int lane = threadIdx.x & 31;
   const Geom g = geom_of(in.op, p.H, p.QD, p.Fc);
   const int items = in.a1 - in.a0;
@@ -1448,14 +1499,10 @@ __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const
         case MK_OP_GATEUP:
           p.h[(size_t)b * p.F + j] = silu(v0) * v1;
           break;
-        case MK_OP_DOWN: {
-          // the chunks of row j run on this SM in order; their sum stays in smem
-          float* acc = dacc + (size_t)(j % p.dacc_rows) * B + b;
-          const float d = in.a2 == 0 ? v0 : *acc + v0;
-          if (in.a2 == kChunks - 1) p.x[(size_t)b * p.H + j] = pre.v[k][b].x + d;
-          else *acc = d;
+        case MK_OP_DOWN:
+          // this chunk's share of row j (the readers add the four shares to xa)
+          p.xpart[((size_t)in.a2 * p.B + b) * p.H + j] = v0;
           break;
-        }
         default:  // MK_OP_LMHEAD
           p.logits[(size_t)b * p.V + j] = v0;
           break;
@@ -1499,7 +1546,6 @@ __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const
 template <int B, int FX>
 __device__ void storer_role(const Params& p, Misc* m, uint8_t* smem, const Instr* q, int n) {
   const int lane = threadIdx.x & 31;
-  float* dacc = reinterpret_cast<float*>(smem + p.off_dacc);
   Instr nxt = n > 0 ? load_instr(q) : Instr{};
   for (int i = 0; i < n; ++i) {
     const Instr in = nxt;
@@ -1511,7 +1557,7 @@ __device__ void storer_role(const Params& p, Misc* m, uint8_t* smem, const Instr
     const bool ok = wait_mbar(p, m, &m->res_full[buf], par, kErrTimeoutRes);
     if (ok && !aborted(m)) {
       const float* res = reinterpret_cast<const float*>(smem + p.off_res) + (size_t)buf * p.res_floats;
-      if (is_gemv(in.op)) epilogue<B, FX>(p, in, res, dacc, pre);
+      if (is_gemv(in.op)) epilogue<B, FX>(p, in, res, pre);
       if (in.sig_ctr >= 0) {
         // the warp barrier orders the other lanes' stores (and, through the
         // result mbarrier, the compute warps' stores) before lane 0's
@@ -1529,6 +1575,7 @@ __device__ void storer_role(const Params& p, Misc* m, uint8_t* smem, const Instr
     __syncwarp();
     if (lane == 0) {
       mbar_arrive(&m->res_empty[buf]);
+      *reinterpret_cast<volatile int*>(&m->published) = i + 1;
       if (p.trace) {
         const int rec = p.trace_base + (int)(q - p.instrs) + i;
         if (rec < p.trace_cap) p.trace[rec].t_stored = globaltimer();
@@ -1556,11 +1603,9 @@ __global__ void __launch_bounds__(kThreads, 1) interp_kernel(const __grid_consta
       mbar_init(&m->res_full[i], kComputeWarps);
       mbar_init(&m->res_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&m->hfull[i], 1);               // the loader's expect-tx arrival
-      mbar_init(&m->hempty[i], kComputeWarps);  // every compute warp
-    }
     m->abort = 0;
+    m->hold = -1;
+    m->published = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   // counters are zero before the launch that uses them (§3.4): this launch

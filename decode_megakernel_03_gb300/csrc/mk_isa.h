@@ -58,14 +58,15 @@ struct Params {
   const uint16_t* final_norm;
   const float2* rope;          // [S][D/2] (cos, sin) of pos * theta^(-2i/D)
   // library scratch (fp32 activations)
-  float* x;      // [B][H] residual stream between layers
   float* xa;     // [B][H] residual after the attention block
   float* q;      // [B][nh*D] rotated queries
   float* part;   // [B][nh][kMaxPartitions][D] attention partials: o
   float* part_ml; // [B][nh][kMaxPartitions][2] attention partials: (m, l)
   float* attn;   // [B][nh*D] reduced attention output
   float* h;      // [B][F] SwiGLU hidden state
-  float* dacc;   // [B][H] down-projection partial sums across chunks
+  float* xpart;  // [kChunks][B][H] down-projection of each chunk of h; the
+                 // layer's output is x = xa + xpart[0] + ... + xpart[3],
+                 // summed in that order by every reader
   float* logits; // [B][V] caller-owned
   int* ctr;      // counters of this step (zero at launch)
   int* ctr_zero; // counters of the next step, zeroed by this launch
@@ -82,13 +83,10 @@ struct Params {
   // shared-memory layout (bytes from the dynamic smem base)
   int n_pages;
   int off_x, off_h, off_res, off_misc;
-  int off_dacc, dacc_rows;     // down-projection chunk sums, row j at slot j % dacc_rows
   int x_floats, h_floats, res_floats;
   int alias_xh;                // x and h staging share one buffer
   int fused_red;               // one sequence: the O-projection's staging reduces the
                                // attention partials itself (no reduction instruction)
-  int h_ring;                  // one sequence: the loader fetches each down-projection
-                               // chunk of h into one of h_ring slots (at off_h; 0: none)
   // paged KV cache (block_table null: each layer's cache is [B][nkv][S][D]):
   // each layer's pool is [n_blocks][nkv][kv_block][D]; position t of
   // sequence b lives in block block_table[b * max_blocks + t / kv_block]

@@ -151,13 +151,12 @@ extern "C" int mk_decode_step_noalloc(const mk_config* cfg, const mk_weights* w,
   CounterMap cm{s.L, s.nkv, s.B};
   const int n_ctr = cm.count();
   const size_t sizes[] = {
-      sizeof(float) * (size_t)B * s.H,                                // x
+      sizeof(float) * (size_t)kChunks * B * s.H,                      // down-projection shares
       sizeof(float) * (size_t)B * s.H,                                // xa
       sizeof(float) * (size_t)B * s.QD(),                             // q
       sizeof(float) * (size_t)B * s.nh * kMaxPartitions * (s.D + 2),  // attention partials
       sizeof(float) * (size_t)B * s.QD(),                             // attention output
       sizeof(float) * (size_t)B * s.F,                                // h
-      sizeof(float) * (size_t)B * s.H,                                // dacc
       sizeof(float2) * (size_t)s.S * (s.D / 2),                       // RoPE table
       sizeof(int) * (size_t)n_ctr,                                    // counters
       sizeof(int) * 64,                                               // error word
@@ -201,7 +200,7 @@ extern "C" int mk_decode_step_noalloc(const mk_config* cfg, const mk_weights* w,
     lp.kc = static_cast<uint16_t*>(k_cache[l]);
     lp.vc = static_cast<uint16_t*>(v_cache[l]);
   }
-  p.x = reinterpret_cast<float*>(base + offs[0]);
+  p.xpart = reinterpret_cast<float*>(base + offs[0]);
   p.xa = reinterpret_cast<float*>(base + offs[1]);
   p.q = reinterpret_cast<float*>(base + offs[2]);
   p.part = reinterpret_cast<float*>(base + offs[3]);
@@ -209,15 +208,14 @@ extern "C" int mk_decode_step_noalloc(const mk_config* cfg, const mk_weights* w,
   p.part_ml = p.part + (size_t)B * s.nh * kMaxPartitions * s.D;
   p.attn = reinterpret_cast<float*>(base + offs[4]);
   p.h = reinterpret_cast<float*>(base + offs[5]);
-  p.dacc = reinterpret_cast<float*>(base + offs[6]);
-  p.rope = reinterpret_cast<const float2*>(base + offs[7]);
-  p.ctr = reinterpret_cast<int*>(base + offs[8]);
+  p.rope = reinterpret_cast<const float2*>(base + offs[6]);
+  p.ctr = reinterpret_cast<int*>(base + offs[7]);
   p.ctr_zero = nullptr;  // cleared by the memset below instead
   p.n_ctr = n_ctr;
-  p.err = reinterpret_cast<int*>(base + offs[9]);
+  p.err = reinterpret_cast<int*>(base + offs[8]);
   p.err_host = nullptr;
-  p.instrs = reinterpret_cast<const Instr*>(base + offs[10]);
-  p.sm_off = reinterpret_cast<const int*>(base + offs[11]);
+  p.instrs = reinterpret_cast<const Instr*>(base + offs[9]);
+  p.sm_off = reinterpret_cast<const int*>(base + offs[10]);
   p.logits = logits_out;
   p.trace = nullptr;
   p.trace_cap = 0;
@@ -245,13 +243,13 @@ extern "C" int mk_decode_step_noalloc(const mk_config* cfg, const mk_weights* w,
   // the host vectors may go out of scope right after the calls
   ce = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (ce == cudaSuccess)
-    ce = cudaMemcpyAsync(base + offs[7], rope.data(), sizes[7], cudaMemcpyHostToDevice, st);
+    ce = cudaMemcpyAsync(base + offs[6], rope.data(), sizes[6], cudaMemcpyHostToDevice, st);
   if (ce == cudaSuccess)
-    ce = cudaMemcpyAsync(base + offs[10], plan.instrs.data(), sizes[10], cudaMemcpyHostToDevice, st);
+    ce = cudaMemcpyAsync(base + offs[9], plan.instrs.data(), sizes[9], cudaMemcpyHostToDevice, st);
   if (ce == cudaSuccess)
-    ce = cudaMemcpyAsync(base + offs[11], plan.sm_off.data(), sizes[11], cudaMemcpyHostToDevice, st);
-  if (ce == cudaSuccess) ce = cudaMemsetAsync(base + offs[8], 0, sizes[8], st);  // counters
-  if (ce == cudaSuccess) ce = cudaMemsetAsync(base + offs[9], 0, sizes[9], st);  // error word
+    ce = cudaMemcpyAsync(base + offs[10], plan.sm_off.data(), sizes[10], cudaMemcpyHostToDevice, st);
+  if (ce == cudaSuccess) ce = cudaMemsetAsync(base + offs[7], 0, sizes[7], st);  // counters
+  if (ce == cudaSuccess) ce = cudaMemsetAsync(base + offs[8], 0, sizes[8], st);  // error word
   if (ce == cudaSuccess) {
     void* args[] = {&p};
     ce = cudaLaunchCooperativeKernel(fn, dim3(ds->n_sm), dim3(kThreads), args, (size_t)smem_bytes, st);
@@ -260,7 +258,7 @@ extern "C" int mk_decode_step_noalloc(const mk_config* cfg, const mk_weights* w,
   int err_word = 0;
   if (ce == cudaSuccess) ce = cudaStreamSynchronize(st);
   if (ce == cudaSuccess)
-    ce = cudaMemcpy(&err_word, base + offs[9], sizeof(int), cudaMemcpyDeviceToHost);
+    ce = cudaMemcpy(&err_word, base + offs[8], sizeof(int), cudaMemcpyDeviceToHost);
   if (ce != cudaSuccess) {
     if (errmsg && errmsg_cap) std::snprintf(errmsg, errmsg_cap, "CUDA: %s", cudaGetErrorString(ce));
     return MK_ERR_CUDA;

@@ -4,15 +4,16 @@
 //
 //   for each layer l:
 //     QKV(l)  ATTN(l)  RED(l)  OPROJ(l)   (one sequence: no RED; OPROJ reduces)
-//     GATEUP(l,0)  GATEUP(l,1) DOWN(l,0)  GATEUP(l,2) DOWN(l,1)  ...  DOWN(l,3)
+//     GATEUP(l,0)  GATEUP(l,1)  GATEUP(l,2)  GATEUP(l,3)  DOWN(l)
 //   LMHEAD
 //
 // and every instruction waits only on counters produced by instructions that
 // precede it in that order. Each SM's queue is that order filtered to the SM,
-// so with all SMs co-resident the step cannot deadlock. The down-projection of
-// chunk c is placed after the gate/up of chunk c+1 so that, on every SM, the
-// wait for chunk c overlaps useful work: "la granularité de la dépendance doit
-// correspondre à la granularité de la production" (§3.4, the four-chunk MLP).
+// so with all SMs co-resident the step cannot deadlock. The hidden state h is
+// produced in four chunks with one counter each, and the down-projection is
+// cut along the same chunks: an instruction reading chunk c waits for chunk
+// c only (§3.4, the four-chunk MLP: the granularity of a dependency follows
+// the granularity of its production).
 #include "mk_sched.h"
 
 #include <algorithm>
@@ -166,7 +167,7 @@ struct Builder {
     {
       Step st{MK_OP_QKV, l, {}};
       int wc = l == 0 ? -1 : cm.xout(l - 1);
-      int wt = l == 0 ? 0 : H;
+      int wt = l == 0 ? 0 : kChunks * H;
       spread(s.pairs(), ppg, rot_of(l, 0), [&](int sm, int a, int b) {
         int g = a / ppg;
         st.items.push_back({sm, make(MK_OP_QKV, l, a, b, 0, wc, wt, cm.qkv(l, g), b - a)});
@@ -210,10 +211,7 @@ struct Builder {
       });
       steps.push_back(std::move(st));
     }
-    // 5-6. the four gate/up chunks, then the four down chunks: down chunk c
-    // waits only for gate/up chunk c (its own counter), which every SM
-    // finished several instructions earlier, so the down-projection rarely
-    // waits and its weights keep streaming
+    // 5. the four gate/up chunks
     auto gateup = [&](int c) {
       Step st{MK_OP_GATEUP, l, {}};
       spread(Fc, 0, rot_of(l, 2 + c), [&](int sm, int a, int b) {
@@ -222,18 +220,23 @@ struct Builder {
       });
       steps.push_back(std::move(st));
     };
-    auto down = [&](int c) {
+    for (int c = 0; c < kChunks; ++c) gateup(c);
+    // 6. the down-projection over the (chunk, row) units of the layer: every
+    // SM takes one contiguous range of them, so it reads one chunk of h (two
+    // where its range crosses a chunk boundary) once, and its instructions
+    // wait for that chunk alone. Each writes its rows' share of chunk c to
+    // xpart[c]; x = xa + the four shares is formed by its readers. The
+    // weights of an SM's range do not depend on anything, so they stream in
+    // while the gate/up chunks still run.
+    {
       Step st{MK_OP_DOWN, l, {}};
-      bool last = c == kChunks - 1;
-      // every chunk of a row stays on one SM: its storer accumulates the chunks
-      spread(H, 0, rot_of(l, 2 + kChunks), [&](int sm, int a, int b) {
-        st.items.push_back({sm, make(MK_OP_DOWN, l, a, b, c, cm.hch(l, c), Fc,
-                                     last ? cm.xout(l) : -1, last ? b - a : 0)});
+      spread(kChunks * H, H, rot_of(l, 2 + kChunks), [&](int sm, int a, int b) {
+        const int c = a / H;
+        st.items.push_back({sm, make(MK_OP_DOWN, l, a - c * H, b - c * H, c, cm.hch(l, c), Fc,
+                                     cm.xout(l), b - a)});
       });
       steps.push_back(std::move(st));
-    };
-    for (int c = 0; c < kChunks; ++c) gateup(c);
-    for (int c = 0; c < kChunks; ++c) down(c);
+    }
   }
 
   void add_lm_head() {
@@ -242,8 +245,8 @@ struct Builder {
     // result buffer, up to the 64 the storer's epilogue takes (fewer
     // instructions for the longest GEMV of the step)
     spread(s.V, 0, rot_of(s.L, 0), [&](int sm, int a, int b) {
-      st.items.push_back({sm, make(MK_OP_LMHEAD, s.L - 1, a, b, 0, cm.xout(s.L - 1), s.H, cm.lm(),
-                                   b - a)});
+      st.items.push_back({sm, make(MK_OP_LMHEAD, s.L - 1, a, b, 0, cm.xout(s.L - 1),
+                                   kChunks * s.H, cm.lm(), b - a)});
     }, std::min(64, 2 * cap));
     steps.push_back(std::move(st));
   }
@@ -380,9 +383,9 @@ bool build_plan_steps(const Shape& s, int n_sm, const int* parts, int k, Plan* o
 }
 
 int smem_layout(const Shape& s, int n_sm, int optin, int misc_bytes, Params* p, std::string* why) {
-  // pages | x staging | h staging (one buffer, or two ring slots) | results |
-  // down-projection chunk sums | barriers; the attention scratch reuses the
-  // staging area
+  // pages | x staging | h staging | results | barriers; the attention
+  // scratch reuses the staging area
+  (void)n_sm;
   const int B = s.B;
   // several sequences: each staged row is padded by 4 words (bank spread of
   // the tensor-core fragments)
@@ -392,51 +395,26 @@ int smem_layout(const Shape& s, int n_sm, int optin, int misc_bytes, Params* p, 
   p->alias_xh = B > 1 ? 1 : 0;
   p->fused_red = fused_reduction(s) ? 1 : 0;
   p->res_floats = item_cap_for(s) * 2 * B;
-  // every SM's down-projection rows form one contiguous range of at most
-  // ceil(H / n_sm) rows, so row j can keep its chunk sum at slot j % dacc_rows
-  p->dacc_rows = (s.H + n_sm - 1) / n_sm;
-  const int dacc_bytes = (p->dacc_rows * B * 4 + 15) / 16 * 16;
   const int att_scratch = kComputeWarps * s.G() * (s.D + 2);
-  auto staging_floats = [&](int ring) {
-    int xh = p->alias_xh ? std::max(p->x_floats, p->h_floats)
-                         : p->x_floats + std::max(1, ring) * p->h_floats;
-    xh = std::max(xh, att_scratch);
-    return (xh + 3) / 4 * 4;
-  };
+  int xh = p->alias_xh ? std::max(p->x_floats, p->h_floats) : p->x_floats + p->h_floats;
+  xh = std::max(xh, att_scratch);
+  const int staging_floats = (xh + 3) / 4 * 4;
   // A page slot is always owned by compute warp (slot % kComputeWarps): with
   // the slot count a multiple of the warp count, page k and page k + n_pages
   // (same slot) have the same owner, which consumes them in order, so no warp
   // can wait on a slot two mbarrier phases ahead of its contents.
-  auto pages_for = [&](int ring) {
-    const int fixed = staging_floats(ring) * 4 + kResBufs * p->res_floats * 4 + dacc_bytes +
-                      ((misc_bytes + 127) / 128) * 128;
-    int n = std::min(kMaxPages, (optin - fixed) / kPageBytes);
-    return n - n % kComputeWarps;
-  };
-  // the h ring (one sequence): two slots for chunks of at most 2048 columns
-  // (the register path takes a chunk out of its slot at once), one slot for
-  // wider chunks (copied into the idle x buffer at once); used only when it
-  // costs no page. The attention scratch must stay inside the x part of the
-  // staging area, clear of the h slots (the loader may fill them while
-  // attention runs).
-  int ring = 0;
-  if (B == 1 && att_scratch <= p->x_floats) {
-    if (s.Fc() <= 2048) ring = 2;
-    else if (s.Fc() <= p->x_floats) ring = 1;
-  }
-  if (ring && pages_for(ring) < pages_for(0)) ring = 0;
-  const int n_pages = pages_for(ring);
+  const int fixed = staging_floats * 4 + kResBufs * p->res_floats * 4 + ((misc_bytes + 127) / 128) * 128;
+  int n_pages = std::min(kMaxPages, (optin - fixed) / kPageBytes);
+  n_pages -= n_pages % kComputeWarps;
   if (n_pages < kComputeWarps) {
     if (why) *why = "configuration leaves too few shared-memory pages";
     return 0;
   }
-  p->h_ring = ring;
   p->n_pages = n_pages;
   p->off_x = n_pages * kPageBytes;
   p->off_h = p->alias_xh ? p->off_x : p->off_x + p->x_floats * 4;
-  p->off_res = p->off_x + staging_floats(ring) * 4;
-  p->off_dacc = p->off_res + kResBufs * p->res_floats * 4;
-  p->off_misc = (p->off_dacc + dacc_bytes + 127) / 128 * 128;
+  p->off_res = p->off_x + staging_floats * 4;
+  p->off_misc = (p->off_res + kResBufs * p->res_floats * 4 + 127) / 128 * 128;
   return p->off_misc + misc_bytes;
 }
 

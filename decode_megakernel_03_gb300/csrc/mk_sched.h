@@ -82,10 +82,10 @@ bool build_plan_steps(const Shape& s, int n_sm, const int* parts, int k, Plan* o
                       std::string* why);
 
 // Shared-memory layout of the interpreter for this shape: fills the n_pages,
-// off_*, *_floats, alias_xh, h_ring and dacc_rows fields of p and returns the
-// dynamic shared memory size in bytes, or 0 (with *why set) when fewer than
-// kComputeWarps pages fit in `optin` bytes. misc_bytes is the size of the
-// kernel's barrier block.
+// off_*, *_floats and alias_xh fields of p and returns the dynamic shared
+// memory size in bytes, or 0 (with *why set) when fewer than kComputeWarps
+// pages fit in `optin` bytes. misc_bytes is the size of the kernel's barrier
+// block.
 int smem_layout(const Shape& s, int n_sm, int optin, int misc_bytes, Params* p, std::string* why);
 
 }  // namespace mk

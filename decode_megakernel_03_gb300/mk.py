@@ -67,7 +67,9 @@ INSTR_DTYPE = np.dtype([("op", "<i2"), ("layer", "<i2"), ("a0", "<i4"), ("a1", "
                         ("sig_ctr", "<i4"), ("sig_amount", "<i4")])
 TRACE_DTYPE = np.dtype([("sm", "<u4"), ("index", "<u4"), ("op", "<i4"), ("layer", "<i4"),
                         ("t_start", "<u8"), ("t_ready", "<u8"), ("t_end", "<u8"),
-                        ("t_stored", "<u8"), ("res_wait_ns", "<u4"), ("stage_ns", "<u4")])
+                        ("t_stored", "<u8"), ("res_wait_ns", "<u4"), ("stage_ns", "<u4"),
+                        ("t_issue_first", "<u8"), ("t_issue_last", "<u8"),
+                        ("page_wait_ns", "<u4"), ("reserved", "<u4")])
 
 _lib = None
 
@@ -298,7 +300,8 @@ class Decoder:
         _check(lib().mk_debug_inject_unsatisfiable_wait(self.h, int(bool(enable))), self.h)
 
     def set_trace(self, buf=None):
-        """buf: a torch uint8 CUDA tensor of n * 56 bytes, or None to disable."""
+        """buf: a torch uint8 CUDA tensor of n * TRACE_DTYPE.itemsize bytes, or
+        None to disable."""
         if buf is None:
             _check(lib().mk_set_trace(self.h, None, 0), self.h)
         else:

@@ -212,6 +212,11 @@ typedef struct {
   uint64_t t_stored;        /* the storer has published it (counter bumped) */
   uint32_t res_wait_ns;     /* compute warp 0: waiting for a free result buffer */
   uint32_t stage_ns;        /* compute warp 0: staging the activations */
+  uint64_t t_issue_first;   /* the loader issues the instruction's first copy
+                               (0: the instruction has no pages) */
+  uint64_t t_issue_last;    /* the loader issues its last copy */
+  uint32_t page_wait_ns;    /* compute warp 0: waiting for its pages to land */
+  uint32_t reserved;
 } mk_trace_record;
 int mk_set_trace(mk_handle* h, mk_trace_record* dev_buf, int capacity);
 

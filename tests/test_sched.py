@@ -221,20 +221,26 @@ def _happens_before(ins, off, n_sm):
 
 def _accesses(ins, shape, B):
     """Exact element keys of the shared scratch each instruction reads and
-    writes (q, x, xa, h, dacc, partials and attention output are one buffer
-    reused by every layer; the KV cache is per layer)."""
+    writes (q, xa, the four down-projection shares, h, partials and attention
+    output are one buffer reused by every layer; the KV cache is per layer).
+    A layer's output x is xa + its four down-projection shares, read by the
+    next layer's QKV (all rows) and O-projection (its rows) and the LM head."""
     L, H, D, nkv = shape.n_layers, shape.hidden, shape.head_dim, shape.n_kv_heads
     G = shape.n_heads // nkv
     half = D // 2
     per = (G + 2) * half
     Fc = shape.ffn // 4
+    def x_rows(lo, hi):
+        return ({("xa", k) for k in range(lo, hi)} |
+                {("xpart", c, k) for c in range(4) for k in range(lo, hi)})
+
     acc = []
     for r in ins:
         op, l, a0, a1, a2 = int(r["op"]), int(r["layer"]), int(r["a0"]), int(r["a1"]), int(r["a2"])
         R, W = set(), set()
         if op == mk.OP_QKV:
             if l > 0:
-                R |= {("x", k) for k in range(H)}
+                R |= x_rows(0, H)
             for j in range(a0, a1):
                 slot = (j % per) // half
                 W.add(("q", j) if slot < G else ("kv", l, j))
@@ -252,22 +258,16 @@ def _accesses(ins, shape, B):
             else:
                 R |= {("attn", b, g) for b in range(B) for g in range(nkv)}
             if l > 0:
-                R |= {("x", k) for k in range(a0, a1)}
+                R |= x_rows(a0, a1)
             W |= {("xa", k) for k in range(a0, a1)}
         elif op == mk.OP_GATEUP:
             R |= {("xa", k) for k in range(H)}
             W |= {("h", j) for j in range(a0, a1)}
         elif op == mk.OP_DOWN:
             R |= {("h", j) for j in range(a2 * Fc, (a2 + 1) * Fc)}
-            if a2 > 0:
-                R |= {("dacc", k) for k in range(a0, a1)}
-            if a2 == 3:
-                R |= {("xa", k) for k in range(a0, a1)}
-                W |= {("x", k) for k in range(a0, a1)}
-            else:
-                W |= {("dacc", k) for k in range(a0, a1)}
+            W |= {("xpart", a2, k) for k in range(a0, a1)}
         elif op == mk.OP_LMHEAD:
-            R |= {("x", k) for k in range(H)}
+            R |= x_rows(0, H)
         acc.append((R, W))
     return acc
 
@@ -300,21 +300,33 @@ def test_no_unordered_hazards(case):
     assert checked > 1000
 
 
-def test_chunked_down_waits_only_for_its_chunk():
+@pytest.mark.parametrize("B", [1, 8])
+def test_chunked_down_waits_only_for_its_chunk(B):
     # the down-projection of chunk c waits for chunk c of h, not for the whole
-    # hidden state; every SM runs the four gate/up chunks before the down chunks
-    ins, off, tg, sm = _plan(synth.LLAMA_1B, 1, 640, 152, [512])
+    # hidden state; every SM runs the four gate/up chunks, then the
+    # down-projection of one chunk (two where its range crosses a boundary)
+    ctx = [512] if B == 1 else list(synth.WORKLOADS["llama1b_b8"].ctx)
+    ins, off, tg, sm = _plan(synth.LLAMA_1B, B, 4160, 152, ctx)
+    n_two = 0
     for s in range(152):
         q = ins[off[s]:off[s + 1]]
         l0 = q[q["layer"] == 0]
         seq = [(int(r["op"]), int(r["a2"])) for r in l0 if r["op"] in (mk.OP_GATEUP, mk.OP_DOWN)]
-        assert seq == [(5, 0), (5, 1), (5, 2), (5, 3), (6, 0), (6, 1), (6, 2), (6, 3)], seq
+        gu = [x for x in seq if x[0] == mk.OP_GATEUP]
+        dn_chunks = sorted(set(c for o, c in seq if o == mk.OP_DOWN))
+        assert [c for _, c in gu] == [0, 1, 2, 3] and seq[:4] == gu, seq
+        assert 1 <= len(dn_chunks) <= 2 and dn_chunks == list(range(dn_chunks[0], dn_chunks[-1] + 1))
+        n_two += len(dn_chunks) == 2
+    assert n_two <= 3  # only at the three chunk boundaries
     dn = ins[ins["op"] == mk.OP_DOWN]
     gu = ins[ins["op"] == mk.OP_GATEUP]
     for c in range(4):
         ctrs_dn = set(dn["wait_ctr"][dn["a2"] == c])
         ctrs_gu = set(gu["sig_ctr"][gu["a2"] == c])
         assert len(ctrs_dn) == 16 and ctrs_dn <= ctrs_gu
+    # every layer's output counter counts the rows of all four chunks
+    qkv = ins[(ins["op"] == mk.OP_QKV) & (ins["layer"] > 0)]
+    assert np.all(qkv["wait_target"] == 4 * synth.LLAMA_1B.hidden)
 
 
 def test_work_is_balanced_across_sms():
