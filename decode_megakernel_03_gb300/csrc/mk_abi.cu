@@ -3,10 +3,12 @@
 // (one per decode step) and of the multi-launch comparison build.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
 #include <memory>
+#include <random>
 #include <string>
 #include <vector>
 
@@ -22,7 +24,7 @@ namespace {
 thread_local std::string g_create_error;
 
 struct PlanEntry {
-  int key[kMaxBatch + 1];  // partitions per sequence + injection flag
+  int key[kMaxBatch + 2];  // partitions per sequence, injection flag, permutation seed
   Plan plan;
   Instr* d_instrs = nullptr;
   int* d_sm_off = nullptr;
@@ -43,6 +45,7 @@ struct mk_handle {
   int device = 0;
   int n_sm = 0;
   int smem_bytes = 0;
+  int smem_optin = 0;     // the device's opt-in maximum of dynamic shared memory per block
   const void* fn = nullptr;  // the interpreter instantiation this handle launches
   const void* fn_fx = nullptr;  // the one with the paged-cache / greedy-decode code
   Params base{};          // launch parameters without the per-step fields
@@ -69,6 +72,7 @@ struct mk_handle {
   unsigned long long steps = 0;
   int cur_set = 0;        // counter set used by the most recent step
   int inject = 0;
+  uint32_t perm_seed = 0; // test hook: queues handed to the CTAs in a seeded order
   std::string err;
 };
 
@@ -142,9 +146,10 @@ void free_plan(PlanEntry* e) {
 int get_plan(mk_handle* h, const int32_t* pos, PlanEntry** out) {
   int parts[kMaxBatch];
   choose_partitions(h->shape, h->n_sm, pos, parts);
-  int key[kMaxBatch + 1];
+  int key[kMaxBatch + 2];
   for (int b = 0; b < kMaxBatch; ++b) key[b] = b < h->shape.B ? parts[b] : 0;
   key[kMaxBatch] = h->inject;
+  key[kMaxBatch + 1] = (int)h->perm_seed;
   for (PlanEntry* e : h->plans)
     if (std::memcmp(e->key, key, sizeof key) == 0) {
       e->last_use = ++h->use_clock;
@@ -164,6 +169,22 @@ int get_plan(mk_handle* h, const int32_t* pos, PlanEntry** out) {
         P.instrs[i].wait_target += 1;
         break;
       }
+  }
+  if (h->perm_seed) {
+    // CTA k runs the queue built for SM perm[k]
+    std::vector<int> perm(h->n_sm);
+    for (int k = 0; k < h->n_sm; ++k) perm[k] = k;
+    std::mt19937 rng(h->perm_seed);
+    std::shuffle(perm.begin(), perm.end(), rng);
+    std::vector<Instr> q;
+    std::vector<int> off(h->n_sm + 1, 0);
+    for (int k = 0; k < h->n_sm; ++k) {
+      off[k] = (int)q.size();
+      q.insert(q.end(), P.instrs.begin() + P.sm_off[perm[k]], P.instrs.begin() + P.sm_off[perm[k] + 1]);
+    }
+    off[h->n_sm] = (int)q.size();
+    P.instrs.swap(q);
+    P.sm_off.swap(off);
   }
   // upload (plans change every few hundred tokens, so a synchronous copy is fine)
   MK_CUDA(h, cudaMalloc(&e->d_instrs, sizeof(Instr) * std::max<size_t>(1, P.instrs.size())));
@@ -285,6 +306,7 @@ int create_impl(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
   if (ce == cudaSuccess)
     ce = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device);
   if (ce != cudaSuccess) return cuda_fail(nullptr, ce, "cudaDeviceGetAttribute");
+  h->smem_optin = optin;
 
   // ---- shared-memory layout
   const int B = s.B;
@@ -391,11 +413,9 @@ int create_impl(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
   h->fn_fx = kernel_features(s);
   ce = cudaMemcpy(h->d_rope, rope.data(), sizeof(float2) * rope.size(), cudaMemcpyHostToDevice);
   if (ce == cudaSuccess)
-    ce = cudaFuncSetAttribute(h->fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              h->smem_bytes);
+    ce = allow_max_smem(h->fn, optin);
   if (ce == cudaSuccess)
-    ce = cudaFuncSetAttribute(h->fn_fx, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              h->smem_bytes);
+    ce = allow_max_smem(h->fn_fx, optin);
   if (ce != cudaSuccess) {
     cudaFree(h->d_scratch);
     return cuda_fail(nullptr, ce, "mk_create upload");
@@ -450,8 +470,14 @@ int mk_debug_use_generic_kernel(mk_handle* h, int enable) {
   if (!h) return MK_ERR_INVALID;
   const Shape& s = h->shape;
   const void* fn = kernel_for(s, enable != 0);
-  MK_CUDA(h, cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, h->smem_bytes));
+  MK_CUDA(h, allow_max_smem(fn, h->smem_optin));
   h->fn = fn;
+  return MK_OK;
+}
+
+int mk_debug_permute_queues(mk_handle* h, uint32_t seed) {
+  if (!h) return MK_ERR_INVALID;
+  h->perm_seed = seed;
   return MK_OK;
 }
 

@@ -26,4 +26,8 @@ const void* kernel_for(const Shape& s, bool generic) {
 
 int misc_bytes() { return (int)sizeof(Misc); }
 
+cudaError_t allow_max_smem(const void* fn, int optin) {
+  return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+}
+
 }  // namespace mk

@@ -1,6 +1,8 @@
 // Entry points of the interpreter kernel's instantiations (host side).
 #pragma once
 
+#include <cuda_runtime_api.h>
+
 namespace mk {
 
 struct Shape;
@@ -24,5 +26,12 @@ const void* kernel_for(const Shape& s, bool generic);
 const void* kernel_features(const Shape& s);
 // Size of the kernel's shared-memory barrier block.
 int misc_bytes();
+
+// Lets `fn` launch with up to `optin` bytes of dynamic shared memory (the
+// device's opt-in maximum). The limit is a property of the kernel function,
+// shared by every handle and call that launches it, so it is always raised to
+// the device maximum and never set to one shape's size: a smaller shape must
+// not lower it under a larger one that launches the same function.
+cudaError_t allow_max_smem(const void* fn, int optin);
 
 }  // namespace mk

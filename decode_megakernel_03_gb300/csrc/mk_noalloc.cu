@@ -231,19 +231,26 @@ extern "C" int mk_decode_step_noalloc(const mk_config* cfg, const mk_weights* w,
   if (!smem_bytes) return set_error(errmsg, errmsg_cap, why.c_str());
 
   // ---- uploads, clears, launch: no allocation anywhere below
-  std::vector<float2> rope((size_t)s.S * (s.D / 2));
-  for (int pos = 0; pos < s.S; ++pos)
-    for (int i = 0; i < s.D / 2; ++i) {
-      double ang = (double)pos * std::pow((double)cfg->rope_theta, -2.0 * i / (double)s.D);
-      rope[(size_t)pos * (s.D / 2) + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+  // The step reads the RoPE table only at the B positions it decodes: those
+  // rows alone are computed (angle = pos * theta^(-2i/D), in double, rounded
+  // to fp32, as mk_create does for the whole table) and copied to their
+  // offsets in the table piece.
+  const int half = s.D / 2;
+  std::vector<float2> rope((size_t)B * half);
+  for (int b = 0; b < B; ++b)
+    for (int i = 0; i < half; ++i) {
+      double ang = (double)positions[b] * std::pow((double)cfg->rope_theta, -2.0 * i / (double)s.D);
+      rope[(size_t)b * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
     }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const void* fn = kernel_for(s, false);
   // pageable-source copies are staged by the driver before they return, so
   // the host vectors may go out of scope right after the calls
-  ce = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-  if (ce == cudaSuccess)
-    ce = cudaMemcpyAsync(base + offs[6], rope.data(), sizes[6], cudaMemcpyHostToDevice, st);
+  ce = allow_max_smem(fn, ds->optin);
+  for (int b = 0; b < B && ce == cudaSuccess; ++b)
+    ce = cudaMemcpyAsync(base + offs[6] + sizeof(float2) * (size_t)positions[b] * half,
+                         rope.data() + (size_t)b * half, sizeof(float2) * half,
+                         cudaMemcpyHostToDevice, st);
   if (ce == cudaSuccess)
     ce = cudaMemcpyAsync(base + offs[9], plan.instrs.data(), sizes[9], cudaMemcpyHostToDevice, st);
   if (ce == cudaSuccess)

@@ -24,7 +24,8 @@ EXPORTS = ("mk_create", "mk_decode_step", "mk_decode_step_multilaunch", "mk_get_
            "mk_destroy", "mk_last_error", "mk_read_counters", "mk_set_timeout",
            "mk_debug_inject_unsatisfiable_wait", "mk_set_trace", "mk_schedule_build",
            "mk_decode_step_noalloc", "mk_debug_use_generic_kernel", "mk_decode_greedy",
-           "mk_create_paged", "mk_decode_step_paged", "mk_decode_greedy_persistent")
+           "mk_create_paged", "mk_decode_step_paged", "mk_decode_greedy_persistent",
+           "mk_debug_permute_queues")
 
 MAX_STEPS_PER_LAUNCH = 32  # MK_MAX_STEPS_PER_LAUNCH
 
@@ -99,6 +100,7 @@ def lib():
         L.mk_set_timeout.argtypes = [vp, ctypes.c_uint64]
         L.mk_debug_inject_unsatisfiable_wait.argtypes = [vp, ctypes.c_int]
         L.mk_debug_use_generic_kernel.argtypes = [vp, ctypes.c_int]
+        L.mk_debug_permute_queues.argtypes = [vp, ctypes.c_uint32]
         L.mk_set_trace.argtypes = [vp, vp, ctypes.c_int]
         L.mk_schedule_build.argtypes = [ctypes.POINTER(MkConfig), ctypes.c_int, i32p,
                                         ctypes.POINTER(MkInstr), ctypes.c_int,
@@ -295,6 +297,10 @@ class Decoder:
     def use_generic_kernel(self, enable: bool):
         """Test hook: launch the instantiation that reads the head shape at run time."""
         _check(lib().mk_debug_use_generic_kernel(self.h, int(bool(enable))), self.h)
+
+    def permute_queues(self, seed: int):
+        """Test hook: hand the per-SM queues to the CTAs in a seeded order."""
+        _check(lib().mk_debug_permute_queues(self.h, int(seed)), self.h)
 
     def inject_unsatisfiable_wait(self, enable: bool):
         _check(lib().mk_debug_inject_unsatisfiable_wait(self.h, int(bool(enable))), self.h)

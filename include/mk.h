@@ -187,6 +187,12 @@ int mk_set_timeout(mk_handle* h, uint64_t timeout_ns);
    MK_ERR_TIMEOUT (device waits are bounded; nothing faults). */
 int mk_debug_inject_unsatisfiable_wait(mk_handle* h, int enable);
 
+/* Test-only: with a non-zero seed the handle's plans hand the per-SM queues
+   to the CTAs in a seeded random order (CTA k runs the queue the schedule
+   built for SM perm[k]); 0 restores the identity. Every CTA is co-resident,
+   so any assignment runs, and the results must not depend on it. */
+int mk_debug_permute_queues(mk_handle* h, uint32_t seed);
+
 /* Test-only: with `enable` non-zero the handle launches the interpreter
    instantiation that reads the head dimension and q-heads per kv-head at run
    time, instead of one specialised to the model's head shape (the default

@@ -93,6 +93,9 @@ class Tally:
         self.rows.extend(stats)
 
     def check(self):
+        """Every step within the rel-L2 and max-abs bounds, and top-1
+        agreement of at least 99 % over the run. The oracle's top-1/top-2
+        margin of every disagreement is reported, not excused."""
         assert self.rows
         worst_rel = max(r["rel_l2"] for r in self.rows)
         worst_abs = max(r["max_abs"] for r in self.rows)
@@ -100,8 +103,9 @@ class Tally:
         misses = [r["margin"] for r in self.rows if not r["top1"]]
         assert worst_rel <= REL_L2, f"rel-L2 {worst_rel}"
         assert worst_abs <= MAX_ABS, f"max-abs {worst_abs}"
-        assert agree >= TOP1 or all(m < 1e-3 for m in misses), f"top-1 {agree}, margins {misses}"
-        return dict(rel_l2=worst_rel, max_abs=worst_abs, top1=agree, n=len(self.rows))
+        assert agree >= TOP1, f"top-1 agreement {agree} over {len(self.rows)} steps, margins {misses}"
+        return dict(rel_l2=worst_rel, max_abs=worst_abs, top1=agree, n=len(self.rows),
+                    miss_margins=misses)
 
 
 def check_kv_step(pair: Pair, pos, before_k, before_v):
@@ -118,6 +122,40 @@ def check_kv_step(pair: Pair, pos, before_k, before_v):
                                        rtol=KV_RTOL, atol=KV_ATOL)
             np.testing.assert_allclose(bits_to_f64(gv[b][:, p]), bits_to_f64(pair.ov[l][b][:, p]),
                                        rtol=KV_RTOL, atol=KV_ATOL)
+
+
+def written_rows(pair: Pair, pos):
+    """The k and v rows this step wrote (slot positions[b] of every layer and
+    sequence) on the GPU, as bf16 bits [L][B][nkv][D]; a small gather."""
+    ks = np.stack([np.stack([bf16_bits(pair.kc[l][b, :, p]) for b, p in enumerate(pos)])
+                   for l in range(pair.shape.n_layers)])
+    vs = np.stack([np.stack([bf16_bits(pair.vc[l][b, :, p]) for b, p in enumerate(pos)])
+                   for l in range(pair.shape.n_layers)])
+    return ks, vs
+
+
+def check_written_rows(pair: Pair, pos):
+    """The slot each step writes agrees with the oracle's within one bf16 ulp
+    (the oracle has appended its own row at the same slot)."""
+    gk, gv = written_rows(pair, pos)
+    for l in range(pair.shape.n_layers):
+        for b, p in enumerate(pos):
+            np.testing.assert_allclose(bits_to_f64(gk[l][b]), bits_to_f64(pair.ok[l][b][:, p]),
+                                       rtol=KV_RTOL, atol=KV_ATOL)
+            np.testing.assert_allclose(bits_to_f64(gv[l][b]), bits_to_f64(pair.ov[l][b][:, p]),
+                                       rtol=KV_RTOL, atol=KV_ATOL)
+
+
+def check_untouched(pair: Pair, before_k, before_v, written):
+    """Bit-exact: after a run, every slot that no step wrote still holds its
+    initial bits. written: per sequence, the set of positions the run wrote."""
+    for l in range(pair.shape.n_layers):
+        gk, gv = bf16_bits(pair.kc[l]), bf16_bits(pair.vc[l])
+        for b in range(pair.batch):
+            mask = np.ones(pair.capacity, bool)
+            mask[sorted(written[b])] = False
+            np.testing.assert_array_equal(gk[b][:, mask], before_k[l][b][:, mask])
+            np.testing.assert_array_equal(gv[b][:, mask], before_v[l][b][:, mask])
 
 
 def counters_match(pair: Pair, pos):

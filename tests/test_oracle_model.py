@@ -210,3 +210,83 @@ def test_logit_scale_is_sane():
     assert np.all(np.isfinite(lg))
     sd = lg.std(axis=1)
     assert np.all(sd > 0.05) and np.all(sd < 50)
+
+
+def _composed_step(cfg, w, ks, vs, tok, pos):
+    """One decode step of one sequence written out from the single ops pinned
+    in test_oracle_pins.py, in the order of the seven fused instructions
+    ("3 · L'interpréteur sur GPU", §3.2): attention scale 1/sqrt(head_dim),
+    rotate-half RoPE on every q-head and every k-head at the absolute
+    position, k/v rounded to bf16 through fp32 before they enter the cache,
+    q-head h reading kv-head h // (n_heads / n_kv_heads) over slots 0..pos."""
+    H, D, nh, nkv = cfg["hidden"], cfg["head_dim"], cfg["n_heads"], cfg["n_kv_heads"]
+    group, eps, theta = nh // nkv, cfg["rms_eps"], cfg["rope_theta"]
+    x = _f(w["embed"][tok])
+    for l in range(cfg["n_layers"]):
+        n = O.rmsnorm(x, w["attn_norm"][l], eps)
+        q = O.matvec(w["wq"][l], n)
+        k = O.matvec(w["wk"][l], n)
+        v = O.matvec(w["wv"][l], n)
+        q = np.concatenate([O.rope(q[h * D:(h + 1) * D], pos, theta) for h in range(nh)])
+        k = np.concatenate([O.rope(k[h * D:(h + 1) * D], pos, theta) for h in range(nkv)])
+        for h in range(nkv):
+            ks[l][0, h, pos] = _b(k[h * D:(h + 1) * D].astype(np.float32))
+            vs[l][0, h, pos] = _b(v[h * D:(h + 1) * D].astype(np.float32))
+        att = np.concatenate([
+            O.attend(q[h * D:(h + 1) * D], ks[l][0, h // group, :pos + 1],
+                     vs[l][0, h // group, :pos + 1], 1.0 / np.sqrt(D)) for h in range(nh)])
+        x = x + O.matvec(w["wo"][l], att)
+        n = O.rmsnorm(x, w["mlp_norm"][l], eps)
+        g = O.matvec(w["wgate"][l], n)
+        u = O.matvec(w["wup"][l], n)
+        hh = np.array([O.silu(z) for z in g]) * u
+        x = x + O.matvec(w["wdown"][l], hh)
+    lm = w["embed"] if cfg["tied"] else w["lm_head"]
+    return O.matvec(lm, O.rmsnorm(x, w["final_norm"], eps))
+
+
+@pytest.mark.parametrize("tied", [False, True])
+def test_decode_step_equals_composition_of_pinned_ops(tied):
+    """Two layers with every weight random (Wq and Wk included, so the scores,
+    their 1/sqrt(head_dim) scale and the rotation of q AND k all matter): the
+    whole decode step equals its composition from the individually pinned
+    ops at several positions, including slot 0 and the last slot. A wrong
+    scale (1/sqrt(hidden), none), k left unrotated, a wrong GQA mapping or a
+    wrong slot range would all change these logits."""
+    cfg = dict(SMALL, n_layers=2, tied=tied)
+    rng = np.random.default_rng(31)
+    w = _weights(cfg, rng)
+    m = O.Model(cfg, w)
+    S = 12
+    for pos in (0, 5, S - 1):
+        ks, vs = _cache(cfg, 1, S, rng)
+        ks2 = [k.copy() for k in ks]
+        vs2 = [v.copy() for v in vs]
+        tok = int(rng.integers(cfg["vocab"]))
+        got = m.decode_step(ks, vs, [tok], [pos], nthreads=1)[0]
+        want = _composed_step(cfg, w, ks2, vs2, tok, pos)
+        np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+        for a, b in zip(ks + vs, ks2 + vs2):
+            np.testing.assert_array_equal(a, b)
+        # the scores are far from zero: the test is sensitive to the scale
+        assert np.std(want) > 1e-3
+
+
+def test_composition_detects_a_wrong_attention_scale():
+    """The composed reference is sensitive to what it pins: with the scale
+    1/sqrt(hidden) instead of 1/sqrt(head_dim) its logits move well past the
+    comparison tolerance above."""
+    cfg = dict(SMALL, n_layers=1)
+    rng = np.random.default_rng(32)
+    w = _weights(cfg, rng)
+    S, pos = 12, 9
+    ks, vs = _cache(cfg, 1, S, rng)
+    tok = 7
+    good = _composed_step(cfg, w, [k.copy() for k in ks], [v.copy() for v in vs], tok, pos)
+    real_attend = O.attend
+    try:
+        O.attend = lambda q, K, V, scale: real_attend(q, K, V, 1.0 / np.sqrt(cfg["hidden"]))
+        bad = _composed_step(cfg, w, [k.copy() for k in ks], [v.copy() for v in vs], tok, pos)
+    finally:
+        O.attend = real_attend
+    assert np.max(np.abs(good - bad)) > 1e-3
