@@ -384,6 +384,49 @@ static __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, cons
   }
 }
 
+// Four floats as bf16 pairs {hi(a, b), lo(a, b), hi(c, d), lo(c, d)} with
+// v = hi + lo: a tensor-core operand that keeps about 16 bits of each value.
+__device__ __forceinline__ uint4 split_hi_lo(float a, float b, float c, float d) {
+  const uint32_t h01 = bf16x2_rn(a, b), h23 = bf16x2_rn(c, d);
+  return make_uint4(h01, bf16x2_rn(a - bf_lo(h01), b - bf_hi(h01)), h23,
+                    bf16x2_rn(c - bf_lo(h23), d - bf_hi(h23)));
+}
+
+// One sequence, 2048-column rows: the staged activations are kept as the B
+// fragments of the tensor-core GEMV (rows4_mma), built once per staging and
+// shared by the compute warps. Lane l of a warp takes the 64 words at
+// l * 64 .. + 63 of the buffer: word 4 tp + q is its B register for the step
+// pair tp (q = 0, 1: step 2 tp; q = 2, 3: step 2 tp + 1). The 16-byte chunks
+// of lane l are stored rotated by l % 8, so that the 8 lanes of one
+// shared-memory phase read different banks.
+__device__ __forceinline__ int frag_word(int l, int tp, int q) { return l * 64 + 4 * (tp ^ (l & 7)) + q; }
+
+// Writes columns c .. c + 3 (c % 4 == 0) of a 2048-column activation vector
+// into the fragment buffer: column c of segment sg = c / 512, u = c % 512,
+// sits in step pair tp = (u / 32) ^ sg of lane 8 sg + (u / 8) % 4 (its bf16 hi
+// part) and of lane 8 sg + 4 + (u / 8) % 4 (its lo part), word q = (u % 8) / 2.
+__device__ __forceinline__ void put_frag(uint32_t* fb, int c, float4 x) {
+  const int sg = c >> 9, u = c & 511;
+  const int tp = (u >> 5) ^ sg, tig = (u >> 3) & 3, q = (u & 7) >> 1;
+  const uint4 f = split_hi_lo(x.x, x.y, x.z, x.w);  // {hi01, lo01, hi23, lo23}
+  const int lh = 8 * sg + tig;
+  *reinterpret_cast<uint2*>(fb + frag_word(lh, tp, q)) = make_uint2(f.x, f.z);
+  *reinterpret_cast<uint2*>(fb + frag_word(lh + 4, tp, q)) = make_uint2(f.y, f.w);
+}
+
+// This lane's 64 B fragment registers from the fragment buffer.
+__device__ __forceinline__ void load_frag(float (&bx)[64], const uint32_t* fb) {
+  const int l = threadIdx.x & 31;
+#pragma unroll
+  for (int tp = 0; tp < 16; ++tp) {
+    const uint4 v = lds128(fb + frag_word(l, tp, 0));
+    bx[4 * tp + 0] = __uint_as_float(v.x);
+    bx[4 * tp + 1] = __uint_as_float(v.y);
+    bx[4 * tp + 2] = __uint_as_float(v.z);
+    bx[4 * tp + 3] = __uint_as_float(v.w);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // compute role: activation staging
 // ---------------------------------------------------------------------------
@@ -441,7 +484,7 @@ template <int B, int NS, int NB, int KU, int FX>
 __device__ __forceinline__ void stage_pass(const Params& p, float* dst, int K, int Ks,
                                            const uint16_t* normw, bool from_embed,
                                            const float* base, size_t stride, int b0, int step,
-                                           float (&ss)[NB]) {
+                                           float (&ss)[NB], bool frag) {
   constexpr bool kFrag = B > 1;
   constexpr int kPass = kComputeThreads * 4 * KU;  // columns per pass
   const int tid = compute_tid();
@@ -498,7 +541,9 @@ __device__ __forceinline__ void stage_pass(const Params& p, float* dst, int K, i
             x.w *= bf_hi(wv[u].y);
           }
           float* d = dst + (size_t)(b0 + bb) * Ks + c;
-          if (kFrag) {
+          if (B == 1 && frag) {
+            put_frag(reinterpret_cast<uint32_t*>(dst), c, x);
+          } else if (kFrag) {
             const uint32_t h01 = bf16x2_rn(x.x, x.y), h23 = bf16x2_rn(x.z, x.w);
             const uint32_t l01 = bf16x2_rn(x.x - bf_lo(h01), x.y - bf_hi(h01));
             const uint32_t l23 = bf16x2_rn(x.z - bf_lo(h23), x.w - bf_hi(h23));
@@ -523,7 +568,7 @@ __device__ __forceinline__ void stage_pass(const Params& p, float* dst, int K, i
 // lo(c+2, c+3)}: the A fragment of the tensor-core product (page_rows_mma).
 // kWide: rows may be wider than 3072 columns (one sequence): six column groups
 // per thread, so that 4608 columns still take one L2 round trip
-template <int B, int FX, bool kWide>
+template <int B, int FX, bool kWide, int KW>
 __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, Staged& st, int kind,
                                       int layer, int chunk, int key, int step) {
   constexpr bool kFrag = B > 1;
@@ -533,6 +578,8 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
   float* dst = reinterpret_cast<float*>(smem + (to_h ? p.off_h : p.off_x));
   const int K = kind == kActAttnOut ? p.QD : (to_h ? p.Fc : p.H);
   const int Ks = kFrag ? K + 4 : K;  // row stride of the buffer, in words
+  // one sequence, 2048 columns: the buffer holds the GEMV's B fragments
+  const bool frag = B == 1 && (KW == 2048 || K == 2048);
   const uint16_t* normw = norm_weight(p, kind, layer);
   const bool from_embed = kind == kActAttnNorm && layer == 0;
   // x = xa + the four down-projection shares of the previous layer
@@ -545,15 +592,18 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
   else base = p.h + (size_t)chunk * p.Fc, stride = p.F;
   const int par = st.stage_cnt & 1;
   compute_bar();  // everyone is done reading the buffer's previous contents
-  // one sequence: four (six if wide) column groups per thread and pass; with
-  // five sources, four. Several sequences: all of them and three groups per
-  // pass; with five sources, two sequences and two groups (register budget)
+  // one sequence: four (six if rows may be wider than 3072 columns) column
+  // groups per thread and pass, so 2048 (4608) columns take one L2 round
+  // trip; with five sources two (one if wide) for the register budget.
+  // Several sequences: all of them and three groups per pass; with five
+  // sources, two sequences and one group
   constexpr int kNB1 = B, kU1 = B == 1 ? (kWide ? 6 : 4) : 3;
   constexpr int kNB5 = B == 1 ? 1 : 2, kU5 = B == 1 && !kWide ? 2 : 1;
   if (sum_x) {
     for (int b0 = 0; b0 < B; b0 += kNB5) {
       float ss[kNB5];
-      stage_pass<B, 5, kNB5, kU5, FX>(p, dst, K, Ks, normw, false, base, stride, b0, step, ss);
+      stage_pass<B, 5, kNB5, kU5, FX>(p, dst, K, Ks, normw, false, base, stride, b0, step, ss,
+                                      frag);
       if (normw) {
 #pragma unroll
         for (int bb = 0; bb < kNB5; ++bb) {
@@ -565,7 +615,8 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
     }
   } else {
     float ss[kNB1];
-    stage_pass<B, 1, kNB1, kU1, FX>(p, dst, K, Ks, normw, from_embed, base, stride, 0, step, ss);
+    stage_pass<B, 1, kNB1, kU1, FX>(p, dst, K, Ks, normw, from_embed, base, stride, 0, step, ss,
+                                    frag);
     if (normw) {
 #pragma unroll
       for (int bb = 0; bb < kNB1; ++bb) {
@@ -676,8 +727,10 @@ __device__ __forceinline__ void stage_attn_fused(const Params& p, uint8_t* smem,
       const int c = (q0 + i * kComputeThreads) * 4;
       if (c < p.QD) {
         const float inv = 1.f / den[i];
-        *reinterpret_cast<float4*>(dst + c) =
-            make_float4(acc[i].x * inv, acc[i].y * inv, acc[i].z * inv, acc[i].w * inv);
+        const float4 o4 = make_float4(acc[i].x * inv, acc[i].y * inv, acc[i].z * inv, acc[i].w * inv);
+        // 2048 attention columns: the O-projection's B fragments
+        if (p.QD == 2048) put_frag(reinterpret_cast<uint32_t*>(dst), c, o4);
+        else *reinterpret_cast<float4*>(dst + c) = o4;
       }
     }
   }
@@ -689,7 +742,7 @@ __device__ __forceinline__ void stage_attn_fused(const Params& p, uint8_t* smem,
   if (p.alias_xh) st.key_h = -1;
 }
 
-// One sequence, rows of at most 2048 columns: each compute warp copies the
+// One sequence, rows narrower than 2048 columns: each compute warp copies the
 // staged vector into registers in the layout of the page dot products (lane
 // l, block j: columns j*256 + l*8 .. +8), scaled by 1/rms for the norms.
 __device__ __forceinline__ void load_regs(float (&a)[64], const float* act, float scale, int K) {
@@ -713,15 +766,86 @@ __device__ __forceinline__ void load_regs(float (&a)[64], const float* act, floa
 }
 
 // ---------------------------------------------------------------------------
+// One sequence, 2048-column rows, on the tensor cores (mma.sync m16n8k16,
+// bf16 in, fp32 accumulate). A page holds 4 rows of 2048 columns; the
+// product sees it as 16 "virtual rows", row m = page row m / 4 restricted to
+// column segment s = m % 4 (512 columns each): the A operand. The B operand
+// has 8 columns, column n = the bf16 hi (n even) or lo (n odd) part of the
+// activations' segment n / 2, so x = hi + lo enters at about 16-bit
+// precision per term. D[m][n] is a partial dot product when the segments of
+// m and n agree (m % 4 == n / 2); the other entries are never used. A page
+// is 32 products over the segment's 512 columns; its 4 row results are the
+// sums of 4 segment partials. Inside a segment the order of the 16 columns
+// of one product is free as long as A and B follow it: step t of segment s
+// takes column pairs (tig) from P, P + 1 and (tig + 4) from P + 2, P + 3,
+// P = 32 ((t / 2) ^ s) + 8 tig + 4 (t % 2), so one 16-byte load of a page row
+// feeds two steps, and the XOR by s puts the two virtual rows that one
+// shared-memory phase reads (segments s and s ^ 1 of one page row) on
+// different banks.
+
+// The 4 rows of one page (rows past n_rows hold an earlier page's data, stay
+// inside the slot and are never stored): page row pr's result goes to
+// res_page[(k * R + r)], pr = r * n_in + k.
+__device__ __forceinline__ void rows4_mma(const uint8_t* page, int n_rows, int n_in, int R,
+                                          const float (&bx)[64], float scale, float* res_page,
+                                          int lane) {
+  const int grp = lane >> 2, tig = lane & 3;
+  const int sg = grp & 3;        // segment of virtual rows grp and grp + 8
+  const int ra = grp >> 2;       // page row of virtual row grp (grp + 8: ra + 2)
+  const uint8_t* pa = page + ra * 4096 + sg * 1024 + 16 * tig;
+  const uint8_t* pb = pa + 2 * 4096;
+  // four independent accumulator chains (an mma.sync waits for the previous
+  // one on the same accumulator), summed at the end
+  float d4[4][4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) d4[c][0] = d4[c][1] = d4[c][2] = d4[c][3] = 0.f;
+#pragma unroll
+  for (int tp = 0; tp < 16; ++tp) {
+    const int off = 64 * (tp ^ sg);
+    const uint4 ua = lds128(pa + off), ub = lds128(pb + off);
+    const int c = 2 * (tp & 1);
+    mma_bf16_16816(d4[c], make_uint4(ua.x, ub.x, ua.y, ub.y), __float_as_uint(bx[4 * tp]),
+                   __float_as_uint(bx[4 * tp + 1]));
+    mma_bf16_16816(d4[c + 1], make_uint4(ua.z, ub.z, ua.w, ub.w), __float_as_uint(bx[4 * tp + 2]),
+                   __float_as_uint(bx[4 * tp + 3]));
+  }
+  float d[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) d[e] = (d4[0][e] + d4[1][e]) + (d4[2][e] + d4[3][e]);
+  // the useful columns 2 sg (hi) and 2 sg + 1 (lo) sit in the lanes with
+  // tig == sg: lanes 0, 5, 10, 15 (page rows 0 and 2) and 16, 21, 26, 31
+  // (rows 1 and 3), one segment each
+  float v01 = tig == sg ? d[0] + d[1] : 0.f;  // page row ra
+  float v23 = tig == sg ? d[2] + d[3] : 0.f;  // page row ra + 2
+  v01 += __shfl_xor_sync(0xffffffffu, v01, 5);
+  v23 += __shfl_xor_sync(0xffffffffu, v23, 5);
+  v01 += __shfl_xor_sync(0xffffffffu, v01, 10);
+  v23 += __shfl_xor_sync(0xffffffffu, v23, 10);
+  if ((lane & 15) == 0) {
+    const int r0 = lane >> 4;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int pr = r0 + 2 * e;
+      if (pr < n_rows) {
+        const int r = pr / n_in, k = pr - r * n_in;
+        res_page[k * R + r] = (e == 0 ? v01 : v23) * scale;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // compute role: GEMV pages
 // ---------------------------------------------------------------------------
 // Each compute warp owns whole pages, dealt round-robin over the CTA's page
 // stream, and dots every row of its page with the activations of all B
-// sequences. One sequence runs on the CUDA cores: lane l covers columns
-// j*256 + l*8 .. +8 of each 256-column block, i.e. every block is one
-// 512-byte contiguous read of the row per warp, and four rows are in flight
-// at once (two accumulator chains each) for ILP; with rows of at most 2048
-// columns the activations sit in registers, otherwise they are read from the
+// sequences. One sequence with 2048-column rows runs on the tensor cores
+// (rows4_mma: the activations' B fragments in registers). One sequence with
+// other widths runs on the CUDA cores: lane l covers columns j*256 + l*8 ..
+// +8 of each 256-column block, i.e. every block is one 512-byte contiguous
+// read of the row per warp, and four rows are in flight at once (two
+// accumulator chains each) for ILP; with rows narrower than 2048 columns the
+// activations sit in registers, with wider rows they are read from the
 // staged buffer block by block. Several sequences run on the tensor cores
 // (page_rows_mma): there every weight meets B activations, which the FMA
 // pipes and the shared-memory reads of fp32 activations could not keep up
@@ -735,11 +859,10 @@ __device__ __forceinline__ void warp_sum4(float (&v)[4]) {
   }
 }
 
-// B == 1, K <= 2048: activations a[j*8 + e] in registers. Rows 0..n_rows-1
+// B == 1, K < 2048: activations a[j*8 + e] in registers. Rows 0..n_rows-1
 // (n_rows <= 4) of the page starting at `rows`; lane q < n_rows stores row
 // q's result to *dst (every lane passes its own row's destination, so no
 // array of pointers is needed).
-template <int NB>
 __device__ __forceinline__ void rows4_reg(const uint8_t* rows, int n_rows, int row_bytes,
                                           int nblk, const float (&a)[64], float* dst,
                                           int lane) {
@@ -750,11 +873,11 @@ __device__ __forceinline__ void rows4_reg(const uint8_t* rows, int n_rows, int r
   for (int q = 0; q < 4; ++q) acc[q][0] = acc[q][1] = 0ull;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    if (NB == 8 || j < nblk) {
+    if (j < nblk) {
       uint4 w[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        w[q] = (NB == 8 || q < n_rows)
+        w[q] = q < n_rows
                    ? *reinterpret_cast<const uint4*>(rows + (size_t)q * row_bytes + j * 512 + lane * 16)
                    : make_uint4(0, 0, 0, 0);
 #pragma unroll
@@ -926,19 +1049,14 @@ __device__ __forceinline__ void gemv_run(const Params& p, Misc* m, uint8_t* smem
       if (kRegs) {
         if (KW == 2048 || nblk == 8) {
           // pages of 2048-column rows, full or the short last page of an
-          // instruction: one call site of the full-page code (a second copy
-          // costs instruction-cache space). It dots all four row slots; on a
-          // short page the ones past n_rows hold an earlier page's rows, stay
-          // inside the slot and are never stored.
-          const int pr = min(lane & 3, n_rows - 1);
-          const int r = pr / n_in, k = pr - r * n_in;
-          rows4_reg<8>(page, n_rows, row_bytes, 8, a, res_page + ((size_t)k * g.R + r) * B, lane);
+          // instruction, on the tensor cores (a[] holds the B fragments)
+          rows4_mma(page, n_rows, n_in, g.R, a, inv.v[0], res_page, lane);
         } else if constexpr (KW == 0) {
           for (int r0 = 0; r0 < n_rows; r0 += 4) {
             const int pr = min(r0 + (lane & 3), n_rows - 1);
             const int r = pr / n_in, k = pr - r * n_in;
-            rows4_reg<0>(page + (size_t)r0 * row_bytes, n_rows - r0, row_bytes, nblk, a,
-                         res_page + ((size_t)k * g.R + r) * B, lane);
+            rows4_reg(page + (size_t)r0 * row_bytes, n_rows - r0, row_bytes, nblk, a,
+                      res_page + ((size_t)k * g.R + r) * B, lane);
           }
         }
       } else if constexpr (B > 1) {
@@ -987,11 +1105,6 @@ __device__ __forceinline__ void gemv_run(const Params& p, Misc* m, uint8_t* smem
 // partial is (o, m, l) = (v, q.k, 1); its k and v rows load from global
 // memory together with the queries.
 
-__device__ __forceinline__ uint4 split_hi_lo(float a, float b, float c, float d) {
-  const uint32_t h01 = bf16x2_rn(a, b), h23 = bf16x2_rn(c, d);
-  return make_uint4(h01, bf16x2_rn(a - bf_lo(h01), b - bf_hi(h01)), h23,
-                    bf16x2_rn(c - bf_lo(h23), d - bf_hi(h23)));
-}
 
 template <int D, int FX>
 __device__ void attn_unit(const Params& p, Misc* m, uint8_t* smem, const Instr& in,
@@ -1325,7 +1438,7 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
             }
           }
           if (!staged)
-            stage<B, FX, (B == 1 && KW == 0)>(p, m, smem, st, kind, layer_of(in), chunk, key,
+            stage<B, FX, (B == 1 && KW == 0), KW>(p, m, smem, st, kind, layer_of(in), chunk, key,
                                                step_of(in));
         }
         act = reinterpret_cast<const float*>(smem + (to_h ? p.off_h : p.off_x));
@@ -1335,8 +1448,13 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
 #pragma unroll
       for (int b = 0; b < kMaxBatch; ++b) one.v[b] = 1.f;
       if (regs) {
-        load_regs(ax, act, norm ? st.inv_x.v[0] : 1.f, g.K);
-        gemv_run<B, true, KW>(p, m, smem, in, g, act, one, ax, res, page_cnt, pwait);
+        // 2048 columns: the staged B fragments (the 1/rms of the norms
+        // scales the results); narrower rows: fp32 values scaled here
+        const bool mma = KW == 2048 || g.K == 2048;
+        if (mma) load_frag(ax, reinterpret_cast<const uint32_t*>(act));
+        else load_regs(ax, act, norm ? st.inv_x.v[0] : 1.f, g.K);
+        gemv_run<B, true, KW>(p, m, smem, in, g, act, mma && norm ? st.inv_x : one, ax, res,
+                              page_cnt, pwait);
       } else {
         if constexpr (KW == 0)
           gemv_run<B, false, KW>(p, m, smem, in, g, act, to_h ? one : st.inv_x, ax, res, page_cnt,
@@ -1408,7 +1526,6 @@ __device__ __forceinline__ void epilogue_prefetch(const Params& p, Misc* m, cons
                                                   EpiPre<B>& pre) {
   const int lane = threadIdx.x & 31;
   const int items = in.a1 - in.a0;
-  const bool resid = in.op == MK_OP_OPROJ;
   if (in.op == MK_OP_QKV) {
     const int half = p.D / 2;
 #pragma unroll
@@ -1423,8 +1540,8 @@ __device__ __forceinline__ void epilogue_prefetch(const Params& p, Misc* m, cons
         }
       }
     }
-  } else if (resid) {
-    const bool from_embed = in.op == MK_OP_OPROJ && layer_of(in) == 0;
+  } else if (in.op == MK_OP_OPROJ) {
+    const bool from_embed = layer_of(in) == 0;
     if (!from_embed && !p.no_waits && in.wait_ctr >= 0) {
       // the residual rows were written by other SMs before the instruction's
       // input counter completed: acquire that counter (the compute warps
@@ -1432,6 +1549,7 @@ __device__ __forceinline__ void epilogue_prefetch(const Params& p, Misc* m, cons
       bool ok = true;
       if (lane == 0) ok = wait_counter(p, m, in.wait_ctr, in.wait_target);
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) return;
+      __syncwarp();  // lane 0's acquire, then every lane's loads
     }
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
@@ -1444,10 +1562,10 @@ __device__ __forceinline__ void epilogue_prefetch(const Params& p, Misc* m, cons
             pre.v[k][b].x = bf16f(p.embed[(size_t)token_of<FX>(p, b, step_of(in)) * p.H + j]);
           } else {
             const size_t o = (size_t)b * p.H + j, cs = (size_t)p.B * p.H;
-            const float x0 = __ldcg(p.xa + o), x1 = __ldcg(p.xpart + o),
-                        x2 = __ldcg(p.xpart + cs + o), x3 = __ldcg(p.xpart + 2 * cs + o),
-                        x4 = __ldcg(p.xpart + 3 * cs + o);
-            pre.v[k][b].x = x0 + x1 + x2 + x3 + x4;
+            float acc = __ldcg(p.xa + o);
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c) acc += __ldcg(p.xpart + c * cs + o);
+            pre.v[k][b].x = acc;
           }
         }
       }

@@ -225,9 +225,11 @@ struct Builder {
     // SM takes one contiguous range of them, so it reads one chunk of h (two
     // where its range crosses a chunk boundary) once, and its instructions
     // wait for that chunk alone. Each writes its rows' share of chunk c to
-    // xpart[c]; x = xa + the four shares is formed by its readers. The
-    // weights of an SM's range do not depend on anything, so they stream in
-    // while the gate/up chunks still run.
+    // xpart[c]; x = xa + the four shares is formed by its readers (an
+    // instruction that added them up and published x would put one more
+    // release and round trip on the step's critical path: measured slower).
+    // The weights of an SM's range do not depend on anything, so they stream
+    // in while the gate/up chunks still run.
     {
       Step st{MK_OP_DOWN, l, {}};
       spread(kChunks * H, H, rot_of(l, 2 + kChunks), [&](int sm, int a, int b) {
@@ -305,26 +307,23 @@ bool build_plan(const Shape& s, int n_sm, const int* parts, Plan* out, std::stri
     }
 
   // multi-launch build: one kernel per (layer, instruction type); the gate/up
-  // chunks form one kernel and the down chunks the next
+  // chunks form one kernel and the down-projection the next
   out->phases.clear();
   size_t i = 0;
   while (i < bld.steps.size()) {
     int op = bld.steps[i].op, layer = bld.steps[i].layer;
     std::vector<const std::vector<std::pair<int, Instr>>*> lists;
-    if (op == MK_OP_GATEUP || op == MK_OP_DOWN) {
-      // collect all GATEUP steps of this layer, then all DOWN steps
+    if (op == MK_OP_GATEUP) {
+      // collect all GATEUP steps of this layer into one kernel
       size_t j = i;
-      std::vector<const std::vector<std::pair<int, Instr>>*> gu, dn;
-      while (j < bld.steps.size() && bld.steps[j].layer == layer &&
-             (bld.steps[j].op == MK_OP_GATEUP || bld.steps[j].op == MK_OP_DOWN)) {
-        (bld.steps[j].op == MK_OP_GATEUP ? gu : dn).push_back(&bld.steps[j].items);
+      std::vector<const std::vector<std::pair<int, Instr>>*> gu;
+      while (j < bld.steps.size() && bld.steps[j].layer == layer && bld.steps[j].op == MK_OP_GATEUP) {
+        gu.push_back(&bld.steps[j].items);
         ++j;
       }
-      Phase p1{MK_OP_GATEUP, layer, {}, {}}, p2{MK_OP_DOWN, layer, {}, {}};
+      Phase p1{MK_OP_GATEUP, layer, {}, {}};
       cut_queues(gu, n_sm, &p1.instrs, &p1.sm_off);
-      cut_queues(dn, n_sm, &p2.instrs, &p2.sm_off);
       out->phases.push_back(std::move(p1));
-      out->phases.push_back(std::move(p2));
       i = j;
       continue;
     }
