@@ -42,11 +42,15 @@
 
 namespace mk {
 
+constexpr int kBtCache = 256;  // block-table entries of one attention unit (paged cache)
+
 struct Misc {
   uint64_t full[kMaxPages];
   uint64_t empty[kMaxPages];
   uint64_t res_full[kResBufs];
   uint64_t res_empty[kResBufs];
+  uint64_t bt_full;    // paged cache: the unit's block-table entries landed
+  alignas(16) int bt[kBtCache];  // paged cache: a window of the block table (bulk-copy target)
   float red[2][kComputeWarps][kMaxBatch];  // RMSNorm partial sums, double-buffered
   int abort;
   int hold;       // queue index of the latency-critical instruction being computed (-1: none)
@@ -280,6 +284,8 @@ static __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, cons
   int slot = 0;           // page_cnt % n_pages
   uint32_t round = 0;     // page_cnt / n_pages
   int acq_step = 0;       // greedy steps whose LM head this loader has acquired
+  uint32_t bt_par = 0;    // parity of the next block-table copy
+  bool bt_pending = false;  // a block-table copy was issued and has not been seen landing
   bool ok = true;
   // trace: when this instruction's first and last copies went out
   const int rec0 = p.trace_base + (int)(q - p.instrs);
@@ -315,6 +321,32 @@ static __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, cons
           acq_step = st;
         }
       }
+      // paged cache: the table entries of the unit's cached keys, in one
+      // bulk copy (a 16-byte aligned window of at most kBtCache entries;
+      // every earlier page of this loader has been issued, so the slice is
+      // not in use by a copy still going out)
+      int bt_base = -1;
+      if (FX && p.block_table && sp.nc > 0) {
+        const int e0 = in.a0 * p.max_blocks + sp.t0 / p.kv_block;
+        const int e1 = in.a0 * p.max_blocks + (sp.t0 + sp.nc - 1) / p.kv_block;
+        const int w0 = e0 & ~3;
+        const int nw = (e1 + 1 - w0 + 3) & ~3;
+        if (nw <= kBtCache) {
+          // this thread's reads of the previous window are done; order them
+          // before the copy's writes (generic then async proxy)
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          bt_pending = true;
+          mbar_arrive_expect_tx(&m->bt_full, (uint32_t)nw * 4u);
+          bulk_g2s(m->bt, p.block_table + w0, (uint32_t)nw * 4u, &m->bt_full);
+          if (!wait_mbar(p, m, &m->bt_full, bt_par, kErrTimeoutPage)) {
+            ok = false;
+            break;
+          }
+          bt_pending = false;
+          bt_par ^= 1u;
+          bt_base = w0;
+        }
+      }
       for (int pg = 0; pg < sp.npages; ++pg) {
         if (!wait_mbar(p, m, &m->empty[slot], (round & 1u) ^ 1u, kErrTimeoutPage) ||
             !hold_wait(p, m, i)) {
@@ -327,16 +359,27 @@ static __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, cons
         const uint32_t bytes = (uint32_t)nk * (uint32_t)p.D * 2u;
         uint8_t* dst = smem + (size_t)slot * kPageBytes;
         mbar_arrive_expect_tx(&m->full[slot], 2u * bytes);
-        // one copy per run of keys that are contiguous in the cache (a paged
-        // cache breaks runs at block boundaries)
-        for (int t = k0, off = 0; t < k0 + nk;) {
-          const int run = FX && p.block_table ? min(k0 + nk - t, p.kv_block - t % p.kv_block) : nk;
-          const size_t row = kv_row<FX>(p, in.a0, in.a1, t);
-          const uint32_t rb = (uint32_t)run * (uint32_t)p.D * 2u;
-          bulk_g2s_hint(dst + off, L.kc + row, rb, &m->full[slot], pol);
-          bulk_g2s_hint(dst + kPageBytes / 2 + off, L.vc + row, rb, &m->full[slot], pol);
-          t += run;
-          off += (int)rb;
+        if (!FX || !p.block_table) {
+          // the page's keys are one contiguous run of the cache
+          const size_t row = kv_row<FX>(p, in.a0, in.a1, k0);
+          bulk_g2s_hint(dst, L.kc + row, bytes, &m->full[slot], pol);
+          bulk_g2s_hint(dst + kPageBytes / 2, L.vc + row, bytes, &m->full[slot], pol);
+        } else {
+          // a paged cache: one copy per run of keys inside one block, its
+          // block from the table slice in shared memory (or, for a unit
+          // wider than the slice, from the table itself)
+          const int* bt = p.block_table + (size_t)in.a0 * p.max_blocks;
+          for (int t = k0, off = 0; t < k0 + nk;) {
+            const int run = min(k0 + nk - t, p.kv_block - t % p.kv_block);
+            const int e = in.a0 * p.max_blocks + t / p.kv_block - bt_base;
+            const int blk = bt_base >= 0 && e < kBtCache ? m->bt[e] : __ldg(bt + t / p.kv_block);
+            const size_t row = (((size_t)blk * p.nkv + in.a1) * p.kv_block + t % p.kv_block) * p.D;
+            const uint32_t rb = (uint32_t)run * (uint32_t)p.D * 2u;
+            bulk_g2s_hint(dst + off, L.kc + row, rb, &m->full[slot], pol);
+            bulk_g2s_hint(dst + kPageBytes / 2 + off, L.vc + row, rb, &m->full[slot], pol);
+            t += run;
+            off += (int)rb;
+          }
         }
         ++page_cnt;
         if (++slot == p.n_pages) {
@@ -372,6 +415,12 @@ static __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, cons
   }
   if (!ok) {
     // drain: every issued copy must land before the CTA's shared memory goes away
+    if (bt_pending) {
+      const uint64_t t0 = globaltimer();
+      while (!mbar_try_wait(&m->bt_full, bt_par)) {
+        if (globaltimer() - t0 > p.timeout_ns) break;
+      }
+    }
     const uint32_t first = page_cnt > (uint32_t)p.n_pages ? page_cnt - p.n_pages : 0u;
     for (uint32_t k = first; k < page_cnt; ++k) {
       const int sl = (int)(k % (uint32_t)p.n_pages);
@@ -1721,6 +1770,7 @@ __global__ void __launch_bounds__(kThreads, 1) interp_kernel(const __grid_consta
       mbar_init(&m->res_full[i], kComputeWarps);
       mbar_init(&m->res_empty[i], 1);
     }
+    mbar_init(&m->bt_full, 1);
     m->abort = 0;
     m->hold = -1;
     m->published = 0;
