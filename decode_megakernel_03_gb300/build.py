@@ -19,6 +19,7 @@ LIB = os.path.join(HERE, "libmk.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 
 SOURCES = ["mk_kernel.cu", "mk_kernel_fixed_a.cu", "mk_kernel_fixed_b.cu", "mk_kernel_fx.cu",
+           "mk_kernel_dyn.cu",
            "mk_abi.cu", "mk_sched.cpp",
            "mk_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -24,7 +24,7 @@ namespace {
 thread_local std::string g_create_error;
 
 struct PlanEntry {
-  int key[kMaxBatch + 2];  // partitions per sequence, injection flag, permutation seed
+  int key[kMaxBatch + 3];  // partitions per sequence, injection flag, permutation seed, dynamic flags
   Plan plan;
   Instr* d_instrs = nullptr;
   int* d_sm_off = nullptr;
@@ -48,6 +48,7 @@ struct mk_handle {
   int smem_optin = 0;     // the device's opt-in maximum of dynamic shared memory per block
   const void* fn = nullptr;  // the interpreter instantiation this handle launches
   const void* fn_fx = nullptr;  // the one with the paged-cache / greedy-decode code
+  const void* fn_dyn = nullptr; // the one with dynamic work distribution (or nullptr)
   Params base{};          // launch parameters without the per-step fields
   void* d_scratch = nullptr;
   float2* d_rope = nullptr;
@@ -73,6 +74,7 @@ struct mk_handle {
   int cur_set = 0;        // counter set used by the most recent step
   int inject = 0;
   uint32_t perm_seed = 0; // test hook: queues handed to the CTAs in a seeded order
+  int dyn = 0;            // MK_DYN_* flags of the plans
   std::string err;
 };
 
@@ -142,14 +144,17 @@ void free_plan(PlanEntry* e) {
   delete e;
 }
 
-// Returns the plan for these positions, building and uploading it if needed.
-int get_plan(mk_handle* h, const int32_t* pos, PlanEntry** out) {
+// Returns the plan for these positions, building and uploading it if needed
+// (dyn: MK_DYN_* flags of the plan; greedy decode and paged steps run
+// kernels without dynamic distribution and pass 0).
+int get_plan(mk_handle* h, const int32_t* pos, PlanEntry** out, int dyn) {
   int parts[kMaxBatch];
   choose_partitions(h->shape, h->n_sm, pos, parts);
-  int key[kMaxBatch + 2];
+  int key[kMaxBatch + 3];
   for (int b = 0; b < kMaxBatch; ++b) key[b] = b < h->shape.B ? parts[b] : 0;
   key[kMaxBatch] = h->inject;
   key[kMaxBatch + 1] = (int)h->perm_seed;
+  key[kMaxBatch + 2] = dyn;
   for (PlanEntry* e : h->plans)
     if (std::memcmp(e->key, key, sizeof key) == 0) {
       e->last_use = ++h->use_clock;
@@ -159,7 +164,8 @@ int get_plan(mk_handle* h, const int32_t* pos, PlanEntry** out) {
   std::unique_ptr<PlanEntry> e(new PlanEntry());
   std::memcpy(e->key, key, sizeof key);
   std::string why;
-  if (!build_plan(h->shape, h->n_sm, parts, &e->plan, &why)) return fail(h, MK_ERR_INVALID, why);
+  if (!build_plan(h->shape, h->n_sm, parts, &e->plan, &why, dyn))
+    return fail(h, MK_ERR_INVALID, why);
   Plan& P = e->plan;
   if (h->inject) {
     // raise the first wait of the last SM's queue past what can ever be produced
@@ -411,11 +417,13 @@ int create_impl(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
   }
   h->fn = kernel_for(s, false);
   h->fn_fx = kernel_features(s);
+  h->fn_dyn = kernel_dynamic(s);
   ce = cudaMemcpy(h->d_rope, rope.data(), sizeof(float2) * rope.size(), cudaMemcpyHostToDevice);
   if (ce == cudaSuccess)
     ce = allow_max_smem(h->fn, optin);
   if (ce == cudaSuccess)
     ce = allow_max_smem(h->fn_fx, optin);
+  if (ce == cudaSuccess && h->fn_dyn) ce = allow_max_smem(h->fn_dyn, optin);
   if (ce != cudaSuccess) {
     cudaFree(h->d_scratch);
     return cuda_fail(nullptr, ce, "mk_create upload");
@@ -475,6 +483,15 @@ int mk_debug_use_generic_kernel(mk_handle* h, int enable) {
   return MK_OK;
 }
 
+int mk_set_dynamic(mk_handle* h, int flags) {
+  if (!h) return MK_ERR_INVALID;
+  if (flags & ~MK_DYN_LMHEAD) return fail(h, MK_ERR_INVALID, "unknown dynamic distribution flag");
+  if (flags && !h->fn_dyn)
+    return fail(h, MK_ERR_INVALID, "dynamic distribution is not built for this model shape");
+  h->dyn = flags;
+  return MK_OK;
+}
+
 int mk_debug_permute_queues(mk_handle* h, uint32_t seed) {
   if (!h) return MK_ERR_INVALID;
   h->perm_seed = seed;
@@ -504,7 +521,7 @@ int mk_decode_step_paged(mk_handle* h, const int32_t* tok, const int32_t* pos,
   rc = check_sticky(h);
   if (rc) return rc;
   PlanEntry* e = nullptr;
-  rc = get_plan(h, pos, &e);
+  rc = get_plan(h, pos, &e, 0);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // pageable source: the copy has read the table when the call returns
@@ -536,7 +553,7 @@ int mk_decode_step(mk_handle* h, const int32_t* tok, const int32_t* pos, float* 
   rc = check_sticky(h);
   if (rc) return rc;
   PlanEntry* e = nullptr;
-  rc = get_plan(h, pos, &e);
+  rc = get_plan(h, pos, &e, h->dyn);
   if (rc) return rc;
   Params p = step_params(h, tok, pos, logits);
   p.instrs = e->d_instrs;
@@ -544,7 +561,8 @@ int mk_decode_step(mk_handle* h, const int32_t* tok, const int32_t* pos, float* 
   p.no_waits = 0;
   p.trace_base = 0;
   void* args[] = {&p};
-  cudaError_t ce = cudaLaunchCooperativeKernel(h->fn, dim3(h->n_sm),
+  // dynamic distribution is compiled into its own instantiations
+  cudaError_t ce = cudaLaunchCooperativeKernel(h->dyn ? h->fn_dyn : h->fn, dim3(h->n_sm),
                                                dim3(kThreads), args, (size_t)h->smem_bytes,
                                                static_cast<cudaStream_t>(stream));
   if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaLaunchCooperativeKernel");
@@ -576,7 +594,7 @@ int mk_decode_greedy(mk_handle* h, const int32_t* tok, const int32_t* pos, int n
   for (int s = 0; s < n_steps; ++s) {
     for (int b = 0; b < B; ++b) ps[b] = pos[b] + s;
     PlanEntry* e = nullptr;
-    rc = get_plan(h, ps, &e);
+    rc = get_plan(h, ps, &e, 0);
     if (rc) return rc;
     Params p = step_params(h, tok, ps, logits);
     p.tok_keys = s > 0 ? h->d_keys + (size_t)(s - 1) * B : nullptr;
@@ -683,13 +701,13 @@ int mk_decode_step_multilaunch(mk_handle* h, const int32_t* tok, const int32_t* 
   rc = check_sticky(h);
   if (rc) return rc;
   PlanEntry* e = nullptr;
-  rc = get_plan(h, pos, &e);
+  rc = get_plan(h, pos, &e, h->dyn);
   if (rc) return rc;
   Params p = step_params(h, tok, pos, logits);
   p.no_waits = 1;
   p.trace = nullptr;
   p.trace_cap = 0;
-  const void* fn = h->fn;
+  const void* fn = h->dyn ? h->fn_dyn : h->fn;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t nph = e->plan.phases.size();
   std::vector<Params> ps(nph, p);
@@ -768,9 +786,10 @@ int mk_read_counters(mk_handle* h, int32_t* out, int capacity, int* n_out) {
   return MK_OK;
 }
 
-int mk_schedule_build(const mk_config* cfg, int n_sm, const int32_t* positions, mk_instr* instrs,
-                      int instr_capacity, int* n_instr, int32_t* sm_offsets, int32_t* targets,
-                      int counter_capacity, int* n_counters) {
+int mk_schedule_build_dynamic(const mk_config* cfg, int n_sm, const int32_t* positions,
+                              int dyn_flags, mk_instr* instrs, int instr_capacity, int* n_instr,
+                              int32_t* sm_offsets, int32_t* targets, int counter_capacity,
+                              int* n_counters) {
   int rc = check_config(cfg, nullptr);
   if (rc) return rc;
   if (n_sm < 1 || !positions) return fail(nullptr, MK_ERR_INVALID, "n_sm / positions");
@@ -782,7 +801,8 @@ int mk_schedule_build(const mk_config* cfg, int n_sm, const int32_t* positions, 
   choose_partitions(s, n_sm, positions, parts);
   Plan P;
   std::string why;
-  if (!build_plan(s, n_sm, parts, &P, &why)) return fail(nullptr, MK_ERR_INVALID, why);
+  if (dyn_flags & ~MK_DYN_LMHEAD) return fail(nullptr, MK_ERR_INVALID, "unknown dynamic flag");
+  if (!build_plan(s, n_sm, parts, &P, &why, dyn_flags)) return fail(nullptr, MK_ERR_INVALID, why);
   if (n_instr) *n_instr = (int)P.instrs.size();
   if (n_counters) *n_counters = (int)P.targets.size();
   if (instrs) {
@@ -797,6 +817,14 @@ int mk_schedule_build(const mk_config* cfg, int n_sm, const int32_t* positions, 
     std::memcpy(targets, P.targets.data(), sizeof(int) * P.targets.size());
   }
   return MK_OK;
+}
+
+
+int mk_schedule_build(const mk_config* cfg, int n_sm, const int32_t* positions, mk_instr* instrs,
+                      int instr_capacity, int* n_instr, int32_t* sm_offsets, int32_t* targets,
+                      int counter_capacity, int* n_counters) {
+  return mk_schedule_build_dynamic(cfg, n_sm, positions, 0, instrs, instr_capacity, n_instr,
+                                   sm_offsets, targets, counter_capacity, n_counters);
 }
 
 }  // extern "C"

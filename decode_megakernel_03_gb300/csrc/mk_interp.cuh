@@ -43,12 +43,19 @@
 namespace mk {
 
 constexpr int kBtCache = 256;  // block-table entries of one attention unit (paged cache)
+constexpr int kTk = 4;         // ticket slots between the loader and the compute warps and storer
+constexpr int kFxPaged = 1;    // feature bit: paged KV cache and greedy decode
+constexpr int kFxDyn = 2;      // feature bit: dynamic work distribution
 
 struct Misc {
   uint64_t full[kMaxPages];
   uint64_t empty[kMaxPages];
   uint64_t res_full[kResBufs];
   uint64_t res_empty[kResBufs];
+  uint64_t tk_full[kTk];   // dynamic instructions: the loader published a ticket
+  uint64_t tk_empty[kTk];  // compute warp 0 and the storer have read it
+  int tk[kTk];             // the tickets (-1: none left)
+  int tk_cur[2];           // compute warp 0 passes each ticket to the other compute warps
   uint64_t bt_full;    // paged cache: the unit's block-table entries landed
   alignas(16) int bt[kBtCache];  // paged cache: a window of the block table (bulk-copy target)
   float red[2][kComputeWarps][kMaxBatch];  // RMSNorm partial sums, double-buffered
@@ -181,6 +188,47 @@ __device__ __forceinline__ Instr load_instr(const Instr* q) {
 }
 
 // ---------------------------------------------------------------------------
+// dynamic work distribution
+// ---------------------------------------------------------------------------
+// A dynamic instruction (the LM head with a2 > 0) is not a fixed row range:
+// every SM's queue holds one, and the SMs take row blocks of a0 rows out of
+// [0, a1) from a per-step ticket counter (counter a2 - 1, zero at launch)
+// until none is left, so an SM that reaches the LM head early takes more of
+// it ("3 · L'interpréteur sur GPU", §3.6: instructions distributed over the
+// SMs dynamically). The loader takes each ticket (before it streams the
+// block's rows) and publishes it through a small ring to the compute warps
+// and the storer, which then run the block as a plain instruction.
+
+// (compiled into the kernels with feature bit kFxDyn only)
+__device__ __forceinline__ bool is_dyn(const Instr& in) { return in.op == MK_OP_LMHEAD && in.a2 > 0; }
+
+// the plain instruction of ticket t of dynamic instruction `in`
+__device__ __forceinline__ Instr dyn_item(const Instr& in, int t) {
+  Instr it = in;
+  it.a0 = t * in.a0;
+  it.a1 = min(in.a1, it.a0 + in.a0);
+  it.a2 = 0;
+  it.sig_amount = it.a1 - it.a0;
+  return it;
+}
+
+// Loader: the next ticket of `in` (-1: none left), published to the ring.
+__device__ __forceinline__ int loader_ticket(const Params& p, Misc* m, const Instr& in,
+                                             uint32_t& tk_n, bool& ok) {
+  const int slot = (int)(tk_n % kTk);
+  if (!wait_mbar(p, m, &m->tk_empty[slot], ((tk_n / kTk) & 1u) ^ 1u, kErrTimeoutRes)) {
+    ok = false;
+    return -1;
+  }
+  const int t = atomicAdd(p.ctr + in.a2 - 1, 1);
+  const int v = (long)t * in.a0 < (long)in.a1 ? t : -1;
+  *reinterpret_cast<volatile int*>(&m->tk[slot]) = v;
+  mbar_arrive(&m->tk_full[slot]);  // release (CTA scope) of the ticket to its readers
+  ++tk_n;
+  return v;
+}
+
+// ---------------------------------------------------------------------------
 // weight rows of a GEMV item
 // ---------------------------------------------------------------------------
 
@@ -220,11 +268,12 @@ __device__ __forceinline__ RowSrc row_src_of(const Params& p, const Instr& in) {
 
 // element offset of key/value row t of (sequence b, kv-head g) in a layer's
 // cache, contiguous or paged; rows of one block are contiguous
-// FX: the interpreter is built with the paged-cache and greedy-decode code
-// (kernels without it carry none of that code: the instruction cache)
+// FX: feature bits of the interpreter build (kernels without a feature carry
+// none of its code: the instruction cache). kFxPaged: the paged-cache and
+// greedy-decode code; kFxDyn: dynamic work distribution.
 template <int FX>
 __device__ __forceinline__ size_t kv_row(const Params& p, int b, int g, int t) {
-  if (!FX || !p.block_table) return (((size_t)b * p.nkv + g) * (size_t)p.S + t) * p.D;
+  if (!(FX & kFxPaged) || !p.block_table) return (((size_t)b * p.nkv + g) * (size_t)p.S + t) * p.D;
   const int blk = __ldg(p.block_table + b * p.max_blocks + t / p.kv_block);
   return (((size_t)blk * p.nkv + g) * p.kv_block + t % p.kv_block) * p.D;
 }
@@ -295,10 +344,25 @@ static __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, cons
       p.trace[rec0 + i].t_issue_last = globaltimer();
     }
   };
+  uint32_t tk_n = 0;      // tickets published (dynamic instructions)
   Instr nxt = n > 0 ? load_instr(q) : Instr{};
-  for (int i = 0; i < n && ok; ++i) {
-    const Instr in = nxt;
-    if (i + 1 < n) nxt = load_instr(q + i + 1);
+  Instr in0 = nxt;
+  int adv = 1;  // 0 while a dynamic instruction still has tickets
+  for (int i = 0; i < n && ok; i += adv) {
+    if (adv) {
+      in0 = nxt;
+      if (i + 1 < n) nxt = load_instr(q + i + 1);
+    }
+    // a dynamic instruction is entered once per ticket it takes (the queue
+    // index stays), a plain one once
+    Instr in = in0;
+    adv = 1;
+    if ((FX & kFxDyn) && is_dyn(in0)) {
+      const int t = loader_ticket(p, m, in0, tk_n, ok);
+      if (t < 0) continue;  // none left (or an abort): the next entry
+      in = dyn_item(in0, t);
+      adv = 0;
+    }
     uint64_t t_first = 0;
     if (in.op == MK_OP_ATTN) {
       // the unit's cached keys, K and V rows of kpp keys per page; they do
@@ -306,7 +370,7 @@ static __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, cons
       // still waits for its queries
       const AttnSpan sp = attn_span(p.pos[in.a0] + step_of(in), in.a2 >> 16, in.a2 & 0xffff, p.D);
       const LayerPtrs& L = p.layers[layer_of(in)];
-      if constexpr (FX) {
+      if constexpr ((FX & kFxPaged) != 0) {
         // keys written by an earlier step of this launch: every write of step
         // s - 1 is ordered before its LM head's count (and the bulk copies
         // below after this acquire)
@@ -326,7 +390,7 @@ static __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, cons
       // every earlier page of this loader has been issued, so the slice is
       // not in use by a copy still going out)
       int bt_base = -1;
-      if (FX && p.block_table && sp.nc > 0) {
+      if ((FX & kFxPaged) && p.block_table && sp.nc > 0) {
         const int e0 = in.a0 * p.max_blocks + sp.t0 / p.kv_block;
         const int e1 = in.a0 * p.max_blocks + (sp.t0 + sp.nc - 1) / p.kv_block;
         const int w0 = e0 & ~3;
@@ -359,7 +423,7 @@ static __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, cons
         const uint32_t bytes = (uint32_t)nk * (uint32_t)p.D * 2u;
         uint8_t* dst = smem + (size_t)slot * kPageBytes;
         mbar_arrive_expect_tx(&m->full[slot], 2u * bytes);
-        if (!FX || !p.block_table) {
+        if (!(FX & kFxPaged) || !p.block_table) {
           // the page's keys are one contiguous run of the cache
           const size_t row = kv_row<FX>(p, in.a0, in.a1, k0);
           bulk_g2s_hint(dst, L.kc + row, bytes, &m->full[slot], pol);
@@ -508,8 +572,9 @@ struct Staged {
 // previous step's argmax
 template <int FX>
 __device__ __forceinline__ int token_of(const Params& p, int b, int step) {
-  if (FX && step > 0) return key_token(__ldcg(p.argmax_out + (size_t)(step - 1) * p.B + b));
-  return FX && p.tok_keys ? key_token(__ldcg(p.tok_keys + b)) : p.tok[b];
+  if ((FX & kFxPaged) && step > 0)
+    return key_token(__ldcg(p.argmax_out + (size_t)(step - 1) * p.B + b));
+  return (FX & kFxPaged) && p.tok_keys ? key_token(__ldcg(p.tok_keys + b)) : p.tok[b];
 }
 
 __device__ __forceinline__ int act_key(int kind, int layer, int chunk) {
@@ -1439,13 +1504,39 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
   // reloaded from the staged smem vector at every instruction
   float ax[64];
   uint32_t page_cnt = 0;
+  uint32_t seq = 0;   // instructions (dynamic tickets included) handed to the storer
+  uint32_t tk_n = 0;  // tickets read
   int known_ctr = -1, known_tgt = 0;
   Instr nxt = n > 0 ? load_instr(q) : Instr{};
-  for (int i = 0; i < n; ++i) {
-    const Instr in = nxt;
-    if (i + 1 < n) nxt = load_instr(q + i + 1);
-    const int buf = i % kResBufs;
-    const uint32_t rpar = ((uint32_t)i / kResBufs) & 1u;
+  Instr in0 = nxt;
+  int adv = 1;  // 0 while a dynamic instruction still has tickets
+  for (int i = 0; i < n; i += adv) {
+    if (adv) {
+      in0 = nxt;
+      if (i + 1 < n) nxt = load_instr(q + i + 1);
+    }
+    Instr in = in0;
+    adv = 1;
+    if ((FX & kFxDyn) && is_dyn(in0)) {
+      // warp 0 reads the loader's ticket and passes it to the other warps
+      const int slot = (int)(tk_n % kTk);
+      if (warp == 0 && lane == 0) {
+        int t = -1;
+        if (wait_mbar(p, m, &m->tk_full[slot], (tk_n / kTk) & 1u, kErrTimeoutRes))
+          t = *reinterpret_cast<volatile int*>(&m->tk[slot]);
+        *reinterpret_cast<volatile int*>(&m->tk_cur[tk_n & 1u]) = t;
+        mbar_arrive(&m->tk_empty[slot]);
+      }
+      compute_bar();
+      const int t = *reinterpret_cast<volatile int*>(&m->tk_cur[tk_n & 1u]);
+      ++tk_n;
+      if (t < 0) continue;
+      in = dyn_item(in0, t);
+      adv = 0;
+    }
+    const int buf = (int)(seq % kResBufs);
+    const uint32_t rpar = (seq / kResBufs) & 1u;
+    ++seq;
     uint64_t t_start = 0, t_ready = 0, pwait = 0;
     const bool tracing = p.trace != nullptr && warp == 0 && lane == 0;
     if (tracing) t_start = globaltimer();
@@ -1676,7 +1767,7 @@ __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const
       }
     }
   }
-  if (FX && in.op == MK_OP_LMHEAD && p.argmax_out) {
+  if ((FX & kFxPaged) && in.op == MK_OP_LMHEAD && p.argmax_out) {
     // greedy decode: the instruction's best row per sequence joins the
     // step's argmax (atomicMax of order-preserving keys: any order of the
     // SMs gives the same result)
@@ -1713,12 +1804,35 @@ __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const
 template <int B, int FX>
 __device__ void storer_role(const Params& p, Misc* m, uint8_t* smem, const Instr* q, int n) {
   const int lane = threadIdx.x & 31;
+  uint32_t seq = 0;   // instructions (dynamic tickets included) taken from the compute warps
+  uint32_t tk_n = 0;  // tickets read
   Instr nxt = n > 0 ? load_instr(q) : Instr{};
-  for (int i = 0; i < n; ++i) {
-    const Instr in = nxt;
-    if (i + 1 < n) nxt = load_instr(q + i + 1);
-    const int buf = i % kResBufs;
-    const uint32_t par = ((uint32_t)i / kResBufs) & 1u;
+  Instr in0 = nxt;
+  int adv = 1;  // 0 while a dynamic instruction still has tickets
+  for (int i = 0; i < n; i += adv) {
+    if (adv) {
+      in0 = nxt;
+      if (i + 1 < n) nxt = load_instr(q + i + 1);
+    }
+    Instr in = in0;
+    adv = 1;
+    if ((FX & kFxDyn) && is_dyn(in0)) {
+      const int slot = (int)(tk_n % kTk);
+      int t = -1;
+      if (lane == 0) {
+        if (wait_mbar(p, m, &m->tk_full[slot], (tk_n / kTk) & 1u, kErrTimeoutRes))
+          t = *reinterpret_cast<volatile int*>(&m->tk[slot]);
+        mbar_arrive(&m->tk_empty[slot]);
+      }
+      t = __shfl_sync(0xffffffffu, t, 0);
+      ++tk_n;
+      if (t < 0) continue;
+      in = dyn_item(in0, t);
+      adv = 0;
+    }
+    const int buf = (int)(seq % kResBufs);
+    const uint32_t par = (seq / kResBufs) & 1u;
+    ++seq;
     EpiPre<B> pre;
     if (is_gemv(in.op) && !aborted(m)) epilogue_prefetch<B, FX>(p, m, in, pre);
     const bool ok = wait_mbar(p, m, &m->res_full[buf], par, kErrTimeoutRes);
@@ -1734,7 +1848,8 @@ __device__ void storer_role(const Params& p, Misc* m, uint8_t* smem, const Instr
         // would wait for this SM's weight copies in flight.
         __syncwarp();
         if (lane == 0) {
-          if (in.op == MK_OP_LMHEAD && !FX) red_relaxed_add(p.ctr + in.sig_ctr, in.sig_amount);
+          if (in.op == MK_OP_LMHEAD && !(FX & kFxPaged))
+            red_relaxed_add(p.ctr + in.sig_ctr, in.sig_amount);
           else red_release_add(p.ctr + in.sig_ctr, in.sig_amount);
         }
       }
@@ -1771,6 +1886,10 @@ __global__ void __launch_bounds__(kThreads, 1) interp_kernel(const __grid_consta
       mbar_init(&m->res_empty[i], 1);
     }
     mbar_init(&m->bt_full, 1);
+    for (int i = 0; i < kTk; ++i) {
+      mbar_init(&m->tk_full[i], 1);   // the loader
+      mbar_init(&m->tk_empty[i], 2);  // compute warp 0 and the storer
+    }
     m->abort = 0;
     m->hold = -1;
     m->published = 0;

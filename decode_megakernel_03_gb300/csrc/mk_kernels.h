@@ -24,6 +24,10 @@ const void* kernel_for(const Shape& s, bool generic);
 // shape (specialised for the Llama-1B shape at batch 1 and 8 and the Llama-8B
 // shape, else generic).
 const void* kernel_features(const Shape& s);
+// The instantiation with dynamic work distribution for this shape (the
+// Llama-1B shape at batch 1 and 8, the Llama-8B shape, and one sequence with
+// head_dim 64 and two q-heads per kv-head), or nullptr.
+const void* kernel_dynamic(const Shape& s);
 // Size of the kernel's shared-memory barrier block.
 int misc_bytes();
 

@@ -241,8 +241,18 @@ struct Builder {
     }
   }
 
-  void add_lm_head() {
+  void add_lm_head(bool dyn) {
     Step st{MK_OP_LMHEAD, -1, {}};
+    if (dyn) {
+      // one dynamic instruction per SM: row blocks of the static item size,
+      // taken from the ticket counter (its count is set to V below)
+      const int rows = std::min(64, 2 * cap);
+      for (int sm = 0; sm < n_sm; ++sm)
+        st.items.push_back({sm, make(MK_OP_LMHEAD, s.L - 1, rows, s.V, cm.dyn() + 1,
+                                     cm.xout(s.L - 1), kChunks * s.H, cm.lm(), 0)});
+      steps.push_back(std::move(st));
+      return;
+    }
     // one row per item: twice the items of a row-pair instruction fit the
     // result buffer, up to the 64 the storer's epilogue takes (fewer
     // instructions for the longest GEMV of the step)
@@ -270,7 +280,8 @@ void cut_queues(const std::vector<const std::vector<std::pair<int, Instr>>*>& li
 
 }  // namespace
 
-bool build_plan(const Shape& s, int n_sm, const int* parts, Plan* out, std::string* why) {
+bool build_plan(const Shape& s, int n_sm, const int* parts, Plan* out, std::string* why,
+                int dyn_flags) {
   std::string e = check_shape(s);
   if (!e.empty()) {
     if (why) *why = e;
@@ -287,7 +298,7 @@ bool build_plan(const Shape& s, int n_sm, const int* parts, Plan* out, std::stri
     }
   Builder bld(s, n_sm);
   for (int l = 0; l < s.L; ++l) bld.add_layer(l, parts, (l * 37) % n_sm);
-  bld.add_lm_head();
+  bld.add_lm_head((dyn_flags & MK_DYN_LMHEAD) != 0);
 
   out->n_sm = n_sm;
   for (int b = 0; b < kMaxBatch; ++b) out->parts[b] = b < s.B ? parts[b] : 0;
@@ -300,6 +311,8 @@ bool build_plan(const Shape& s, int n_sm, const int* parts, Plan* out, std::stri
   out->targets.assign(cm.count(), 0);
   for (auto& in : out->instrs)
     if (in.sig_ctr >= 0) out->targets[in.sig_ctr] += in.sig_amount;
+  // a dynamic LM head counts the rows of the tickets it runs: all V of them
+  if (dyn_flags & MK_DYN_LMHEAD) out->targets[cm.lm()] = s.V;
   for (auto& in : out->instrs)
     if (in.wait_ctr >= 0 && in.wait_target != out->targets[in.wait_ctr]) {
       if (why) *why = "internal: a wait target differs from its counter's production";
@@ -338,7 +351,7 @@ bool build_plan(const Shape& s, int n_sm, const int* parts, Plan* out, std::stri
 }
 
 bool build_plan_steps(const Shape& s, int n_sm, const int* parts, int k, Plan* out,
-                      std::string* why) {
+                      std::string* why, int dyn_flags) {
   if (k < 1 || k > kMaxLaunchSteps) {
     if (why) *why = "steps per launch out of range";
     return false;
@@ -349,7 +362,7 @@ bool build_plan_steps(const Shape& s, int n_sm, const int* parts, int k, Plan* o
   }
   std::vector<Plan> pl(k);
   for (int st = 0; st < k; ++st)
-    if (!build_plan(s, n_sm, parts + st * kMaxBatch, &pl[st], why)) return false;
+    if (!build_plan(s, n_sm, parts + st * kMaxBatch, &pl[st], why, dyn_flags)) return false;
   const int nc = (int)pl[0].targets.size();  // counters per step
   const CounterMap cm{s.L, s.nkv, s.B};
   out->n_sm = n_sm;
@@ -368,6 +381,7 @@ bool build_plan_steps(const Shape& s, int n_sm, const int* parts, int k, Plan* o
         in.layer = (int16_t)(in.layer | (st << kStepShift));
         if (in.wait_ctr >= 0) in.wait_ctr += st * nc;
         if (in.sig_ctr >= 0) in.sig_ctr += st * nc;
+        if (in.op == MK_OP_LMHEAD && in.a2 > 0) in.a2 += st * nc;  // its ticket counter
         if (st > 0 && in.op == MK_OP_QKV && layer_of(in) == 0) {
           // the token is the previous step's argmax
           in.wait_ctr = cm.lm() + (st - 1) * nc;

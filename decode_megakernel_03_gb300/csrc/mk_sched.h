@@ -32,7 +32,8 @@ struct CounterMap {
   int red(int l) const { return 2 * L + L * nkv + L * B * nkv + l; }   // B * nkv
   int hch(int l, int c) const { return 3 * L + L * nkv + L * B * nkv + l * kChunks + c; }
   int lm() const { return 3 * L + L * nkv + L * B * nkv + L * kChunks; }
-  int count() const { return lm() + 1; }
+  int dyn() const { return lm() + 1; }  // ticket counter of a dynamic LM head
+  int count() const { return lm() + 2; }
 };
 
 struct Phase {                 // one kernel of the multi-launch build
@@ -70,7 +71,9 @@ inline bool fused_reduction(const Shape& s) { return s.B == 1 && s.QD() <= 2048;
 // buffer the storer drains.
 int item_cap_for(const Shape& s);
 
-bool build_plan(const Shape& s, int n_sm, const int* parts, Plan* out, std::string* why);
+// dyn_flags: MK_DYN_* (0: every instruction a fixed work range)
+bool build_plan(const Shape& s, int n_sm, const int* parts, Plan* out, std::string* why,
+                int dyn_flags = 0);
 
 // k greedy steps in one launch (1 <= k <= kMaxLaunchSteps): the plans of the
 // steps (parts: k rows of kMaxBatch partition counts), each SM's queues
@@ -79,7 +82,7 @@ bool build_plan(const Shape& s, int n_sm, const int* parts, Plan* out, std::stri
 // step s > 0's layer-0 QKV instructions wait for step s - 1's LM head (their
 // token is its argmax). No multi-launch phases.
 bool build_plan_steps(const Shape& s, int n_sm, const int* parts, int k, Plan* out,
-                      std::string* why);
+                      std::string* why, int dyn_flags = 0);
 
 // Shared-memory layout of the interpreter for this shape: fills the n_pages,
 // off_*, *_floats and alias_xh fields of p and returns the dynamic shared

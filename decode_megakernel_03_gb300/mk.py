@@ -25,7 +25,7 @@ EXPORTS = ("mk_create", "mk_decode_step", "mk_decode_step_multilaunch", "mk_get_
            "mk_debug_inject_unsatisfiable_wait", "mk_set_trace", "mk_schedule_build",
            "mk_decode_step_noalloc", "mk_debug_use_generic_kernel", "mk_decode_greedy",
            "mk_create_paged", "mk_decode_step_paged", "mk_decode_greedy_persistent",
-           "mk_debug_permute_queues")
+           "mk_debug_permute_queues", "mk_set_dynamic", "mk_schedule_build_dynamic")
 
 MAX_STEPS_PER_LAUNCH = 32  # MK_MAX_STEPS_PER_LAUNCH
 
@@ -101,6 +101,11 @@ def lib():
         L.mk_debug_inject_unsatisfiable_wait.argtypes = [vp, ctypes.c_int]
         L.mk_debug_use_generic_kernel.argtypes = [vp, ctypes.c_int]
         L.mk_debug_permute_queues.argtypes = [vp, ctypes.c_uint32]
+        L.mk_set_dynamic.argtypes = [vp, ctypes.c_int]
+        L.mk_schedule_build_dynamic.argtypes = [ctypes.POINTER(MkConfig), ctypes.c_int, i32p,
+                                                ctypes.c_int, ctypes.POINTER(MkInstr),
+                                                ctypes.c_int, ctypes.POINTER(ctypes.c_int), i32p,
+                                                i32p, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
         L.mk_set_trace.argtypes = [vp, vp, ctypes.c_int]
         L.mk_schedule_build.argtypes = [ctypes.POINTER(MkConfig), ctypes.c_int, i32p,
                                         ctypes.POINTER(MkInstr), ctypes.c_int,
@@ -134,19 +139,25 @@ def _i32(vals):
     return a
 
 
-def schedule(shape, batch: int, capacity: int, n_sm: int, positions):
-    """Host-only schedule: (instrs structured array, sm_offsets, counter targets)."""
+DYN_LMHEAD = 1  # MK_DYN_LMHEAD
+
+
+def schedule(shape, batch: int, capacity: int, n_sm: int, positions, dyn: int = 0):
+    """Host-only schedule: (instrs structured array, sm_offsets, counter targets).
+    dyn: MK_DYN_* flags (0: the static plan)."""
     cfg = make_config(shape, batch, capacity)
     n_instr, n_ctr = ctypes.c_int(0), ctypes.c_int(0)
     pos = _i32(positions)
-    rc = lib().mk_schedule_build(ctypes.byref(cfg), n_sm, pos, None, 0, ctypes.byref(n_instr),
-                                 None, None, 0, ctypes.byref(n_ctr))
+    rc = lib().mk_schedule_build_dynamic(ctypes.byref(cfg), n_sm, pos, int(dyn), None, 0,
+                                         ctypes.byref(n_instr), None, None, 0,
+                                         ctypes.byref(n_ctr))
     _check(rc)
     instrs = (MkInstr * n_instr.value)()
     offs = (ctypes.c_int32 * (n_sm + 1))()
     tg = (ctypes.c_int32 * n_ctr.value)()
-    rc = lib().mk_schedule_build(ctypes.byref(cfg), n_sm, pos, instrs, n_instr.value,
-                                 ctypes.byref(n_instr), offs, tg, n_ctr.value, ctypes.byref(n_ctr))
+    rc = lib().mk_schedule_build_dynamic(ctypes.byref(cfg), n_sm, pos, int(dyn), instrs,
+                                         n_instr.value, ctypes.byref(n_instr), offs, tg,
+                                         n_ctr.value, ctypes.byref(n_ctr))
     _check(rc)
     arr = np.frombuffer(bytes(instrs), dtype=INSTR_DTYPE).copy()
     return arr, np.array(offs, dtype=np.int64), np.array(tg, dtype=np.int64)
@@ -297,6 +308,10 @@ class Decoder:
     def use_generic_kernel(self, enable: bool):
         """Test hook: launch the instantiation that reads the head shape at run time."""
         _check(lib().mk_debug_use_generic_kernel(self.h, int(bool(enable))), self.h)
+
+    def set_dynamic(self, flags: int):
+        """mk_set_dynamic: MK_DYN_* flags (0: the static plan)."""
+        _check(lib().mk_set_dynamic(self.h, int(flags)), self.h)
 
     def permute_queues(self, seed: int):
         """Test hook: hand the per-SM queues to the CTAs in a seeded order."""

@@ -233,7 +233,7 @@ int mk_set_trace(mk_handle* h, mk_trace_record* dev_buf, int capacity);
 #define MK_OP_RED 3   /* attention partial reduction           (instr. 3) */
 #define MK_OP_OPROJ 4 /* O-projection + residual               (instr. 4) */
 #define MK_OP_GATEUP 5 /* RMSNorm + up/gate + SiLU, one chunk  (instr. 5) */
-#define MK_OP_DOWN 6  /* down-projection (+ residual on last chunk) (instr. 6) */
+#define MK_OP_DOWN 6  /* down-projection share of one chunk of h (instr. 6) */
 #define MK_OP_LMHEAD 7 /* final RMSNorm + LM head              (instr. 7) */
 
 /* One queue entry as the host scheduler emits it (32 bytes). Exported for
@@ -244,7 +244,10 @@ int mk_set_trace(mk_handle* h, mk_trace_record* dev_buf, int capacity);
      OPROJ:  output rows [a0, a1)
      GATEUP: hidden units [a0, a1) of chunk a2
      DOWN:   output rows [a0, a1), input chunk a2
-     LMHEAD: vocabulary rows [a0, a1)
+     LMHEAD: vocabulary rows [a0, a1) (a2 = 0), or, dynamic (a2 > 0): row
+             blocks of a0 rows out of [0, a1), taken from ticket counter
+             a2 - 1 by whichever SM reaches the instruction first
+             (sig_amount is then the rows of each block it runs)
    wait_ctr < 0 means no wait; sig_ctr < 0 means no signal. */
 typedef struct {
   int16_t op, layer;
@@ -252,6 +255,22 @@ typedef struct {
   int32_t wait_ctr, wait_target;
   int32_t sig_ctr, sig_amount;
 } mk_instr;
+
+/* Dynamic work distribution ("3 · L'interpréteur sur GPU", §3.6: the
+   instructions dealt to the SMs at run time instead of by a fixed plan).
+   MK_DYN_LMHEAD: the LM head's row blocks are taken from a per-step atomic
+   ticket counter by the SMs as they reach it. Off by default (the static
+   plan); the results are the same either way (each row's arithmetic does
+   not depend on which SM computes it). Steps of a handle with a flag set run
+   the interpreter build that also carries the paged-cache and greedy code. */
+#define MK_DYN_LMHEAD 1
+int mk_set_dynamic(mk_handle* h, int flags);
+
+/* mk_schedule_build with dynamic work distribution flags (MK_DYN_*). */
+int mk_schedule_build_dynamic(const mk_config* cfg, int n_sm, const int32_t* positions,
+                              int dyn_flags, mk_instr* instrs, int instr_capacity, int* n_instr,
+                              int32_t* sm_offsets, int32_t* targets, int counter_capacity,
+                              int* n_counters);
 
 /* Host-only (no CUDA call): builds the schedule that mk_decode_step would run
    for `cfg` on n_sm SMs at these positions (host array of cfg->batch).

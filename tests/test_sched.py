@@ -340,3 +340,70 @@ def test_work_is_balanced_across_sms():
         if int(r["op"]) in rowb:
             per_sm[s] += (int(r["a1"]) - int(r["a0"])) * rowb[int(r["op"])]
     assert per_sm.max() / per_sm.mean() < 1.02
+
+
+def _simulate_dynamic(ins, off, tg, n_sm, pick):
+    """_simulate for a plan with a dynamic LM head: an SM whose head is the
+    dynamic instruction (its wait met) may take the next ticket -- a row block
+    counted into the LM head's counter -- until none is left, then moves on."""
+    ctr = np.zeros(len(tg), dtype=np.int64)
+    head = [int(off[s]) for s in range(n_sm)]
+    end = [int(off[s + 1]) for s in range(n_sm)]
+    next_ticket = 0
+    taken = np.zeros(n_sm, dtype=np.int64)
+    while any(head[s] < end[s] for s in range(n_sm)):
+        ready = []
+        for s in range(n_sm):
+            if head[s] < end[s]:
+                i = head[s]
+                c = ins["wait_ctr"][i]
+                if c < 0 or ctr[c] >= ins["wait_target"][i]:
+                    ready.append(s)
+        if not ready:
+            return False, None
+        s = pick(ready)
+        r = ins[head[s]]
+        if r["op"] == mk.OP_LMHEAD and r["a2"] > 0:
+            rows, total = int(r["a0"]), int(r["a1"])
+            if next_ticket * rows < total:
+                ctr[r["sig_ctr"]] += min(total, (next_ticket + 1) * rows) - next_ticket * rows
+                next_ticket += 1
+                taken[s] += 1
+                continue
+            head[s] += 1  # no ticket left
+            continue
+        if r["sig_ctr"] >= 0:
+            ctr[r["sig_ctr"]] += r["sig_amount"]
+        head[s] += 1
+    return np.array_equal(ctr, tg), taken
+
+
+@pytest.mark.parametrize("case", [CASES[0], CASES[2], (synth.LLAMA_1B, 1, 640, 24, [600]),
+                                  (synth.LLAMA_1B, 8, 4160, 40, list(synth.WORKLOADS["llama1b_b8"].ctx))],
+                         ids=lambda c: f"{c[0].name}-B{c[1]}-sm{c[3]}")
+def test_dynamic_lm_head_plan(case):
+    """Dynamic LM head (MK_DYN_LMHEAD): every SM's queue ends with one
+    dynamic instruction over all vocabulary rows, its counter's target is the
+    vocabulary size, and under any interleaving the SMs take every ticket
+    exactly once, the counters reach their targets and nothing deadlocks;
+    an SM that runs ahead takes more of the LM head."""
+    shape, B, S, n_sm, pos = case
+    ins, off, tg = mk.schedule(shape, B, S, n_sm, pos, dyn=mk.DYN_LMHEAD)
+    st, _, tg_static = mk.schedule(shape, B, S, n_sm, pos)
+    lm = ins[ins["op"] == mk.OP_LMHEAD]
+    assert len(lm) == n_sm and np.all(lm["a2"] > 0) and np.all(lm["a1"] == shape.vocab)
+    for s in range(n_sm):
+        q = ins[off[s]:off[s + 1]]
+        assert q[-1]["op"] == mk.OP_LMHEAD
+    np.testing.assert_array_equal(tg, tg_static)
+    # everything before the LM head is the static plan
+    np.testing.assert_array_equal(ins[ins["op"] != mk.OP_LMHEAD], st[st["op"] != mk.OP_LMHEAD])
+    rng = random.Random(3)
+    ok, taken = _simulate_dynamic(ins, off, tg, n_sm, lambda r: r[0])
+    assert ok
+    n_tickets = -(-shape.vocab // int(lm["a0"][0]))
+    assert taken.sum() == n_tickets
+    assert taken[0] > taken[-1]  # SM 0 always runs first here: it takes the most
+    for _ in range(2):
+        ok, taken = _simulate_dynamic(ins, off, tg, n_sm, lambda r: rng.choice(r))
+        assert ok and taken.sum() == n_tickets
