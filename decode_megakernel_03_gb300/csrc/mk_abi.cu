@@ -61,6 +61,7 @@ struct mk_handle {
   int max_blocks = 0;     // paged KV cache: block-table entries per sequence
   int* d_table = nullptr; // paged KV cache: the step's block table [B][max_blocks]
   int* d_ctr_steps = nullptr;  // counters of a several-step launch [kMaxLaunchSteps][n_ctr]
+  float* d_plogits = nullptr;  // prefill: the logits of every row of a chunk [B][V]
   struct StepsPlan {
     std::vector<int> key;  // steps, then each step's partition counts
     Instr* d_instrs = nullptr;
@@ -348,6 +349,7 @@ int create_impl(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
       sizeof(unsigned long long) * (size_t)MK_MAX_GREEDY_STEPS * B,      // argmax keys
       sizeof(int) * (size_t)B * std::max(1, h->max_blocks),               // block table
       sizeof(int) * (size_t)kMaxLaunchSteps * h->n_ctr,                   // several-step counters
+      sizeof(float) * (size_t)B * s.V,                                    // prefill logits
   };
   const int npieces = sizeof(sizes) / sizeof(sizes[0]);
   size_t offs[npieces], total = 0;
@@ -372,6 +374,7 @@ int create_impl(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
   h->d_keys = reinterpret_cast<unsigned long long*>(base + offs[9]);
   h->d_table = reinterpret_cast<int*>(base + offs[10]);
   h->d_ctr_steps = reinterpret_cast<int*>(base + offs[11]);
+  h->d_plogits = reinterpret_cast<float*>(base + offs[12]);
   p.block_table = nullptr;  // set per step (paged handles)
   p.max_blocks = h->max_blocks;
   p.kv_block = kv_block;
@@ -568,6 +571,58 @@ int mk_decode_step(mk_handle* h, const int32_t* tok, const int32_t* pos, float* 
   if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaLaunchCooperativeKernel");
   h->cur_set = (int)(h->steps & 1ull);
   h->steps++;
+  return MK_OK;
+}
+
+int mk_prefill(mk_handle* h, const int32_t* tokens, int n_tokens, int start_pos,
+               float* logits_out, void* stream) {
+  if (!h) return MK_ERR_INVALID;
+  if (h->kv_block) return fail(h, MK_ERR_INVALID, "paged handle: prefill needs contiguous caches");
+  const int B = h->shape.B;
+  if (!tokens || n_tokens < 1) return fail(h, MK_ERR_INVALID, "tokens must be non-NULL, n_tokens >= 1");
+  const int chunks = (n_tokens + B - 1) / B;
+  if (start_pos < 0 || (long)start_pos + (long)chunks * B > h->shape.S)
+    return fail(h, MK_ERR_INVALID,
+                "start_pos + n_tokens rounded up to whole chunks of batch rows must fit kv_capacity");
+  for (int i = 0; i < n_tokens; ++i)
+    if (tokens[i] < 0 || tokens[i] >= h->shape.V)
+      return fail(h, MK_ERR_INVALID, "token id out of range [0, vocab)");
+  if (!logits_out || !aligned16(logits_out))
+    return fail(h, MK_ERR_INVALID, "logits must be 16-byte aligned");
+  int rc = check_sticky(h);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  for (int c = 0; c < chunks; ++c) {
+    // row b: token c * B + b at position start_pos + c * B + b; the rows past
+    // the last token (a partial last chunk) repeat it at the positions after
+    // the prompt, whose cache slots the decode steps that follow overwrite
+    // before anything reads them
+    int32_t tk[kMaxBatch], ps[kMaxBatch];
+    for (int b = 0; b < B; ++b) {
+      const int i = std::min(c * B + b, n_tokens - 1);
+      tk[b] = tokens[i];
+      ps[b] = start_pos + c * B + b;
+    }
+    PlanEntry* e = nullptr;
+    rc = get_plan(h, ps, &e, 0);
+    if (rc) return rc;
+    Params p = step_params(h, tk, ps, h->d_plogits);
+    p.prefill = 1;
+    p.instrs = e->d_instrs;
+    p.sm_off = e->d_sm_off;
+    p.no_waits = 0;
+    p.trace_base = 0;
+    void* args[] = {&p};
+    cudaError_t ce = cudaLaunchCooperativeKernel(h->fn, dim3(h->n_sm), dim3(kThreads), args,
+                                                 (size_t)h->smem_bytes, st);
+    if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaLaunchCooperativeKernel");
+    h->cur_set = (int)(h->steps & 1ull);
+    h->steps++;
+  }
+  // the last prompt token's row of the last chunk
+  const int last_row = (n_tokens - 1) - (chunks - 1) * B;
+  MK_CUDA(h, cudaMemcpyAsync(logits_out, h->d_plogits + (size_t)last_row * h->shape.V,
+                             sizeof(float) * (size_t)h->shape.V, cudaMemcpyDeviceToDevice, st));
   return MK_OK;
 }
 

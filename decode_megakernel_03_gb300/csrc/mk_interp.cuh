@@ -273,6 +273,7 @@ __device__ __forceinline__ RowSrc row_src_of(const Params& p, const Instr& in) {
 // greedy-decode code; kFxDyn: dynamic work distribution.
 template <int FX>
 __device__ __forceinline__ size_t kv_row(const Params& p, int b, int g, int t) {
+  if (p.prefill) b = 0;  // every row of a prefill chunk is sequence 0
   if (!(FX & kFxPaged) || !p.block_table) return (((size_t)b * p.nkv + g) * (size_t)p.S + t) * p.D;
   const int blk = __ldg(p.block_table + b * p.max_blocks + t / p.kv_block);
   return (((size_t)blk * p.nkv + g) * p.kv_block + t % p.kv_block) * p.D;
@@ -384,6 +385,17 @@ static __device__ void loader_role(const Params& p, Misc* m, uint8_t* smem, cons
           fence_proxy_async_global();
           acq_step = st;
         }
+      }
+      // prefill: the unit's keys include the chunk's own, which this step's
+      // QKV instructions write: fetch them after the unit's counter (every
+      // QKV instruction precedes this one in every SM's queue, so the wait
+      // ends), then order the acquire before the bulk copies' reads
+      if (p.prefill && !p.no_waits && sp.nc > 0) {
+        if (!wait_counter(p, m, in.wait_ctr, in.wait_target)) {
+          ok = false;
+          break;
+        }
+        fence_proxy_async_global();
       }
       // paged cache: the table entries of the unit's cached keys, in one
       // bulk copy (a 16-byte aligned window of at most kBtCache entries;

@@ -103,6 +103,11 @@ struct Params {
   // argmax_out[(s - 1) * B + b]; counters of step s are offset by
   // s * n_ctr_step; lm_ctr is the LM head's counter of step 0
   int n_ctr_step, lm_ctr;
+  // prefill: the B rows are consecutive tokens of ONE sequence (cache
+  // sequence 0, positions pos[0] < pos[1] < ...), each attending causally
+  // to the keys before it, the chunk's own included; the loader fetches an
+  // attention unit's keys after the unit's counter (they may be this step's)
+  int prefill;
   // per step
   int tok[kMaxBatch];
   int pos[kMaxBatch];

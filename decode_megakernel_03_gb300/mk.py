@@ -25,7 +25,8 @@ EXPORTS = ("mk_create", "mk_decode_step", "mk_decode_step_multilaunch", "mk_get_
            "mk_debug_inject_unsatisfiable_wait", "mk_set_trace", "mk_schedule_build",
            "mk_decode_step_noalloc", "mk_debug_use_generic_kernel", "mk_decode_greedy",
            "mk_create_paged", "mk_decode_step_paged", "mk_decode_greedy_persistent",
-           "mk_debug_permute_queues", "mk_set_dynamic", "mk_schedule_build_dynamic")
+           "mk_debug_permute_queues", "mk_set_dynamic", "mk_schedule_build_dynamic",
+           "mk_prefill")
 
 MAX_STEPS_PER_LAUNCH = 32  # MK_MAX_STEPS_PER_LAUNCH
 
@@ -102,6 +103,7 @@ def lib():
         L.mk_debug_use_generic_kernel.argtypes = [vp, ctypes.c_int]
         L.mk_debug_permute_queues.argtypes = [vp, ctypes.c_uint32]
         L.mk_set_dynamic.argtypes = [vp, ctypes.c_int]
+        L.mk_prefill.argtypes = [vp, i32p, ctypes.c_int, ctypes.c_int, vp, vp]
         L.mk_schedule_build_dynamic.argtypes = [ctypes.POINTER(MkConfig), ctypes.c_int, i32p,
                                                 ctypes.c_int, ctypes.POINTER(MkInstr),
                                                 ctypes.c_int, ctypes.POINTER(ctypes.c_int), i32p,
@@ -250,6 +252,15 @@ class Decoder:
     def step(self, tokens, positions, logits, stream=None) -> int:
         rc = lib().mk_decode_step(self.h, _i32(tokens), _i32(positions),
                                   ctypes.c_void_p(logits.data_ptr()), _stream_ptr(stream))
+        _check(rc, self.h)
+        return rc
+
+    def prefill(self, tokens, start_pos: int, logits, stream=None) -> int:
+        """mk_prefill: the prompt into sequence 0 of the cache, in chunks of
+        `batch` tokens; logits (device fp32 [vocab]) receives the logits after
+        the last prompt token."""
+        rc = lib().mk_prefill(self.h, _i32(tokens), len(tokens), int(start_pos),
+                              ctypes.c_void_p(logits.data_ptr()), _stream_ptr(stream))
         _check(rc, self.h)
         return rc
 

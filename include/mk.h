@@ -118,6 +118,25 @@ int mk_decode_step_paged(mk_handle* h, const int32_t* token_ids, const int32_t* 
 int mk_decode_step(mk_handle* h, const int32_t* token_ids, const int32_t* positions,
                    float* logits_out, void* stream);
 
+/* Prefill of a prompt of n_tokens tokens into sequence 0 of the handle's
+   cache, at positions start_pos .. start_pos + n_tokens - 1, in chunks of
+   `batch` tokens (the handle's batch size): each chunk is ONE interpreter
+   launch in which the batch rows are the chunk's consecutive tokens of that
+   one sequence. Every GEMV of the step is then a small GEMM over the chunk's
+   tokens on the tensor cores, and each token attends causally to the keys
+   before it, the chunk's own included ("9 · Quand ne pas le faire", §9.1,
+   prefill; "3 · L'interpréteur sur GPU", §3.2, the same instructions).
+   tokens: HOST int32 [n_tokens]. The k/v rows of every prompt token are
+   written into cache sequence 0; a partial last chunk is padded with rows at
+   the positions after the prompt (start_pos + n_tokens rounded up to whole
+   chunks must fit kv_capacity), whose slots the next decode steps overwrite
+   before reading them. logits_out: DEVICE fp32 [vocab], the logits after
+   the last prompt token. Asynchronous on `stream`. Errors as
+   mk_decode_step, and MK_ERR_INVALID for a paged handle or out-of-range
+   arguments (before any launch). */
+int mk_prefill(mk_handle* h, const int32_t* tokens, int n_tokens, int start_pos,
+               float* logits_out, void* stream);
+
 /* Greedy decode of n_steps tokens per sequence in one call, the next token
    fed back on the device (no host round trip between steps): step s
    (0 <= s < n_steps) consumes token_ids[b] (s = 0, HOST) or the argmax of
