@@ -133,6 +133,106 @@ def cpu_oracle_rate(wl, w_host, target_s=12.0, max_steps=64):
     return n * wl.batch / dt, n, dt, threads
 
 
+def oracle_timings(names=("tiny", "llama1b", "llama8b"), steps=2):
+    """The oracle as it stands, timed on this host: one decode step of each
+    workload (its first teacher-forced step, on its seeded context) with one
+    thread and with every host thread. Prints one JSON line."""
+    from oracle import oracle as O
+    from decode_megakernel_03_gb300 import synth
+    out = {"kind": "oracle", "cores": O.default_threads(), "workloads": {}}
+    for name in names:
+        wl = synth.WORKLOADS[name]
+        w = synth.make_weights(wl.shape, seed=wl.weight_seed)
+        model = O.Model(wl.shape.as_dict(), synth.oracle_weights(w))
+        del w
+        kc, vc = synth.make_kv(wl.shape, wl.batch, wl.capacity, wl.ctx, seed=wl.kv_seed)
+        ks = [synth.bits(t).copy() for t in kc]
+        vs = [synth.bits(t).copy() for t in vc]
+        toks = synth.step_tokens(wl)
+        res = {}
+        for threads in (1, O.default_threads()):
+            dt = []
+            for s in range(steps):
+                t0 = time.perf_counter()
+                model.decode_step(ks, vs, [int(t) for t in toks[s]], synth.step_positions(wl, s),
+                                  nthreads=threads)
+                dt.append(time.perf_counter() - t0)
+            res[f"s_per_step_{threads}_threads"] = min(dt)
+        res["tokens_per_s_all_threads"] = wl.batch / res[f"s_per_step_{O.default_threads()}_threads"]
+        out["workloads"][name] = res
+        print(name, res, file=sys.stderr, flush=True)
+    print(json.dumps(out), flush=True)
+
+
+def trace_summary(args, wl):
+    """One decode step of the workload with the per-instruction trace on
+    (mk_set_trace), summarised: per layer the time from its QKV's ready to the
+    next layer's, per instruction kind the mean staging, compute, page-wait
+    and publication times, the dependency hops (consumer ready - last
+    producer published), and the LM head's span. Prints one JSON line."""
+    import numpy as np
+    import torch
+    from decode_megakernel_03_gb300 import build as mkbuild
+    from decode_megakernel_03_gb300 import mk, synth
+    mkbuild.build()
+    dev = torch.device("cuda")
+    shape = wl.shape
+    w = synth.make_weights(shape, seed=wl.weight_seed, device=dev)
+    kc, vc = synth.make_kv(shape, wl.batch, wl.capacity, wl.ctx, seed=wl.kv_seed, device=dev)
+    dec = mk.Decoder(shape, w, kc, vc, wl.batch)
+    logits = torch.empty((wl.batch, shape.vocab), dtype=torch.float32, device=dev)
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    tok = [int(t) for t in synth.step_tokens(wl)[0]]
+    pos = synth.step_positions(wl, 0)
+    ins, off, _ = mk.schedule(shape, wl.batch, wl.capacity, n_sm, pos)
+    buf = torch.zeros(len(ins) * mk.TRACE_DTYPE.itemsize, dtype=torch.uint8, device=dev)
+    for _ in range(5):
+        dec.step(tok, pos, logits)
+    dec.set_trace(buf)
+    dec.step(tok, pos, logits)
+    torch.cuda.synchronize()
+    assert dec.status() == mk.MK_OK, dec.last_error()
+    dec.set_trace(None)
+    dec.close()
+    rec = np.frombuffer(buf.cpu().numpy().tobytes(), dtype=mk.TRACE_DTYPE)
+    t0 = rec["t_start"].min()
+    us = lambda a: (a.astype(np.float64) - t0) / 1e3
+    ts, tr, te, tst = us(rec["t_start"]), us(rec["t_ready"]), us(rec["t_end"]), us(rec["t_stored"])
+    op, layer = rec["op"], rec["layer"]
+    L = shape.n_layers
+    ready = [float(tr[(layer == l) & (op == mk.OP_QKV)].min()) for l in range(L)]
+    lm = op == mk.OP_LMHEAD
+    ready.append(float(tr[lm].min()))
+    out = {"workload": wl.name, "step_us": float(te.max()), "layer_us": np.diff(ready).round(2).tolist(),
+           "lm_head_us": float(te[lm].max() - tr[lm].min()), "per_op": {}, "hops_us": {}}
+    mid = (layer >= 2) & (layer < L - 2)
+    for o, name in mk.OPS.items():
+        m = (op == o) & (mid | (o == mk.OP_LMHEAD))
+        if not m.any():
+            continue
+        out["per_op"][name] = {
+            "n": int(m.sum()),
+            "stage_us": float(rec["stage_ns"][m].mean() / 1e3),
+            "ready_to_end_us": float(np.mean(te[m] - tr[m])),
+            "page_wait_us": float(rec["page_wait_ns"][m].mean() / 1e3),
+            "end_to_published_us": float(np.mean(tst[m] - te[m])),
+            "idle_before_start_us": float(np.mean(tr[m] - ts[m])),
+        }
+    prod = {}
+    for k in range(len(ins)):
+        c = int(ins["sig_ctr"][k])
+        if c >= 0:
+            prod[c] = max(prod.get(c, -1e18), tst[k])
+    hops = {}
+    for k in range(len(ins)):
+        c = int(ins["wait_ctr"][k])
+        if c >= 0 and c in prod and mid[k]:
+            hops.setdefault(mk.OPS[int(ins["op"][k])], []).append(tr[k] - prod[c])
+    out["hops_us"] = {k: {"median": float(np.median(v)), "p90": float(np.percentile(v, 90))}
+                      for k, v in hops.items()}
+    print(json.dumps(out), flush=True)
+
+
 def replica_env():
     """(world, rank, local rank) from the launcher's environment; one rank
     and no process group without torchrun."""
@@ -344,6 +444,43 @@ def run_gpu(args, wl):
     dp.close()
     del kp, vp
 
+    # host side of a step (no device work timed): the C-ABI call with its plan
+    # cached (argument checks, plan lookup, launch), and building a plan
+    # (the host scheduler alone, what a plan miss adds before its upload)
+    n_sm = torch.cuda.get_device_properties(local).multi_processor_count
+    t, p = tok_pos(0)
+    torch.cuda.synchronize()
+    reps = 200
+    t0h = time.perf_counter()
+    for _ in range(reps):
+        dec.step(t, p, logits)
+    host_call_us = (time.perf_counter() - t0h) / reps * 1e6
+    torch.cuda.synchronize()
+    t0h = time.perf_counter()
+    for _ in range(20):
+        mk.schedule(shape, wl.batch, wl.capacity, n_sm, p)
+    host_plan_us = (time.perf_counter() - t0h) / 20 * 1e6
+
+    # prefill through mk_prefill: a 512-token prompt of this model in chunks of
+    # 8 tokens (a batch-8 handle on its own cache), tokens/s
+    prefill_tps = None
+    if wl.batch == 1 and shape.name.startswith("llama-3.2-1b"):
+        kp, vp = synth.empty_kv(shape, 8, 640, device=dev)
+        dpre = mk.Decoder(shape, w, kp, vp, 8)
+        plog = torch.empty(shape.vocab, dtype=torch.float32, device=dev)
+        prompt = [int(x) for x in synth.make_tokens(shape.vocab, 512, seed=5)]
+        dpre.prefill(prompt, 0, plog)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(3):
+            dpre.prefill(prompt, 0, plog)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        assert dpre.status() == mk.MK_OK, dpre.last_error()
+        prefill_tps = 512 * 3 / (e0.elapsed_time(e1) * 1e-3)
+        dpre.close()
+        del kp, vp
+
     ms = sum(per_mega) / K
     ms_all = max_over_ranks(ms, world, dev)
 
@@ -415,6 +552,10 @@ def run_gpu(args, wl):
                 "greedy_one_launch_us_per_step": greedy_one_ms * 1e3,
                 "paged_kv_us_per_step": paged_ms * 1e3,
                 "paged_kv_block_size": bs,
+                "host_step_call_us": host_call_us,
+                "host_plan_build_us": host_plan_us,
+                "prefill_tokens_per_s": prefill_tps,
+                "prefill_chunk": 8,
             },
         }
         print(json.dumps(line), flush=True)
@@ -463,7 +604,18 @@ def main():
     ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
     ap.add_argument("--workload", default="llama1b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--trace", action="store_true",
+                    help="summarise the per-instruction trace of one step of --workload")
+    ap.add_argument("--oracle-timings", action="store_true",
+                    help="time the CPU oracle (1 and all host threads) on tiny, 1B and 8B; no GPU")
     args = ap.parse_args()
+    if args.oracle_timings:
+        oracle_timings()
+        return
+    if args.trace:
+        from decode_megakernel_03_gb300 import synth as _s
+        trace_summary(args, _s.WORKLOADS[args.workload])
+        return
     from decode_megakernel_03_gb300 import synth
     wl = synth.WORKLOADS[args.workload]
     if args.warmup < 3 and args.impl != "reference":
