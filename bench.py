@@ -412,6 +412,29 @@ def run_gpu(args, wl):
     torch.cuda.synchronize()
     assert dec.status() == mk.MK_OK, dec.last_error()
     greedy_one_ms = e0.elapsed_time(e1) / (g_calls * g_steps)
+    # the same greedy decode as a host loop: one step per call, the logits read
+    # back and their argmax taken on the host before the next call (what the
+    # device-fed argmax removes), wall-clock tokens/s of 32 steps
+    def host_loop(n):
+        tk = [int(x) for x in t0_]
+        for s_ in range(n):
+            dec.step(tk, [q + s_ for q in p0_], logits)
+            host = logits.cpu()
+            tk = [int(i) for i in torch.argmax(host, dim=1)]
+        return tk
+    host_loop(4)
+    torch.cuda.synchronize()
+    t0w = time.perf_counter()
+    host_loop(32)
+    host_loop_tps = 32 * wl.batch / (time.perf_counter() - t0w)
+    # one-launch greedy, 32 steps per call, tokens read back, wall clock
+    tok32 = torch.empty(32 * wl.batch, dtype=torch.int32, device=dev)
+    dec.decode_greedy_persistent(t0_, p0_, 32, tok32, logits)
+    torch.cuda.synchronize()
+    t0w = time.perf_counter()
+    dec.decode_greedy_persistent(t0_, p0_, 32, tok32, logits)
+    tok32.cpu()
+    greedy32_tps = 32 * wl.batch / (time.perf_counter() - t0w)
 
     # the same steps on a paged KV cache: the caches' contents in pools of
     # 16-position blocks in shuffled order, a host block table per step
@@ -550,6 +573,8 @@ def run_gpu(args, wl):
                 "greedy_us_per_step": greedy_ms * 1e3,
                 "greedy_steps_per_call": g_steps,
                 "greedy_one_launch_us_per_step": greedy_one_ms * 1e3,
+                "greedy_32_one_launch_tokens_per_s": greedy32_tps,
+                "greedy_32_host_argmax_loop_tokens_per_s": host_loop_tps,
                 "paged_kv_us_per_step": paged_ms * 1e3,
                 "paged_kv_block_size": bs,
                 "host_step_call_us": host_call_us,
