@@ -875,6 +875,45 @@ int mk_schedule_build_dynamic(const mk_config* cfg, int n_sm, const int32_t* pos
 }
 
 
+int mk_schedule_build_steps(const mk_config* cfg, int n_sm, const int32_t* positions, int n_steps,
+                            mk_instr* instrs, int instr_capacity, int* n_instr,
+                            int32_t* sm_offsets, int32_t* targets, int counter_capacity,
+                            int* n_counters) {
+  int rc = check_config(cfg, nullptr);
+  if (rc) return rc;
+  if (n_sm < 1 || !positions) return fail(nullptr, MK_ERR_INVALID, "n_sm / positions");
+  if (n_steps < 1 || n_steps > MK_MAX_STEPS_PER_LAUNCH)
+    return fail(nullptr, MK_ERR_INVALID, "n_steps must be in [1, MK_MAX_STEPS_PER_LAUNCH]");
+  Shape s = shape_of(*cfg);
+  for (int b = 0; b < s.B; ++b)
+    if (positions[b] < 0 || positions[b] + n_steps - 1 >= s.S)
+      return fail(nullptr, MK_ERR_INVALID, "positions + n_steps - 1 must be in [0, kv_capacity)");
+  std::vector<int> parts((size_t)n_steps * kMaxBatch, 0);
+  for (int st = 0; st < n_steps; ++st) {
+    int32_t ps[kMaxBatch] = {0};
+    for (int b = 0; b < s.B; ++b) ps[b] = positions[b] + st;
+    choose_partitions(s, n_sm, ps, parts.data() + (size_t)st * kMaxBatch);
+  }
+  Plan P;
+  std::string why;
+  if (!build_plan_steps(s, n_sm, parts.data(), n_steps, &P, &why))
+    return fail(nullptr, MK_ERR_INVALID, why);
+  if (n_instr) *n_instr = (int)P.instrs.size();
+  if (n_counters) *n_counters = (int)P.targets.size();
+  if (instrs) {
+    if (instr_capacity < (int)P.instrs.size())
+      return fail(nullptr, MK_ERR_INVALID, "instruction capacity too small");
+    std::memcpy(instrs, P.instrs.data(), sizeof(Instr) * P.instrs.size());
+  }
+  if (sm_offsets) std::memcpy(sm_offsets, P.sm_off.data(), sizeof(int) * P.sm_off.size());
+  if (targets) {
+    if (counter_capacity < (int)P.targets.size())
+      return fail(nullptr, MK_ERR_INVALID, "counter capacity too small");
+    std::memcpy(targets, P.targets.data(), sizeof(int) * P.targets.size());
+  }
+  return MK_OK;
+}
+
 int mk_schedule_build(const mk_config* cfg, int n_sm, const int32_t* positions, mk_instr* instrs,
                       int instr_capacity, int* n_instr, int32_t* sm_offsets, int32_t* targets,
                       int counter_capacity, int* n_counters) {

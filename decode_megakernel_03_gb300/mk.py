@@ -26,7 +26,7 @@ EXPORTS = ("mk_create", "mk_decode_step", "mk_decode_step_multilaunch", "mk_get_
            "mk_decode_step_noalloc", "mk_debug_use_generic_kernel", "mk_decode_greedy",
            "mk_create_paged", "mk_decode_step_paged", "mk_decode_greedy_persistent",
            "mk_debug_permute_queues", "mk_set_dynamic", "mk_schedule_build_dynamic",
-           "mk_prefill")
+           "mk_schedule_build_steps", "mk_prefill")
 
 MAX_STEPS_PER_LAUNCH = 32  # MK_MAX_STEPS_PER_LAUNCH
 
@@ -104,6 +104,10 @@ def lib():
         L.mk_debug_permute_queues.argtypes = [vp, ctypes.c_uint32]
         L.mk_set_dynamic.argtypes = [vp, ctypes.c_int]
         L.mk_prefill.argtypes = [vp, i32p, ctypes.c_int, ctypes.c_int, vp, vp]
+        L.mk_schedule_build_steps.argtypes = [ctypes.POINTER(MkConfig), ctypes.c_int, i32p,
+                                              ctypes.c_int, ctypes.POINTER(MkInstr),
+                                              ctypes.c_int, ctypes.POINTER(ctypes.c_int), i32p,
+                                              i32p, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
         L.mk_schedule_build_dynamic.argtypes = [ctypes.POINTER(MkConfig), ctypes.c_int, i32p,
                                                 ctypes.c_int, ctypes.POINTER(MkInstr),
                                                 ctypes.c_int, ctypes.POINTER(ctypes.c_int), i32p,
@@ -160,6 +164,26 @@ def schedule(shape, batch: int, capacity: int, n_sm: int, positions, dyn: int = 
     rc = lib().mk_schedule_build_dynamic(ctypes.byref(cfg), n_sm, pos, int(dyn), instrs,
                                          n_instr.value, ctypes.byref(n_instr), offs, tg,
                                          n_ctr.value, ctypes.byref(n_ctr))
+    _check(rc)
+    arr = np.frombuffer(bytes(instrs), dtype=INSTR_DTYPE).copy()
+    return arr, np.array(offs, dtype=np.int64), np.array(tg, dtype=np.int64)
+
+
+def schedule_steps(shape, batch: int, capacity: int, n_sm: int, positions, n_steps: int):
+    """Host-only schedule of n_steps greedy steps in one launch (the plan of
+    mk_decode_greedy_persistent): (instrs, sm_offsets, counter targets)."""
+    cfg = make_config(shape, batch, capacity)
+    n_instr, n_ctr = ctypes.c_int(0), ctypes.c_int(0)
+    pos = _i32(positions)
+    rc = lib().mk_schedule_build_steps(ctypes.byref(cfg), n_sm, pos, int(n_steps), None, 0,
+                                       ctypes.byref(n_instr), None, None, 0, ctypes.byref(n_ctr))
+    _check(rc)
+    instrs = (MkInstr * n_instr.value)()
+    offs = (ctypes.c_int32 * (n_sm + 1))()
+    tg = (ctypes.c_int32 * n_ctr.value)()
+    rc = lib().mk_schedule_build_steps(ctypes.byref(cfg), n_sm, pos, int(n_steps), instrs,
+                                       n_instr.value, ctypes.byref(n_instr), offs, tg,
+                                       n_ctr.value, ctypes.byref(n_ctr))
     _check(rc)
     arr = np.frombuffer(bytes(instrs), dtype=INSTR_DTYPE).copy()
     return arr, np.array(offs, dtype=np.int64), np.array(tg, dtype=np.int64)

@@ -304,6 +304,20 @@ int mk_schedule_build(const mk_config* cfg, int n_sm, const int32_t* positions,
                       int32_t* sm_offsets, int32_t* targets, int counter_capacity,
                       int* n_counters);
 
+/* Host-only (no CUDA call): the schedule that mk_decode_greedy_persistent
+   runs for n_steps steps (1 <= n_steps <= MK_MAX_STEPS_PER_LAUNCH) from these
+   positions: each SM's queue holds the steps one after the other; an
+   instruction's step is (layer >> 10) & 31 and its layer layer & 1023;
+   counters of step s are those of one step offset by s times the per-step
+   count (targets has n_steps times that many entries); step s > 0's layer-0
+   QKV instructions wait for step s - 1's LM head. Outputs, capacities and
+   errors as for mk_schedule_build; MK_ERR_INVALID also when n_steps is out of
+   range or a position + n_steps - 1 reaches kv_capacity. */
+int mk_schedule_build_steps(const mk_config* cfg, int n_sm, const int32_t* positions, int n_steps,
+                            mk_instr* instrs, int instr_capacity, int* n_instr,
+                            int32_t* sm_offsets, int32_t* targets, int counter_capacity,
+                            int* n_counters);
+
 /* ---- decode step without any allocation -------------------------------- */
 
 /* The pages have no counterpart of this call; it exists for callers that may

@@ -407,3 +407,277 @@ def test_dynamic_lm_head_plan(case):
     for _ in range(2):
         ok, taken = _simulate_dynamic(ins, off, tg, n_sm, lambda r: rng.choice(r))
         assert ok and taken.sum() == n_tickets
+
+
+# ---------------------------------------------------------------------------
+# A model of the three warp roles of every SM, not only of the instruction
+# waits: the loader issues each instruction's pages in queue order into a ring
+# of `ring` slots (a slot frees when the compute warps have read its page),
+# and holds -- issues no page of a later instruction -- while a
+# latency-critical instruction (attention, O-projection, last chunk of the
+# down-projection) is being computed and not yet published; in a prefill step
+# it fetches an attention unit's keys only once the unit's counter is met.
+# The compute warps raise the hold on reaching a critical instruction (before
+# its waits), run an instruction once its counter is met and one of the
+# kResBufs result buffers is free, and read its pages as they arrive. The
+# storer publishes the computed instructions in order.
+
+RESBUFS = 4
+
+
+def _pages(r, shape, B, pos):
+    """Pages the loader issues for instruction r (the kernel's page geometry)."""
+    op, a0, a1, a2 = int(r["op"]), int(r["a0"]), int(r["a1"]), int(r["a2"])
+    H, D, QD, Fc = shape.hidden, shape.head_dim, shape.n_heads * shape.head_dim, shape.ffn // 4
+    if op == mk.OP_ATTN:
+        p = pos[a0] + ((int(r["layer"]) >> 10) & 31)
+        pidx, P = a2 >> 16, a2 & 0xFFFF
+        t0, t1 = pidx * (p + 1) // P, (pidx + 1) * (p + 1) // P
+        nc = max(0, min(t1, p) - t0)
+        kpp = 16384 // (4 * D)
+        return -(-nc // kpp)
+    if op == mk.OP_RED:
+        return 0
+    K = {mk.OP_QKV: H, mk.OP_OPROJ: QD, mk.OP_GATEUP: H, mk.OP_DOWN: Fc, mk.OP_LMHEAD: H}[op]
+    R = 2 if op in (mk.OP_QKV, mk.OP_GATEUP) else 1
+    ipp = 16384 // (R * K * 2)
+    return -(-(a1 - a0) // ipp)
+
+
+def _critical(r):
+    return r["op"] in (mk.OP_ATTN, mk.OP_OPROJ) or (r["op"] == mk.OP_DOWN and r["a2"] == 3)
+
+
+def _simulate_roles(ins, off, tg, n_sm, shape, B, pos, ring, pick, prefill=False,
+                    hold_own_pages=False, lm_of_step=None):
+    """Runs the role model; returns True when every queue completes with the
+    counters at their targets, False on a deadlock (no role can move).
+    lm_of_step: for a plan of several steps in one launch, the LM-head counter
+    of each step; the loader fetches a step s > 0 attention unit's keys only
+    once step s - 1's LM head is complete (its keys were written by step
+    s - 1). hold_own_pages plants a mistake for the model's own check: the
+    hold also stops the pages of the critical instruction itself."""
+    ctr = np.zeros(len(tg), dtype=np.int64)
+    pages = [[_pages(ins[i], shape, B, pos) for i in range(int(off[s]), int(off[s + 1]))]
+             for s in range(n_sm)]
+    n = [int(off[s + 1] - off[s]) for s in range(n_sm)]
+    lp = [0] * n_sm      # loader: instruction, pages issued of it
+    lpg = [0] * n_sm
+    issued = [0] * n_sm  # pages issued in total
+    used = [0] * n_sm    # pages read by the compute warps in total
+    cp = [0] * n_sm      # compute: instruction, and whether its wait is met
+    cwait = [False] * n_sm
+    cpg = [0] * n_sm     # pages of it read
+    sp = [0] * n_sm      # storer: instructions published
+    hold = [-1] * n_sm
+
+    def I(s, k):
+        return ins[int(off[s]) + k]
+
+    def met(r):
+        c = int(r["wait_ctr"])
+        return c < 0 or ctr[c] >= r["wait_target"]
+
+    def enter(s):
+        if cp[s] < n[s] and _critical(I(s, cp[s])):
+            hold[s] = cp[s]
+
+    for s in range(n_sm):
+        enter(s)
+
+    while any(sp[s] < n[s] for s in range(n_sm)):
+        acts = []
+        for s in range(n_sm):
+            # loader: the next page
+            if lp[s] < n[s]:
+                if lpg[s] >= pages[s][lp[s]]:
+                    acts.append(("ladv", s))
+                else:
+                    h = hold[s]
+                    held = h >= 0 and sp[s] <= h and (lp[s] > h or (hold_own_pages and lp[s] == h))
+                    r = I(s, lp[s])
+                    gated = prefill and r["op"] == mk.OP_ATTN and not met(r)
+                    st = (int(r["layer"]) >> 10) & 31
+                    if lm_of_step is not None and r["op"] == mk.OP_ATTN and st > 0:
+                        c = lm_of_step[st - 1]
+                        gated = gated or ctr[c] < tg[c]
+                    if issued[s] - used[s] < ring and not held and not gated:
+                        acts.append(("load", s))
+            # compute
+            if cp[s] < n[s]:
+                r = I(s, cp[s])
+                if not cwait[s]:
+                    if met(r) and cp[s] - sp[s] < RESBUFS:
+                        acts.append(("cwait", s))
+                elif cpg[s] < pages[s][cp[s]]:
+                    if used[s] < issued[s]:
+                        acts.append(("use", s))
+                else:
+                    acts.append(("cdone", s))
+            # storer
+            if sp[s] < cp[s]:
+                acts.append(("store", s))
+        if not acts:
+            return False
+        kind, s = pick(acts)
+        if kind == "ladv":
+            lp[s] += 1
+            lpg[s] = 0
+        elif kind == "load":
+            # every page that fits: the ring state after a run of single
+            # issues, with fewer interleavings to walk through
+            k = min(pages[s][lp[s]] - lpg[s], ring - (issued[s] - used[s]))
+            lpg[s] += k
+            issued[s] += k
+        elif kind == "cwait":
+            cwait[s] = True
+        elif kind == "use":
+            k = min(pages[s][cp[s]] - cpg[s], issued[s] - used[s])
+            cpg[s] += k
+            used[s] += k
+        elif kind == "cdone":
+            cp[s] += 1
+            cwait[s] = False
+            cpg[s] = 0
+            enter(s)
+        else:
+            r = I(s, sp[s])
+            if r["sig_ctr"] >= 0:
+                ctr[r["sig_ctr"]] += r["sig_amount"]
+            sp[s] += 1
+    return bool(np.array_equal(ctr, tg))
+
+
+ROLE_CASES = [
+    (synth.TINY, 1, 128, 8, [70], 12),
+    (synth.TINY, 2, 128, 5, [3, 127], 6),
+    (synth.TINY, 8, 128, 7, [5 * b + 1 for b in range(8)], 6),
+    (synth.LLAMA_1B, 1, 640, 24, [600], 6),
+    (synth.LLAMA_8B, 1, 2112, 16, [2048], 12),
+]
+
+
+@pytest.mark.parametrize("case", ROLE_CASES, ids=lambda c: f"{c[0].name}-B{c[1]}-sm{c[3]}-ring{c[5]}")
+def test_roles_cannot_deadlock(case):
+    """Loader, compute warps and storer of every SM, with the page ring, the
+    result buffers and the loader's hold: every random interleaving finishes
+    and the counters reach their targets."""
+    shape, B, S, n_sm, pos, ring = case
+    ins, off, tg, sm = _plan(shape, B, S, n_sm, pos)
+    rng = random.Random(11)
+    picks = [lambda a: a[0], lambda a: rng.choice(a)]
+    if shape is synth.TINY:
+        picks += [lambda a: a[-1]] + [lambda a: rng.choice(a)] * 3
+    for pick in picks:
+        assert _simulate_roles(ins, off, tg, n_sm, shape, B, pos, ring, pick)
+
+
+def test_roles_prefill_cannot_deadlock():
+    """A prefill step (the batch rows are consecutive tokens of one sequence):
+    the loader also waits for each attention unit's counter before its keys."""
+    shape = synth.TINY
+    pos = [40 + b for b in range(8)]
+    ins, off, tg, sm = _plan(shape, 8, 128, 6, pos)
+    rng = random.Random(12)
+    for pick in (lambda a: a[0], lambda a: a[-1], lambda a: rng.choice(a)):
+        assert _simulate_roles(ins, off, tg, 6, shape, 8, pos, 6, pick, prefill=True)
+
+
+def test_role_model_detects_a_hold_on_the_critical_instructions_own_pages():
+    """The same model deadlocks when the hold also stops the critical
+    instruction's own pages: its compute waits for pages the loader will not
+    issue until the instruction is published."""
+    shape, pos = synth.LLAMA_1B, [600]
+    ins, off, tg, sm = _plan(shape, 1, 640, 24, pos)
+    assert not _simulate_roles(ins, off, tg, 24, shape, 1, pos, 12, lambda a: a[0],
+                               hold_own_pages=True)
+
+
+# ---------------------------------------------------------------------------
+# Several greedy steps in one launch (the plan of mk_decode_greedy_persistent)
+
+STEP_CASES = [
+    (synth.TINY, 2, 128, 5, [3, 60], 3),
+    (synth.TINY, 1, 128, 8, [0], 4),
+    (synth.TINY, 8, 128, 7, [5 * b + 1 for b in range(8)], 2),
+    (synth.LLAMA_1B, 1, 640, 24, [500], 2),
+]
+
+
+def _lm_counter(shape, B):
+    L, nkv = shape.n_layers, shape.n_kv_heads
+    return 3 * L + L * nkv + L * B * nkv + L * 4
+
+
+@pytest.mark.parametrize("case", STEP_CASES, ids=lambda c: f"{c[0].name}-B{c[1]}-k{c[5]}")
+def test_steps_plan_is_the_step_plans_in_sequence(case):
+    """Step s of the one-launch plan is the single-step plan at positions + s
+    with its counters offset by s times the per-step count; only step s > 0's
+    layer-0 QKV instructions differ: they wait for step s - 1's LM head (their
+    token is its argmax), which every queue holds before them."""
+    shape, B, S, n_sm, pos, k = case
+    ins, off, tg = mk.schedule_steps(shape, B, S, n_sm, pos, k)
+    n = len(tg) // k
+    assert len(tg) == k * n
+    lm = _lm_counter(shape, B)
+    st = (ins["layer"] >> 10) & 31
+    for m in range(n_sm):
+        q = st[off[m]:off[m + 1]]
+        assert np.all(np.diff(q) >= 0), "each queue runs its steps in order"
+    for s_ in range(k):
+        one, o1, t1 = mk.schedule(shape, B, S, n_sm, [p + s_ for p in pos])
+        np.testing.assert_array_equal(tg[s_ * n:(s_ + 1) * n], t1)
+        for m in range(n_sm):
+            q = ins[off[m]:off[m + 1]]
+            q = q[((q["layer"] >> 10) & 31) == s_].copy()
+            r = one[o1[m]:o1[m + 1]]
+            q["layer"] &= 1023
+            g = q["sig_ctr"] >= 0
+            q["sig_ctr"][g] -= s_ * n
+            first = (q["op"] == mk.OP_QKV) & (q["layer"] == 0)
+            if s_ > 0:
+                assert np.all(q["wait_ctr"][first] == (s_ - 1) * n + lm)
+                assert np.all(q["wait_target"][first] == shape.vocab)
+                q["wait_ctr"][first] = r["wait_ctr"][first]
+                q["wait_target"][first] = r["wait_target"][first]
+            w = (q["wait_ctr"] >= 0) & ~(first & (s_ > 0))
+            q["wait_ctr"][w] -= s_ * n
+            np.testing.assert_array_equal(q, r)
+
+
+@pytest.mark.parametrize("case", STEP_CASES, ids=lambda c: f"{c[0].name}-B{c[1]}-k{c[5]}")
+def test_steps_plan_cannot_deadlock(case):
+    """Instruction-level waits and the three-role model with the loader's
+    acquire of the previous step's LM head before a later step's keys."""
+    shape, B, S, n_sm, pos, k = case
+    ins, off, tg = mk.schedule_steps(shape, B, S, n_sm, pos, k)
+    n = len(tg) // k
+    lm = [s_ * n + _lm_counter(shape, B) for s_ in range(k)]
+    rng = random.Random(13)
+    picks = [lambda a: a[0]]
+    if shape is synth.TINY:
+        picks += [lambda a: a[-1], lambda a: rng.choice(a), lambda a: rng.choice(a)]
+    for pick in picks:
+        assert _simulate(ins, off, tg, n_sm, pick)
+        assert _simulate_roles(ins, off, tg, n_sm, shape, B, pos, 6, pick, lm_of_step=lm)
+
+
+def test_role_model_detects_a_key_fetch_gated_on_its_own_steps_lm_head():
+    """Gating step s's key fetch on step s's own LM head (which follows the
+    attention in every queue) deadlocks the model."""
+    shape, B, S, n_sm, pos, k = STEP_CASES[0]
+    ins, off, tg = mk.schedule_steps(shape, B, S, n_sm, pos, k)
+    n = len(tg) // k
+    lm = [s_ * n + _lm_counter(shape, B) for s_ in range(k)]
+    assert not _simulate_roles(ins, off, tg, n_sm, shape, B, pos, 6, lambda a: a[0],
+                               lm_of_step=lm[1:])
+
+
+def test_steps_schedule_rejects_bad_arguments():
+    with pytest.raises(mk.MkError):
+        mk.schedule_steps(synth.TINY, 1, 128, 4, [0], 0)
+    with pytest.raises(mk.MkError):
+        mk.schedule_steps(synth.TINY, 1, 128, 4, [0], mk.MAX_STEPS_PER_LAUNCH + 1)
+    with pytest.raises(mk.MkError):
+        mk.schedule_steps(synth.TINY, 1, 128, 4, [126], 3)  # 126 + 2 reaches capacity
+    mk.schedule_steps(synth.TINY, 1, 128, 4, [125], 3)
