@@ -62,6 +62,10 @@ struct mk_handle {
   int* d_table = nullptr; // paged KV cache: the step's block table [B][max_blocks]
   int* d_ctr_steps = nullptr;  // counters of a several-step launch [kMaxLaunchSteps][n_ctr]
   float* d_plogits = nullptr;  // prefill: the logits of every row of a chunk [B][V]
+  // stamped hand-off words: the first stamped_bytes of the scratch; the
+  // next step stamps with stamp_serial & 1 (each step adds one)
+  size_t stamped_bytes = 0;
+  uint32_t stamp_serial = 1;
   struct StepsPlan {
     std::vector<int> key;  // steps, then each step's partition counts
     Instr* d_instrs = nullptr;
@@ -241,6 +245,7 @@ Params step_params(mk_handle* h, const int32_t* tok, const int32_t* pos, float* 
   const int set = (int)(h->steps & 1ull);
   p.ctr = h->d_ctr + (size_t)set * h->n_ctr;
   p.ctr_zero = h->d_ctr + (size_t)(set ^ 1) * h->n_ctr;
+  p.stamp = h->stamp_serial & 1u;
   return p;
 }
 
@@ -336,13 +341,16 @@ int create_impl(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
   // ---- scratch: one allocation, 256-byte aligned pieces
   CounterMap cm{s.L, s.nkv, s.B};
   h->n_ctr = cm.count();
+  // pieces 0..5 hold the stamped hand-off words (cleared here and after a
+  // failed step; the next step then runs with stamp 1)
   size_t sizes[] = {
       sizeof(float) * (size_t)kChunks * B * s.H,                          // xpart
       sizeof(float) * (size_t)B * s.H,                                    // xa
       sizeof(float) * (size_t)B * s.QD(),                                 // q
-      sizeof(float) * (size_t)B * s.nh * kMaxPartitions * (s.D + 2),      // part
       sizeof(float) * (size_t)B * s.QD(),                                 // attn
       sizeof(float) * (size_t)B * s.F,                                    // h
+      sizeof(float) * (size_t)B * s.nkv * 2 * s.D,                        // new k/v rows
+      sizeof(float) * (size_t)B * s.nh * kMaxPartitions * (s.D + 2),      // part
       sizeof(float2) * (size_t)s.S * (s.D / 2),                           // rope
       sizeof(int) * (size_t)2 * h->n_ctr,                                 // counters
       sizeof(int) * 64,                                                   // error word
@@ -363,18 +371,21 @@ int create_impl(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
   p.xpart = reinterpret_cast<float*>(base + offs[0]);
   p.xa = reinterpret_cast<float*>(base + offs[1]);
   p.q = reinterpret_cast<float*>(base + offs[2]);
-  p.part = reinterpret_cast<float*>(base + offs[3]);
+  p.attn = reinterpret_cast<float*>(base + offs[3]);
+  p.h = reinterpret_cast<float*>(base + offs[4]);
+  p.kvn = reinterpret_cast<float*>(base + offs[5]);
+  h->stamped_bytes = offs[6];
+  h->stamp_serial = 1;  // the cleared words carry stamp 0
+  p.part = reinterpret_cast<float*>(base + offs[6]);
   // (m, l) after the o rows, in the same piece
   p.part_ml = p.part + (size_t)B * s.nh * kMaxPartitions * s.D;
-  p.attn = reinterpret_cast<float*>(base + offs[4]);
-  p.h = reinterpret_cast<float*>(base + offs[5]);
-  h->d_rope = reinterpret_cast<float2*>(base + offs[6]);
-  h->d_ctr = reinterpret_cast<int*>(base + offs[7]);
-  h->d_err = reinterpret_cast<int*>(base + offs[8]);
-  h->d_keys = reinterpret_cast<unsigned long long*>(base + offs[9]);
-  h->d_table = reinterpret_cast<int*>(base + offs[10]);
-  h->d_ctr_steps = reinterpret_cast<int*>(base + offs[11]);
-  h->d_plogits = reinterpret_cast<float*>(base + offs[12]);
+  h->d_rope = reinterpret_cast<float2*>(base + offs[7]);
+  h->d_ctr = reinterpret_cast<int*>(base + offs[8]);
+  h->d_err = reinterpret_cast<int*>(base + offs[9]);
+  h->d_keys = reinterpret_cast<unsigned long long*>(base + offs[10]);
+  h->d_table = reinterpret_cast<int*>(base + offs[11]);
+  h->d_ctr_steps = reinterpret_cast<int*>(base + offs[12]);
+  h->d_plogits = reinterpret_cast<float*>(base + offs[13]);
   p.block_table = nullptr;  // set per step (paged handles)
   p.max_blocks = h->max_blocks;
   p.kv_block = kv_block;
@@ -543,6 +554,7 @@ int mk_decode_step_paged(mk_handle* h, const int32_t* tok, const int32_t* pos,
   if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaLaunchCooperativeKernel");
   h->cur_set = (int)(h->steps & 1ull);
   h->steps++;
+  h->stamp_serial++;
   return MK_OK;
 }
 
@@ -571,6 +583,7 @@ int mk_decode_step(mk_handle* h, const int32_t* tok, const int32_t* pos, float* 
   if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaLaunchCooperativeKernel");
   h->cur_set = (int)(h->steps & 1ull);
   h->steps++;
+  h->stamp_serial++;
   return MK_OK;
 }
 
@@ -618,6 +631,7 @@ int mk_prefill(mk_handle* h, const int32_t* tokens, int n_tokens, int start_pos,
     if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaLaunchCooperativeKernel");
     h->cur_set = (int)(h->steps & 1ull);
     h->steps++;
+    h->stamp_serial++;
   }
   // the last prompt token's row of the last chunk
   const int last_row = (n_tokens - 1) - (chunks - 1) * B;
@@ -664,6 +678,7 @@ int mk_decode_greedy(mk_handle* h, const int32_t* tok, const int32_t* pos, int n
     if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaLaunchCooperativeKernel");
     h->cur_set = (int)(h->steps & 1ull);
     h->steps++;
+    h->stamp_serial++;
   }
   const int n = n_steps * B;
   keys_to_tokens<<<(n + 255) / 256, 256, 0, st>>>(h->d_keys, n, tokens_out);
@@ -740,6 +755,7 @@ int mk_decode_greedy_persistent(mk_handle* h, const int32_t* tok, const int32_t*
   cudaError_t ce = cudaLaunchCooperativeKernel(h->fn_fx, dim3(h->n_sm), dim3(kThreads), args,
                                                (size_t)h->smem_bytes, st);
   if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaLaunchCooperativeKernel");
+  h->stamp_serial += (uint32_t)n_steps;
   const int n = n_steps * B;
   keys_to_tokens<<<(n + 255) / 256, 256, 0, st>>>(h->d_keys, n, tokens_out);
   MK_CUDA(h, cudaGetLastError());
@@ -812,6 +828,7 @@ int mk_decode_step_multilaunch(mk_handle* h, const int32_t* tok, const int32_t* 
   }
   h->cur_set = (int)(h->steps & 1ull);
   h->steps++;
+  h->stamp_serial++;
   return MK_OK;
 }
 
@@ -823,6 +840,10 @@ int mk_get_status(mk_handle* h, void* stream) {
   if (h->h_err_mirror) *reinterpret_cast<volatile int*>(h->h_err_mirror) = 0;
   if (e != 0) {
     MK_CUDA(h, cudaMemset(h->d_err, 0, sizeof e));
+    // the failed step may have left stamped words unwritten: clear them all
+    // so that no stale word can carry the next step's stamp
+    MK_CUDA(h, cudaMemset(h->d_scratch, 0, h->stamped_bytes));
+    h->stamp_serial = 1;
     int code = (e >> 24) & 0xff;
     char buf[128];
     std::snprintf(buf, sizeof buf, "device error word 0x%08x (code %d, site %d)", e, code, e & 0xffffff);

@@ -107,19 +107,14 @@ __device__ __forceinline__ bool wait_mbar(const Params& p, Misc* m, uint64_t* ba
   }
 }
 
-// Latency-critical instructions: the attention units, the O-projection and
-// the down-projection of the last chunk of h (the last to start), whose
-// outputs every SM's next hop waits for. While the compute warps run one of
-// them, the loader issues no copy for a later instruction: the storer's
-// release fence waits for the SM's bulk copies in flight, so with nothing new
-// in flight it publishes sooner (measured on the 1B shape: 698 -> 660
-// us/step; holding during the QKV instruction as well was slower, the pages
-// issued then are needed next). The ring is full during these hops anyway,
-// so the hold costs little bandwidth.
-__device__ __forceinline__ bool critical_op(const Instr& in) {
-  return in.op == MK_OP_ATTN || in.op == MK_OP_OPROJ ||
-         (in.op == MK_OP_DOWN && in.a2 == kChunks - 1);
-}
+// The latency-critical instruction whose output still goes out behind a
+// release fence: the attention unit (its partials are read as plain words
+// after an acquire of its counter). While the compute warps run one, the
+// loader issues no copy for a later instruction: the storer's release fence
+// waits for the SM's bulk copies in flight, so with nothing new in flight it
+// publishes sooner. The other hand-offs are stamped words and publish
+// without a fence, so they need no hold.
+__device__ __forceinline__ bool critical_op(const Instr& in) { return in.op == MK_OP_ATTN; }
 
 // Loader: before issuing a copy for queue entry j, wait while an earlier
 // critical instruction is computing and not yet published (bounded).
@@ -166,6 +161,97 @@ __device__ __forceinline__ bool wait_counter(const Params& p, Misc* m, int ctr, 
     }
   }
 }
+
+// ---- stamped hand-offs ------------------------------------------------------
+// A value one instruction hands to another within a step (q, the new k/v
+// rows, the attention output, xa, h, the down-projection shares) is an fp32
+// word whose lowest mantissa bit holds the step's stamp, written with a
+// relaxed store. Each such word is written exactly once per step, so until
+// this step's write lands it holds the previous step's stamp: a reader
+// checks the stamp of every word it loads and reloads the stale ones. The
+// producer then needs no release fence, which would wait for its SM's weight
+// copies in flight (about 2 us per hand-off); the counters stay as
+// scheduling hints, bumped without a fence, and the readers still poll them
+// before loading. A reader clears the stamp bit, so every value is used
+// rounded toward zero to 22 mantissa bits whatever the step's stamp, and the
+// results do not depend on it.
+
+__device__ __forceinline__ uint32_t stamp_of(const Params& p, int step) {
+  return (p.stamp + (uint32_t)step) & 1u;
+}
+
+__device__ __forceinline__ float stamped(float v, uint32_t s) {
+  return __uint_as_float((__float_as_uint(v) & ~1u) | s);
+}
+
+// A reader loads every word of a batch first, then tests the whole batch
+// (stale*), and only when some word is stale takes the slow path that
+// reloads the stale ones: a call between two loads would keep the compiler
+// from issuing the second before the first returned.
+__device__ __forceinline__ bool stale4(const float4& v, uint32_t s) {
+  return (((__float_as_uint(v.x) ^ s) | (__float_as_uint(v.y) ^ s) | (__float_as_uint(v.z) ^ s) |
+           (__float_as_uint(v.w) ^ s)) & 1u) != 0u;
+}
+
+__device__ __forceinline__ bool stale2(const float2& v, uint32_t s) {
+  return (((__float_as_uint(v.x) ^ s) | (__float_as_uint(v.y) ^ s)) & 1u) != 0u;
+}
+
+__device__ __forceinline__ bool stale1(float v, uint32_t s) {
+  return ((__float_as_uint(v) ^ s) & 1u) != 0u;
+}
+
+__device__ __forceinline__ float clear1(float v) { return __uint_as_float(__float_as_uint(v) & ~1u); }
+
+__device__ __forceinline__ float4 clear4(const float4& v) {
+  return make_float4(clear1(v.x), clear1(v.y), clear1(v.z), clear1(v.w));
+}
+
+__device__ __forceinline__ float2 clear2(const float2& v) { return make_float2(clear1(v.x), clear1(v.y)); }
+
+// The slow path: reload four words until all carry stamp s (bounded; on a
+// timeout or an abort the last, stale, words are returned and the step's
+// results are void). The words keep their stamp bits.
+static __device__ __noinline__ float4 reload_stamped4(const Params& p, Misc* m, const float* src,
+                                               uint32_t s) {
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    float4 v = ld_relaxed4(src);
+    if (!stale4(v, s)) return v;
+    if ((it & 7) == 0) {
+      if (aborted(m)) return v;
+      if (ld_volatile(p.err) != 0) {
+        *reinterpret_cast<volatile int*>(&m->abort) = 1;
+        return v;
+      }
+      if (globaltimer() - t0 > p.timeout_ns) {
+        raise_error(p, m, kErrTimeoutStamp);
+        return v;
+      }
+    }
+  }
+}
+
+static __device__ __noinline__ float reload_stamped1(const Params& p, Misc* m, const float* src,
+                                              uint32_t s) {
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    float v = ld_relaxed(src);
+    if (!stale1(v, s)) return v;
+    if ((it & 7) == 0) {
+      if (aborted(m)) return v;
+      if (ld_volatile(p.err) != 0) {
+        *reinterpret_cast<volatile int*>(&m->abort) = 1;
+        return v;
+      }
+      if (globaltimer() - t0 > p.timeout_ns) {
+        raise_error(p, m, kErrTimeoutStamp);
+        return v;
+      }
+    }
+  }
+}
+
 
 // Instruction descriptors are read-only for the whole launch: two 16-byte
 // loads through the non-coherent path. Every role fetches the next descriptor
@@ -605,9 +691,10 @@ __device__ __forceinline__ const uint16_t* norm_weight(const Params& p, int kind
 // xa + its four down-projection shares; NS = 1: one row), the RMSNorm gain is
 // applied, and the result is stored in the staging layout. Every thread
 // issues all of its loads of a column pass before using any, so a pass costs
-// one L2 round trip. Returns the sums of squares per sequence in ss.
+// one L2 round trip; the source rows are stamped words, and a stale vector
+// is reloaded before use. Returns the sums of squares per sequence in ss.
 template <int B, int NS, int NB, int KU, int FX>
-__device__ __forceinline__ void stage_pass(const Params& p, float* dst, int K, int Ks,
+__device__ __forceinline__ void stage_pass(const Params& p, Misc* m, float* dst, int K, int Ks,
                                            const uint16_t* normw, bool from_embed,
                                            const float* base, size_t stride, int b0, int step,
                                            float (&ss)[NB], bool frag) {
@@ -615,11 +702,13 @@ __device__ __forceinline__ void stage_pass(const Params& p, float* dst, int K, i
   constexpr int kPass = kComputeThreads * 4 * KU;  // columns per pass
   const int tid = compute_tid();
   const size_t cs = (size_t)p.B * p.H;  // distance between two down-projection shares
+  const uint32_t st = stamp_of(p, step);
 #pragma unroll
   for (int bb = 0; bb < NB; ++bb) ss[bb] = 0.f;
   for (int c0 = tid * 4; c0 < K; c0 += kPass) {
     float4 v[NS][NB][KU];
     uint2 wv[KU];
+    bool bad = false;  // some source word of the pass carries the previous step's stamp
 #pragma unroll
     for (int u = 0; u < KU; ++u) {
       const int c = c0 + u * kComputeThreads * 4;
@@ -636,11 +725,40 @@ __device__ __forceinline__ void stage_pass(const Params& p, float* dst, int K, i
 #pragma unroll
             for (int sidx = 0; sidx < NS; ++sidx) {
               const float* src = sidx == 0 ? base : p.xpart + (size_t)(sidx - 1) * cs;
-              v[sidx][bb][u] = __ldcg(reinterpret_cast<const float4*>(src + (b0 + bb) * stride + c));
+              v[sidx][bb][u] = ld_relaxed4(src + (b0 + bb) * stride + c);
             }
           }
         }
       }
+    }
+    if (!from_embed) {
+#pragma unroll
+      for (int u = 0; u < KU; ++u)
+#pragma unroll
+        for (int bb = 0; bb < NB; ++bb)
+#pragma unroll
+          for (int sidx = 0; sidx < NS; ++sidx)
+            if (c0 + u * kComputeThreads * 4 < K && b0 + bb < B) bad |= stale4(v[sidx][bb][u], st);
+      if (bad) {
+#pragma unroll
+        for (int u = 0; u < KU; ++u)
+#pragma unroll
+          for (int bb = 0; bb < NB; ++bb)
+#pragma unroll
+            for (int sidx = 0; sidx < NS; ++sidx) {
+              const int c = c0 + u * kComputeThreads * 4;
+              if (c < K && b0 + bb < B && stale4(v[sidx][bb][u], st)) {
+                const float* src = sidx == 0 ? base : p.xpart + (size_t)(sidx - 1) * cs;
+                v[sidx][bb][u] = reload_stamped4(p, m, src + (b0 + bb) * stride + c, st);
+              }
+            }
+      }
+#pragma unroll
+      for (int u = 0; u < KU; ++u)
+#pragma unroll
+        for (int bb = 0; bb < NB; ++bb)
+#pragma unroll
+          for (int sidx = 0; sidx < NS; ++sidx) v[sidx][bb][u] = clear4(v[sidx][bb][u]);
     }
 #pragma unroll
     for (int u = 0; u < KU; ++u) {
@@ -728,7 +846,7 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
   if (sum_x) {
     for (int b0 = 0; b0 < B; b0 += kNB5) {
       float ss[kNB5];
-      stage_pass<B, 5, kNB5, kU5, FX>(p, dst, K, Ks, normw, false, base, stride, b0, step, ss,
+      stage_pass<B, 5, kNB5, kU5, FX>(p, m, dst, K, Ks, normw, false, base, stride, b0, step, ss,
                                       frag);
       if (normw) {
 #pragma unroll
@@ -741,7 +859,7 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
     }
   } else {
     float ss[kNB1];
-    stage_pass<B, 1, kNB1, kU1, FX>(p, dst, K, Ks, normw, from_embed, base, stride, 0, step, ss,
+    stage_pass<B, 1, kNB1, kU1, FX>(p, m, dst, K, Ks, normw, from_embed, base, stride, 0, step, ss,
                                     frag);
     if (normw) {
 #pragma unroll
@@ -1256,33 +1374,78 @@ __device__ void attn_unit(const Params& p, Misc* m, uint8_t* smem, const Instr& 
   // the new key, if in this unit, goes with share 0: k row as the B fragment
   // of key column 0 (lanes grp == 0), v columns 8 nb + 2 tig, +1 of every lane
   const bool new_here = r0 == 0 && sp.t0 <= pos && pos < sp.t1;
+  const uint32_t st = stamp_of(p, step_of(in));
+  // The queries and (if in this unit) the new key and value: stamped words,
+  // all loaded first, then tested, the stale ones reloaded. The new rows are
+  // the stamped copy of what the QKV instruction appended (bf16 bits in the
+  // upper half of each word; two words make one bf16 pair).
+  const float* qs = qhead + (size_t)min(grp, G - 1) * D + 8 * tig;
+  const float* kr = p.kvn + ((size_t)(b * p.nkv + g) * 2) * D;
+  const float* vr = kr + D;
+  float4 qw[KS];      // dimensions 32 (j / 2) + 8 tig + 4 (j % 2) .. + 3
+  float4 kw[D / 32][2];  // k columns 32 i + 8 tig .. + 7 (lanes grp == 0)
+  float2 vw[NB];      // v columns 8 nb + 2 tig, + 1
+#pragma unroll
+  for (int j = 0; j < KS; ++j) qw[j] = ld_relaxed4(qs + 32 * (j / 2) + 4 * (j % 2));
+  const bool kload = new_here && grp == 0;
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) {
+    kw[i][0] = kw[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (kload) {
+      kw[i][0] = ld_relaxed4(kr + 32 * i + 8 * tig);
+      kw[i][1] = ld_relaxed4(kr + 32 * i + 8 * tig + 4);
+    }
+  }
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb) vw[nb] = new_here ? ld_relaxed2(vr + 8 * nb + 2 * tig) : make_float2(0.f, 0.f);
+  {
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < KS; ++j) bad |= stale4(qw[j], st);
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) bad |= kload && (stale4(kw[i][0], st) || stale4(kw[i][1], st));
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) bad |= new_here && stale2(vw[nb], st);
+    if (bad) {
+#pragma unroll
+      for (int j = 0; j < KS; ++j)
+        if (stale4(qw[j], st)) qw[j] = reload_stamped4(p, m, qs + 32 * (j / 2) + 4 * (j % 2), st);
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) {
+        if (kload && stale4(kw[i][0], st)) kw[i][0] = reload_stamped4(p, m, kr + 32 * i + 8 * tig, st);
+        if (kload && stale4(kw[i][1], st)) kw[i][1] = reload_stamped4(p, m, kr + 32 * i + 8 * tig + 4, st);
+      }
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        if (new_here && stale1(vw[nb].x, st)) vw[nb].x = reload_stamped1(p, m, vr + 8 * nb + 2 * tig, st);
+        if (new_here && stale1(vw[nb].y, st)) vw[nb].y = reload_stamped1(p, m, vr + 8 * nb + 2 * tig + 1, st);
+      }
+    }
+  }
+  // the new key as B fragments of key column 0 (lanes grp == 0), the new
+  // value's columns 8 nb + 2 tig, +1 of every lane
   uint4 kn[D / 64][2];
   uint32_t vn[NB];
-  if (new_here) {
-    const LayerPtrs& L = p.layers[layer_of(in)];
-    const size_t row = kv_row<FX>(p, b, g, pos);
 #pragma unroll
-    for (int j2 = 0; j2 < D / 64; ++j2) {
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      kn[j2][0] = grp == 0 ? __ldcg(reinterpret_cast<const uint4*>(L.kc + row + 64 * j2 + 8 * tig)) : z;
-      kn[j2][1] = grp == 0 ? __ldcg(reinterpret_cast<const uint4*>(L.kc + row + 64 * j2 + 32 + 8 * tig)) : z;
+  for (int j2 = 0; j2 < D / 64; ++j2)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const float4 a = kw[2 * j2 + hf][0], c = kw[2 * j2 + hf][1];
+      kn[j2][hf] = make_uint4(__byte_perm(__float_as_uint(a.x), __float_as_uint(a.y), 0x7632),
+                              __byte_perm(__float_as_uint(a.z), __float_as_uint(a.w), 0x7632),
+                              __byte_perm(__float_as_uint(c.x), __float_as_uint(c.y), 0x7632),
+                              __byte_perm(__float_as_uint(c.z), __float_as_uint(c.w), 0x7632));
     }
 #pragma unroll
-    for (int nb = 0; nb < NB; ++nb)
-      vn[nb] = __ldcg(reinterpret_cast<const unsigned int*>(L.vc + row + 8 * nb + 2 * tig));
-  }
+  for (int nb = 0; nb < NB; ++nb)
+    vn[nb] = __byte_perm(__float_as_uint(vw[nb].x), __float_as_uint(vw[nb].y), 0x7632);
   // query fragments of head min(grp, G - 1): step s covers dimensions
   // 32 (s / 2) + 8 tig + 4 (s % 2) .. + 3
   uint4 qa[KS];
-  {
-    const float* qs = qhead + (size_t)min(grp, G - 1) * D + 8 * tig;
 #pragma unroll
-    for (int j = 0; j < KS / 2; ++j) {
-      const float4 x0 = __ldcg(reinterpret_cast<const float4*>(qs + 32 * j));
-      const float4 x1 = __ldcg(reinterpret_cast<const float4*>(qs + 32 * j + 4));
-      qa[2 * j] = split_hi_lo(x0.x * qscale, x0.y * qscale, x0.z * qscale, x0.w * qscale);
-      qa[2 * j + 1] = split_hi_lo(x1.x * qscale, x1.y * qscale, x1.z * qscale, x1.w * qscale);
-    }
+  for (int j = 0; j < KS; ++j) {
+    const float4 x = clear4(qw[j]);
+    qa[j] = split_hi_lo(x.x * qscale, x.y * qscale, x.z * qscale, x.w * qscale);
   }
   float mrow = -INFINITY;  // running maximum of head grp (equal in the group's 4 lanes)
   float lsum = 0.f;        // this lane's share of the running sum
@@ -1498,8 +1661,9 @@ __device__ __forceinline__ void attn_reduce(const Params& p, const Instr& in) {
     }
     const float inv = 1.f / den;
     float* dst = p.attn + (size_t)b * p.QD + (size_t)h * D + lane * PL;
+    const uint32_t st = stamp_of(p, step_of(in));
 #pragma unroll
-    for (int e = 0; e < PL; ++e) dst[e] = acc[e] * inv;
+    for (int e = 0; e < PL; ++e) st_relaxed(dst + e, stamped(acc[e] * inv, st));
   }
 }
 
@@ -1694,33 +1858,79 @@ __device__ __forceinline__ void epilogue_prefetch(const Params& p, Misc* m, cons
     }
   } else if (in.op == MK_OP_OPROJ) {
     const bool from_embed = layer_of(in) == 0;
-    if (!from_embed && !p.no_waits && in.wait_ctr >= 0) {
-      // the residual rows were written by other SMs before the instruction's
-      // input counter completed: acquire that counter (the compute warps
-      // wait on it too) before reading them
+    if (from_embed && (FX & kFxPaged) && step_of(in) > 0 && !p.no_waits && in.wait_ctr >= 0) {
+      // greedy decode: the token is the previous step's argmax, complete
+      // once that step's LM head is (the instruction's input counter follows
+      // it); acquire that counter (the compute warps wait on it too)
       bool ok = true;
       if (lane == 0) ok = wait_counter(p, m, in.wait_ctr, in.wait_target);
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) return;
       __syncwarp();  // lane 0's acquire, then every lane's loads
     }
+    // the residual x = xa + the four down-projection shares of the previous
+    // layer: stamped words, complete before this layer's QKV instructions
+    // started, so read without waiting on a counter (all loads first, then
+    // the stamp test, then the slow path if a word was stale)
+    const uint32_t st = stamp_of(p, step_of(in));
+    const size_t cs = (size_t)p.B * p.H;
+    if (from_embed) {
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int it = lane + 32 * k;
-      if (it < items) {
-        const int j = in.a0 + it;
+      for (int k = 0; k < 2; ++k) {
+        const int it = lane + 32 * k;
+        if (it < items) {
+#pragma unroll
+          for (int b = 0; b < B; ++b)
+            pre.v[k][b].x =
+                bf16f(p.embed[(size_t)token_of<FX>(p, b, step_of(in)) * p.H + in.a0 + it]);
+        }
+      }
+    } else {
+      float r[2][B][1 + kChunks];
+      bool bad = false;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int it = lane + 32 * k;
 #pragma unroll
         for (int b = 0; b < B; ++b) {
-          if (from_embed) {
-            pre.v[k][b].x = bf16f(p.embed[(size_t)token_of<FX>(p, b, step_of(in)) * p.H + j]);
-          } else {
-            const size_t o = (size_t)b * p.H + j, cs = (size_t)p.B * p.H;
-            float acc = __ldcg(p.xa + o);
+          const size_t o = (size_t)b * p.H + in.a0 + it;
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c) acc += __ldcg(p.xpart + c * cs + o);
-            pre.v[k][b].x = acc;
+          for (int c = 0; c <= kChunks; ++c) {
+            r[k][b][c] = 0.f;
+            if (it < items) {
+              r[k][b][c] = ld_relaxed(c == 0 ? p.xa + o : p.xpart + (c - 1) * cs + o);
+            }
           }
         }
       }
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+#pragma unroll
+        for (int b = 0; b < B; ++b)
+#pragma unroll
+          for (int c = 0; c <= kChunks; ++c)
+            if (lane + 32 * k < items) bad |= stale1(r[k][b][c], st);
+      if (bad) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+#pragma unroll
+          for (int b = 0; b < B; ++b)
+#pragma unroll
+            for (int c = 0; c <= kChunks; ++c) {
+              const int it = lane + 32 * k;
+              const size_t o = (size_t)b * p.H + in.a0 + it;
+              if (it < items && stale1(r[k][b][c], st))
+                r[k][b][c] = reload_stamped1(p, m, c == 0 ? p.xa + o : p.xpart + (c - 1) * cs + o, st);
+            }
+      }
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+          float acc = clear1(r[k][b][0]);
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c) acc += clear1(r[k][b][1 + c]);
+          pre.v[k][b].x = acc;
+        }
     }
   }
 }
@@ -1732,6 +1942,7 @@ __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const
   const Geom g = geom_of(in.op, p.H, p.QD, p.Fc);
   const int items = in.a1 - in.a0;
   const LayerPtrs& L = p.layers[layer_of(in)];
+  const uint32_t st = stamp_of(p, step_of(in));
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     const int it = lane + 32 * k;
@@ -1754,24 +1965,30 @@ __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const
           }
           if (pr.which == 0) {
             float* qd = p.q + (size_t)b * p.QD + (size_t)pr.head * p.D + pr.i;
-            qd[0] = o0;
-            qd[half] = o1;
+            st_relaxed(qd, stamped(o0, st));
+            st_relaxed(qd + half, stamped(o1, st));
           } else {
             uint16_t* c = (pr.which == 1 ? L.kc : L.vc) + kv_row<FX>(p, b, pr.head, pos) + pr.i;
-            c[0] = __bfloat16_as_ushort(__float2bfloat16_rn(o0));
-            c[half] = __bfloat16_as_ushort(__float2bfloat16_rn(o1));
+            const uint16_t k0 = __bfloat16_as_ushort(__float2bfloat16_rn(o0));
+            const uint16_t k1 = __bfloat16_as_ushort(__float2bfloat16_rn(o1));
+            c[0] = k0;
+            c[half] = k1;
+            // the stamped copy the attention units of this step read
+            float* w = p.kvn + ((size_t)(b * p.nkv + pr.head) * 2 + (pr.which - 1)) * p.D + pr.i;
+            st_relaxed(w, __uint_as_float(((uint32_t)k0 << 16) | st));
+            st_relaxed(w + half, __uint_as_float(((uint32_t)k1 << 16) | st));
           }
           break;
         }
         case MK_OP_OPROJ:
-          p.xa[(size_t)b * p.H + j] = pre.v[k][b].x + v0;
+          st_relaxed(p.xa + (size_t)b * p.H + j, stamped(pre.v[k][b].x + v0, st));
           break;
         case MK_OP_GATEUP:
-          p.h[(size_t)b * p.F + j] = silu(v0) * v1;
+          st_relaxed(p.h + (size_t)b * p.F + j, stamped(silu(v0) * v1, st));
           break;
         case MK_OP_DOWN:
           // this chunk's share of row j (the readers add the four shares to xa)
-          p.xpart[((size_t)in.a2 * p.B + b) * p.H + j] = v0;
+          st_relaxed(p.xpart + ((size_t)in.a2 * p.B + b) * p.H + j, stamped(v0, st));
           break;
         default:  // MK_OP_LMHEAD
           p.logits[(size_t)b * p.V + j] = v0;
@@ -1852,17 +2069,24 @@ __device__ void storer_role(const Params& p, Misc* m, uint8_t* smem, const Instr
       const float* res = reinterpret_cast<const float*>(smem + p.off_res) + (size_t)buf * p.res_floats;
       if (is_gemv(in.op)) epilogue<B, FX>(p, in, res, pre);
       if (in.sig_ctr >= 0) {
-        // the warp barrier orders the other lanes' stores (and, through the
-        // result mbarrier, the compute warps' stores) before lane 0's
-        // release-add, which publishes them at GPU scope. No instruction
-        // waits for the LM head's logits (the end of the kernel publishes
-        // them), so its count goes out without the release, whose fence
+        // Outputs read as plain words after an acquire of this counter go
+        // out with a release-add: the warp barrier orders the other lanes'
+        // stores (and, through the result mbarrier, the compute warps'
+        // stores) before lane 0's release, which publishes them at GPU scope.
+        // Those are the attention partials; with the paged-cache / greedy
+        // code also the KV rows a later step of the same launch fetches with
+        // bulk copies (after acquiring the LM head's count, released too),
+        // and in a prefill step the chunk's KV rows, which the loader fetches
+        // after the QKV counter. Every other output is stamped words, and its
+        // count is a scheduling hint bumped without the release, whose fence
         // would wait for this SM's weight copies in flight.
+        const bool release = in.op == MK_OP_ATTN ||
+                             ((FX & kFxPaged) && (in.op == MK_OP_QKV || in.op == MK_OP_LMHEAD)) ||
+                             (in.op == MK_OP_QKV && p.prefill);
         __syncwarp();
         if (lane == 0) {
-          if (in.op == MK_OP_LMHEAD && !(FX & kFxPaged))
-            red_relaxed_add(p.ctr + in.sig_ctr, in.sig_amount);
-          else red_release_add(p.ctr + in.sig_ctr, in.sig_amount);
+          if (release) red_release_add(p.ctr + in.sig_ctr, in.sig_amount);
+          else red_relaxed_add(p.ctr + in.sig_ctr, in.sig_amount);
         }
       }
     }

@@ -57,16 +57,25 @@ struct Params {
   const uint16_t* lm;          // == embed when tied
   const uint16_t* final_norm;
   const float2* rope;          // [S][D/2] (cos, sin) of pos * theta^(-2i/D)
-  // library scratch (fp32 activations)
-  float* xa;     // [B][H] residual after the attention block
-  float* q;      // [B][nh*D] rotated queries
+  // library scratch (fp32 activations). The buffers marked "stamped" hand
+  // values from one instruction to another within a step: the lowest
+  // mantissa bit of every word carries the step's stamp (see stamp below).
+  float* xa;     // [B][H] residual after the attention block (stamped)
+  float* q;      // [B][nh*D] rotated queries (stamped)
+  float* kvn;    // [B][nkv][2][D] this step's k (0) and v (1) rows as they
+                 // were appended to the cache: bf16 bits << 16 | stamp
   float* part;   // [B][nh][kMaxPartitions][D] attention partials: o
   float* part_ml; // [B][nh][kMaxPartitions][2] attention partials: (m, l)
-  float* attn;   // [B][nh*D] reduced attention output
-  float* h;      // [B][F] SwiGLU hidden state
+  float* attn;   // [B][nh*D] reduced attention output (stamped)
+  float* h;      // [B][F] SwiGLU hidden state (stamped)
   float* xpart;  // [kChunks][B][H] down-projection of each chunk of h; the
                  // layer's output is x = xa + xpart[0] + ... + xpart[3],
-                 // summed in that order by every reader
+                 // summed in that order by every reader (stamped)
+  // stamp of step 0 of this launch (0 or 1); step s of the launch stamps
+  // with (stamp + s) & 1. Every stamped word is written exactly once per
+  // step, so before this step's write it holds the previous step's stamp
+  // and a reader can tell the two apart word by word.
+  unsigned stamp;
   float* logits; // [B][V] caller-owned
   int* ctr;      // counters of this step (zero at launch)
   int* ctr_zero; // counters of the next step, zeroed by this launch
@@ -118,6 +127,7 @@ constexpr int kErrTimeoutCounter = (MK_ERR_TIMEOUT << 24) | 1;
 constexpr int kErrTimeoutPage = (MK_ERR_TIMEOUT << 24) | 2;
 constexpr int kErrTimeoutRes = (MK_ERR_TIMEOUT << 24) | 3;
 constexpr int kErrBadInstr = (MK_ERR_INVALID << 24) | 4;
+constexpr int kErrTimeoutStamp = (MK_ERR_TIMEOUT << 24) | 5;
 
 // ---- geometry of the GEMV-shaped instructions -----------------------------
 // A GEMV instruction walks "items": one weight row, or a pair of rows whose

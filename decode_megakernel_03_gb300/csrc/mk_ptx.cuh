@@ -124,6 +124,34 @@ __device__ __forceinline__ int ld_volatile(const int* p) {
   return v;
 }
 
+// ---- stamped hand-off words: 32-bit relaxed accesses at GPU scope ----------------
+// (each word single-copy atomic and morally strong between the writer and
+// a reader on another SM; a vector load is four such word accesses)
+
+__device__ __forceinline__ void st_relaxed(float* p, float v) {
+  asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(p), "f"(v));
+}
+
+__device__ __forceinline__ float ld_relaxed(const float* p) {
+  float v;
+  asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float2 ld_relaxed2(const float* p) {
+  float2 v;
+  asm volatile("ld.relaxed.gpu.global.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float4 ld_relaxed4(const float* p) {
+  float4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
+}
+
 // orders this thread's earlier generic-proxy accesses (an acquire) before its
 // later async-proxy accesses of global memory (a bulk copy)
 __device__ __forceinline__ void fence_proxy_async_global() {

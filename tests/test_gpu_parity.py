@@ -194,6 +194,53 @@ def test_repeated_steps_are_bitwise_deterministic():
     pair.close()
 
 
+@pytest.mark.parametrize("wl_name", ["tiny_b2", "llama1b"])
+def test_builds_interleaved_on_one_handle(wl_name):
+    """Values handed between instructions carry the step's stamp, which
+    alternates from step to step on a handle. One handle that interleaves the
+    megakernel, the multi-launch build (plain and as a CUDA graph) and
+    several-step greedy launches gives, step for step, the same bits as a
+    handle that runs only megakernel steps: the results do not depend on the
+    stamp, and every build keeps the stamp sequence consistent."""
+    if wl_name == "tiny_b2":
+        shape, batch, cap, ctx = synth.TINY, 2, 128, (40, 71)
+    else:
+        wl = synth.WORKLOADS["llama1b"]
+        shape, batch, cap, ctx = wl.shape, 1, wl.capacity, wl.ctx
+    a = Pair(shape, batch, cap, ctx=ctx)
+    b = Pair(shape, batch, cap, ctx=ctx)
+    dev = torch.device("cuda")
+    toks_out = torch.empty((8, batch), dtype=torch.int32, device=dev)
+    modes = ["mega", "multi", "graph", "greedy3", "mega", "graph", "greedy2", "multi", "mega"]
+    s = 0
+    for mode in modes:
+        tok = [(29 * s + 5 * i + 3) % shape.vocab for i in range(batch)]
+        pos = [c + s for c in ctx]
+        if mode.startswith("greedy"):
+            n = int(mode[-1])
+            a.dec.decode_greedy_persistent(tok, pos, n, toks_out, a.logits)
+            assert a.dec.status() == mk.MK_OK, a.dec.last_error()
+            got = a.logits.cpu().numpy().astype(np.float64)
+            seq = toks_out[:n].cpu().numpy()
+            cur = tok
+            for k in range(n):
+                want = b.gpu_step(cur, [c + s + k for c in ctx]).copy()
+                nxt = [int(np.argmax(want[i].astype(np.float32))) for i in range(batch)]
+                assert list(seq[k]) == nxt
+                cur = nxt
+            np.testing.assert_array_equal(got, want)
+            s += n
+        else:
+            got = a.gpu_step(tok, pos, mode=mode).copy()
+            want = b.gpu_step(tok, pos)
+            np.testing.assert_array_equal(got, want)
+            s += 1
+    for x, y in zip(a.kc + a.vc, b.kc + b.vc):
+        assert torch.equal(x, y)
+    a.close()
+    b.close()
+
+
 def test_unsatisfiable_wait_times_out_and_recovers():
     """A host-built schedule with one wait that can never be met: the bounded
     device wait expires, the step reports MK_ERR_TIMEOUT, the next step call is

@@ -413,9 +413,8 @@ def test_dynamic_lm_head_plan(case):
 # A model of the three warp roles of every SM, not only of the instruction
 # waits: the loader issues each instruction's pages in queue order into a ring
 # of `ring` slots (a slot frees when the compute warps have read its page),
-# and holds -- issues no page of a later instruction -- while a
-# latency-critical instruction (attention, O-projection, last chunk of the
-# down-projection) is being computed and not yet published; in a prefill step
+# and holds -- issues no page of a later instruction -- while an attention
+# unit is being computed and not yet published; in a prefill step
 # it fetches an attention unit's keys only once the unit's counter is met.
 # The compute warps raise the hold on reaching a critical instruction (before
 # its waits), run an instruction once its counter is met and one of the
@@ -445,7 +444,8 @@ def _pages(r, shape, B, pos):
 
 
 def _critical(r):
-    return r["op"] in (mk.OP_ATTN, mk.OP_OPROJ) or (r["op"] == mk.OP_DOWN and r["a2"] == 3)
+    # the instruction whose output goes out behind a release fence
+    return r["op"] == mk.OP_ATTN
 
 
 def _simulate_roles(ins, off, tg, n_sm, shape, B, pos, ring, pick, prefill=False,
@@ -586,11 +586,13 @@ def test_roles_prefill_cannot_deadlock():
 def test_role_model_detects_a_hold_on_the_critical_instructions_own_pages():
     """The same model deadlocks when the hold also stops the critical
     instruction's own pages: its compute waits for pages the loader will not
-    issue until the instruction is published."""
+    issue until the instruction is published (8 SMs: attention units of 10
+    key pages, more than the 6-page ring lets the loader issue ahead)."""
     shape, pos = synth.LLAMA_1B, [600]
-    ins, off, tg, sm = _plan(shape, 1, 640, 24, pos)
-    assert not _simulate_roles(ins, off, tg, 24, shape, 1, pos, 12, lambda a: a[0],
+    ins, off, tg, sm = _plan(shape, 1, 640, 8, pos)
+    assert not _simulate_roles(ins, off, tg, 8, shape, 1, pos, 6, lambda a: a[0],
                                hold_own_pages=True)
+    assert _simulate_roles(ins, off, tg, 8, shape, 1, pos, 6, lambda a: a[0])
 
 
 # ---------------------------------------------------------------------------
