@@ -75,6 +75,10 @@ __device__ __forceinline__ int compute_warp() {
 __device__ __forceinline__ int compute_tid() { return compute_warp() * 32 + (threadIdx.x & 31); }
 
 __device__ __forceinline__ void compute_bar() { named_bar(kBarCompute, kComputeThreads); }
+// the compute warps' barrier, returning whether any of their threads passed v
+__device__ __forceinline__ bool compute_bar_or(bool v) {
+  return named_bar_or(kBarCompute, kComputeThreads, v);
+}
 
 __device__ __forceinline__ bool aborted(const Misc* m) {
   return *reinterpret_cast<const volatile int*>(&m->abort) != 0;
@@ -209,49 +213,30 @@ __device__ __forceinline__ float4 clear4(const float4& v) {
 
 __device__ __forceinline__ float2 clear2(const float2& v) { return make_float2(clear1(v.x), clear1(v.y)); }
 
-// The slow path: reload four words until all carry stamp s (bounded; on a
-// timeout or an abort the last, stale, words are returned and the step's
-// results are void). The words keep their stamp bits.
-static __device__ __noinline__ float4 reload_stamped4(const Params& p, Misc* m, const float* src,
-                                               uint32_t s) {
-  const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    float4 v = ld_relaxed4(src);
-    if (!stale4(v, s)) return v;
-    if ((it & 7) == 0) {
-      if (aborted(m)) return v;
-      if (ld_volatile(p.err) != 0) {
-        *reinterpret_cast<volatile int*>(&m->abort) = 1;
-        return v;
-      }
-      if (globaltimer() - t0 > p.timeout_ns) {
-        raise_error(p, m, kErrTimeoutStamp);
-        return v;
-      }
+// A batch of loads that found a stale word is loaded again, whole: no
+// per-word slow path, so the batch's code appears once (it is almost never
+// repeated: the counter a reader polls first is bumped after the words were
+// stored). Whether to try again: false on an abort, an error raised by
+// another CTA, or after the timeout (the step's results are then void).
+static __device__ __noinline__ bool retry_stale(const Params& p, Misc* m, uint32_t& it,
+                                                uint64_t& t0) {
+  if (it++ == 0) {
+    t0 = globaltimer();
+    return true;
+  }
+  if ((it & 7) == 0) {
+    if (aborted(m)) return false;
+    if (ld_volatile(p.err) != 0) {
+      *reinterpret_cast<volatile int*>(&m->abort) = 1;
+      return false;
+    }
+    if (globaltimer() - t0 > p.timeout_ns) {
+      raise_error(p, m, kErrTimeoutStamp);
+      return false;
     }
   }
+  return true;
 }
-
-static __device__ __noinline__ float reload_stamped1(const Params& p, Misc* m, const float* src,
-                                              uint32_t s) {
-  const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    float v = ld_relaxed(src);
-    if (!stale1(v, s)) return v;
-    if ((it & 7) == 0) {
-      if (aborted(m)) return v;
-      if (ld_volatile(p.err) != 0) {
-        *reinterpret_cast<volatile int*>(&m->abort) = 1;
-        return v;
-      }
-      if (globaltimer() - t0 > p.timeout_ns) {
-        raise_error(p, m, kErrTimeoutStamp);
-        return v;
-      }
-    }
-  }
-}
-
 
 // Instruction descriptors are read-only for the whole launch: two 16-byte
 // loads through the non-coherent path. Every role fetches the next descriptor
@@ -691,13 +676,14 @@ __device__ __forceinline__ const uint16_t* norm_weight(const Params& p, int kind
 // xa + its four down-projection shares; NS = 1: one row), the RMSNorm gain is
 // applied, and the result is stored in the staging layout. Every thread
 // issues all of its loads of a column pass before using any, so a pass costs
-// one L2 round trip; the source rows are stamped words, and a stale vector
-// is reloaded before use. Returns the sums of squares per sequence in ss.
+// one L2 round trip. The source rows are stamped words: the pass uses them
+// as loaded and sets `bad` if one was stale, and the caller then stages the
+// whole vector again. Returns the sums of squares per sequence in ss.
 template <int B, int NS, int NB, int KU, int FX>
-__device__ __forceinline__ void stage_pass(const Params& p, Misc* m, float* dst, int K, int Ks,
+__device__ __forceinline__ void stage_pass(const Params& p, float* dst, int K, int Ks,
                                            const uint16_t* normw, bool from_embed,
                                            const float* base, size_t stride, int b0, int step,
-                                           float (&ss)[NB], bool frag) {
+                                           float (&ss)[NB], bool frag, bool& bad) {
   constexpr bool kFrag = B > 1;
   constexpr int kPass = kComputeThreads * 4 * KU;  // columns per pass
   const int tid = compute_tid();
@@ -708,7 +694,6 @@ __device__ __forceinline__ void stage_pass(const Params& p, Misc* m, float* dst,
   for (int c0 = tid * 4; c0 < K; c0 += kPass) {
     float4 v[NS][NB][KU];
     uint2 wv[KU];
-    bool bad = false;  // some source word of the pass carries the previous step's stamp
 #pragma unroll
     for (int u = 0; u < KU; ++u) {
       const int c = c0 + u * kComputeThreads * 4;
@@ -737,28 +722,10 @@ __device__ __forceinline__ void stage_pass(const Params& p, Misc* m, float* dst,
 #pragma unroll
         for (int bb = 0; bb < NB; ++bb)
 #pragma unroll
-          for (int sidx = 0; sidx < NS; ++sidx)
+          for (int sidx = 0; sidx < NS; ++sidx) {
             if (c0 + u * kComputeThreads * 4 < K && b0 + bb < B) bad |= stale4(v[sidx][bb][u], st);
-      if (bad) {
-#pragma unroll
-        for (int u = 0; u < KU; ++u)
-#pragma unroll
-          for (int bb = 0; bb < NB; ++bb)
-#pragma unroll
-            for (int sidx = 0; sidx < NS; ++sidx) {
-              const int c = c0 + u * kComputeThreads * 4;
-              if (c < K && b0 + bb < B && stale4(v[sidx][bb][u], st)) {
-                const float* src = sidx == 0 ? base : p.xpart + (size_t)(sidx - 1) * cs;
-                v[sidx][bb][u] = reload_stamped4(p, m, src + (b0 + bb) * stride + c, st);
-              }
-            }
-      }
-#pragma unroll
-      for (int u = 0; u < KU; ++u)
-#pragma unroll
-        for (int bb = 0; bb < NB; ++bb)
-#pragma unroll
-          for (int sidx = 0; sidx < NS; ++sidx) v[sidx][bb][u] = clear4(v[sidx][bb][u]);
+            v[sidx][bb][u] = clear4(v[sidx][bb][u]);
+          }
     }
 #pragma unroll
     for (int u = 0; u < KU; ++u) {
@@ -843,34 +810,44 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
   // sources, two sequences and one group
   constexpr int kNB1 = B, kU1 = B == 1 ? (kWide ? 6 : 4) : 3;
   constexpr int kNB5 = B == 1 ? 1 : 2, kU5 = B == 1 && !kWide ? 2 : 1;
-  if (sum_x) {
-    for (int b0 = 0; b0 < B; b0 += kNB5) {
-      float ss[kNB5];
-      stage_pass<B, 5, kNB5, kU5, FX>(p, m, dst, K, Ks, normw, false, base, stride, b0, step, ss,
-                                      frag);
+  // the whole vector is staged again if any compute thread loaded a stale
+  // word (the decision is taken at the barrier, so it is uniform)
+  uint32_t tries = 0;
+  uint64_t t0 = 0;
+  for (;;) {
+    bool bad = false;
+    if (sum_x) {
+      for (int b0 = 0; b0 < B; b0 += kNB5) {
+        float ss[kNB5];
+        stage_pass<B, 5, kNB5, kU5, FX>(p, dst, K, Ks, normw, false, base, stride, b0, step, ss,
+                                        frag, bad);
+        if (normw) {
+#pragma unroll
+          for (int bb = 0; bb < kNB5; ++bb) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ss[bb] += __shfl_xor_sync(0xffffffffu, ss[bb], o);
+            if (lane == 0 && b0 + bb < B) m->red[par][warp][b0 + bb] = ss[bb];
+          }
+        }
+      }
+    } else {
+      float ss[kNB1];
+      stage_pass<B, 1, kNB1, kU1, FX>(p, dst, K, Ks, normw, from_embed, base, stride, 0, step, ss,
+                                      frag, bad);
       if (normw) {
 #pragma unroll
-        for (int bb = 0; bb < kNB5; ++bb) {
+        for (int bb = 0; bb < kNB1; ++bb) {
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) ss[bb] += __shfl_xor_sync(0xffffffffu, ss[bb], o);
-          if (lane == 0 && b0 + bb < B) m->red[par][warp][b0 + bb] = ss[bb];
+          if (lane == 0) m->red[par][warp][bb] = ss[bb];
         }
       }
     }
-  } else {
-    float ss[kNB1];
-    stage_pass<B, 1, kNB1, kU1, FX>(p, m, dst, K, Ks, normw, from_embed, base, stride, 0, step, ss,
-                                    frag);
-    if (normw) {
-#pragma unroll
-      for (int bb = 0; bb < kNB1; ++bb) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss[bb] += __shfl_xor_sync(0xffffffffu, ss[bb], o);
-        if (lane == 0) m->red[par][warp][bb] = ss[bb];
-      }
-    }
+    if (!compute_bar_or(bad)) break;
+    // some word was stale: stage again, unless this thread gives up (abort,
+    // error, timeout), in which case every thread does
+    if (compute_bar_or(!retry_stale(p, m, tries, t0))) break;
   }
-  compute_bar();
   InvScale inv;
 #pragma unroll
   for (int b = 0; b < kMaxBatch; ++b) {
@@ -1385,41 +1362,32 @@ __device__ void attn_unit(const Params& p, Misc* m, uint8_t* smem, const Instr& 
   float4 qw[KS];      // dimensions 32 (j / 2) + 8 tig + 4 (j % 2) .. + 3
   float4 kw[D / 32][2];  // k columns 32 i + 8 tig .. + 7 (lanes grp == 0)
   float2 vw[NB];      // v columns 8 nb + 2 tig, + 1
-#pragma unroll
-  for (int j = 0; j < KS; ++j) qw[j] = ld_relaxed4(qs + 32 * (j / 2) + 4 * (j % 2));
   const bool kload = new_here && grp == 0;
-#pragma unroll
-  for (int i = 0; i < D / 32; ++i) {
-    kw[i][0] = kw[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (kload) {
-      kw[i][0] = ld_relaxed4(kr + 32 * i + 8 * tig);
-      kw[i][1] = ld_relaxed4(kr + 32 * i + 8 * tig + 4);
-    }
-  }
-#pragma unroll
-  for (int nb = 0; nb < NB; ++nb) vw[nb] = new_here ? ld_relaxed2(vr + 8 * nb + 2 * tig) : make_float2(0.f, 0.f);
   {
-    bool bad = false;
+    uint32_t tries = 0;
+    uint64_t t0 = 0;
+    for (;;) {
 #pragma unroll
-    for (int j = 0; j < KS; ++j) bad |= stale4(qw[j], st);
-#pragma unroll
-    for (int i = 0; i < D / 32; ++i) bad |= kload && (stale4(kw[i][0], st) || stale4(kw[i][1], st));
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb) bad |= new_here && stale2(vw[nb], st);
-    if (bad) {
-#pragma unroll
-      for (int j = 0; j < KS; ++j)
-        if (stale4(qw[j], st)) qw[j] = reload_stamped4(p, m, qs + 32 * (j / 2) + 4 * (j % 2), st);
+      for (int j = 0; j < KS; ++j) qw[j] = ld_relaxed4(qs + 32 * (j / 2) + 4 * (j % 2));
 #pragma unroll
       for (int i = 0; i < D / 32; ++i) {
-        if (kload && stale4(kw[i][0], st)) kw[i][0] = reload_stamped4(p, m, kr + 32 * i + 8 * tig, st);
-        if (kload && stale4(kw[i][1], st)) kw[i][1] = reload_stamped4(p, m, kr + 32 * i + 8 * tig + 4, st);
+        kw[i][0] = kw[i][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (kload) {
+          kw[i][0] = ld_relaxed4(kr + 32 * i + 8 * tig);
+          kw[i][1] = ld_relaxed4(kr + 32 * i + 8 * tig + 4);
+        }
       }
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb) {
-        if (new_here && stale1(vw[nb].x, st)) vw[nb].x = reload_stamped1(p, m, vr + 8 * nb + 2 * tig, st);
-        if (new_here && stale1(vw[nb].y, st)) vw[nb].y = reload_stamped1(p, m, vr + 8 * nb + 2 * tig + 1, st);
-      }
+      for (int nb = 0; nb < NB; ++nb)
+        vw[nb] = new_here ? ld_relaxed2(vr + 8 * nb + 2 * tig) : make_float2(0.f, 0.f);
+      bool bad = false;
+#pragma unroll
+      for (int j = 0; j < KS; ++j) bad |= stale4(qw[j], st);
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) bad |= kload && (stale4(kw[i][0], st) || stale4(kw[i][1], st));
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) bad |= new_here && stale2(vw[nb], st);
+      if (!bad || !retry_stale(p, m, tries, t0)) break;
     }
   }
   // the new key as B fragments of key column 0 (lanes grp == 0), the new
@@ -1886,41 +1854,31 @@ __device__ __forceinline__ void epilogue_prefetch(const Params& p, Misc* m, cons
       }
     } else {
       float r[2][B][1 + kChunks];
-      bool bad = false;
+      uint32_t tries = 0;
+      uint64_t t0 = 0;
+      for (;;) {
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int it = lane + 32 * k;
+        for (int k = 0; k < 2; ++k) {
+          const int it = lane + 32 * k;
 #pragma unroll
-        for (int b = 0; b < B; ++b) {
-          const size_t o = (size_t)b * p.H + in.a0 + it;
+          for (int b = 0; b < B; ++b) {
+            const size_t o = (size_t)b * p.H + in.a0 + it;
 #pragma unroll
-          for (int c = 0; c <= kChunks; ++c) {
-            r[k][b][c] = 0.f;
-            if (it < items) {
-              r[k][b][c] = ld_relaxed(c == 0 ? p.xa + o : p.xpart + (c - 1) * cs + o);
+            for (int c = 0; c <= kChunks; ++c) {
+              r[k][b][c] = 0.f;
+              if (it < items) r[k][b][c] = ld_relaxed(c == 0 ? p.xa + o : p.xpart + (c - 1) * cs + o);
             }
           }
         }
-      }
-#pragma unroll
-      for (int k = 0; k < 2; ++k)
-#pragma unroll
-        for (int b = 0; b < B; ++b)
-#pragma unroll
-          for (int c = 0; c <= kChunks; ++c)
-            if (lane + 32 * k < items) bad |= stale1(r[k][b][c], st);
-      if (bad) {
+        bool bad = false;
 #pragma unroll
         for (int k = 0; k < 2; ++k)
 #pragma unroll
           for (int b = 0; b < B; ++b)
 #pragma unroll
-            for (int c = 0; c <= kChunks; ++c) {
-              const int it = lane + 32 * k;
-              const size_t o = (size_t)b * p.H + in.a0 + it;
-              if (it < items && stale1(r[k][b][c], st))
-                r[k][b][c] = reload_stamped1(p, m, c == 0 ? p.xa + o : p.xpart + (c - 1) * cs + o, st);
-            }
+            for (int c = 0; c <= kChunks; ++c)
+              if (lane + 32 * k < items) bad |= stale1(r[k][b][c], st);
+        if (!bad || !retry_stale(p, m, tries, t0)) break;
       }
 #pragma unroll
       for (int k = 0; k < 2; ++k)

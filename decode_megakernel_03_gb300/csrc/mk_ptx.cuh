@@ -176,6 +176,20 @@ __device__ __forceinline__ void named_bar(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// the same barrier, returning whether any participating thread passed v true
+__device__ __forceinline__ bool named_bar_or(int id, int threads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\t"
+      "setp.ne.u32 pi, %1, 0;\n\t"
+      "bar.red.or.pred po, %2, %3, pi;\n\t"
+      "selp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0u;
+}
+
 // ---- shared-memory vector loads -------------------------------------------------
 
 __device__ __forceinline__ uint4 lds128(const void* p) {
