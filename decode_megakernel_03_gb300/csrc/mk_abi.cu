@@ -62,8 +62,8 @@ struct mk_handle {
   int* d_table = nullptr; // paged KV cache: the step's block table [B][max_blocks]
   int* d_ctr_steps = nullptr;  // counters of a several-step launch [kMaxLaunchSteps][n_ctr]
   float* d_plogits = nullptr;  // prefill: the logits of every row of a chunk [B][V]
-  // stamped hand-off words: the first stamped_bytes of the scratch; the
-  // next step stamps with stamp_serial & 1 (each step adds one)
+  // stamped hand-off words: the first stamped_bytes of the scratch; layer l
+  // of the next step stamps with (stamp_serial + l) & 1 (each step adds L)
   size_t stamped_bytes = 0;
   uint32_t stamp_serial = 1;
   struct StepsPlan {
@@ -554,7 +554,7 @@ int mk_decode_step_paged(mk_handle* h, const int32_t* tok, const int32_t* pos,
   if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaLaunchCooperativeKernel");
   h->cur_set = (int)(h->steps & 1ull);
   h->steps++;
-  h->stamp_serial++;
+  h->stamp_serial += (uint32_t)h->shape.L;
   return MK_OK;
 }
 
@@ -583,7 +583,7 @@ int mk_decode_step(mk_handle* h, const int32_t* tok, const int32_t* pos, float* 
   if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaLaunchCooperativeKernel");
   h->cur_set = (int)(h->steps & 1ull);
   h->steps++;
-  h->stamp_serial++;
+  h->stamp_serial += (uint32_t)h->shape.L;
   return MK_OK;
 }
 
@@ -631,7 +631,7 @@ int mk_prefill(mk_handle* h, const int32_t* tokens, int n_tokens, int start_pos,
     if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaLaunchCooperativeKernel");
     h->cur_set = (int)(h->steps & 1ull);
     h->steps++;
-    h->stamp_serial++;
+    h->stamp_serial += (uint32_t)h->shape.L;
   }
   // the last prompt token's row of the last chunk
   const int last_row = (n_tokens - 1) - (chunks - 1) * B;
@@ -678,7 +678,7 @@ int mk_decode_greedy(mk_handle* h, const int32_t* tok, const int32_t* pos, int n
     if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaLaunchCooperativeKernel");
     h->cur_set = (int)(h->steps & 1ull);
     h->steps++;
-    h->stamp_serial++;
+    h->stamp_serial += (uint32_t)h->shape.L;
   }
   const int n = n_steps * B;
   keys_to_tokens<<<(n + 255) / 256, 256, 0, st>>>(h->d_keys, n, tokens_out);
@@ -755,7 +755,7 @@ int mk_decode_greedy_persistent(mk_handle* h, const int32_t* tok, const int32_t*
   cudaError_t ce = cudaLaunchCooperativeKernel(h->fn_fx, dim3(h->n_sm), dim3(kThreads), args,
                                                (size_t)h->smem_bytes, st);
   if (ce != cudaSuccess) return cuda_fail(h, ce, "cudaLaunchCooperativeKernel");
-  h->stamp_serial += (uint32_t)n_steps;
+  h->stamp_serial += (uint32_t)n_steps * (uint32_t)h->shape.L;
   const int n = n_steps * B;
   keys_to_tokens<<<(n + 255) / 256, 256, 0, st>>>(h->d_keys, n, tokens_out);
   MK_CUDA(h, cudaGetLastError());
@@ -828,7 +828,7 @@ int mk_decode_step_multilaunch(mk_handle* h, const int32_t* tok, const int32_t* 
   }
   h->cur_set = (int)(h->steps & 1ull);
   h->steps++;
-  h->stamp_serial++;
+  h->stamp_serial += (uint32_t)h->shape.L;
   return MK_OK;
 }
 

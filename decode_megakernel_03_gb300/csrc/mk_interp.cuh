@@ -169,19 +169,21 @@ __device__ __forceinline__ bool wait_counter(const Params& p, Misc* m, int ctr, 
 // ---- stamped hand-offs ------------------------------------------------------
 // A value one instruction hands to another within a step (q, the new k/v
 // rows, the attention output, xa, h, the down-projection shares) is an fp32
-// word whose lowest mantissa bit holds the step's stamp, written with a
-// relaxed store. Each such word is written exactly once per step, so until
-// this step's write lands it holds the previous step's stamp: a reader
-// checks the stamp of every word it loads and reloads the stale ones. The
-// producer then needs no release fence, which would wait for its SM's weight
-// copies in flight (about 2 us per hand-off); the counters stay as
-// scheduling hints, bumped without a fence, and the readers still poll them
-// before loading. A reader clears the stamp bit, so every value is used
-// rounded toward zero to 22 mantissa bits whatever the step's stamp, and the
-// results do not depend on it.
+// word whose lowest mantissa bit holds a stamp, written with a relaxed
+// store. Each such word is written exactly once per layer, and the stamp is
+// the parity of its layer's index in the launch sequence (layer l of step s
+// of a launch: stamp + s * L + l), so every write flips it: until a layer's
+// write lands, the word holds the previous layer's stamp, and a reader
+// checks the stamp of every word it loads and loads again if one is stale.
+// The producer then needs no release fence, which would wait for its SM's
+// weight copies in flight (about 2 us per hand-off); the counters stay as
+// scheduling hints, bumped without a fence. A reader clears the stamp bit,
+// so every value is used rounded toward zero to 22 mantissa bits whatever
+// its stamp, and the results do not depend on it.
 
-__device__ __forceinline__ uint32_t stamp_of(const Params& p, int step) {
-  return (p.stamp + (uint32_t)step) & 1u;
+// the stamp of the words layer `layer` of step `step` of this launch writes
+__device__ __forceinline__ uint32_t stamp_of(const Params& p, int step, int layer) {
+  return (p.stamp + (uint32_t)step * (uint32_t)p.L + (uint32_t)layer) & 1u;
 }
 
 __device__ __forceinline__ float stamped(float v, uint32_t s) {
@@ -683,12 +685,11 @@ template <int B, int NS, int NB, int KU, int FX>
 __device__ __forceinline__ void stage_pass(const Params& p, float* dst, int K, int Ks,
                                            const uint16_t* normw, bool from_embed,
                                            const float* base, size_t stride, int b0, int step,
-                                           float (&ss)[NB], bool frag, bool& bad) {
+                                           uint32_t st, float (&ss)[NB], bool frag, bool& bad) {
   constexpr bool kFrag = B > 1;
   constexpr int kPass = kComputeThreads * 4 * KU;  // columns per pass
   const int tid = compute_tid();
   const size_t cs = (size_t)p.B * p.H;  // distance between two down-projection shares
-  const uint32_t st = stamp_of(p, step);
 #pragma unroll
   for (int bb = 0; bb < NB; ++bb) ss[bb] = 0.f;
   for (int c0 = tid * 4; c0 < K; c0 += kPass) {
@@ -802,6 +803,10 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
   else if (kind == kActAttnOut) base = p.attn, stride = p.QD;
   else base = p.h + (size_t)chunk * p.Fc, stride = p.F;
   const int par = st.stage_cnt & 1;
+  // the stamp of the source words: the previous layer's output for the
+  // attention norm, the last layer's for the final norm, else this layer's
+  const uint32_t wst =
+      stamp_of(p, step, kind == kActAttnNorm ? layer - 1 : (kind == kActFinalNorm ? p.L - 1 : layer));
   compute_bar();  // everyone is done reading the buffer's previous contents
   // one sequence: four (six if rows may be wider than 3072 columns) column
   // groups per thread and pass, so 2048 (4608) columns take one L2 round
@@ -819,8 +824,8 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
     if (sum_x) {
       for (int b0 = 0; b0 < B; b0 += kNB5) {
         float ss[kNB5];
-        stage_pass<B, 5, kNB5, kU5, FX>(p, dst, K, Ks, normw, false, base, stride, b0, step, ss,
-                                        frag, bad);
+        stage_pass<B, 5, kNB5, kU5, FX>(p, dst, K, Ks, normw, false, base, stride, b0, step, wst,
+                                        ss, frag, bad);
         if (normw) {
 #pragma unroll
           for (int bb = 0; bb < kNB5; ++bb) {
@@ -832,8 +837,8 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
       }
     } else {
       float ss[kNB1];
-      stage_pass<B, 1, kNB1, kU1, FX>(p, dst, K, Ks, normw, from_embed, base, stride, 0, step, ss,
-                                      frag, bad);
+      stage_pass<B, 1, kNB1, kU1, FX>(p, dst, K, Ks, normw, from_embed, base, stride, 0, step, wst,
+                                      ss, frag, bad);
       if (normw) {
 #pragma unroll
         for (int bb = 0; bb < kNB1; ++bb) {
@@ -1351,7 +1356,7 @@ __device__ void attn_unit(const Params& p, Misc* m, uint8_t* smem, const Instr& 
   // the new key, if in this unit, goes with share 0: k row as the B fragment
   // of key column 0 (lanes grp == 0), v columns 8 nb + 2 tig, +1 of every lane
   const bool new_here = r0 == 0 && sp.t0 <= pos && pos < sp.t1;
-  const uint32_t st = stamp_of(p, step_of(in));
+  const uint32_t st = stamp_of(p, step_of(in), layer_of(in));
   // The queries and (if in this unit) the new key and value: stamped words,
   // all loaded first, then tested, the stale ones reloaded. The new rows are
   // the stamped copy of what the QKV instruction appended (bf16 bits in the
@@ -1629,7 +1634,7 @@ __device__ __forceinline__ void attn_reduce(const Params& p, const Instr& in) {
     }
     const float inv = 1.f / den;
     float* dst = p.attn + (size_t)b * p.QD + (size_t)h * D + lane * PL;
-    const uint32_t st = stamp_of(p, step_of(in));
+    const uint32_t st = stamp_of(p, step_of(in), layer_of(in));
 #pragma unroll
     for (int e = 0; e < PL; ++e) st_relaxed(dst + e, stamped(acc[e] * inv, st));
   }
@@ -1686,8 +1691,14 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
     if (tracing) t_start = globaltimer();
     if (warp == 0 && lane == 0 && critical_op(in))
       *reinterpret_cast<volatile int*>(&m->hold) = i;
-    // 1. dependency: one thread polls, the other compute warps meet it at a barrier
-    if (!p.no_waits && in.wait_ctr >= 0 &&
+    // 1. dependency: one thread polls, the other compute warps meet it at a
+    // barrier. An instruction whose inputs are all stamped words and small
+    // polls the words themselves instead (the attention's q and new k/v rows;
+    // with one sequence also the gate/up's xa and the down-projection's
+    // chunk of h): the counter would only add a round trip
+    const bool polls_inputs =
+        in.op == MK_OP_ATTN || (B == 1 && (in.op == MK_OP_GATEUP || in.op == MK_OP_DOWN));
+    if (!p.no_waits && in.wait_ctr >= 0 && !polls_inputs &&
         !(in.wait_ctr == known_ctr && in.wait_target <= known_tgt)) {
       if (warp == 0 && lane == 0) wait_counter(p, m, in.wait_ctr, in.wait_target);
       compute_bar();
@@ -1839,7 +1850,7 @@ __device__ __forceinline__ void epilogue_prefetch(const Params& p, Misc* m, cons
     // layer: stamped words, complete before this layer's QKV instructions
     // started, so read without waiting on a counter (all loads first, then
     // the stamp test, then the slow path if a word was stale)
-    const uint32_t st = stamp_of(p, step_of(in));
+    const uint32_t st = stamp_of(p, step_of(in), layer_of(in) - 1);
     const size_t cs = (size_t)p.B * p.H;
     if (from_embed) {
 #pragma unroll
@@ -1900,7 +1911,7 @@ __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const
   const Geom g = geom_of(in.op, p.H, p.QD, p.Fc);
   const int items = in.a1 - in.a0;
   const LayerPtrs& L = p.layers[layer_of(in)];
-  const uint32_t st = stamp_of(p, step_of(in));
+  const uint32_t st = stamp_of(p, step_of(in), layer_of(in));
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     const int it = lane + 32 * k;

@@ -71,10 +71,10 @@ struct Params {
   float* xpart;  // [kChunks][B][H] down-projection of each chunk of h; the
                  // layer's output is x = xa + xpart[0] + ... + xpart[3],
                  // summed in that order by every reader (stamped)
-  // stamp of step 0 of this launch (0 or 1); step s of the launch stamps
-  // with (stamp + s) & 1. Every stamped word is written exactly once per
-  // step, so before this step's write it holds the previous step's stamp
-  // and a reader can tell the two apart word by word.
+  // stamp of layer 0 of step 0 of this launch (0 or 1); layer l of step s
+  // stamps with (stamp + s * L + l) & 1. Every stamped word is written
+  // exactly once per layer, so before a layer's write it holds the previous
+  // layer's stamp and a reader can tell the two apart word by word.
   unsigned stamp;
   float* logits; // [B][V] caller-owned
   int* ctr;      // counters of this step (zero at launch)
