@@ -560,11 +560,14 @@ def run_gpu(args, wl):
                 "multilaunch_us": multi_ms * 1e3,
                 "multilaunch_graph_us": graph_ms * 1e3,
                 # per layer QKV, attention, (reduction,) O-projection, gate/up,
-                # down; one sequence with at most 2048 attention columns has
-                # no reduction instruction (the O-projection's staging reduces)
+                # down (, down chunk 3): one sequence with at most 2048
+                # attention columns has no reduction instruction (the
+                # O-projection's staging reduces); several sequences or rows
+                # wider than 2048 columns run the chunk-3 down-projection,
+                # which writes the layer output whole, as a kernel of its own
                 "multilaunch_launches_per_step":
-                    (5 if wl.batch == 1 and shape.n_heads * shape.head_dim <= 2048 else 6)
-                    * shape.n_layers + 1,
+                    (5 + (0 if wl.batch == 1 and shape.n_heads * shape.head_dim <= 2048 else 1)
+                     + (1 if wl.batch > 1 or shape.hidden > 2048 else 0)) * shape.n_layers + 1,
                 "recovered_overhead_vs_multilaunch": (multi_ms - ms) / (multi_ms - t_min_ms),
                 "recovered_overhead_vs_graph": (graph_ms - ms) / (graph_ms - t_min_ms),
                 "overhead_megakernel": (ms - t_min_ms) / ms,

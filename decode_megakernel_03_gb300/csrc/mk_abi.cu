@@ -341,7 +341,7 @@ int create_impl(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
   // ---- scratch: one allocation, 256-byte aligned pieces
   CounterMap cm{s.L, s.nkv, s.B};
   h->n_ctr = cm.count();
-  // pieces 0..5 hold the stamped hand-off words (cleared here and after a
+  // pieces 0..6 hold the stamped hand-off words (cleared here and after a
   // failed step; the next step then runs with stamp 1)
   size_t sizes[] = {
       sizeof(float) * (size_t)kChunks * B * s.H,                          // xpart
@@ -350,6 +350,7 @@ int create_impl(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
       sizeof(float) * (size_t)B * s.QD(),                                 // attn
       sizeof(float) * (size_t)B * s.F,                                    // h
       sizeof(float) * (size_t)B * s.nkv * 2 * s.D,                        // new k/v rows
+      sizeof(float) * (size_t)B * s.H,                                    // x
       sizeof(float) * (size_t)B * s.nh * kMaxPartitions * (s.D + 2),      // part
       sizeof(float2) * (size_t)s.S * (s.D / 2),                           // rope
       sizeof(int) * (size_t)2 * h->n_ctr,                                 // counters
@@ -374,18 +375,19 @@ int create_impl(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
   p.attn = reinterpret_cast<float*>(base + offs[3]);
   p.h = reinterpret_cast<float*>(base + offs[4]);
   p.kvn = reinterpret_cast<float*>(base + offs[5]);
-  h->stamped_bytes = offs[6];
+  p.x = reinterpret_cast<float*>(base + offs[6]);
+  h->stamped_bytes = offs[7];
   h->stamp_serial = 1;  // the cleared words carry stamp 0
-  p.part = reinterpret_cast<float*>(base + offs[6]);
+  p.part = reinterpret_cast<float*>(base + offs[7]);
   // (m, l) after the o rows, in the same piece
   p.part_ml = p.part + (size_t)B * s.nh * kMaxPartitions * s.D;
-  h->d_rope = reinterpret_cast<float2*>(base + offs[7]);
-  h->d_ctr = reinterpret_cast<int*>(base + offs[8]);
-  h->d_err = reinterpret_cast<int*>(base + offs[9]);
-  h->d_keys = reinterpret_cast<unsigned long long*>(base + offs[10]);
-  h->d_table = reinterpret_cast<int*>(base + offs[11]);
-  h->d_ctr_steps = reinterpret_cast<int*>(base + offs[12]);
-  h->d_plogits = reinterpret_cast<float*>(base + offs[13]);
+  h->d_rope = reinterpret_cast<float2*>(base + offs[8]);
+  h->d_ctr = reinterpret_cast<int*>(base + offs[9]);
+  h->d_err = reinterpret_cast<int*>(base + offs[10]);
+  h->d_keys = reinterpret_cast<unsigned long long*>(base + offs[11]);
+  h->d_table = reinterpret_cast<int*>(base + offs[12]);
+  h->d_ctr_steps = reinterpret_cast<int*>(base + offs[13]);
+  h->d_plogits = reinterpret_cast<float*>(base + offs[14]);
   p.block_table = nullptr;  // set per step (paged handles)
   p.max_blocks = h->max_blocks;
   p.kv_block = kv_block;

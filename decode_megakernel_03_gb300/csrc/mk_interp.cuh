@@ -186,6 +186,16 @@ __device__ __forceinline__ uint32_t stamp_of(const Params& p, int step, int laye
   return (p.stamp + (uint32_t)step * (uint32_t)p.L + (uint32_t)layer) & 1u;
 }
 
+// Whether the layer output x is written whole by the storers of the chunk-3
+// down-projection instructions (several sequences, or rows wider than 2048
+// columns), or left as xa and four shares that every reader adds up (one
+// sequence of 2048 columns: five sources still stage in two round trips,
+// and the extra poll in the chunk-3 storer costs as much as it saves).
+template <int B>
+__device__ __forceinline__ bool x_whole(const Params& p) {
+  return B > 1 || p.H > 2048;
+}
+
 __device__ __forceinline__ float stamped(float v, uint32_t s) {
   return __uint_as_float((__float_as_uint(v) & ~1u) | s);
 }
@@ -799,7 +809,9 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
   // sequence b's source row: base + b * stride
   const float* base;
   size_t stride;
-  if (sum_x || kind == kActMlpNorm) base = p.xa, stride = p.H;
+  const bool whole = x_whole<B>(p);
+  if (sum_x) base = whole ? p.x : p.xa, stride = p.H;
+  else if (kind == kActMlpNorm) base = p.xa, stride = p.H;
   else if (kind == kActAttnOut) base = p.attn, stride = p.QD;
   else base = p.h + (size_t)chunk * p.Fc, stride = p.F;
   const int par = st.stage_cnt & 1;
@@ -810,29 +822,27 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
   compute_bar();  // everyone is done reading the buffer's previous contents
   // one sequence: four (six if rows may be wider than 3072 columns) column
   // groups per thread and pass, so 2048 (4608) columns take one L2 round
-  // trip; with five sources two (one if wide) for the register budget.
-  // Several sequences: all of them and three groups per pass; with five
-  // sources, two sequences and one group
+  // trip; with five sources (x not written whole) two, for the register
+  // budget. Several sequences: all of them and three groups per pass
   constexpr int kNB1 = B, kU1 = B == 1 ? (kWide ? 6 : 4) : 3;
-  constexpr int kNB5 = B == 1 ? 1 : 2, kU5 = B == 1 && !kWide ? 2 : 1;
+  constexpr int kU5 = kWide ? 1 : 2;
+  bool five = false;  // x = xa + the four shares, summed here
+  if constexpr (B == 1) five = sum_x && !whole;
   // the whole vector is staged again if any compute thread loaded a stale
   // word (the decision is taken at the barrier, so it is uniform)
   uint32_t tries = 0;
   uint64_t t0 = 0;
   for (;;) {
     bool bad = false;
-    if (sum_x) {
-      for (int b0 = 0; b0 < B; b0 += kNB5) {
-        float ss[kNB5];
-        stage_pass<B, 5, kNB5, kU5, FX>(p, dst, K, Ks, normw, false, base, stride, b0, step, wst,
-                                        ss, frag, bad);
+    if (five) {
+      if constexpr (B == 1) {
+        float ss[1];
+        stage_pass<B, 5, 1, kU5, FX>(p, dst, K, Ks, normw, false, base, stride, 0, step, wst, ss,
+                                     frag, bad);
         if (normw) {
 #pragma unroll
-          for (int bb = 0; bb < kNB5; ++bb) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) ss[bb] += __shfl_xor_sync(0xffffffffu, ss[bb], o);
-            if (lane == 0 && b0 + bb < B) m->red[par][warp][b0 + bb] = ss[bb];
-          }
+          for (int o = 16; o > 0; o >>= 1) ss[0] += __shfl_xor_sync(0xffffffffu, ss[0], o);
+          if (lane == 0) m->red[par][warp][0] = ss[0];
         }
       }
     } else {
@@ -1816,6 +1826,54 @@ struct EpiPre {
   float2 v[2][B];
 };
 
+// The storer's rows j = in.a0 + lane (+ 32) of every sequence: the sum of NS
+// stamped sources, xa and xpart[0..NS-2] (NS > 1) or x alone (NS = 1), left
+// to right, into pre.v[k][b].x. All loads are issued first, then the stamps
+// are tested, and the whole set is loaded again if one was stale.
+template <int B, int NS>
+__device__ __forceinline__ void load_stamped_rows(const Params& p, Misc* m, const Instr& in,
+                                                  int items, uint32_t st, EpiPre<B>& pre) {
+  const int lane = threadIdx.x & 31;
+  const size_t cs = (size_t)p.B * p.H;
+  float r[2][B][NS];
+  uint32_t tries = 0;
+  uint64_t t0 = 0;
+  for (;;) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int it = lane + 32 * k;
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const size_t o = (size_t)b * p.H + in.a0 + it;
+#pragma unroll
+        for (int c = 0; c < NS; ++c) {
+          r[k][b][c] = 0.f;
+          if (it < items)
+            r[k][b][c] = ld_relaxed(NS == 1 ? p.x + o : (c == 0 ? p.xa + o : p.xpart + (c - 1) * cs + o));
+        }
+      }
+    }
+    bool bad = false;
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+#pragma unroll
+      for (int b = 0; b < B; ++b)
+#pragma unroll
+        for (int c = 0; c < NS; ++c)
+          if (lane + 32 * k < items) bad |= stale1(r[k][b][c], st);
+    if (!bad || !retry_stale(p, m, tries, t0)) break;
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k)
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      float acc = clear1(r[k][b][0]);
+#pragma unroll
+      for (int c = 1; c < NS; ++c) acc += clear1(r[k][b][c]);
+      pre.v[k][b].x = acc;
+    }
+}
+
 template <int B, int FX>
 __device__ __forceinline__ void epilogue_prefetch(const Params& p, Misc* m, const Instr& in,
                                                   EpiPre<B>& pre) {
@@ -1846,12 +1904,9 @@ __device__ __forceinline__ void epilogue_prefetch(const Params& p, Misc* m, cons
       if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) return;
       __syncwarp();  // lane 0's acquire, then every lane's loads
     }
-    // the residual x = xa + the four down-projection shares of the previous
-    // layer: stamped words, complete before this layer's QKV instructions
-    // started, so read without waiting on a counter (all loads first, then
-    // the stamp test, then the slow path if a word was stale)
-    const uint32_t st = stamp_of(p, step_of(in), layer_of(in) - 1);
-    const size_t cs = (size_t)p.B * p.H;
+    // the residual, the previous layer's output x: stamped words, complete
+    // before this layer's QKV instructions started, so read without waiting
+    // on a counter (all loads first, then the stamp test, again if stale)
     if (from_embed) {
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
@@ -1864,43 +1919,15 @@ __device__ __forceinline__ void epilogue_prefetch(const Params& p, Misc* m, cons
         }
       }
     } else {
-      float r[2][B][1 + kChunks];
-      uint32_t tries = 0;
-      uint64_t t0 = 0;
-      for (;;) {
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const int it = lane + 32 * k;
-#pragma unroll
-          for (int b = 0; b < B; ++b) {
-            const size_t o = (size_t)b * p.H + in.a0 + it;
-#pragma unroll
-            for (int c = 0; c <= kChunks; ++c) {
-              r[k][b][c] = 0.f;
-              if (it < items) r[k][b][c] = ld_relaxed(c == 0 ? p.xa + o : p.xpart + (c - 1) * cs + o);
-            }
-          }
-        }
-        bool bad = false;
-#pragma unroll
-        for (int k = 0; k < 2; ++k)
-#pragma unroll
-          for (int b = 0; b < B; ++b)
-#pragma unroll
-            for (int c = 0; c <= kChunks; ++c)
-              if (lane + 32 * k < items) bad |= stale1(r[k][b][c], st);
-        if (!bad || !retry_stale(p, m, tries, t0)) break;
-      }
-#pragma unroll
-      for (int k = 0; k < 2; ++k)
-#pragma unroll
-        for (int b = 0; b < B; ++b) {
-          float acc = clear1(r[k][b][0]);
-#pragma unroll
-          for (int c = 0; c < kChunks; ++c) acc += clear1(r[k][b][1 + c]);
-          pre.v[k][b].x = acc;
-        }
+      const uint32_t st = stamp_of(p, step_of(in), layer_of(in) - 1);
+      if (x_whole<B>(p)) load_stamped_rows<B, 1>(p, m, in, items, st, pre);
+      else load_stamped_rows<B, 1 + kChunks>(p, m, in, items, st, pre);
     }
+  } else if (in.op == MK_OP_DOWN && in.a2 == kChunks - 1 && x_whole<B>(p)) {
+    // chunk 3: its rows' xa and shares of chunks 0..2, written this layer
+    // by other SMs' storers (polled), summed in order; the epilogue adds
+    // this instruction's share and writes x
+    load_stamped_rows<B, kChunks>(p, m, in, items, stamp_of(p, step_of(in), layer_of(in)), pre);
   }
 }
 
@@ -1956,8 +1983,11 @@ __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const
           st_relaxed(p.h + (size_t)b * p.F + j, stamped(silu(v0) * v1, st));
           break;
         case MK_OP_DOWN:
-          // this chunk's share of row j (the readers add the four shares to xa)
-          st_relaxed(p.xpart + ((size_t)in.a2 * p.B + b) * p.H + j, stamped(v0, st));
+          // this chunk's share of row j, or (chunk 3, x written whole) the row of x
+          if (in.a2 == kChunks - 1 && x_whole<B>(p))
+            st_relaxed(p.x + (size_t)b * p.H + j, stamped(pre.v[k][b].x + v0, st));
+          else
+            st_relaxed(p.xpart + ((size_t)in.a2 * p.B + b) * p.H + j, stamped(v0, st));
           break;
         default:  // MK_OP_LMHEAD
           p.logits[(size_t)b * p.V + j] = v0;

@@ -68,9 +68,12 @@ struct Params {
   float* part_ml; // [B][nh][kMaxPartitions][2] attention partials: (m, l)
   float* attn;   // [B][nh*D] reduced attention output (stamped)
   float* h;      // [B][F] SwiGLU hidden state (stamped)
-  float* xpart;  // [kChunks][B][H] down-projection of each chunk of h; the
-                 // layer's output is x = xa + xpart[0] + ... + xpart[3],
-                 // summed in that order by every reader (stamped)
+  float* xpart;  // [kChunks][B][H] down-projection of each chunk of h (stamped)
+  float* x;      // [B][H] the layer's output x = xa + xpart[0] + ... + xpart[3]
+                 // (stamped). With several sequences, or rows wider than 2048
+                 // columns, the storer of the row's chunk-3 instruction sums it
+                 // (its own share in place of xpart[3]) and writes it here;
+                 // otherwise every reader sums the five sources itself
   // stamp of layer 0 of step 0 of this launch (0 or 1); layer l of step s
   // stamps with (stamp + s * L + l) & 1. Every stamped word is written
   // exactly once per layer, so before a layer's write it holds the previous

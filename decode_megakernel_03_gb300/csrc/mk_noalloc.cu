@@ -150,7 +150,7 @@ extern "C" int mk_decode_step_noalloc(const mk_config* cfg, const mk_weights* w,
   const int B = s.B;
   CounterMap cm{s.L, s.nkv, s.B};
   const int n_ctr = cm.count();
-  // pieces 0..5 hold the stamped hand-off words (cleared before each call,
+  // pieces 0..6 hold the stamped hand-off words (cleared before each call,
   // which then runs with stamp 1)
   const size_t sizes[] = {
       sizeof(float) * (size_t)kChunks * B * s.H,                      // down-projection shares
@@ -159,6 +159,7 @@ extern "C" int mk_decode_step_noalloc(const mk_config* cfg, const mk_weights* w,
       sizeof(float) * (size_t)B * s.QD(),                             // attention output
       sizeof(float) * (size_t)B * s.F,                                // h
       sizeof(float) * (size_t)B * s.nkv * 2 * s.D,                    // new k/v rows
+      sizeof(float) * (size_t)B * s.H,                                // layer output x
       sizeof(float) * (size_t)B * s.nh * kMaxPartitions * (s.D + 2),  // attention partials
       sizeof(float2) * (size_t)s.S * (s.D / 2),                       // RoPE table
       sizeof(int) * (size_t)n_ctr,                                    // counters
@@ -209,18 +210,19 @@ extern "C" int mk_decode_step_noalloc(const mk_config* cfg, const mk_weights* w,
   p.attn = reinterpret_cast<float*>(base + offs[3]);
   p.h = reinterpret_cast<float*>(base + offs[4]);
   p.kvn = reinterpret_cast<float*>(base + offs[5]);
+  p.x = reinterpret_cast<float*>(base + offs[6]);
   p.stamp = 1u;  // the cleared words carry stamp 0
-  p.part = reinterpret_cast<float*>(base + offs[6]);
+  p.part = reinterpret_cast<float*>(base + offs[7]);
   // (m, l) after the o rows, in the same piece
   p.part_ml = p.part + (size_t)B * s.nh * kMaxPartitions * s.D;
-  p.rope = reinterpret_cast<const float2*>(base + offs[7]);
-  p.ctr = reinterpret_cast<int*>(base + offs[8]);
+  p.rope = reinterpret_cast<const float2*>(base + offs[8]);
+  p.ctr = reinterpret_cast<int*>(base + offs[9]);
   p.ctr_zero = nullptr;  // cleared by the memset below instead
   p.n_ctr = n_ctr;
-  p.err = reinterpret_cast<int*>(base + offs[9]);
+  p.err = reinterpret_cast<int*>(base + offs[10]);
   p.err_host = nullptr;
-  p.instrs = reinterpret_cast<const Instr*>(base + offs[10]);
-  p.sm_off = reinterpret_cast<const int*>(base + offs[11]);
+  p.instrs = reinterpret_cast<const Instr*>(base + offs[11]);
+  p.sm_off = reinterpret_cast<const int*>(base + offs[12]);
   p.logits = logits_out;
   p.trace = nullptr;
   p.trace_cap = 0;
@@ -253,16 +255,16 @@ extern "C" int mk_decode_step_noalloc(const mk_config* cfg, const mk_weights* w,
   // the host vectors may go out of scope right after the calls
   ce = allow_max_smem(fn, ds->optin);
   for (int b = 0; b < B && ce == cudaSuccess; ++b)
-    ce = cudaMemcpyAsync(base + offs[7] + sizeof(float2) * (size_t)positions[b] * half,
+    ce = cudaMemcpyAsync(base + offs[8] + sizeof(float2) * (size_t)positions[b] * half,
                          rope.data() + (size_t)b * half, sizeof(float2) * half,
                          cudaMemcpyHostToDevice, st);
   if (ce == cudaSuccess)
-    ce = cudaMemcpyAsync(base + offs[10], plan.instrs.data(), sizes[10], cudaMemcpyHostToDevice, st);
+    ce = cudaMemcpyAsync(base + offs[11], plan.instrs.data(), sizes[11], cudaMemcpyHostToDevice, st);
   if (ce == cudaSuccess)
-    ce = cudaMemcpyAsync(base + offs[11], plan.sm_off.data(), sizes[11], cudaMemcpyHostToDevice, st);
-  if (ce == cudaSuccess) ce = cudaMemsetAsync(base, 0, offs[6], st);  // stamped words
-  if (ce == cudaSuccess) ce = cudaMemsetAsync(base + offs[8], 0, sizes[8], st);  // counters
-  if (ce == cudaSuccess) ce = cudaMemsetAsync(base + offs[9], 0, sizes[9], st);  // error word
+    ce = cudaMemcpyAsync(base + offs[12], plan.sm_off.data(), sizes[12], cudaMemcpyHostToDevice, st);
+  if (ce == cudaSuccess) ce = cudaMemsetAsync(base, 0, offs[7], st);  // stamped words
+  if (ce == cudaSuccess) ce = cudaMemsetAsync(base + offs[9], 0, sizes[9], st);  // counters
+  if (ce == cudaSuccess) ce = cudaMemsetAsync(base + offs[10], 0, sizes[10], st);  // error word
   if (ce == cudaSuccess) {
     void* args[] = {&p};
     ce = cudaLaunchCooperativeKernel(fn, dim3(ds->n_sm), dim3(kThreads), args, (size_t)smem_bytes, st);
@@ -271,7 +273,7 @@ extern "C" int mk_decode_step_noalloc(const mk_config* cfg, const mk_weights* w,
   int err_word = 0;
   if (ce == cudaSuccess) ce = cudaStreamSynchronize(st);
   if (ce == cudaSuccess)
-    ce = cudaMemcpy(&err_word, base + offs[9], sizeof(int), cudaMemcpyDeviceToHost);
+    ce = cudaMemcpy(&err_word, base + offs[10], sizeof(int), cudaMemcpyDeviceToHost);
   if (ce != cudaSuccess) {
     if (errmsg && errmsg_cap) std::snprintf(errmsg, errmsg_cap, "CUDA: %s", cudaGetErrorString(ce));
     return MK_ERR_CUDA;

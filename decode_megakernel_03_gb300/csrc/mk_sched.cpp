@@ -224,20 +224,27 @@ struct Builder {
     // 6. the down-projection over the (chunk, row) units of the layer: every
     // SM takes one contiguous range of them, so it reads one chunk of h (two
     // where its range crosses a chunk boundary) once, and its instructions
-    // wait for that chunk alone. Each writes its rows' share of chunk c to
-    // xpart[c]; x = xa + the four shares is formed by its readers (an
-    // instruction that added them up and published x would put one more
-    // release and round trip on the step's critical path: measured slower).
-    // The weights of an SM's range do not depend on anything, so they stream
-    // in while the gate/up chunks still run.
+    // wait for that chunk alone. Chunks 0..2 write their rows' shares to
+    // xpart[c]; with several sequences or rows wider than 2048 columns the
+    // storer of a chunk-3 instruction reads those shares of its rows
+    // (stamped words, polled) and writes x = xa + the four shares, so the
+    // layer's readers load one vector instead of five (else chunk 3 writes
+    // its share too and the readers add them up). The weights of
+    // an SM's range do not depend on anything, so they stream in while the
+    // gate/up chunks still run. When x is written whole, chunk 3 is its own
+    // step (after the others in every queue), so the multi-launch build runs
+    // it as a kernel of its own after theirs.
     {
-      Step st{MK_OP_DOWN, l, {}};
+      const bool whole = x_written_whole(s);
+      Step st{MK_OP_DOWN, l, {}}, st3{MK_OP_DOWN, l, {}};
       spread(kChunks * H, H, rot_of(l, 2 + kChunks), [&](int sm, int a, int b) {
         const int c = a / H;
-        st.items.push_back({sm, make(MK_OP_DOWN, l, a - c * H, b - c * H, c, cm.hch(l, c), Fc,
-                                     cm.xout(l), b - a)});
+        (whole && c == kChunks - 1 ? st3 : st)
+            .items.push_back({sm, make(MK_OP_DOWN, l, a - c * H, b - c * H, c, cm.hch(l, c), Fc,
+                                       cm.xout(l), b - a)});
       });
       steps.push_back(std::move(st));
+      if (whole) steps.push_back(std::move(st3));
     }
   }
 

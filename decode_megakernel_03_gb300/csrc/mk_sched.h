@@ -67,6 +67,12 @@ void choose_partitions(const Shape& s, int n_sm, const int* positions, int* part
 // cheaper despite its extra hop (8B shape: 3520 -> 3478 us/step).
 inline bool fused_reduction(const Shape& s) { return s.B == 1 && s.QD() <= 2048; }
 
+// Several sequences, or rows wider than 2048 columns: the storers of the
+// chunk-3 down-projection instructions write the layer output x whole
+// (the interpreter's x_whole); otherwise its readers sum xa and the four
+// down-projection shares.
+inline bool x_written_whole(const Shape& s) { return s.B > 1 || s.H > 2048; }
+
 // Items (rows or row pairs) per GEMV instruction, bounded by the result
 // buffer the storer drains.
 int item_cap_for(const Shape& s);

@@ -128,12 +128,37 @@ def test_counter_targets(case):
     assert np.all(tg[ins["wait_ctr"][w]] > 0), "every awaited counter is produced"
 
 
+def _x_whole(shape, B):
+    """Whether the chunk-3 down-projection storers write the layer output x
+    whole (several sequences, or rows wider than 2048 columns)."""
+    return B > 1 or shape.hidden > 2048
+
+
+def _data_deps(ins, whole=True):
+    """The waits that are not counters: when x is written whole, the storer
+    of a chunk-3 down-projection instruction polls the shares of chunks 0..2
+    (stamped words) before it writes the layer's output, so it publishes only
+    after every chunk-0..2 instruction of its layer (and step) has published.
+    Returns {instruction index: [instruction indices it waits for]}. (The
+    simulations always add these waits: more waits cannot hide a deadlock.)"""
+    if not whole:
+        return {}
+    dn = np.nonzero(ins["op"] == mk.OP_DOWN)[0]
+    by_layer = {}
+    for i in dn:
+        if int(ins["a2"][i]) < 3:
+            by_layer.setdefault(int(ins["layer"][i]), []).append(int(i))
+    return {int(i): by_layer.get(int(ins["layer"][i]), []) for i in dn if int(ins["a2"][i]) == 3}
+
+
 def _simulate(ins, off, tg, n_sm, pick):
     """Runs the queues on a CPU model: an SM may run the head of its queue
     once that instruction's counter reached its target."""
     ctr = np.zeros(len(tg), dtype=np.int64)
     head = [int(off[s]) for s in range(n_sm)]
     end = [int(off[s + 1]) for s in range(n_sm)]
+    deps = _data_deps(ins)
+    finished = np.zeros(len(ins), dtype=bool)
     done = 0
     total = int(off[-1])
     while done < total:
@@ -142,7 +167,7 @@ def _simulate(ins, off, tg, n_sm, pick):
             if head[s] < end[s]:
                 i = head[s]
                 c = ins["wait_ctr"][i]
-                if c < 0 or ctr[c] >= ins["wait_target"][i]:
+                if (c < 0 or ctr[c] >= ins["wait_target"][i]) and all(finished[d] for d in deps.get(i, ())):
                     ready.append(s)
         if not ready:
             return False
@@ -150,6 +175,7 @@ def _simulate(ins, off, tg, n_sm, pick):
         i = head[s]
         if ins["sig_ctr"][i] >= 0:
             ctr[ins["sig_ctr"][i]] += ins["sig_amount"][i]
+        finished[i] = True
         head[s] += 1
         done += 1
     np.testing.assert_array_equal(ctr, tg)
@@ -177,7 +203,7 @@ def test_simulation_detects_a_bad_schedule():
     assert not _simulate(bad, off, tg, 4, lambda r: r[0])
 
 
-def _happens_before(ins, off, n_sm):
+def _happens_before(ins, off, n_sm, whole=True):
     """Ancestor sets (as Python int bitmasks) of the DAG made of per-SM program
     order and counter edges (every producer of a counter precedes every
     instruction that waits for it)."""
@@ -195,6 +221,8 @@ def _happens_before(ins, off, n_sm):
         c = int(ins["wait_ctr"][i])
         if c >= 0:
             preds[i].extend(producers[c])
+    for i, ds in _data_deps(ins, whole).items():
+        preds[i].extend(ds)
     # topological order by Kahn
     indeg = [len(p) for p in preds]
     succ = [[] for _ in range(n)]
@@ -221,16 +249,21 @@ def _happens_before(ins, off, n_sm):
 
 def _accesses(ins, shape, B):
     """Exact element keys of the shared scratch each instruction reads and
-    writes (q, xa, the four down-projection shares, h, partials and attention
+    writes (q, xa, the down-projection shares, x, h, partials and attention
     output are one buffer reused by every layer; the KV cache is per layer).
-    A layer's output x is xa + its four down-projection shares, read by the
-    next layer's QKV (all rows) and O-projection (its rows) and the LM head."""
+    A layer's output x (xa + its four down-projection shares, summed by the
+    chunk-3 instructions' storers) is read by the next layer's QKV (all rows)
+    and O-projection (its rows) and the LM head."""
     L, H, D, nkv = shape.n_layers, shape.hidden, shape.head_dim, shape.n_kv_heads
     G = shape.n_heads // nkv
     half = D // 2
     per = (G + 2) * half
     Fc = shape.ffn // 4
+    whole = _x_whole(shape, B)
+
     def x_rows(lo, hi):
+        if whole:
+            return {("x", k) for k in range(lo, hi)}
         return ({("xa", k) for k in range(lo, hi)} |
                 {("xpart", c, k) for c in range(4) for k in range(lo, hi)})
 
@@ -265,22 +298,30 @@ def _accesses(ins, shape, B):
             W |= {("h", j) for j in range(a0, a1)}
         elif op == mk.OP_DOWN:
             R |= {("h", j) for j in range(a2 * Fc, (a2 + 1) * Fc)}
-            W |= {("xpart", a2, k) for k in range(a0, a1)}
+            if a2 == 3 and whole:  # the storer sums xa and the other shares into x
+                R |= {("xa", k) for k in range(a0, a1)}
+                R |= {("xpart", c, k) for c in range(3) for k in range(a0, a1)}
+                W |= x_rows(a0, a1)
+            else:
+                W |= {("xpart", a2, k) for k in range(a0, a1)}
         elif op == mk.OP_LMHEAD:
             R |= x_rows(0, H)
         acc.append((R, W))
     return acc
 
 
+WIDE = synth.ModelShape("wide", 2, 2304, 4, 2, 64, 1024, 512, tied=False, rope_theta=1e4)
+
+
 @pytest.mark.parametrize("case", [(synth.TINY, 1, 128, 7, [70]), (synth.TINY, 2, 128, 3, [5, 90]),
-                                  (synth.TINY, 1, 128, 152, [100])],
+                                  (synth.TINY, 1, 128, 152, [100]), (WIDE, 1, 128, 5, [40])],
                          ids=lambda c: f"B{c[1]}-sm{c[3]}")
 def test_no_unordered_hazards(case):
     """Every pair of accesses to one scratch element, at least one of them a
     write (RAW, WAR, WAW), is ordered by program order or a counter chain."""
     shape, B, S, n_sm, pos = case
     ins, off, tg, sm = _plan(*case)
-    anc = _happens_before(ins, off, n_sm)
+    anc = _happens_before(ins, off, n_sm, _x_whole(shape, B))
     touches = {}
     for i, (R, W) in enumerate(_accesses(ins, shape, B)):
         for k in R:
@@ -298,6 +339,32 @@ def test_no_unordered_hazards(case):
                     raise AssertionError(f"unordered access to {key}: #{wi} {ins[wi]} / #{j} {ins[j]}")
                 checked += 1
     assert checked > 1000
+
+
+def _unordered(ins, anc, accs):
+    touches = {}
+    for i, (R, W) in enumerate(accs):
+        for k in R:
+            touches.setdefault(k, []).append((i, False))
+        for k in W:
+            touches.setdefault(k, []).append((i, True))
+    for key, lst in touches.items():
+        for wi in [i for i, w in lst if w]:
+            for j, _ in lst:
+                if j != wi and not ((anc[j] >> wi) & 1 or (anc[wi] >> j) & 1):
+                    return key
+    return None
+
+
+def test_hazard_model_needs_the_chunk3_poll():
+    """Without the chunk-3 storers' poll of the other shares, writing x whole
+    would read the shares unordered: the hazard check must find it."""
+    case = (synth.TINY, 2, 128, 3, [5, 90])
+    ins, off, tg, sm = _plan(*case)
+    accs = _accesses(ins, synth.TINY, 2)
+    assert _unordered(ins, _happens_before(ins, off, 3, True), accs) is None
+    key = _unordered(ins, _happens_before(ins, off, 3, False), accs)
+    assert key is not None and key[0] == "xpart"
 
 
 @pytest.mark.parametrize("B", [1, 8])
@@ -351,13 +418,15 @@ def _simulate_dynamic(ins, off, tg, n_sm, pick):
     end = [int(off[s + 1]) for s in range(n_sm)]
     next_ticket = 0
     taken = np.zeros(n_sm, dtype=np.int64)
+    deps = _data_deps(ins)
+    finished = np.zeros(len(ins), dtype=bool)
     while any(head[s] < end[s] for s in range(n_sm)):
         ready = []
         for s in range(n_sm):
             if head[s] < end[s]:
                 i = head[s]
                 c = ins["wait_ctr"][i]
-                if c < 0 or ctr[c] >= ins["wait_target"][i]:
+                if (c < 0 or ctr[c] >= ins["wait_target"][i]) and all(finished[d] for d in deps.get(i, ())):
                     ready.append(s)
         if not ready:
             return False, None
@@ -374,6 +443,7 @@ def _simulate_dynamic(ins, off, tg, n_sm, pick):
             continue
         if r["sig_ctr"] >= 0:
             ctr[r["sig_ctr"]] += r["sig_amount"]
+        finished[head[s]] = True
         head[s] += 1
     return np.array_equal(ctr, tg), taken
 
@@ -478,6 +548,9 @@ def _simulate_roles(ins, off, tg, n_sm, shape, B, pos, ring, pick, prefill=False
         c = int(r["wait_ctr"])
         return c < 0 or ctr[c] >= r["wait_target"]
 
+    deps = _data_deps(ins)
+    stored = np.zeros(len(ins), dtype=bool)
+
     def enter(s):
         if cp[s] < n[s] and _critical(I(s, cp[s])):
             hold[s] = cp[s]
@@ -514,8 +587,9 @@ def _simulate_roles(ins, off, tg, n_sm, shape, B, pos, ring, pick, prefill=False
                         acts.append(("use", s))
                 else:
                     acts.append(("cdone", s))
-            # storer
-            if sp[s] < cp[s]:
+            # storer (a chunk-3 down-projection's storer polls the other
+            # chunks' shares first)
+            if sp[s] < cp[s] and all(stored[d] for d in deps.get(int(off[s]) + sp[s], ())):
                 acts.append(("store", s))
         if not acts:
             return False
@@ -544,6 +618,7 @@ def _simulate_roles(ins, off, tg, n_sm, shape, B, pos, ring, pick, prefill=False
             r = I(s, sp[s])
             if r["sig_ctr"] >= 0:
                 ctr[r["sig_ctr"]] += r["sig_amount"]
+            stored[int(off[s]) + sp[s]] = True
             sp[s] += 1
     return bool(np.array_equal(ctr, tg))
 
