@@ -230,7 +230,70 @@ def trace_summary(args, wl):
             hops.setdefault(mk.OPS[int(ins["op"][k])], []).append(tr[k] - prod[c])
     out["hops_us"] = {k: {"median": float(np.median(v)), "p90": float(np.percentile(v, 90))}
                       for k, v in hops.items()}
+    out["copy_issue"] = copy_issue_profile(rec, ins, shape, wl, pos, tr)
     print(json.dumps(out), flush=True)
+
+
+def copy_issue_profile(rec, ins, shape, wl, pos, tr):
+    """How fast the loaders hand bytes to the memory system, from the trace's
+    per-instruction copy issue windows: each instruction's bytes (weight rows,
+    or an attention unit's cached K and V rows) spread evenly over its window
+    [first copy issued, last copy issued] on its SM, summed over SMs in
+    0.25 us bins. A loader issues a page only into a free ring slot, so while
+    the rate stays below the HBM bandwidth the memory system has less work
+    than it could do. Per middle layer (2 .. L-3), between its first QKV
+    instruction's input and the next layer's: the mean rate over the
+    attention chain (until the first gate/up instruction's input) and over
+    the MLP, and the fraction of the layer's bins below half the measured
+    HBM peak."""
+    import numpy as np
+    from decode_megakernel_03_gb300 import mk
+    peak_gbs, _ = read_peaks()
+    H, D, QD, F = shape.hidden, shape.head_dim, shape.n_heads * shape.head_dim, shape.ffn
+    nbytes = np.zeros(len(rec))
+    for k in range(len(rec)):
+        op, a0, a1, a2 = int(ins["op"][k]), int(ins["a0"][k]), int(ins["a1"][k]), int(ins["a2"][k])
+        items = a1 - a0
+        if op == mk.OP_QKV or op == mk.OP_GATEUP:
+            nbytes[k] = items * 2 * H * 2
+        elif op == mk.OP_OPROJ:
+            nbytes[k] = items * QD * 2
+        elif op == mk.OP_DOWN:
+            nbytes[k] = items * (F // 4) * 2
+        elif op == mk.OP_LMHEAD:
+            nbytes[k] = items * H * 2
+        elif op == mk.OP_ATTN:
+            p = pos[a0] + 1
+            pidx, P = a2 >> 16, a2 & 0xFFFF
+            keys = max(0, min((pidx + 1) * p // P, p - 1) - pidx * p // P)
+            nbytes[k] = keys * D * 2 * 2
+    t0 = rec["t_start"].min()
+    f = (rec["t_issue_first"].astype(np.float64) - t0) / 1e3
+    l_ = (rec["t_issue_last"].astype(np.float64) - t0) / 1e3
+    ok = (nbytes > 0) & (rec["t_issue_first"] > 0) & (rec["t_issue_last"] >= rec["t_issue_first"])
+    width = 0.25
+    nb = int(np.ceil(l_[ok].max() / width)) + 2
+    rate = np.zeros(nb)  # bytes per bin
+    for a, b, n in zip(f[ok], l_[ok], nbytes[ok]):
+        i0, i1 = int(a // width), int(b // width)
+        rate[i0:i1 + 1] += n / (i1 - i0 + 1)
+    gbs = rate / (width * 1e3)  # bytes per us / 1e3 = GB/s
+    op, layer = rec["op"], rec["layer"]
+    L = shape.n_layers
+    res = []
+    for l in range(2, L - 2):
+        a = tr[(layer == l) & (op == mk.OP_QKV)].min()
+        m = tr[(layer == l) & (op == mk.OP_GATEUP)].min()
+        e = tr[(layer == l + 1) & (op == mk.OP_QKV)].min()
+        ia, im, ie = int(a // width), int(m // width), int(e // width)
+        res.append((gbs[ia:im].mean(), gbs[im:ie].mean(), float(np.mean(gbs[ia:ie] < peak_gbs / 2)),
+                    m - a, e - m))
+    r = np.array(res)
+    return {"bin_us": width, "peak_gbs": peak_gbs,
+            "attention_chain_us": float(r[:, 3].mean()), "mlp_us": float(r[:, 4].mean()),
+            "attention_chain_issue_gbs": float(r[:, 0].mean()),
+            "mlp_issue_gbs": float(r[:, 1].mean()),
+            "layer_fraction_below_half_peak": float(r[:, 2].mean())}
 
 
 def replica_env():
@@ -437,35 +500,39 @@ def run_gpu(args, wl):
     greedy32_tps = 32 * wl.batch / (time.perf_counter() - t0w)
 
     # the same steps on a paged KV cache: the caches' contents in pools of
-    # 16-position blocks in shuffled order, a host block table per step
-    bs = 16
-    mb = wl.capacity // bs
-    n_blocks = wl.batch * mb
-    perm = torch.randperm(n_blocks, generator=torch.Generator().manual_seed(7))
-    table = perm.view(wl.batch, mb).numpy().astype(np.int32)
-    def to_pool(c):
-        blocks = c[:, :, :mb * bs].reshape(wl.batch, shape.n_kv_heads, mb, bs, shape.head_dim)
-        blocks = blocks.permute(0, 2, 1, 3, 4).reshape(n_blocks, shape.n_kv_heads, bs,
-                                                       shape.head_dim)
-        pool = torch.empty_like(blocks)
-        pool[perm.to(dev)] = blocks
-        return pool
-    kp, vp = [to_pool(c) for c in kc], [to_pool(c) for c in vc]
-    dp = mk.Decoder(shape, w, kp, vp, wl.batch, paged=(bs, n_blocks, mb * bs))
-    for s in range(W):
-        t, p = tok_pos(s)
-        dp.step_paged(t, p, table, logits)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for s in range(K):
-        t, p = tok_pos(s)
-        dp.step_paged(t, p, table, logits)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    assert dp.status() == mk.MK_OK, dp.last_error()
-    paged_ms = e0.elapsed_time(e1) / K
-    dp.close()
-    del kp, vp
+    # 16-position blocks (and, second, 64-position blocks: one run per
+    # 64-key page boundary instead of four) in shuffled order, a host block
+    # table per step
+    paged_ms = {}
+    for bs in (16, 64):
+        mb = wl.capacity // bs
+        n_blocks = wl.batch * mb
+        perm = torch.randperm(n_blocks, generator=torch.Generator().manual_seed(7))
+        table = perm.view(wl.batch, mb).numpy().astype(np.int32)
+
+        def to_pool(c):
+            blocks = c[:, :, :mb * bs].reshape(wl.batch, shape.n_kv_heads, mb, bs, shape.head_dim)
+            blocks = blocks.permute(0, 2, 1, 3, 4).reshape(n_blocks, shape.n_kv_heads, bs,
+                                                           shape.head_dim)
+            pool = torch.empty_like(blocks)
+            pool[perm.to(dev)] = blocks
+            return pool
+        kp, vp = [to_pool(c) for c in kc], [to_pool(c) for c in vc]
+        dp = mk.Decoder(shape, w, kp, vp, wl.batch, paged=(bs, n_blocks, mb * bs))
+        for s in range(W):
+            t, p = tok_pos(s)
+            dp.step_paged(t, p, table, logits)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for s in range(K):
+            t, p = tok_pos(s)
+            dp.step_paged(t, p, table, logits)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        assert dp.status() == mk.MK_OK, dp.last_error()
+        paged_ms[bs] = e0.elapsed_time(e1) / K
+        dp.close()
+        del kp, vp
 
     # host side of a step (no device work timed): the C-ABI call with its plan
     # cached (argument checks, plan lookup, launch), and building a plan
@@ -560,14 +627,11 @@ def run_gpu(args, wl):
                 "multilaunch_us": multi_ms * 1e3,
                 "multilaunch_graph_us": graph_ms * 1e3,
                 # per layer QKV, attention, (reduction,) O-projection, gate/up,
-                # down (, down chunk 3): one sequence with at most 2048
-                # attention columns has no reduction instruction (the
-                # O-projection's staging reduces); several sequences or rows
-                # wider than 2048 columns run the chunk-3 down-projection,
-                # which writes the layer output whole, as a kernel of its own
+                # down; one sequence with at most 2048 attention columns has
+                # no reduction instruction (the O-projection's staging reduces)
                 "multilaunch_launches_per_step":
-                    (5 + (0 if wl.batch == 1 and shape.n_heads * shape.head_dim <= 2048 else 1)
-                     + (1 if wl.batch > 1 or shape.hidden > 2048 else 0)) * shape.n_layers + 1,
+                    (5 if wl.batch == 1 and shape.n_heads * shape.head_dim <= 2048 else 6)
+                    * shape.n_layers + 1,
                 "recovered_overhead_vs_multilaunch": (multi_ms - ms) / (multi_ms - t_min_ms),
                 "recovered_overhead_vs_graph": (graph_ms - ms) / (graph_ms - t_min_ms),
                 "overhead_megakernel": (ms - t_min_ms) / ms,
@@ -578,8 +642,9 @@ def run_gpu(args, wl):
                 "greedy_one_launch_us_per_step": greedy_one_ms * 1e3,
                 "greedy_32_one_launch_tokens_per_s": greedy32_tps,
                 "greedy_32_host_argmax_loop_tokens_per_s": host_loop_tps,
-                "paged_kv_us_per_step": paged_ms * 1e3,
-                "paged_kv_block_size": bs,
+                "paged_kv_us_per_step": paged_ms[16] * 1e3,
+                "paged_kv_block_size": 16,
+                "paged_kv_64_us_per_step": paged_ms[64] * 1e3,
                 "host_step_call_us": host_call_us,
                 "host_plan_build_us": host_plan_us,
                 "prefill_tokens_per_s": prefill_tps,

@@ -190,10 +190,13 @@ __device__ __forceinline__ uint32_t stamp_of(const Params& p, int step, int laye
 // down-projection instructions (several sequences, or rows wider than 2048
 // columns), or left as xa and four shares that every reader adds up (one
 // sequence of 2048 columns: five sources still stage in two round trips,
-// and the extra poll in the chunk-3 storer costs as much as it saves).
+// and the extra poll in the chunk-3 storer costs as much as it saves; and
+// the multi-launch build, whose kernel boundaries leave nothing to poll).
+// Both forms give the same bits: x = ((((xa + s0) + s1) + s2) + s3), each
+// term and the sum rounded toward zero to 22 mantissa bits.
 template <int B>
 __device__ __forceinline__ bool x_whole(const Params& p) {
-  return B > 1 || p.H > 2048;
+  return !p.no_waits && (B > 1 || p.H > 2048);
 }
 
 __device__ __forceinline__ float stamped(float v, uint32_t s) {
@@ -754,6 +757,8 @@ __device__ __forceinline__ void stage_pass(const Params& p, float* dst, int K, i
               x.z += v[sidx][bb][u].z;
               x.w += v[sidx][bb][u].w;
             }
+            // the layer output as the chunk-3 storer would have written it
+            if (NS > 1) x = clear4(x);
           }
           ss[bb] += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
           if (normw) {
@@ -822,12 +827,12 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
   compute_bar();  // everyone is done reading the buffer's previous contents
   // one sequence: four (six if rows may be wider than 3072 columns) column
   // groups per thread and pass, so 2048 (4608) columns take one L2 round
-  // trip; with five sources (x not written whole) two, for the register
-  // budget. Several sequences: all of them and three groups per pass
+  // trip; with five sources (x not written whole) two (one if wide), for
+  // the register budget. Several sequences: all of them and three groups per
+  // pass; with five sources, two sequences and one group
   constexpr int kNB1 = B, kU1 = B == 1 ? (kWide ? 6 : 4) : 3;
-  constexpr int kU5 = kWide ? 1 : 2;
-  bool five = false;  // x = xa + the four shares, summed here
-  if constexpr (B == 1) five = sum_x && !whole;
+  constexpr int kNB5 = B == 1 ? 1 : 2, kU5 = B == 1 && !kWide ? 2 : 1;
+  const bool five = sum_x && !whole;  // x = xa + the four shares, summed here
   // the whole vector is staged again if any compute thread loaded a stale
   // word (the decision is taken at the barrier, so it is uniform)
   uint32_t tries = 0;
@@ -835,14 +840,17 @@ __device__ __forceinline__ void stage(const Params& p, Misc* m, uint8_t* smem, S
   for (;;) {
     bool bad = false;
     if (five) {
-      if constexpr (B == 1) {
-        float ss[1];
-        stage_pass<B, 5, 1, kU5, FX>(p, dst, K, Ks, normw, false, base, stride, 0, step, wst, ss,
-                                     frag, bad);
+      for (int b0 = 0; b0 < B; b0 += kNB5) {
+        float ss[kNB5];
+        stage_pass<B, 5, kNB5, kU5, FX>(p, dst, K, Ks, normw, false, base, stride, b0, step, wst,
+                                        ss, frag, bad);
         if (normw) {
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) ss[0] += __shfl_xor_sync(0xffffffffu, ss[0], o);
-          if (lane == 0) m->red[par][warp][0] = ss[0];
+          for (int bb = 0; bb < kNB5; ++bb) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ss[bb] += __shfl_xor_sync(0xffffffffu, ss[bb], o);
+            if (lane == 0 && b0 + bb < B) m->red[par][warp][b0 + bb] = ss[bb];
+          }
         }
       }
     } else {
@@ -1920,8 +1928,16 @@ __device__ __forceinline__ void epilogue_prefetch(const Params& p, Misc* m, cons
       }
     } else {
       const uint32_t st = stamp_of(p, step_of(in), layer_of(in) - 1);
-      if (x_whole<B>(p)) load_stamped_rows<B, 1>(p, m, in, items, st, pre);
-      else load_stamped_rows<B, 1 + kChunks>(p, m, in, items, st, pre);
+      if (x_whole<B>(p)) {
+        load_stamped_rows<B, 1>(p, m, in, items, st, pre);
+      } else {
+        load_stamped_rows<B, 1 + kChunks>(p, m, in, items, st, pre);
+        // the layer output as the chunk-3 storer would have written it
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+#pragma unroll
+          for (int b = 0; b < B; ++b) pre.v[k][b].x = clear1(pre.v[k][b].x);
+      }
     }
   } else if (in.op == MK_OP_DOWN && in.a2 == kChunks - 1 && x_whole<B>(p)) {
     // chunk 3: its rows' xa and shares of chunks 0..2, written this layer
@@ -1985,7 +2001,7 @@ __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const
         case MK_OP_DOWN:
           // this chunk's share of row j, or (chunk 3, x written whole) the row of x
           if (in.a2 == kChunks - 1 && x_whole<B>(p))
-            st_relaxed(p.x + (size_t)b * p.H + j, stamped(pre.v[k][b].x + v0, st));
+            st_relaxed(p.x + (size_t)b * p.H + j, stamped(pre.v[k][b].x + clear1(v0), st));
           else
             st_relaxed(p.xpart + ((size_t)in.a2 * p.B + b) * p.H + j, stamped(v0, st));
           break;

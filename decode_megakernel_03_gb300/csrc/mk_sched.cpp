@@ -232,8 +232,8 @@ struct Builder {
     // its share too and the readers add them up). The weights of
     // an SM's range do not depend on anything, so they stream in while the
     // gate/up chunks still run. When x is written whole, chunk 3 is its own
-    // step (after the others in every queue), so the multi-launch build runs
-    // it as a kernel of its own after theirs.
+    // step (after the others in every queue); the multi-launch build, where
+    // the readers add the shares up, still runs them as one kernel.
     {
       const bool whole = x_written_whole(s);
       Step st{MK_OP_DOWN, l, {}}, st3{MK_OP_DOWN, l, {}};
@@ -327,21 +327,21 @@ bool build_plan(const Shape& s, int n_sm, const int* parts, Plan* out, std::stri
     }
 
   // multi-launch build: one kernel per (layer, instruction type); the gate/up
-  // chunks form one kernel and the down-projection the next
+  // chunks form one kernel and the down-projection chunks the next
   out->phases.clear();
   size_t i = 0;
   while (i < bld.steps.size()) {
     int op = bld.steps[i].op, layer = bld.steps[i].layer;
     std::vector<const std::vector<std::pair<int, Instr>>*> lists;
-    if (op == MK_OP_GATEUP) {
-      // collect all GATEUP steps of this layer into one kernel
+    if (op == MK_OP_GATEUP || op == MK_OP_DOWN) {
+      // collect all GATEUP (DOWN) steps of this layer into one kernel
       size_t j = i;
       std::vector<const std::vector<std::pair<int, Instr>>*> gu;
-      while (j < bld.steps.size() && bld.steps[j].layer == layer && bld.steps[j].op == MK_OP_GATEUP) {
+      while (j < bld.steps.size() && bld.steps[j].layer == layer && bld.steps[j].op == op) {
         gu.push_back(&bld.steps[j].items);
         ++j;
       }
-      Phase p1{MK_OP_GATEUP, layer, {}, {}};
+      Phase p1{op, layer, {}, {}};
       cut_queues(gu, n_sm, &p1.instrs, &p1.sm_off);
       out->phases.push_back(std::move(p1));
       i = j;
