@@ -179,7 +179,12 @@ int mk_decode_step_multilaunch(mk_handle* h, const int32_t* token_ids,
                                void* stream, int use_graph);
 
 /* Synchronises `stream`, reads the device error word and clears it.
-   Returns MK_OK, MK_ERR_TIMEOUT or MK_ERR_CUDA. */
+   Returns MK_OK, MK_ERR_TIMEOUT or MK_ERR_CUDA. The error word is
+   code << 24 | site (reported in mk_last_error): site 1 a counter wait,
+   2 a page or block-table copy, 3 a result buffer or ticket, 5 a value
+   handed between instructions that kept its previous layer's stamp. After
+   an error the handle also clears those hand-off values, so the next step
+   starts from a known state. */
 int mk_get_status(mk_handle* h, void* stream);
 
 /* Frees everything the handle owns (synchronising the device first).

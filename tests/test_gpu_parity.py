@@ -111,6 +111,36 @@ def test_multilaunch_graph_and_generic_kernel_are_bit_identical(shape_name):
             np.testing.assert_array_equal(a, b)
 
 
+WIDE = synth.ModelShape("wide", 2, 2304, 4, 2, 64, 1024, 4096, tied=False, rope_theta=10000.0)
+
+
+@pytest.mark.parametrize("batch", [1, 2])
+def test_wide_rows_whole_x_matches_the_oracle_and_the_multilaunch_build(batch):
+    """Rows wider than 2048 columns: the chunk-3 down-projection storers write
+    the layer output whole in the megakernel, while the multi-launch build's
+    readers add up its five sources; both round the same way, so the builds
+    agree bit for bit, and both match the oracle."""
+    cap = 128
+    ctx = tuple(40 + 17 * b for b in range(batch))
+    outs = {}
+    tally = Tally()
+    for mode in ("mega", "multi", "graph"):
+        pair = Pair(WIDE, batch, cap, ctx=ctx)
+        res = []
+        for s_ in range(3):
+            tok = [(71 * s_ + 13 * b + 5) % WIDE.vocab for b in range(batch)]
+            pos = [c + s_ for c in ctx]
+            got = pair.gpu_step(tok, pos, mode=mode).copy()
+            if mode == "mega":
+                tally.add(compare_logits(got, pair.oracle_step(tok, pos)))
+            res.append(got)
+        outs[mode] = np.stack(res)
+        pair.close()
+    np.testing.assert_array_equal(outs["mega"], outs["multi"])
+    np.testing.assert_array_equal(outs["mega"], outs["graph"])
+    print("wide", batch, tally.check())
+
+
 @pytest.mark.parametrize("name", ["llama1b", "llama1b_ctx8k", "llama8b", "llama1b_b8"])
 def test_full_size_parity(name):
     """Each workload at full size on its seeded context, over every one of its
