@@ -1712,10 +1712,13 @@ __device__ void compute_role(const Params& p, Misc* m, uint8_t* smem, const Inst
     // 1. dependency: one thread polls, the other compute warps meet it at a
     // barrier. An instruction whose inputs are all stamped words and small
     // polls the words themselves instead (the attention's q and new k/v rows;
-    // with one sequence also the gate/up's xa and the down-projection's
-    // chunk of h): the counter would only add a round trip
+    // with one sequence also the gate/up's xa, the down-projection's chunk of
+    // h, and the QKV staging's x where it is written whole): the counter
+    // would only add a round trip. (Polling x's five sources, or eight
+    // sequences' x, was slower: 613.5 vs 607.0 and 1491.1 vs 1426.7 us/step.)
     const bool polls_inputs =
-        in.op == MK_OP_ATTN || (B == 1 && (in.op == MK_OP_GATEUP || in.op == MK_OP_DOWN));
+        in.op == MK_OP_ATTN || (B == 1 && (in.op == MK_OP_GATEUP || in.op == MK_OP_DOWN)) ||
+        (B == 1 && in.op == MK_OP_QKV && layer_of(in) > 0 && x_whole<B>(p) && !(FX & kFxPaged));
     if (!p.no_waits && in.wait_ctr >= 0 && !polls_inputs &&
         !(in.wait_ctr == known_ctr && in.wait_target <= known_tgt)) {
       if (warp == 0 && lane == 0) wait_counter(p, m, in.wait_ctr, in.wait_target);
