@@ -2,26 +2,32 @@
 // instruction queue ("3 · L'interpréteur sur GPU", §3.2). Every instruction is
 // split over three warp roles that walk the same queue independently:
 //
-//   loader  (1 warp)   streams the instruction's bf16 weight rows into 16 KB
-//                      shared-memory pages with bulk asynchronous copies; it
-//                      waits only for free pages, never for counters, so the
-//                      next instruction's weights load while the current one
-//                      still waits or computes (§3.3, the page allocator);
-//   compute (6 warps)  waits for the instruction's input counter, stages the
+//   loader  (1 warp)   streams the instruction's bf16 weight rows (and an
+//                      attention unit's cached keys) into 16 KB shared-memory
+//                      pages with bulk asynchronous copies; it waits for free
+//                      pages, and for a counter only where a copy would read
+//                      this launch's own writes, so the next instruction's
+//                      weights load while the current one still waits or
+//                      computes (§3.3, the page allocator);
+//   compute (6 warps)  waits for the instruction's input (its counter, or for
+//                      small stamped inputs the words themselves), stages the
 //                      activations, and runs the dot products / attention;
 //                      each page is handed back as soon as it has been read;
 //   storer  (1 warp)   applies the epilogue (RoPE + KV append, residual adds,
-//                      SiLU, chunk accumulation), writes the outputs, then
-//                      fences and bumps the output counter with release
-//                      semantics (§3.4, counters in global memory).
+//                      SiLU, the layer output), writes the outputs as stamped
+//                      words and bumps the output counter (§3.4, counters in
+//                      global memory): a scheduling hint without a fence, or
+//                      a release where a reader reads plain words after an
+//                      acquire (see "stamped hand-offs" below).
 //
 // The same kernel also serves the multi-launch comparison build: launched once
 // per (layer, instruction type) with counter waits switched off, kernel
 // boundaries order the work instead.
 //
-// Every wait (counter, page, result buffer) is bounded by a %globaltimer
-// deadline; on expiry the kernel records MK_ERR_TIMEOUT in the error word,
-// the other CTAs notice it and all of them drain their copies and return.
+// Every wait (counter, page, result buffer, stamped word) is bounded by a
+// %globaltimer deadline; on expiry the kernel records MK_ERR_TIMEOUT in the
+// error word, the other CTAs notice it and all of them drain their copies
+// and return.
 //
 // The kernel is a template over the batch B and, optionally, the head
 // dimension DS and the q-heads per kv-head GS (0: read from the parameters
@@ -168,7 +174,8 @@ __device__ __forceinline__ bool wait_counter(const Params& p, Misc* m, int ctr, 
 
 // ---- stamped hand-offs ------------------------------------------------------
 // A value one instruction hands to another within a step (q, the new k/v
-// rows, the attention output, xa, h, the down-projection shares) is an fp32
+// rows, the attention output, xa, h, the down-projection shares, the layer
+// output x where it is written whole) is an fp32
 // word whose lowest mantissa bit holds a stamp, written with a relaxed
 // store. Each such word is written exactly once per layer, and the stamp is
 // the parity of its layer's index in the launch sequence (layer l of step s
@@ -229,9 +236,10 @@ __device__ __forceinline__ float4 clear4(const float4& v) {
 __device__ __forceinline__ float2 clear2(const float2& v) { return make_float2(clear1(v.x), clear1(v.y)); }
 
 // A batch of loads that found a stale word is loaded again, whole: no
-// per-word slow path, so the batch's code appears once (it is almost never
-// repeated: the counter a reader polls first is bumped after the words were
-// stored). Whether to try again: false on an abort, an error raised by
+// per-word slow path, so the batch's code appears once (after a counter
+// wait it is almost never repeated, the counter being bumped after the words
+// were stored; an instruction that polls its input words instead repeats it
+// until they land). Whether to try again: false on an abort, an error raised by
 // another CTA, or after the timeout (the step's results are then void).
 static __device__ __noinline__ bool retry_stale(const Params& p, Misc* m, uint32_t& it,
                                                 uint64_t& t0) {
@@ -2043,9 +2051,11 @@ __device__ __forceinline__ void epilogue(const Params& p, const Instr& in, const
 }
 
 // The storer drains finished instructions in order: epilogue, then lane 0
-// publishes the instruction with a release-add on its counter. What the
-// epilogue needs from global memory is fetched before waiting for the compute
-// warps, so the epilogue itself touches only registers and shared memory.
+// bumps the instruction's counter, with a release-add where a reader reads
+// plain words after acquiring it and as a relaxed hint where the outputs are
+// stamped words. What the epilogue needs from global memory is fetched
+// before waiting for the compute warps, so the epilogue itself touches only
+// registers and shared memory.
 // (Publishing several instructions behind one fence was measured slower: it
 // delays the first counter of each batch, which sits on the critical path.)
 template <int B, int FX>
