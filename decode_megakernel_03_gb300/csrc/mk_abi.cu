@@ -166,7 +166,8 @@ int get_plan(mk_handle* h, const int32_t* pos, PlanEntry** out, int dyn) {
       *out = e;
       return MK_OK;
     }
-  std::unique_ptr<PlanEntry> e(new PlanEntry());
+  // on an error below, the deleter frees what was already uploaded
+  std::unique_ptr<PlanEntry, void (*)(PlanEntry*)> e(new PlanEntry(), free_plan);
   std::memcpy(e->key, key, sizeof key);
   std::string why;
   if (!build_plan(h->shape, h->n_sm, parts, &e->plan, &why, dyn))
@@ -395,19 +396,24 @@ int create_impl(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
   p.err = h->d_err;
   p.n_ctr = h->n_ctr;
 
+  // what a failure below must give back before the handle goes away
+  auto release = [&h]() {
+    if (h->h_err_mirror) cudaFreeHost(h->h_err_mirror);
+    cudaFree(h->d_scratch);
+  };
   ce = cudaMemset(h->d_scratch, 0, total);
   if (ce != cudaSuccess) {
-    cudaFree(h->d_scratch);
+    release();
     return cuda_fail(nullptr, ce, "cudaMemset(scratch)");
   }
   ce = cudaHostAlloc(reinterpret_cast<void**>(&h->h_err_mirror), sizeof(int), cudaHostAllocMapped);
+  if (ce != cudaSuccess) h->h_err_mirror = nullptr;
   if (ce == cudaSuccess) {
     *h->h_err_mirror = 0;
     ce = cudaHostGetDevicePointer(reinterpret_cast<void**>(&p.err_host), h->h_err_mirror, 0);
   }
   if (ce != cudaSuccess) {
-    if (h->h_err_mirror) cudaFreeHost(h->h_err_mirror);
-    cudaFree(h->d_scratch);
+    release();
     return cuda_fail(nullptr, ce, "cudaHostAlloc(error mirror)");
   }
   // RoPE table: angle = pos * theta^(-2i/D), in double, rounded to fp32
@@ -441,7 +447,7 @@ int create_impl(const mk_config* cfg, const mk_weights* w, void* const* k_cache,
     ce = allow_max_smem(h->fn_fx, optin);
   if (ce == cudaSuccess && h->fn_dyn) ce = allow_max_smem(h->fn_dyn, optin);
   if (ce != cudaSuccess) {
-    cudaFree(h->d_scratch);
+    release();
     return cuda_fail(nullptr, ce, "mk_create upload");
   }
   *out = h.release();
@@ -731,12 +737,19 @@ int mk_decode_greedy_persistent(mk_handle* h, const int32_t* tok, const int32_t*
     }
     mk_handle::StepsPlan c;
     c.key = key;
-    MK_CUDA(h, cudaMalloc(&c.d_instrs, sizeof(Instr) * std::max<size_t>(1, P.instrs.size())));
-    MK_CUDA(h, cudaMalloc(&c.d_sm_off, sizeof(int) * P.sm_off.size()));
-    MK_CUDA(h, cudaMemcpy(c.d_instrs, P.instrs.data(), sizeof(Instr) * P.instrs.size(),
-                          cudaMemcpyHostToDevice));
-    MK_CUDA(h, cudaMemcpy(c.d_sm_off, P.sm_off.data(), sizeof(int) * P.sm_off.size(),
-                          cudaMemcpyHostToDevice));
+    cudaError_t ue = cudaMalloc(&c.d_instrs, sizeof(Instr) * std::max<size_t>(1, P.instrs.size()));
+    if (ue == cudaSuccess) ue = cudaMalloc(&c.d_sm_off, sizeof(int) * P.sm_off.size());
+    if (ue == cudaSuccess)
+      ue = cudaMemcpy(c.d_instrs, P.instrs.data(), sizeof(Instr) * P.instrs.size(),
+                      cudaMemcpyHostToDevice);
+    if (ue == cudaSuccess)
+      ue = cudaMemcpy(c.d_sm_off, P.sm_off.data(), sizeof(int) * P.sm_off.size(),
+                      cudaMemcpyHostToDevice);
+    if (ue != cudaSuccess) {
+      cudaFree(c.d_instrs);
+      cudaFree(c.d_sm_off);
+      return cuda_fail(h, ue, "uploading the several-step plan");
+    }
     h->steps_plans.push_back(c);
     sp = &h->steps_plans.back();
   }

@@ -32,7 +32,6 @@ std::string check_shape(const Shape& s) {
   if (s.D != 64 && s.D != 128) return bad("head_dim must be 64 or 128");
   if (s.nh < 1 || s.nkv < 1 || s.nh % s.nkv) return bad("n_heads must be a multiple of n_kv_heads");
   if (s.G() > 8) return bad("at most 8 query heads per kv head");
-  if (s.nh / s.nkv > 8) return bad("at most 8 q-heads per kv-head");
   if (s.QD() % 256 || s.QD() > 4096) return bad("n_heads*head_dim must be a multiple of 256, <= 4096");
   if (s.F < 256 * kChunks || s.F % (256 * kChunks) || s.Fc() > 8192)
     return bad("ffn must be a multiple of 1024 with ffn/4 <= 8192");

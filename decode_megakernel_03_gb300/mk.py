@@ -140,9 +140,22 @@ def make_config(shape, batch: int, capacity: int) -> MkConfig:
                     float(shape.rope_theta), int(batch), int(capacity))
 
 
-def _i32(vals):
+def _i32(vals, n: int | None = None):
+    """A host int32 array of vals; n: the length the library will read."""
+    if n is not None and len(vals) != n:
+        raise MkError(MK_ERR_INVALID, f"expected {n} values, got {len(vals)}")
     a = (ctypes.c_int32 * len(vals))(*[int(v) for v in vals])
     return a
+
+
+def _dev(t, n: int, dtype: str, what: str) -> ctypes.c_void_p:
+    """The device pointer of tensor t after checking that the library may
+    write n elements of dtype there (it cannot check that itself)."""
+    if not t.is_cuda or str(t.dtype) != "torch." + dtype or not t.is_contiguous():
+        raise MkError(MK_ERR_INVALID, f"{what} must be a contiguous CUDA {dtype} tensor")
+    if t.numel() < n:
+        raise MkError(MK_ERR_INVALID, f"{what} holds {t.numel()} elements, {n} are written")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 DYN_LMHEAD = 1  # MK_DYN_LMHEAD
@@ -222,9 +235,10 @@ def decode_step_noalloc(shape, weights: dict, k_cache: list, v_cache: list, batc
     cfg, w, kc, vc, keep = _model_structs(shape, weights, k_cache, v_cache, batch)
     msg = ctypes.create_string_buffer(512)
     rc = lib().mk_decode_step_noalloc(ctypes.byref(cfg), ctypes.byref(w), ctypes.cast(kc, _vpp),
-                                      ctypes.cast(vc, _vpp), _i32(tokens), _i32(positions),
-                                      ctypes.c_void_p(logits.data_ptr()), _stream_ptr(stream),
-                                      msg, len(msg))
+                                      ctypes.cast(vc, _vpp), _i32(tokens, batch),
+                                      _i32(positions, batch),
+                                      _dev(logits, batch * shape.vocab, "float32", "logits"),
+                                      _stream_ptr(stream), msg, len(msg))
     del keep
     return rc, msg.value.decode()
 
@@ -245,6 +259,8 @@ class Decoder:
         self.shape = shape
         self.batch = batch
         self.capacity = int(k_cache[0].shape[2]) if paged is None else int(paged[2])
+        # block-table entries per sequence of a paged handle
+        self.max_blocks = 0 if paged is None else -(-self.capacity // int(paged[0]))
         L = shape.n_layers
         self._keep = (weights, k_cache, v_cache)
         arrs = {}
@@ -273,9 +289,19 @@ class Decoder:
         self.h = h
 
     # -- decode ----------------------------------------------------------
+    def _logits(self, logits, rows: int | None = None) -> ctypes.c_void_p:
+        n = (self.batch if rows is None else rows) * self.shape.vocab
+        return _dev(logits, n, "float32", "logits")
+
+    def _tokens_out(self, t, n_steps: int, most: int) -> ctypes.c_void_p:
+        # a step count out of range is refused by the library before it
+        # writes anything, so only a valid count sizes the check
+        n = n_steps * self.batch if 1 <= n_steps <= most else 0
+        return _dev(t, n, "int32", "tokens_out")
+
     def step(self, tokens, positions, logits, stream=None) -> int:
-        rc = lib().mk_decode_step(self.h, _i32(tokens), _i32(positions),
-                                  ctypes.c_void_p(logits.data_ptr()), _stream_ptr(stream))
+        rc = lib().mk_decode_step(self.h, _i32(tokens, self.batch), _i32(positions, self.batch),
+                                  self._logits(logits), _stream_ptr(stream))
         _check(rc, self.h)
         return rc
 
@@ -284,7 +310,7 @@ class Decoder:
         `batch` tokens; logits (device fp32 [vocab]) receives the logits after
         the last prompt token."""
         rc = lib().mk_prefill(self.h, _i32(tokens), len(tokens), int(start_pos),
-                              ctypes.c_void_p(logits.data_ptr()), _stream_ptr(stream))
+                              self._logits(logits, 1), _stream_ptr(stream))
         _check(rc, self.h)
         return rc
 
@@ -292,10 +318,12 @@ class Decoder:
         """mk_decode_step_paged; block_table: int32 numpy array
         [batch][ceil(kv_capacity / block_size)] on the host."""
         tbl = np.ascontiguousarray(block_table, dtype=np.int32)
-        rc = lib().mk_decode_step_paged(self.h, _i32(tokens), _i32(positions),
+        if self.max_blocks and tbl.size != self.batch * self.max_blocks:
+            raise MkError(MK_ERR_INVALID, f"block_table must hold batch x {self.max_blocks} entries")
+        rc = lib().mk_decode_step_paged(self.h, _i32(tokens, self.batch),
+                                        _i32(positions, self.batch),
                                         tbl.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
-                                        ctypes.c_void_p(logits.data_ptr()),
-                                        _stream_ptr(stream))
+                                        self._logits(logits), _stream_ptr(stream))
         _check(rc, self.h)
         return rc
 
@@ -303,25 +331,26 @@ class Decoder:
                       stream=None) -> int:
         """mk_decode_greedy: n_steps greedy steps, the tokens fed back on the
         device; tokens_out is a device int32 tensor of n_steps * batch."""
-        rc = lib().mk_decode_greedy(self.h, _i32(tokens), _i32(positions), int(n_steps),
-                                    ctypes.c_void_p(tokens_out.data_ptr()),
-                                    ctypes.c_void_p(logits.data_ptr()), _stream_ptr(stream))
+        rc = lib().mk_decode_greedy(self.h, _i32(tokens, self.batch), _i32(positions, self.batch),
+                                    int(n_steps), self._tokens_out(tokens_out, n_steps,
+                                                                   MAX_GREEDY_STEPS),
+                                    self._logits(logits), _stream_ptr(stream))
         _check(rc, self.h)
         return rc
 
     def decode_greedy_persistent(self, tokens, positions, n_steps: int, tokens_out, logits,
                                  stream=None) -> int:
         """mk_decode_greedy_persistent: n_steps greedy steps in one launch."""
-        rc = lib().mk_decode_greedy_persistent(self.h, _i32(tokens), _i32(positions),
-                                               int(n_steps), ctypes.c_void_p(tokens_out.data_ptr()),
-                                               ctypes.c_void_p(logits.data_ptr()),
-                                               _stream_ptr(stream))
+        rc = lib().mk_decode_greedy_persistent(
+            self.h, _i32(tokens, self.batch), _i32(positions, self.batch), int(n_steps),
+            self._tokens_out(tokens_out, n_steps, MAX_STEPS_PER_LAUNCH), self._logits(logits),
+            _stream_ptr(stream))
         _check(rc, self.h)
         return rc
 
     def step_multilaunch(self, tokens, positions, logits, stream=None, graph: bool = False) -> int:
-        rc = lib().mk_decode_step_multilaunch(self.h, _i32(tokens), _i32(positions),
-                                              ctypes.c_void_p(logits.data_ptr()),
+        rc = lib().mk_decode_step_multilaunch(self.h, _i32(tokens, self.batch),
+                                              _i32(positions, self.batch), self._logits(logits),
                                               _stream_ptr(stream), int(bool(graph)))
         _check(rc, self.h)
         return rc

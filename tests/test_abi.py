@@ -79,3 +79,21 @@ def test_unsupported_shapes(L, field, value):
     rc = L.mk_schedule_build(ctypes.byref(cfg), 4, pos, None, 0, ctypes.byref(n), None, None, 0,
                              ctypes.byref(n))
     assert rc == mk.MK_ERR_INVALID
+
+
+def test_binding_checks_what_the_library_cannot():
+    """The library reads B host token ids and positions and writes B x vocab
+    logits through bare pointers; the binding refuses lists of another length
+    and output tensors that are not contiguous CUDA tensors of the right type
+    and size, before anything is passed on."""
+    import torch
+
+    with pytest.raises(mk.MkError) as e:
+        mk._i32([1, 2], 3)
+    assert e.value.code == mk.MK_ERR_INVALID
+    assert list(mk._i32([4, 5, 6], 3)) == [4, 5, 6]
+    for t, n, dt in ((torch.empty(8), 8, "float32"),                     # host memory
+                     (torch.empty(8, dtype=torch.int32), 8, "float32")):  # wrong type
+        with pytest.raises(mk.MkError) as e:
+            mk._dev(t, n, dt, "logits")
+        assert e.value.code == mk.MK_ERR_INVALID
