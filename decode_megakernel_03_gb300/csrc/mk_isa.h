@@ -32,7 +32,7 @@ constexpr int kResBufs = 4;      // result hand-offs in flight between compute a
 using Instr = mk_instr;
 static_assert(sizeof(Instr) == 32, "instruction descriptor is 32 bytes");
 
-// Per-layer weight and cache pointers, uploaded once to device memory.
+// Per-layer weight and cache pointers (they travel in the kernel parameters).
 struct LayerPtrs {
   const uint16_t* attn_norm;
   const uint16_t* wq;
@@ -174,10 +174,11 @@ MK_HD Geom geom_of(int op, int H, int QD, int Fc) {
 // One split-KV attention unit: keys [t0, t1) of the keys 0..pos of its
 // sequence, partition pidx of P (the host picks P; the device recomputes the
 // range from the exact position). The new key (pos), whose k/v row this step
-// writes, is read from the cache after the unit's counter wait; the other
-// nc = |[t0, min(t1, pos))| keys are cached already and stream through
-// shared-memory pages ahead of that wait, kpp keys per page: K rows in the
-// page's first half, V rows in its second.
+// writes, is taken from the stamped copy the QKV instruction writes beside
+// its cache append (Params::kvn); the other nc = |[t0, min(t1, pos))| keys
+// are cached already and stream through shared-memory pages before the
+// unit's inputs arrive, kpp keys per page: K rows in the page's first half,
+// V rows in its second.
 struct AttnSpan {
   int t0, t1;   // the unit's keys
   int nc;       // cached keys [t0, t0 + nc), all below pos

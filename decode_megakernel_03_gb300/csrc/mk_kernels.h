@@ -9,7 +9,8 @@ struct Shape;
 
 // interp_kernel<B, DS, GS, KW, FX>: batch, head dimension (0: read at run
 // time), q-heads per kv-head (0: run time), GEMV width (2048, or 0: any),
-// and FX = 1 for the build with the paged-cache and greedy-decode code.
+// and the feature bits FX: kFxPaged for the build with the paged-cache and
+// greedy-decode code, kFxDyn for the one with the dynamic LM head.
 // interp_kernel<B, 0, 0, 0, 0>: head dimension and q-heads per kv-head read at
 // run time, any GEMV width (B = 1, 2, 4 or 8).
 const void* kernel_generic(int B);

@@ -13,8 +13,9 @@
 // cudaMalloc, cudaFree, pinned host memory or allocating library routine.
 //
 // Sharing rules: every call on a device uses the same array and leaves its
-// contents behind. Each call clears what must start at zero (the counters and
-// the error word) before it launches, and uploads its queue and RoPE table.
+// contents behind. Each call clears what must start at zero (the counters,
+// the error word and the values handed between instructions) before it
+// launches, and uploads its queue and the RoPE rows of its positions.
 // Calls that overlap on the GPU (on different streams, or from several host
 // threads) race on the array; serialise them.
 #include <cuda_runtime.h>

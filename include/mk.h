@@ -285,8 +285,10 @@ typedef struct {
    MK_DYN_LMHEAD: the LM head's row blocks are taken from a per-step atomic
    ticket counter by the SMs as they reach it. Off by default (the static
    plan); the results are the same either way (each row's arithmetic does
-   not depend on which SM computes it). Steps of a handle with a flag set run
-   the interpreter build that also carries the paged-cache and greedy code. */
+   not depend on which SM computes it). Steps of a handle with a flag set
+   (mk_decode_step and the multi-launch build) run an interpreter build of
+   their own that carries the ticket code; every other step runs one without
+   it. */
 #define MK_DYN_LMHEAD 1
 int mk_set_dynamic(mk_handle* h, int flags);
 
@@ -351,7 +353,8 @@ int mk_schedule_build_steps(const mk_config* cfg, int n_sm, const int32_t* posit
    The call is synchronous: it waits for the step on `stream` and returns
    MK_ERR_TIMEOUT if a device wait expired.
    Every call shares the array and leaves its contents behind; each call
-   clears the counters and the error word itself. Calls that overlap on the
+   clears the counters, the error word and the values handed between
+   instructions itself. Calls that overlap on the
    GPU (several streams or host threads) race on the array: serialise them.
    Errors: MK_ERR_INVALID (bad or unsupported arguments, or a configuration
    whose scratch exceeds the 16 MiB array, reported with the size it needs),
