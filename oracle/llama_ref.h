@@ -27,6 +27,29 @@
  *
  * Layouts: matrices are row-major [out][in] (the nn.Linear convention); the
  * KV cache of one layer is [batch][n_kv_heads][capacity][head_dim] bf16.
+ *
+ * What pins each function to something other than itself (the CPU tests
+ * test_oracle_pins.py and test_oracle_model.py; "golden" is the file of
+ * hand-derived values, each with its derivation):
+ *   ref_bf16_to_f64 / ref_f64_to_bf16  exact widening of every bit pattern;
+ *                     rounding against an independent library rounding;
+ *                     golden rounding cases
+ *   ref_rmsnorm       golden values; a constant vector's closed form; scale
+ *                     invariance and unit RMS
+ *   ref_rope          golden rotations; identity at position 0; pair norms
+ *                     kept; scores that depend on the position difference
+ *                     only; each pair's frequency theta^(-2i/D)
+ *   ref_silu          golden values; its limits; SiLU(z) - SiLU(-z) = z
+ *   ref_matvec        brute force on small matrices
+ *   ref_attend        golden values; one key returns its value; equal keys
+ *                     average the values; a library softmax;
+ *                     split-and-combine equals one pass
+ *   ref_decode_step   wiring cases with special weights (GQA map, attended
+ *                     range, residual, MLP order, tied head, independent
+ *                     batch rows); a whole step against the composition of
+ *                     the pinned operations with nonzero q/k weights (a
+ *                     planted wrong scale fails it)
+ *   ref_forward_full  incremental decoding equals the full recompute
  */
 #ifndef LLAMA_REF_H
 #define LLAMA_REF_H
