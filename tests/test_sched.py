@@ -116,6 +116,25 @@ def test_every_output_produced_exactly_once(case):
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0].name}-B{c[1]}-sm{c[3]}")
+def test_every_gemv_fits_the_result_buffer_and_the_epilogue(case):
+    """A GEMV instruction's results (items x rows per item x batch floats)
+    fit one of the storer's result buffers, sized for the item cap of a
+    row-pair instruction (64 items at batch 1, 32 at batch 2, 16 beyond), and
+    its items fit the epilogue's two items per lane (at most 64)."""
+    shape, B = case[0], case[1]
+    ins, off, tg, sm = _plan(*case)
+    cap = 64 if B == 1 else (32 if B == 2 else 16)
+    res_floats = cap * 2 * B
+    for op in (mk.OP_QKV, mk.OP_OPROJ, mk.OP_GATEUP, mk.OP_DOWN, mk.OP_LMHEAD):
+        r = ins[ins["op"] == op]
+        items = r["a1"] - r["a0"]
+        rows = 2 if op in (mk.OP_QKV, mk.OP_GATEUP) else 1
+        assert np.all(items >= 1)
+        assert np.all(items <= 64), mk.OPS[op]
+        assert np.all(items * rows * B <= res_floats), mk.OPS[op]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"{c[0].name}-B{c[1]}-sm{c[3]}")
 def test_counter_targets(case):
     ins, off, tg, sm = _plan(*case)
     sums = np.zeros_like(tg)
