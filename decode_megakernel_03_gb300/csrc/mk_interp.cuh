@@ -233,8 +233,6 @@ __device__ __forceinline__ float4 clear4(const float4& v) {
   return make_float4(clear1(v.x), clear1(v.y), clear1(v.z), clear1(v.w));
 }
 
-__device__ __forceinline__ float2 clear2(const float2& v) { return make_float2(clear1(v.x), clear1(v.y)); }
-
 // A batch of loads that found a stale word is loaded again, whole: no
 // per-word slow path, so the batch's code appears once (after a counter
 // wait it is almost never repeated, the counter being bumped after the words

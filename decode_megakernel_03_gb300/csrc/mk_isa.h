@@ -129,7 +129,6 @@ struct Params {
 constexpr int kErrTimeoutCounter = (MK_ERR_TIMEOUT << 24) | 1;
 constexpr int kErrTimeoutPage = (MK_ERR_TIMEOUT << 24) | 2;
 constexpr int kErrTimeoutRes = (MK_ERR_TIMEOUT << 24) | 3;
-constexpr int kErrBadInstr = (MK_ERR_INVALID << 24) | 4;
 constexpr int kErrTimeoutStamp = (MK_ERR_TIMEOUT << 24) | 5;
 
 // ---- geometry of the GEMV-shaped instructions -----------------------------
