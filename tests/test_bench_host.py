@@ -1,8 +1,12 @@
-"""The roofline's numerator: the bytes one decode step must move, counted by
+"""Host-side pieces of the benchmark, no GPU.
+
+The roofline's numerator: the bytes one decode step must move, counted by
 hand for the Llama-1B and Llama-8B shapes and compared with the benchmark's
 count (weights, norm gains, the LM head, one embedding row per sequence, and
 the KV read over slots 0..pos of every layer and sequence — the minimal
-bytes that "9 · Quand ne pas le faire", §9.1, asks to count)."""
+bytes that "9 · Quand ne pas le faire", §9.1, asks to count). And the clock
+record of the timed region: the throttle reasons that void a measurement
+are read from the sampled lines."""
 import bench
 from decode_megakernel_03_gb300 import synth
 
@@ -36,3 +40,18 @@ def test_llama8b_and_batch_bytes_by_hand():
     w1, _ = bench.algorithmic_bytes(synth.LLAMA_1B, 1, [0])
     assert w8 == w1 + 7 * 2 * 2048
     assert kv8 == 32_768 * sum(101 + b for b in range(8))
+
+
+def test_clock_record_reads_the_throttle_reasons():
+    c = bench.ClockSampler()
+    # index, clocks.sm, clocks.max.sm, power.draw, reasons.active, then
+    # hw_slowdown, hw_thermal_slowdown, sw_thermal_slowdown, sw_power_cap
+    c.lines = ["0, 2070, 2070, 900.1, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+               "0, 1995, 2070, 1390.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+               "0, 2070, 2070, 1200.0, 0x0000000000000008, Active, Not Active, Not Active, Not Active",
+               "garbled line"]
+    s = c.summary()
+    assert s["samples"] == 3
+    assert s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    assert bench.ClockSampler().summary()["reasons"] == ["unsampled"]
